@@ -1,0 +1,176 @@
+"""Thin ctypes binding over the C ABI declared in ``include/fa2.h``.
+
+Argument marshalling only: each function takes torch tensors that already live
+on the GPU, checks shapes / dtypes / contiguity, and passes raw device pointers,
+sizes and the current CUDA stream to the library function of the same name.
+Every step of the computation runs in the library's CUDA kernels.  If the
+shared library has not been built, the first call raises :class:`Fa2Error`;
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libfa2_gb300.so"
+LIB_PATH = os.path.join(_HERE, LIB_NAME)
+
+FA2_OK = 0
+DTYPE_F32, DTYPE_F16, DTYPE_BF16 = 0, 1, 2
+
+# every exported symbol, as declared in include/fa2.h
+EXPORTS = (
+    "fa2_forward",
+    "fa2_backward_workspace_size",
+    "fa2_backward",
+    "psa_pack_qkv",
+    "psa_merge_attn_nchw",
+    "fa2_device_status",
+    "fa2_status_string",
+)
+
+
+class Fa2Error(RuntimeError):
+    """A non-zero fa2_status, or the library missing."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa2_status_string(status) if status >= 0 else 'library not built'} (status {status})")
+
+
+_lib = None
+
+_c_ptr = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_f32 = ctypes.c_float
+
+
+def _declare(lib):
+    sig = {
+        "fa2_forward": (ctypes.c_int, [_c_ptr] * 5 + [_i64, _i64, _i64, _i32, _i32, _f32, _c_ptr]),
+        "fa2_backward_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
+        "fa2_backward": (ctypes.c_int, [_c_ptr] * 10 + [ctypes.c_size_t, _i64, _i64, _i64, _i32, _i32, _f32, _c_ptr]),
+        "psa_pack_qkv": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
+        "psa_merge_attn_nchw": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
+        "fa2_device_status": (ctypes.c_int, [_c_ptr]),
+        "fa2_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+def library(path: str | None = None):
+    """The loaded shared library (loaded once).  Raises Fa2Error if it is not built."""
+    global _lib
+    if _lib is None:
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise Fa2Error(-1, f"{p} not found (run __graft_entry__.build())")
+        _lib = _declare(ctypes.CDLL(p))
+    return _lib
+
+
+_MESSAGES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned pointer",
+             4: "CUDA error", 5: "device wait timed out", 6: "bad workspace"}
+
+
+def fa2_status_string(status: int) -> str:
+    try:
+        return library().fa2_status_string(int(status)).decode()
+    except Fa2Error:
+        return _MESSAGES.get(int(status), "unknown status")
+
+
+def _check(status: int, where: str):
+    if status != FA2_OK:
+        raise Fa2Error(status, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.float32: DTYPE_F32, torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name, ndim=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def fa2_forward(q, k, v, o, lse, softmax_scale: float, stream=None) -> None:
+    """O and LSE of attention; q [BH,Nq,d], k/v [BH,Nk,d], o like q, lse [BH,Nq] float32."""
+    import torch
+    bh, n_q, d = q.shape
+    n_k = k.shape[1]
+    if k.shape != (bh, n_k, d) or v.shape != k.shape or o.shape != q.shape or lse.shape != (bh, n_q):
+        raise ValueError("inconsistent shapes")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype) or lse.dtype != torch.float32:
+        raise TypeError("q, k, v, o share one dtype; lse is float32")
+    st = library().fa2_forward(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(o, "o", 3), _dev(lse, "lse", 2),
+                               bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
+    _check(st, "fa2_forward")
+
+
+def fa2_backward_workspace_size(bh: int, n_q: int, n_k: int, head_dim: int, dtype_code: int) -> int:
+    return int(library().fa2_backward_workspace_size(bh, n_q, n_k, head_dim, dtype_code))
+
+
+def fa2_backward(q, k, v, o, d_o, lse, dq, dk, dv, workspace, softmax_scale: float, stream=None) -> None:
+    """dQ, dK, dV of attention; workspace is a CUDA uint8 tensor of fa2_backward_workspace_size bytes."""
+    import torch
+    bh, n_q, d = q.shape
+    n_k = k.shape[1]
+    if (k.shape != (bh, n_k, d) or v.shape != k.shape or o.shape != q.shape or d_o.shape != q.shape
+            or lse.shape != (bh, n_q) or dq.shape != q.shape or dk.shape != k.shape or dv.shape != k.shape):
+        raise ValueError("inconsistent shapes")
+    if lse.dtype != torch.float32:
+        raise TypeError("lse is float32")
+    st = library().fa2_backward(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(o, "o", 3), _dev(d_o, "d_o", 3),
+                                _dev(lse, "lse", 2), _dev(dq, "dq", 3), _dev(dk, "dk", 3), _dev(dv, "dv", 3),
+                                _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
+    _check(st, "fa2_backward")
+
+
+def psa_pack_qkv(qkv, packed, num_heads: int, stream=None) -> None:
+    """qkv NCHW [B, qkv_h, H, W] -> packed [4, B*num_heads, H*W, qkv_h/(4*num_heads)]."""
+    b, qkv_h, h, w = qkv.shape
+    if packed.numel() != qkv.numel() or packed.dtype != qkv.dtype:
+        raise ValueError("packed must hold as many elements as qkv, same dtype")
+    st = library().psa_pack_qkv(_dev(qkv, "qkv", 4), _dev(packed, "packed"), qkv_h, h, w, b, num_heads,
+                                _dtype_code(qkv), _stream(stream))
+    _check(st, "psa_pack_qkv")
+
+
+def psa_merge_attn_nchw(lo, hi, out, num_heads: int, stream=None) -> None:
+    """lo, hi [B*num_heads, H*W, KD] -> out NCHW [B, num_heads*2*KD, H, W]."""
+    b, c, h, w = out.shape
+    if lo.shape != hi.shape or lo.numel() * 2 != out.numel() or lo.dtype != out.dtype or hi.dtype != out.dtype:
+        raise ValueError("lo and hi must together hold out's elements, same dtype")
+    st = library().psa_merge_attn_nchw(_dev(lo, "lo"), _dev(hi, "hi"), _dev(out, "out", 4), c, h, w, b, num_heads,
+                                       _dtype_code(out), _stream(stream))
+    _check(st, "psa_merge_attn_nchw")
+
+
+def fa2_device_status(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel gave up a bounded wait."""
+    _check(library().fa2_device_status(_stream(stream)), "fa2_device_status")

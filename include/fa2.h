@@ -1,0 +1,169 @@
+/*
+ * fa2.h - C ABI of the GB300 (sm_103a) FlashAttention-2 + PSA library.
+ *
+ * Every entry point enqueues its work on `stream` (a cudaStream_t passed as a
+ * plain pointer; NULL means the legacy default stream) and returns at once.  No
+ * entry point allocates device memory, synchronises, or throws; each returns an
+ * fa2_status.  Arguments are validated on the host before anything is launched:
+ * a call that returns anything but FA2_OK has launched nothing, except
+ * FA2_ERR_CUDA, which reports a failed launch.
+ *
+ * Common conventions
+ *  - All tensor pointers are caller-owned DEVICE memory, contiguous, row-major,
+ *    in the layouts given per call.  The library keeps no pointer after the call
+ *    returns; the caller keeps the buffers alive until the stream work is done.
+ *  - Outputs must not alias inputs or each other.
+ *  - Base pointers must be 16-byte aligned (FA2_ERR_MISALIGNED otherwise).
+ *  - Sizes are 64-bit where a product can pass 2^31; every size must be > 0
+ *    (FA2_ERR_INVALID_ARG), following the pages' rule that an empty sequence or
+ *    head dimension is an error ("vyre-libs 0.7.2 flash_attention_2.rs",
+ *    flash_attention_2: a trap program for seq_len, head_dim or tile_size 0).
+ *  - Layout of attention tensors: [BH, N, HEAD_DIM] with BH = BATCH * N_HEADS
+ *    ("vision-rs 0.1.1 flash_attn2.rs", module comment: all tensors stored as
+ *    [BATCH * N_HEADS, N_CTX, HEAD_DIM] row-major, contiguous).
+ */
+#ifndef FA2_GB300_H
+#define FA2_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA2_OK = 0,
+    FA2_ERR_INVALID_ARG = 1,     /* a size <= 0, a null pointer, inconsistent shapes, bad scale */
+    FA2_ERR_UNSUPPORTED = 2,     /* valid arguments this build has no kernel for (head_dim, dtype) */
+    FA2_ERR_MISALIGNED = 3,      /* a base pointer not 16-byte aligned */
+    FA2_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed */
+    FA2_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up a bounded wait (reported by fa2_device_status) */
+    FA2_ERR_WORKSPACE = 6        /* workspace pointer null/misaligned or smaller than required */
+} fa2_status;
+
+typedef enum {
+    FA2_DTYPE_F32 = 0,   /* IEEE binary32 */
+    FA2_DTYPE_F16 = 1,   /* IEEE binary16 */
+    FA2_DTYPE_BF16 = 2   /* bfloat16 */
+} fa2_dtype;
+
+/*
+ * fa2_forward - attention forward with the saved row log-sum-exp.
+ *
+ * Defined by "vision-rs 0.1.1 flash_attn2.rs", kernel flash_attention2_forward:
+ * for each (bh, i): s_ij = softmax_scale * sum_d q[bh,i,d] k[bh,j,d];
+ * O[bh,i,:] = sum_j softmax_j(s_i.) v[bh,j,:]; LSE[bh,i] = m_i + ln l_i with
+ * m_i = max_j s_ij and l_i = sum_j exp(s_ij - m_i) (the online-softmax
+ * recurrence of that kernel reaches this up to rounding).  No masking.
+ *
+ *   q    [bh, n_q, head_dim]   dtype, device, read
+ *   k, v [bh, n_k, head_dim]   dtype, device, read
+ *   o    [bh, n_q, head_dim]   dtype, device, written (rounded to nearest even)
+ *   lse  [bh, n_q]             float32, device, written, natural log of the
+ *                              scaled scores (the page stores it in the input
+ *                              dtype; this library always stores float32)
+ *   softmax_scale              > 0 and finite; callers normally pass 1/sqrt(head_dim)
+ *
+ * dtype BF16 / F16: head_dim in {32, 64, 128}; tensor-core kernel, float32
+ * accumulation, the probabilities rounded to dtype before the P.V product.
+ * dtype F32: head_dim in {32, 64, 128}; a float32 CUDA-core kernel (meant for
+ * small problems; float32 products and sums throughout).
+ * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED, FA2_ERR_CUDA.
+ */
+fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
+                       fa2_dtype dtype, float softmax_scale, void* stream);
+
+/*
+ * fa2_backward_workspace_size - bytes of device workspace fa2_backward needs
+ * for these sizes (0 if the sizes are invalid).  The workspace holds the row
+ * sums D = rowsum(O * dO) in float32.
+ */
+size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype);
+
+/*
+ * fa2_backward - dQ, dK and dV of attention from dO, O and the saved LSE.
+ *
+ * Defined by "vision-rs 0.1.1 flash_attn2.rs", kernels
+ * flash_attention2_backward_dq and flash_attention2_backward_dkv:
+ * D_i = sum_d O_id dO_id;  P_ij = exp(s_ij - LSE_i);  dV_j = sum_i P_ij dO_i;
+ * dS_ij = P_ij (dO_i . v_j - D_i);  dQ_i = scale sum_j dS_ij k_j;
+ * dK_j = scale sum_i dS_ij q_i.  Structure as on that page: a pass over key
+ * tiles (dK, dV) and a pass over query tiles (dQ), plus a row-sum pass for D.
+ *
+ *   q, o, d_o   [bh, n_q, head_dim]  dtype, device, read (o and lse as written by fa2_forward)
+ *   k, v        [bh, n_k, head_dim]  dtype, device, read
+ *   lse         [bh, n_q]            float32, device, read
+ *   dq          [bh, n_q, head_dim]  dtype, device, written
+ *   dk, dv      [bh, n_k, head_dim]  dtype, device, written
+ *   workspace   caller-owned device scratch of at least
+ *               fa2_backward_workspace_size(...) bytes, 16-byte aligned; its
+ *               contents on entry do not matter; the call overwrites it.
+ *
+ * dtype BF16 / F16 with head_dim in {32, 64, 128}; float32 accumulation.
+ * dtype F32 returns FA2_ERR_UNSUPPORTED.
+ * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED,
+ *         FA2_ERR_WORKSPACE, FA2_ERR_CUDA.
+ */
+fa2_status fa2_backward(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                        const float* lse, void* dq, void* dk, void* dv,
+                        void* workspace, size_t workspace_bytes,
+                        int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
+                        fa2_dtype dtype, float softmax_scale, void* stream);
+
+/*
+ * psa_pack_qkv - NCHW QKV to the packed [4, B*num_heads, H*W, KEY_DIM] buffer.
+ *
+ * Defined by "vision_rs/models/yolo/kernels/attention/psa.rs", kernel
+ * psa_pack_qkv (same argument order): KEY_DIM = qkv_h / (4 * num_heads) and
+ * packed[s, b*num_heads + h, n, dd] = qkv[b, h*4*KEY_DIM + s*KEY_DIM + dd, n]
+ * for section s (0 Q, 1 K, 2 V_lo, 3 V_hi) and n = y*W + x.  The memory order
+ * is section-major, as in that kernel's store and in FlashAttn2PsaRuntimeOp's
+ * pointer arithmetic.
+ *
+ *   qkv     [B, qkv_h, H, W]              dtype, device, read
+ *   packed  [4, B*num_heads, H*W, KEY_DIM] dtype, device, written
+ *
+ * A pure copy of 2- or 4-byte words: the result is bit-exact for any bit
+ * pattern.  qkv_h must be a multiple of 4*num_heads (FA2_ERR_INVALID_ARG).
+ */
+fa2_status psa_pack_qkv(const void* qkv, void* packed, int32_t qkv_h, int32_t H, int32_t W,
+                        int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream);
+
+/*
+ * psa_merge_attn_nchw - the two attention outputs (V_lo and V_hi) back to NCHW.
+ *
+ * Defined by "vision_rs/models/yolo/kernels/attention/psa.rs", kernel
+ * psa_merge_attn_nchw: with KEY_DIM = c / (2 * num_heads),
+ * out[b, h*2*KEY_DIM + dd, n] = lo[b*num_heads + h, n, dd] and
+ * out[b, h*2*KEY_DIM + KEY_DIM + dd, n] = hi[b*num_heads + h, n, dd].
+ * The page's kernel takes no B (it comes from its grid); here B is explicit.
+ *
+ *   lo, hi  [B*num_heads, H*W, KEY_DIM]  dtype, device, read
+ *   out     [B, c, H, W]                 dtype, device, written
+ *
+ * Bit-exact copy.  c must be a multiple of 2*num_heads (FA2_ERR_INVALID_ARG).
+ */
+fa2_status psa_merge_attn_nchw(const void* lo, const void* hi, void* out, int32_t c, int32_t H,
+                               int32_t W, int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream);
+
+/*
+ * fa2_device_status - the watchdog word of the library's kernels.
+ *
+ * Every wait inside the library's kernels is bounded in time.  A kernel that
+ * gives up a wait records it in a device-side word, drains the copies it has
+ * in flight, frees its tensor memory and returns.  This call synchronises
+ * `stream`, reads that word on the current device, clears it and returns
+ * FA2_OK or FA2_ERR_DEVICE_TIMEOUT (FA2_ERR_CUDA if the synchronisation failed).
+ */
+fa2_status fa2_device_status(void* stream);
+
+/* fa2_status_string - a static, human-readable message for a status code. */
+const char* fa2_status_string(fa2_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA2_GB300_H */

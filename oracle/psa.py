@@ -1,0 +1,100 @@
+"""Oracle: the PSA (YOLO C2PSA) rearrangement passes around attention.
+
+Test infrastructure only (see the package docstring).
+
+Source: "vision_rs/models/yolo/kernels/attention/psa.rs" (vision-rs.teenygrad.org),
+module comment and the kernels ``psa_pack_qkv``, ``psa_extract_v_nchw``,
+``psa_merge_attn_nchw`` and their backward kernels.  These are pure index maps,
+written here as one explicit assignment per (section, head) block:
+
+* QKV is NCHW ``[B, qkv_h, H, W]`` with ``qkv_h = num_heads * 4 * KEY_DIM``; for
+  head h the channels ``h*4*KD + s*KD + [0, KD)`` hold section s (0 = Q, 1 = K,
+  2 = V_lo, 3 = V_hi).
+* pack:  ``packed[s, b*nh + h, n, dd] = qkv[b, h*4*KD + s*KD + dd, n]`` with
+  ``n = y*W + x``; ``packed`` is ``[4, B*nh, H*W, KD]`` (section-major, the
+  kernel's own memory order).
+* merge: ``out[b, h*2*KD + dd, n] = lo[b*nh + h, n, dd]`` and
+  ``out[b, h*2*KD + KD + dd, n] = hi[b*nh + h, n, dd]``; ``out`` is
+  ``[B, c, H, W]`` with ``c = nh * 2 * KD``.
+* extract V: ``v[b, h*2*KD + dd, n] = qkv[b, h*4*KD + 2*KD + dd, n]`` and
+  ``v[b, h*2*KD + KD + dd, n] = qkv[b, h*4*KD + 3*KD + dd, n]``.
+
+The functions accept any element dtype (including raw uint16 bit patterns) and
+never look at the values, so equality is bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def key_dim(qkv_h: int, num_heads: int) -> int:
+    if qkv_h % (4 * num_heads) != 0:
+        raise ValueError("qkv_h must be a multiple of 4*num_heads")
+    return qkv_h // (4 * num_heads)
+
+
+def pack_qkv(qkv: np.ndarray, num_heads: int) -> np.ndarray:
+    """psa.rs ``psa_pack_qkv``: NCHW [B, qkv_h, H, W] -> [4, B*nh, H*W, KD]."""
+    b_, qkv_h, h_, w_ = qkv.shape
+    kd = key_dim(qkv_h, num_heads)
+    n = h_ * w_
+    flat = qkv.reshape(b_, qkv_h, n)
+    out = np.empty((4, b_ * num_heads, n, kd), dtype=qkv.dtype)
+    for s in range(4):
+        for b in range(b_):
+            for h in range(num_heads):
+                c0 = h * 4 * kd + s * kd
+                out[s, b * num_heads + h] = flat[b, c0:c0 + kd, :].T
+    return out
+
+
+def merge_attn_nchw(lo: np.ndarray, hi: np.ndarray, batch: int, num_heads: int, height: int, width: int) -> np.ndarray:
+    """psa.rs ``psa_merge_attn_nchw``: lo, hi [B*nh, H*W, KD] -> NCHW [B, nh*2*KD, H, W]."""
+    bh, n, kd = lo.shape
+    assert bh == batch * num_heads and n == height * width and hi.shape == lo.shape
+    c = num_heads * 2 * kd
+    out = np.empty((batch, c, n), dtype=lo.dtype)
+    for b in range(batch):
+        for h in range(num_heads):
+            out[b, h * 2 * kd:h * 2 * kd + kd, :] = lo[b * num_heads + h].T
+            out[b, h * 2 * kd + kd:(h + 1) * 2 * kd, :] = hi[b * num_heads + h].T
+    return out.reshape(batch, c, height, width)
+
+
+def extract_v_nchw(qkv: np.ndarray, num_heads: int) -> np.ndarray:
+    """psa.rs ``psa_extract_v_nchw``: the V_lo / V_hi channels of QKV as NCHW [B, c, H, W]."""
+    b_, qkv_h, h_, w_ = qkv.shape
+    kd = key_dim(qkv_h, num_heads)
+    c = num_heads * 2 * kd
+    out = np.empty((b_, c, h_, w_), dtype=qkv.dtype)
+    for h in range(num_heads):
+        out[:, h * 2 * kd:h * 2 * kd + kd] = qkv[:, h * 4 * kd + 2 * kd:h * 4 * kd + 3 * kd]
+        out[:, h * 2 * kd + kd:(h + 1) * 2 * kd] = qkv[:, h * 4 * kd + 3 * kd:(h + 1) * 4 * kd]
+    return out
+
+
+def pack_qkv_backward(d_packed: np.ndarray, batch: int, num_heads: int, height: int, width: int) -> np.ndarray:
+    """psa.rs ``psa_pack_qkv_backward``: the adjoint of pack (a scatter; no overlaps)."""
+    _, bh, n, kd = d_packed.shape
+    qkv_h = num_heads * 4 * kd
+    out = np.zeros((batch, qkv_h, n), dtype=np.float64)
+    for s in range(4):
+        for b in range(batch):
+            for h in range(num_heads):
+                c0 = h * 4 * kd + s * kd
+                out[b, c0:c0 + kd, :] += np.asarray(d_packed[s, b * num_heads + h], dtype=np.float64).T
+    return out.reshape(batch, qkv_h, height, width)
+
+
+def merge_attn_backward(d_merged: np.ndarray, num_heads: int):
+    """psa.rs ``psa_merge_attn_backward``: NCHW gradient -> (d_lo, d_hi) [B*nh, H*W, KD]."""
+    b_, c, h_, w_ = d_merged.shape
+    kd = c // (2 * num_heads)
+    flat = d_merged.reshape(b_, c, h_ * w_)
+    d_lo = np.empty((b_ * num_heads, h_ * w_, kd), dtype=d_merged.dtype)
+    d_hi = np.empty_like(d_lo)
+    for b in range(b_):
+        for h in range(num_heads):
+            d_lo[b * num_heads + h] = flat[b, h * 2 * kd:h * 2 * kd + kd].T
+            d_hi[b * num_heads + h] = flat[b, h * 2 * kd + kd:(h + 1) * 2 * kd].T
+    return d_lo, d_hi

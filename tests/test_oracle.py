@@ -1,0 +1,375 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+* brute force on tiny inputs (pure-Python loops, no max shift, exact-sum fsum);
+* the worked examples the pages print (tests/golden/);
+* closed forms and invariants of softmax attention;
+* library routines the special cases reduce to (scipy softmax / logsumexp);
+* central finite differences of L = sum(O * dO) for every input element;
+* element-by-element index loops for the PSA rearrangements;
+* planted mistakes: mutated copies of the oracle must fail at least one pin.
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy import special
+
+from oracle import attention as A
+from oracle import psa as P
+from tests.golden.load import load
+from attention_fa2_forward_02_gb300 import synth
+
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+# --------------------------------------------------------------------------- forward pins
+
+def brute_forward(q, k, v, scale):
+    """Independent formulation: exp of raw scores (no max shift), fsum, explicit loops."""
+    bh, nq, d = q.shape
+    nk = k.shape[1]
+    o = np.zeros((bh, nq, v.shape[2]))
+    lse = np.zeros((bh, nq))
+    for b in range(bh):
+        for i in range(nq):
+            e = [math.exp(scale * math.fsum(q[b, i, t] * k[b, j, t] for t in range(d))) for j in range(nk)]
+            z = math.fsum(e)
+            lse[b, i] = math.log(z)
+            for t in range(v.shape[2]):
+                o[b, i, t] = math.fsum(e[j] * v[b, j, t] for j in range(nk)) / z
+    return o, lse
+
+
+def pin_brute(fwd):
+    q, k, v = _rand((2, 3, 4), 1), _rand((2, 5, 4), 2), _rand((2, 5, 4), 3)
+    o, lse = fwd(q, k, v, 0.5)
+    ob, lb = brute_forward(q, k, v, 0.5)
+    return np.allclose(o, ob, atol=1e-12, rtol=0) and np.allclose(lse, lb, atol=1e-12, rtol=0)
+
+
+def pin_golden_one(fwd):
+    g = load("seq_len_one.txt")
+    q = np.array(g["q"]).reshape(1, 1, 4)
+    k = np.array(g["k"]).reshape(1, 1, 4)
+    v = np.array(g["v"]).reshape(1, 1, 4)
+    o, lse = fwd(q, k, v, g["scale"])
+    return np.array_equal(o.ravel(), np.array(g["o"])) and lse.ravel()[0] == g["lse"]
+
+
+def pin_golden_const(fwd):
+    g = load("constant_rows.txt")
+    nq, nk, d = int(g["n_q"]), int(g["n_k"]), int(g["head_dim"])
+    q = np.full((1, nq, d), g["fill_q"])
+    k = np.full((1, nk, d), g["fill_k"])
+    v = np.full((1, nk, d), g["fill_v"])
+    o, lse = fwd(q, k, v, g["scale"])
+    return np.allclose(o, g["fill_o"], atol=1e-14, rtol=0) and np.allclose(lse, g["lse"], atol=1e-13, rtol=0)
+
+
+def pin_library_softmax(fwd):
+    """N_q rows against scipy's softmax-weighted average and logsumexp."""
+    q, k, v = _rand((3, 6, 8), 4), _rand((3, 9, 8), 5), _rand((3, 9, 5), 6)
+    scale = 1 / math.sqrt(8)
+    o, lse = fwd(q, k, v, scale)
+    s = scale * np.einsum("bid,bjd->bij", q, k)
+    w = special.softmax(s, axis=-1)
+    return (np.allclose(o, np.einsum("bij,bjd->bid", w, v), atol=1e-13, rtol=0)
+            and np.allclose(lse, special.logsumexp(s, axis=-1), atol=1e-13, rtol=0))
+
+
+def pin_shift_invariance(fwd):
+    """Adding u to every key row leaves O unchanged and moves LSE_i by scale*q_i.u."""
+    q, k, v = _rand((2, 4, 6), 7), _rand((2, 7, 6), 8), _rand((2, 7, 6), 9)
+    u = _rand((6,), 10)
+    scale = 0.3
+    o0, l0 = fwd(q, k, v, scale)
+    o1, l1 = fwd(q, k + u, v, scale)
+    return np.allclose(o0, o1, atol=1e-12, rtol=0) and np.allclose(l1 - l0, scale * (q @ u), atol=1e-12, rtol=0)
+
+
+def pin_identical_keys(fwd):
+    """Identical K rows: O = mean(V), LSE_i = ln N_k + scale*q_i.k."""
+    q, v = _rand((2, 4, 6), 11), _rand((2, 9, 6), 12)
+    krow = _rand((2, 1, 6), 13)
+    k = np.repeat(krow, 9, axis=1)
+    scale = 0.4
+    o, lse = fwd(q, k, v, scale)
+    want_l = math.log(9) + scale * np.einsum("bid,bd->bi", q, krow[:, 0])
+    return (np.allclose(o, v.mean(axis=1, keepdims=True), atol=1e-13, rtol=0)
+            and np.allclose(lse, want_l, atol=1e-13, rtol=0))
+
+
+FORWARD_PINS = [pin_brute, pin_golden_one, pin_golden_const, pin_library_softmax,
+                pin_shift_invariance, pin_identical_keys]
+
+
+@pytest.mark.parametrize("pin", FORWARD_PINS, ids=lambda f: f.__name__)
+def test_forward_pins(pin):
+    assert pin(A.forward)
+
+
+def test_forward_invariants_random():
+    q, k, v = _rand((2, 33, 16), 20), _rand((2, 47, 16), 21), _rand((2, 47, 16), 22)
+    scale = 0.25
+    o, lse = A.forward(q, k, v, scale)
+    s = A.scores(q, k, scale)
+    # LSE_i lies in [max_j s_ij, max_j s_ij + ln N_k]
+    mx = s.max(-1)
+    assert np.all(lse >= mx - 1e-12) and np.all(lse <= mx + math.log(47) + 1e-12)
+    # rows of P sum to one and P is non-negative
+    p = A.probabilities(q, k, scale)
+    assert np.allclose(p.sum(-1), 1.0, atol=1e-14) and np.all(p >= 0)
+    # constant V gives that constant
+    oc, _ = A.forward(q, k, np.full_like(v, -1.75), scale)
+    assert np.allclose(oc, -1.75, atol=1e-14)
+    # permuting keys and values together changes nothing
+    perm = np.random.default_rng(3).permutation(47)
+    op, lp = A.forward(q, k[:, perm], v[:, perm], scale)
+    assert np.allclose(op, o, atol=1e-13) and np.allclose(lp, lse, atol=1e-13)
+    # a single key passes V through with LSE equal to the score
+    o1, l1 = A.forward(q, k[:, :1], v[:, :1], scale)
+    assert np.allclose(o1, np.broadcast_to(v[:, :1], o1.shape), atol=1e-15)
+    assert np.allclose(l1, s[:, :, 0], atol=1e-14)
+
+
+def test_forward_page_fixtures_brute():
+    """The trig / linear fixtures of the vyre-libs unit tests, oracle vs brute force."""
+    n, d = 8, 16
+    i = np.arange(n * d, dtype=np.float64)
+    q = (np.sin(i * 0.13) - 0.5).reshape(1, n, d)
+    k = (np.cos(i * 0.07) + 0.25).reshape(1, n, d)
+    v = (np.sin(i * 0.19) * 2.0).reshape(1, n, d)
+    o, lse = A.forward(q, k, v, 1 / math.sqrt(d))
+    ob, lb = brute_forward(q, k, v, 1 / math.sqrt(d))
+    assert np.allclose(o, ob, atol=1e-12) and np.allclose(lse, lb, atol=1e-12)
+    for n, d, a, b, c in [(4, 8, (0.1, 0.0), (0.05, 0.2), (0.3, -0.1)), (5, 8, (0.11, 0.0), (0.06, 0.15), (0.25, -0.05))]:
+        i = np.arange(n * d, dtype=np.float64)
+        q = (i * a[0] + a[1]).reshape(1, n, d)
+        k = (i * b[0] + b[1]).reshape(1, n, d)
+        v = (i * c[0] + c[1]).reshape(1, n, d)
+        o, lse = A.forward(q, k, v, 1 / math.sqrt(d))
+        ob, lb = brute_forward(q, k, v, 1 / math.sqrt(d))
+        assert np.allclose(o, ob, rtol=1e-12, atol=1e-12) and np.allclose(lse, lb, rtol=1e-13)
+
+
+def test_forward_rows_matches_full():
+    q, k, v = _rand((3, 20, 8), 30), _rand((3, 25, 8), 31), _rand((3, 25, 8), 32)
+    o, lse = A.forward(q, k, v, 0.35)
+    rows = [0, 7, 19]
+    orow, lrow = A.forward_rows(q, k, v, 0.35, 2, rows)
+    assert np.allclose(orow, o[2, rows], atol=1e-14) and np.allclose(lrow, lse[2, rows], atol=1e-14)
+
+
+def test_forward_rejects_empty():
+    with pytest.raises(ValueError):
+        A.forward(np.zeros((1, 0, 4)), np.zeros((1, 3, 4)), np.zeros((1, 3, 4)), 1.0)
+
+
+# --------------------------------------------------------------------------- backward pins
+
+def _loss(q, k, v, d_o, scale):
+    o, _ = A.forward(q, k, v, scale)
+    return float(np.sum(o * d_o))
+
+
+def pin_finite_differences(bwd):
+    q, k, v, d_o = _rand((1, 3, 4), 40), _rand((1, 5, 4), 41), _rand((1, 5, 4), 42), _rand((1, 3, 4), 43)
+    scale = 0.5
+    dq, dk, dv = bwd(q, k, v, d_o, scale)
+    h = 1e-6
+    ok = True
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            fp = _loss(q, k, v, d_o, scale)
+            x[idx] = old - h
+            fm = _loss(q, k, v, d_o, scale)
+            x[idx] = old
+            num[idx] = (fp - fm) / (2 * h)
+        ok &= bool(np.allclose(g, num, rtol=1e-6, atol=1e-8))
+    return ok
+
+
+def pin_gradient_closed_forms(bwd):
+    q, k, v, d_o = _rand((2, 6, 5), 50), _rand((2, 8, 5), 51), _rand((2, 8, 5), 52), _rand((2, 6, 5), 53)
+    dq, dk, dv = bwd(q, k, v, d_o, 0.45)
+    ok = np.allclose(dk.sum(axis=1), 0.0, atol=1e-12)          # sum_j dS_ij = 0 for every i
+    ok &= np.allclose(dv.sum(axis=1), d_o.sum(axis=1), atol=1e-12)  # rows of P sum to one
+    # a single key: O = v_0 does not depend on q or k
+    dq1, dk1, dv1 = bwd(q, k[:, :1], v[:, :1], d_o, 0.45)
+    ok &= np.allclose(dq1, 0, atol=1e-14) and np.allclose(dk1, 0, atol=1e-14)
+    ok &= np.allclose(dv1[:, 0], d_o.sum(axis=1), atol=1e-13)
+    return bool(ok)
+
+
+BACKWARD_PINS = [pin_finite_differences, pin_gradient_closed_forms]
+
+
+@pytest.mark.parametrize("pin", BACKWARD_PINS, ids=lambda f: f.__name__)
+def test_backward_pins(pin):
+    assert pin(A.backward)
+
+
+def test_backward_slice_pinned():
+    """The chunked per-head backward passes the same pins and matches row chunking of any size."""
+    def sliced(q, k, v, d_o, scale):
+        outs = [A.backward_slice(q, k, v, d_o, scale, b, row_chunk=2) for b in range(q.shape[0])]
+        return tuple(np.stack([o[i] for o in outs]) for i in range(3))
+    assert pin_finite_differences(sliced)
+    assert pin_gradient_closed_forms(sliced)
+
+
+def test_preprocess_loop():
+    o, d_o = _rand((2, 3, 5), 60), _rand((2, 3, 5), 61)
+    want = np.array([[math.fsum(o[b, i, t] * d_o[b, i, t] for t in range(5)) for i in range(3)] for b in range(2)])
+    assert np.allclose(A.bwd_preprocess(o, d_o), want, atol=1e-15)
+
+
+# --------------------------------------------------------------------------- planted mistakes
+
+def _mut_no_scale(q, k, v, scale):
+    return A.forward(q, k, v, 1.0)
+
+
+def _mut_lse_without_max(q, k, v, scale):
+    o, lse = A.forward(q, k, v, scale)
+    return o, lse - A.scores(q, k, scale).max(-1)
+
+
+def _mut_transposed_value(q, k, v, scale):
+    o, lse = A.forward(q, k, v, scale)
+    return o[..., ::-1], lse
+
+
+def _mut_log2(q, k, v, scale):
+    o, lse = A.forward(q, k, v, scale)
+    return o, lse / math.log(2)
+
+
+def _mut_k_dim_swap(q, k, v, scale):
+    return A.forward(q, k[..., ::-1], v, scale)
+
+
+@pytest.mark.parametrize("mutant", [_mut_no_scale, _mut_lse_without_max, _mut_transposed_value, _mut_log2, _mut_k_dim_swap],
+                         ids=lambda f: f.__name__)
+def test_forward_mutants_fail_a_pin(mutant):
+    assert not all(pin(mutant) for pin in FORWARD_PINS)
+
+
+def _bmut_sign(q, k, v, d_o, scale):
+    dq, dk, dv = A.backward(q, k, v, d_o, scale)
+    return dq, -dk, dv
+
+
+def _bmut_no_d(q, k, v, d_o, scale):
+    o, lse = A.forward(q, k, v, scale)
+    p = np.exp(A.scores(q, k, scale) - lse[..., None])
+    ds = p * (d_o @ np.swapaxes(v, -1, -2))
+    return scale * ds @ k, scale * np.swapaxes(ds, -1, -2) @ q, np.swapaxes(p, -1, -2) @ d_o
+
+
+def _bmut_missing_scale(q, k, v, d_o, scale):
+    dq, dk, dv = A.backward(q, k, v, d_o, scale)
+    return dq / scale, dk, dv
+
+
+def _bmut_dv_untransposed(q, k, v, d_o, scale):
+    dq, dk, dv = A.backward(q, k, v, d_o, scale)
+    o, lse = A.forward(q, k, v, scale)
+    return dq, dk, dv[:, ::-1]
+
+
+@pytest.mark.parametrize("mutant", [_bmut_sign, _bmut_no_d, _bmut_missing_scale, _bmut_dv_untransposed],
+                         ids=lambda f: f.__name__)
+def test_backward_mutants_fail_a_pin(mutant):
+    assert not all(pin(mutant) for pin in BACKWARD_PINS)
+
+
+# --------------------------------------------------------------------------- PSA pins
+
+def _brute_pack(qkv, nh):
+    b_, qkv_h, hh, ww = qkv.shape
+    kd = qkv_h // (4 * nh)
+    out = np.zeros((4, b_ * nh, hh * ww, kd), dtype=qkv.dtype)
+    for s in range(4):
+        for bh in range(b_ * nh):
+            for n in range(hh * ww):
+                for dd in range(kd):
+                    b, h = divmod(bh, nh)
+                    out[s, bh, n, dd] = qkv[b, h * 4 * kd + s * kd + dd, n // ww, n % ww]
+    return out
+
+
+def _brute_merge(lo, hi, b_, nh, hh, ww):
+    kd = lo.shape[2]
+    out = np.zeros((b_, nh * 2 * kd, hh, ww), dtype=lo.dtype)
+    for bh in range(b_ * nh):
+        for n in range(hh * ww):
+            for dd in range(kd):
+                b, h = divmod(bh, nh)
+                out[b, h * 2 * kd + dd, n // ww, n % ww] = lo[bh, n, dd]
+                out[b, h * 2 * kd + kd + dd, n // ww, n % ww] = hi[bh, n, dd]
+    return out
+
+
+@pytest.mark.parametrize("b_,nh,kd,hh,ww", [(2, 2, 4, 3, 5), (1, 3, 2, 1, 1), (3, 1, 8, 2, 7)])
+def test_psa_pack_merge_brute(b_, nh, kd, hh, ww):
+    qkv = synth.counter_u16("pin_qkv", (b_, nh * 4 * kd, hh, ww))
+    packed = P.pack_qkv(qkv, nh)
+    assert packed.dtype == np.uint16 and np.array_equal(packed, _brute_pack(qkv, nh))
+    lo = synth.counter_u16("pin_lo", (b_ * nh, hh * ww, kd))
+    hi = synth.counter_u16("pin_hi", (b_ * nh, hh * ww, kd))
+    merged = P.merge_attn_nchw(lo, hi, b_, nh, hh, ww)
+    assert np.array_equal(merged, _brute_merge(lo, hi, b_, nh, hh, ww))
+    # round trip: merging the V_lo / V_hi sections of a pack gives the V channels of QKV
+    rt = P.merge_attn_nchw(packed[2], packed[3], b_, nh, hh, ww)
+    assert np.array_equal(rt, P.extract_v_nchw(qkv, nh))
+    ev = np.zeros_like(rt)
+    for b in range(b_):
+        for h in range(nh):
+            for dd in range(kd):
+                ev[b, h * 2 * kd + dd] = qkv[b, h * 4 * kd + 2 * kd + dd]
+                ev[b, h * 2 * kd + kd + dd] = qkv[b, h * 4 * kd + 3 * kd + dd]
+    assert np.array_equal(rt, ev)
+
+
+def test_psa_adjoints():
+    """<pack(x), y> = <x, pack^T(y)> and the same for merge (dot-product test)."""
+    b_, nh, kd, hh, ww = 2, 3, 4, 3, 2
+    x = _rand((b_, nh * 4 * kd, hh, ww), 70)
+    y = _rand((4, b_ * nh, hh * ww, kd), 71)
+    assert np.isclose(np.sum(P.pack_qkv(x, nh) * y), np.sum(x * P.pack_qkv_backward(y, b_, nh, hh, ww)), rtol=1e-12)
+    lo, hi = _rand((b_ * nh, hh * ww, kd), 72), _rand((b_ * nh, hh * ww, kd), 73)
+    g = _rand((b_, nh * 2 * kd, hh, ww), 74)
+    dlo, dhi = P.merge_attn_backward(g, nh)
+    assert np.isclose(np.sum(P.merge_attn_nchw(lo, hi, b_, nh, hh, ww) * g), np.sum(lo * dlo) + np.sum(hi * dhi), rtol=1e-12)
+
+
+def test_psa_rejects_bad_channels():
+    with pytest.raises(ValueError):
+        P.pack_qkv(np.zeros((1, 10, 2, 2), np.uint16), 1)
+
+
+# --------------------------------------------------------------------------- the generator itself
+
+def test_synth_is_deterministic_and_normal():
+    a = synth.normal(7, "x", 200001)
+    b = synth.normal(7, "x", 200001)
+    assert np.array_equal(a, b)
+    assert abs(a.mean()) < 0.01 and abs(a.std() - 1) < 0.01
+    # counter based: a prefix is the prefix of a longer draw
+    assert np.array_equal(synth.normal(7, "x", 1001), a[:1001])
+    assert not np.array_equal(synth.normal(7, "y", 1000), a[:1000])
+
+
+def test_bf16_rounding():
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 3.0e38], dtype=np.float32)
+    bits = synth.f32_to_bf16_bits(x)
+    back = synth.bf16_bits_to_f64(bits)
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: even mantissa wins (1.0); 1 + 3*2^-8 rounds up
+    assert back[0] == 1.0 and back[1] == 1.0 and back[2] == 1.0 + 2 ** -6 and back[3] == -2.5
+    assert np.all(np.abs(back[:4] - x[:4]) <= np.abs(x[:4]) * 2 ** -8)
