@@ -1,0 +1,205 @@
+// api.cu - the C ABI declared in include/fa2.h: argument validation, dispatch
+// to the kernel translation units, tensor-map encoding and the watchdog word.
+#include <math.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "fa2.h"
+#include "internal.h"
+
+namespace fa2 {
+
+// Watchdog word: kernels OR kStatusTimeout into it when a bounded wait gives up.
+__device__ unsigned int g_watchdog_word;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    });
+    return g_encode;
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSlots = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+std::atomic<uint64_t> g_smem_done[kMaxSlots];
+
+bool status_word(unsigned int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_watchdog_word) != cudaSuccess) return false;
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_dtype(fa2_dtype d) { return d == FA2_DTYPE_F32 || d == FA2_DTYPE_F16 || d == FA2_DTYPE_BF16; }
+
+bool supported_head_dim(int32_t d) { return d == 32 || d == 64 || d == 128; }
+
+constexpr int64_t kMaxGridY = 65535;
+constexpr int64_t kMaxSeq = (int64_t)1 << 30;
+
+// Shared size checks of the attention calls.
+fa2_status check_attention_sizes(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype, float scale) {
+    if (bh <= 0 || n_q <= 0 || n_k <= 0 || head_dim <= 0) return FA2_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return FA2_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return FA2_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return FA2_ERR_UNSUPPORTED;
+    if (bh > kMaxGridY || n_q > kMaxSeq || n_k > kMaxSeq) return FA2_ERR_UNSUPPORTED;
+    return FA2_OK;
+}
+
+}  // namespace
+
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {d0 * (uint64_t)elem_bytes, d0 * d1 * (uint64_t)elem_bytes};
+    const cuuint32_t box[3] = {box0, box1, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (slot < 0 || slot >= kMaxSlots || dev >= 64) return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const uint64_t bit = 1ull << dev;
+    if (g_smem_done[slot].load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_smem_done[slot].fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+}  // namespace fa2
+
+using namespace fa2;
+
+extern "C" {
+
+fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, float* lse, int64_t bh, int64_t n_q,
+                       int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
+    if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
+    fa2_status st = check_attention_sizes(bh, n_q, n_k, head_dim, dtype, softmax_scale);
+    if (st != FA2_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA2_ERR_MISALIGNED;
+    FwdParams p{q, k, v, o, lse, bh, n_q, n_k, head_dim, (int)dtype, softmax_scale, nullptr};
+    if (!status_word(&p.status)) return FA2_ERR_CUDA;
+    const cudaError_t e = dtype == FA2_DTYPE_F32 ? launch_fwd_f32(p, static_cast<cudaStream_t>(stream))
+                                                 : launch_fwd_tc(p, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype) {
+    if (check_attention_sizes(bh, n_q, n_k, head_dim, dtype, 1.0f) != FA2_OK) return 0;
+    const int64_t n_q_pad = (n_q + 127) / 128 * 128;
+    return 2 * (size_t)(bh * n_q_pad) * sizeof(float);
+}
+
+fa2_status fa2_backward(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                        void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int64_t bh, int64_t n_q,
+                        int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
+    if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
+    fa2_status st = check_attention_sizes(bh, n_q, n_k, head_dim, dtype, softmax_scale);
+    if (st != FA2_OK) return st;
+    if (dtype == FA2_DTYPE_F32) return FA2_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) || !aligned16(lse) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return FA2_ERR_MISALIGNED;
+    const size_t need = fa2_backward_workspace_size(bh, n_q, n_k, head_dim, dtype);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA2_ERR_WORKSPACE;
+    BwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.d_o = d_o; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.n_q_pad = (n_q + 127) / 128 * 128;
+    p.delta = static_cast<float*>(workspace);
+    p.lse2 = p.delta + bh * p.n_q_pad;
+    p.bh = bh; p.n_q = n_q; p.n_k = n_k; p.d = head_dim; p.dtype = (int)dtype; p.scale = softmax_scale;
+    if (!status_word(&p.status)) return FA2_ERR_CUDA;
+    return launch_bwd_tc(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+static fa2_status psa_common(int32_t H, int32_t W, int32_t B, int32_t num_heads, fa2_dtype dtype, int* elem_bytes) {
+    if (H <= 0 || W <= 0 || B <= 0 || num_heads <= 0) return FA2_ERR_INVALID_ARG;
+    if (!valid_dtype(dtype)) return FA2_ERR_INVALID_ARG;
+    *elem_bytes = dtype == FA2_DTYPE_F32 ? 4 : 2;
+    if ((int64_t)H * W > kMaxSeq) return FA2_ERR_UNSUPPORTED;
+    return FA2_OK;
+}
+
+fa2_status psa_pack_qkv(const void* qkv, void* packed, int32_t qkv_h, int32_t H, int32_t W, int32_t B, int32_t num_heads,
+                        fa2_dtype dtype, void* stream) {
+    if (!qkv || !packed) return FA2_ERR_INVALID_ARG;
+    int eb = 0;
+    fa2_status st = psa_common(H, W, B, num_heads, dtype, &eb);
+    if (st != FA2_OK) return st;
+    if (qkv_h <= 0 || qkv_h % (4 * num_heads) != 0) return FA2_ERR_INVALID_ARG;
+    if (!aligned16(qkv) || !aligned16(packed)) return FA2_ERR_MISALIGNED;
+    if (4LL * B * num_heads > kMaxGridY) return FA2_ERR_UNSUPPORTED;
+    PsaParams p{qkv, nullptr, packed, 0, eb, B, num_heads, qkv_h / (4 * num_heads), (int64_t)H * W, qkv_h, 0};
+    return launch_psa(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+fa2_status psa_merge_attn_nchw(const void* lo, const void* hi, void* out, int32_t c, int32_t H, int32_t W, int32_t B,
+                               int32_t num_heads, fa2_dtype dtype, void* stream) {
+    if (!lo || !hi || !out) return FA2_ERR_INVALID_ARG;
+    int eb = 0;
+    fa2_status st = psa_common(H, W, B, num_heads, dtype, &eb);
+    if (st != FA2_OK) return st;
+    if (c <= 0 || c % (2 * num_heads) != 0) return FA2_ERR_INVALID_ARG;
+    if (!aligned16(lo) || !aligned16(hi) || !aligned16(out)) return FA2_ERR_MISALIGNED;
+    if (2LL * B * num_heads > kMaxGridY) return FA2_ERR_UNSUPPORTED;
+    PsaParams p{lo, hi, out, 1, eb, B, num_heads, c / (2 * num_heads), (int64_t)H * W, 0, c};
+    return launch_psa(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+fa2_status fa2_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA2_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_watchdog_word, sizeof(word)) != cudaSuccess) return FA2_ERR_CUDA;
+    if (word == 0) return FA2_OK;
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_watchdog_word, &zero, sizeof(zero)) != cudaSuccess) return FA2_ERR_CUDA;
+    return FA2_ERR_DEVICE_TIMEOUT;
+}
+
+const char* fa2_status_string(fa2_status s) {
+    switch (s) {
+        case FA2_OK: return "ok";
+        case FA2_ERR_INVALID_ARG: return "invalid argument (null pointer, size <= 0, inconsistent shape or bad scale)";
+        case FA2_ERR_UNSUPPORTED: return "unsupported (head_dim not in {32, 64, 128}, dtype, or a size beyond the kernels' limits)";
+        case FA2_ERR_MISALIGNED: return "a tensor base pointer is not 16-byte aligned";
+        case FA2_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+        case FA2_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (watchdog)";
+        case FA2_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than fa2_backward_workspace_size";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,505 @@
+// fa2_bwd_tc.cu - attention backward on the sm_103a tensor cores.
+//
+// What it computes: "vision-rs 0.1.1 flash_attn2.rs", kernels
+// flash_attention2_backward_dq and flash_attention2_backward_dkv:
+//   D_i = sum_d O_id dO_id,  P_ij = exp(s_ij - LSE_i),  dV_j = sum_i P_ij dO_i,
+//   dS_ij = P_ij (dO_i . v_j - D_i),  dQ_i = scale sum_j dS_ij k_j,
+//   dK_j = scale sum_i dS_ij q_i.
+// Structure as on that page - a pass over key rows for dK/dV and a pass over
+// query rows for dQ - at tile granularity, in three launches:
+//   1. preprocess: D (float32) and LSE * log2(e), padded per head to a multiple
+//      of 128 rows (+inf / 0 in the padding, which makes those rows' P zero);
+//   2. dK/dV: one CTA per 128-key tile (keys = TMEM lanes), looping over
+//      128-query tiles:  S^T = K Q^T, dP^T = V dO^T, P^T and dS^T elementwise,
+//      dV += P^T dO, dK += dS^T Q;
+//   3. dQ: one CTA per 128-query tile, looping over 128-key tiles:
+//      S = Q K^T, dP = dO V^T, dS elementwise, dQ += dS K.
+// The 16-bit P^T / dS^T / dS are written back into tensor memory over the
+// score columns they came from and consumed from there by the next MMA.
+// Warp roles (192 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue,
+// warps 2-5 elementwise (one thread per TMEM lane).
+#include "common.cuh"
+#include "internal.h"
+
+namespace fa2 {
+namespace {
+
+constexpr int BT = 128;         // rows of every tile (keys or queries)
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------------------------ preprocess
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(256)
+    bwd_preprocess_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o, const float* __restrict__ lse,
+                          float* __restrict__ delta, float* __restrict__ lse2, int n_q, int n_q_pad) {
+    constexpr int TPR = D / 8;             // threads per row, 8 elements (16 bytes) each
+    constexpr int RPC = 256 / TPR;         // rows per CTA
+    const int bh = blockIdx.y;
+    const int r = blockIdx.x * RPC + threadIdx.x / TPR;
+    const int part = threadIdx.x % TPR;
+    float acc = 0.f;
+    if (r < n_q) {
+        const size_t off = ((size_t)bh * n_q + r) * D + part * 8;
+        const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(d_o + off);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 fa, fb;
+            if constexpr (kBf16) {
+                fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[i]));
+                fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[i]));
+            } else {
+                fa = __half22float2(*reinterpret_cast<const __half2*>(&aw[i]));
+                fb = __half22float2(*reinterpret_cast<const __half2*>(&bw[i]));
+            }
+            acc = fmaf(fa.x, fb.x, acc);
+            acc = fmaf(fa.y, fb.y, acc);
+        }
+    }
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
+    if (part == 0 && r < n_q_pad) {
+        const size_t w = (size_t)bh * n_q_pad + r;
+        delta[w] = r < n_q ? acc : 0.f;
+        lse2[w] = r < n_q ? lse[(size_t)bh * n_q + r] * kLog2e : INFINITY;
+    }
+}
+
+// ------------------------------------------------------------------------------ shared pieces
+
+template <int D>
+struct BwdCfg : Tile16<D> {
+    static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
+    static constexpr int kTile = BT * D * 2;
+    // dK/dV kernel: K, V resident; per stage Q_i, dO_i, lse2_i, delta_i
+    static constexpr int kStageDkv = 2 * kTile + 2 * BT * 4;
+    static constexpr int kDkvStages = kStages;
+    static constexpr int kDkvBar = 2 * kTile + kDkvStages * kStageDkv;
+    // dQ kernel: Q, dO resident; per stage K_j, V_j
+    static constexpr int kStageDq = 2 * kTile;
+    static constexpr int kDqBar = 2 * kTile + kStages * kStageDq;
+    static constexpr int kNumBars = 3 + 2 * kStages + 2;
+    static constexpr int kSmemDkv = kDkvBar + kNumBars * 8 + 16 + 1024;
+    static constexpr int kSmemDq = kDqBar + kNumBars * 8 + 16 + 1024;
+    static_assert(kSmemDkv <= 227 * 1024 && kSmemDq <= 227 * 1024, "shared memory budget");
+    static_assert(kStageDkv % 1024 == 0, "stage alignment");
+};
+
+// Barrier block layout shared by both kernels:
+//   0 resident tiles full, 1..S stage full, S+1..2S stage empty, 2S+1 scores done,
+//   2S+2 elementwise done, 2S+3 all MMAs done
+struct Bars {
+    uint32_t base;
+    int S;
+    __device__ uint32_t resident() const { return base; }
+    __device__ uint32_t full(int s) const { return base + 8u * (1 + s); }
+    __device__ uint32_t empty(int s) const { return base + 8u * (1 + S + s); }
+    __device__ uint32_t scores() const { return base + 8u * (1 + 2 * S); }
+    __device__ uint32_t elem() const { return base + 8u * (2 + 2 * S); }
+    __device__ uint32_t done() const { return base + 8u * (3 + 2 * S); }
+};
+
+__device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_flag) {
+    *abort_flag = 0;
+    mbar_init(b.resident(), 1);
+    for (int s = 0; s < b.S; ++s) {
+        mbar_init(b.full(s), 1);
+        mbar_init(b.empty(s), 1);
+    }
+    mbar_init(b.scores(), 1);
+    mbar_init(b.elem(), BT);
+    mbar_init(b.done(), 1);
+    fence_barrier_init();
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void store_row_chunk(void* base, size_t row, int D, int c, const uint32_t (&r)[32], float mul,
+                                                bool valid) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack2<kBf16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    if (valid) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + row * D + 32 * c);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+}
+
+// ------------------------------------------------------------------------------ dK / dV
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dk,
+                    void* __restrict__ dv, int n_q, int n_k, int n_q_pad, float scale, float scale_log2,
+                    unsigned int* status) {
+    using C = BwdCfg<D>;
+    constexpr int S = C::kDkvStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_addr);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y;
+    const int k0 = blockIdx.x * BT;
+    const int n_qt = (n_q + BT - 1) / BT;
+
+    const Bars bars{base + C::kDkvBar, S};
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kDkvBar + C::kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kDkvBar + C::kNumBars * 8 + 4);
+    const Watchdog wd{abort_flag, status};
+    const uint32_t k_smem = base, v_smem = base + C::kTile;
+    auto stage_q = [&](int s) { return base + 2 * C::kTile + s * C::kStageDkv; };
+    auto stage_do = [&](int s) { return stage_q(s) + C::kTile; };
+    auto stage_l2 = [&](int s) { return stage_q(s) + 2 * C::kTile; };
+    auto stage_dl = [&](int s) { return stage_q(s) + 2 * C::kTile + BT * 4; };
+
+    if (threadIdx.x == 0) init_bars(bars, abort_flag);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(bars.resident(), 2 * C::kTile);
+            for (int a = 0; a < C::kAtoms; ++a) {
+                tma_load_3d(k_smem + a * BT * C::kAtomRowBytes, &tm_k, bars.resident(), a * C::kAtomCols, k0, bh);
+                tma_load_3d(v_smem + a * BT * C::kAtomRowBytes, &tm_v, bars.resident(), a * C::kAtomCols, k0, bh);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < n_qt; ++i) {
+                const int s = i % S;
+                if (i >= S && !(ok = mbar_wait(bars.empty(s), ((i / S) & 1) ^ 1, wd))) break;
+                mbar_arrive_expect_tx(bars.full(s), 2 * C::kTile + 2 * BT * 4);
+                for (int a = 0; a < C::kAtoms; ++a) {
+                    tma_load_3d(stage_q(s) + a * BT * C::kAtomRowBytes, &tm_q, bars.full(s), a * C::kAtomCols, i * BT, bh);
+                    tma_load_3d(stage_do(s) + a * BT * C::kAtomRowBytes, &tm_do, bars.full(s), a * C::kAtomCols, i * BT, bh);
+                }
+                const size_t w = (size_t)bh * n_q_pad + (size_t)i * BT;
+                bulk_load(stage_l2(s), lse2 + w, BT * 4, bars.full(s));
+                bulk_load(stage_dl(s), delta + w, BT * 4, bars.full(s));
+                issued = i + 1;
+            }
+            if (!ok) {
+                drain_wait(bars.resident(), 0);
+                for (int i = (issued > S ? issued - S : 0); i < issued; ++i) drain_wait(bars.full(i % S), (i / S) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
+            const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
+            bool ok = mbar_wait(bars.resident(), 0, wd);
+            for (int i = 0; ok && i < n_qt; ++i) {
+                const int s = i % S;
+                if (!(ok = mbar_wait(bars.full(s), (i / S) & 1, wd))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem, C::kmajor(k_smem, kk, BT), C::kmajor(stage_q(s), kk, BT), idesc_s, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128u, C::kmajor(v_smem, kk, BT), C::kmajor(stage_do(s), kk, BT), idesc_s, kk > 0);
+                mma_commit(bars.scores());
+                if (!(ok = mbar_wait(bars.elem(), i & 1, wd))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)
+                    mma_ts(tmem + 256u, tmem + (uint32_t)(kk * 8), C::mnmajor(stage_do(s), kk, BT), idesc_g, (i > 0 || kk > 0));
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)
+                    mma_ts(tmem + 256u + D, tmem + 128u + (uint32_t)(kk * 8), C::mnmajor(stage_q(s), kk, BT), idesc_g,
+                           (i > 0 || kk > 0));
+                mma_commit(bars.empty(s));
+            }
+            mma_commit(bars.done());
+            drain_wait(bars.done(), 0);
+        }
+    } else {
+        const int quarter = warp & 3;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
+        bool ok = true;
+        for (int i = 0; i < n_qt; ++i) {
+            const int s = i % S;
+            if (!(ok = warp_wait(bars.scores(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) break;
+            tc_fence_after();
+            const float* l2 = reinterpret_cast<const float*>(smem + (stage_l2(s) - base));
+            const float* dl = reinterpret_cast<const float*>(smem + (stage_dl(s) - base));
+#pragma unroll
+            for (int c = 0; c < BT / 32; ++c) {
+                uint32_t rs[32], rp[32];
+                tmem_ld32(t_s + 32u * c, rs);
+                tmem_ld32(t_dp + 32u * c, rp);
+                tmem_ld_wait();
+                reg_fence(rs);
+                reg_fence(rp);
+                uint32_t pk_p[16], pk_ds[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int col = 32 * c + 2 * x;
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(rs[2 * x]), scale_log2, -l2[col]));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(rs[2 * x + 1]), scale_log2, -l2[col + 1]));
+                    const float d0 = p0 * (__uint_as_float(rp[2 * x]) - dl[col]);
+                    const float d1 = p1 * (__uint_as_float(rp[2 * x + 1]) - dl[col + 1]);
+                    pk_p[x] = pack2<kBf16>(p0, p1);
+                    pk_ds[x] = pack2<kBf16>(d0, d1);
+                }
+                tmem_st16(t_s + 16u * c, pk_p);
+                tmem_st16(t_dp + 16u * c, pk_ds);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bars.elem());
+        }
+        if (ok) ok = warp_wait(bars.done(), 0, wd);
+        if (ok) {
+            tc_fence_after();
+            const int key = k0 + quarter * 32 + lane;
+            const size_t row = (size_t)bh * n_k + key;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + 256u + 32u * c, r);
+                tmem_ld_wait();
+                reg_fence(r);
+                store_row_chunk<kBf16>(dv, row, D, c, r, 1.f, key < n_k);
+            }
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + 256u + D + 32u * c, r);
+                tmem_ld_wait();
+                reg_fence(r);
+                store_row_chunk<kBf16>(dk, row, D, c, r, scale, key < n_k);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------------ dQ
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dq, int n_q,
+                  int n_k, int n_q_pad, float scale, float scale_log2, unsigned int* status) {
+    using C = BwdCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_addr);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y;
+    const int q0 = blockIdx.x * BT;
+    const int n_kt = (n_k + BT - 1) / BT;
+
+    const Bars bars{base + C::kDqBar, S};
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kDqBar + C::kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kDqBar + C::kNumBars * 8 + 4);
+    const Watchdog wd{abort_flag, status};
+    const uint32_t q_smem = base, do_smem = base + C::kTile;
+    auto stage_k = [&](int s) { return base + 2 * C::kTile + s * C::kStageDq; };
+    auto stage_v = [&](int s) { return stage_k(s) + C::kTile; };
+
+    if (threadIdx.x == 0) init_bars(bars, abort_flag);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(bars.resident(), 2 * C::kTile);
+            for (int a = 0; a < C::kAtoms; ++a) {
+                tma_load_3d(q_smem + a * BT * C::kAtomRowBytes, &tm_q, bars.resident(), a * C::kAtomCols, q0, bh);
+                tma_load_3d(do_smem + a * BT * C::kAtomRowBytes, &tm_do, bars.resident(), a * C::kAtomCols, q0, bh);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < n_kt; ++j) {
+                const int s = j % S;
+                if (j >= S && !(ok = mbar_wait(bars.empty(s), ((j / S) & 1) ^ 1, wd))) break;
+                mbar_arrive_expect_tx(bars.full(s), 2 * C::kTile);
+                for (int a = 0; a < C::kAtoms; ++a) {
+                    tma_load_3d(stage_k(s) + a * BT * C::kAtomRowBytes, &tm_k, bars.full(s), a * C::kAtomCols, j * BT, bh);
+                    tma_load_3d(stage_v(s) + a * BT * C::kAtomRowBytes, &tm_v, bars.full(s), a * C::kAtomCols, j * BT, bh);
+                }
+                issued = j + 1;
+            }
+            if (!ok) {
+                drain_wait(bars.resident(), 0);
+                for (int j = (issued > S ? issued - S : 0); j < issued; ++j) drain_wait(bars.full(j % S), (j / S) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
+            const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
+            bool ok = mbar_wait(bars.resident(), 0, wd);
+            for (int j = 0; ok && j < n_kt; ++j) {
+                const int s = j % S;
+                if (!(ok = mbar_wait(bars.full(s), (j / S) & 1, wd))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem, C::kmajor(q_smem, kk, BT), C::kmajor(stage_k(s), kk, BT), idesc_s, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128u, C::kmajor(do_smem, kk, BT), C::kmajor(stage_v(s), kk, BT), idesc_s, kk > 0);
+                mma_commit(bars.scores());
+                if (!(ok = mbar_wait(bars.elem(), j & 1, wd))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)
+                    mma_ts(tmem + 256u, tmem + 128u + (uint32_t)(kk * 8), C::mnmajor(stage_k(s), kk, BT), idesc_g,
+                           (j > 0 || kk > 0));
+                mma_commit(bars.empty(s));
+            }
+            mma_commit(bars.done());
+            drain_wait(bars.done(), 0);
+        }
+    } else {
+        const int quarter = warp & 3;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
+        const int row = q0 + quarter * 32 + lane;
+        const size_t w = (size_t)bh * n_q_pad + row;  // row < n_q_pad always
+        const float my_l2 = lse2[w];
+        const float my_d = delta[w];
+        bool ok = true;
+        for (int j = 0; j < n_kt; ++j) {
+            if (!(ok = warp_wait(bars.scores(), j & 1, wd))) break;
+            tc_fence_after();
+            const int valid = n_k - j * BT;
+#pragma unroll
+            for (int c = 0; c < BT / 32; ++c) {
+                uint32_t rs[32], rp[32];
+                tmem_ld32(t_s + 32u * c, rs);
+                tmem_ld32(t_dp + 32u * c, rp);
+                tmem_ld_wait();
+                reg_fence(rs);
+                reg_fence(rp);
+                uint32_t pk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int col = 32 * c + 2 * x;
+                    const float p0 = ex2_approx(fmaf(__uint_as_float(rs[2 * x]), scale_log2, -my_l2));
+                    const float p1 = ex2_approx(fmaf(__uint_as_float(rs[2 * x + 1]), scale_log2, -my_l2));
+                    float d0 = p0 * (__uint_as_float(rp[2 * x]) - my_d);
+                    float d1 = p1 * (__uint_as_float(rp[2 * x + 1]) - my_d);
+                    if (col >= valid) d0 = 0.f;
+                    if (col + 1 >= valid) d1 = 0.f;
+                    pk[x] = pack2<kBf16>(d0, d1);
+                }
+                tmem_st16(t_dp + 16u * c, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bars.elem());
+        }
+        if (ok) ok = warp_wait(bars.done(), 0, wd);
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_off + 256u + 32u * c, r);
+                tmem_ld_wait();
+                reg_fence(r);
+                store_row_chunk<kBf16>(dq, (size_t)bh * n_q + row, D, c, r, scale, row < n_q);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------------------ launch
+
+template <int D, bool kBf16>
+cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot) {
+    using C = BwdCfg<D>;
+    {
+        constexpr int RPC = 256 / (D / 8);
+        const dim3 grid((unsigned)((p.n_q_pad + RPC - 1) / RPC), (unsigned)p.bh, 1);
+        bwd_preprocess_kernel<D, kBf16><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(p.o),
+                                                                 static_cast<const uint16_t*>(p.d_o), p.lse, p.delta,
+                                                                 p.lse2, (int)p.n_q, (int)p.n_q_pad);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!encode_tmap_3d(&tq, dt, 2, p.q, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tdo, dt, 2, p.d_o, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tk, dt, 2, p.k, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
+        return cudaErrorInvalidValue;
+    const float scale_log2 = p.scale * kLog2e;
+    auto dkdv = bwd_dkdv_kernel<D, kBf16>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(dkdv), C::kSmemDkv, slot);
+    if (e != cudaSuccess) return e;
+    dkdv<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDkv, stream>>>(
+        tq, tk, tv, tdo, p.lse2, p.delta, p.dk, p.dv, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.scale, scale_log2, p.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto dqk = bwd_dq_kernel<D, kBf16>;
+    e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
+    if (e != cudaSuccess) return e;
+    dqk<<<dim3((unsigned)((p.n_q + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDq, stream>>>(
+        tq, tk, tv, tdo, p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.scale, scale_log2, p.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream) {
+    const bool bf = p.dtype == kBf16;
+    switch (p.d) {
+        case 32: return bf ? launch_impl<32, true>(p, stream, 16) : launch_impl<32, false>(p, stream, 18);
+        case 64: return bf ? launch_impl<64, true>(p, stream, 20) : launch_impl<64, false>(p, stream, 22);
+        case 128: return bf ? launch_impl<128, true>(p, stream, 24) : launch_impl<128, false>(p, stream, 26);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa2

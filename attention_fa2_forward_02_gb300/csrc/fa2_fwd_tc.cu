@@ -1,0 +1,344 @@
+// fa2_fwd_tc.cu - attention forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes: "vision-rs 0.1.1 flash_attn2.rs", flash_attention2_forward
+// (scores scaled by softmax_scale, the online-softmax recurrence over key rows,
+// O = acc / l, LSE = m + ln l), over the flat [BH, N, HEAD_DIM] layout.  The
+// page runs one key row at a time per query row; here the recurrence runs one
+// 128-key tile at a time per 128-row query tile, the tile form of the update
+// that "vyre-libs 0.7.2 flash_attention_2.rs" describes for flash_attention_2
+// (all scores of a tile first, then one (m, l, o_acc) update per tile).
+//
+// CTA shape: two 128-row query tiles (Q0, Q1) sharing every K/V tile.
+//   warp 0      TMA producer: Q0/Q1 once, then a K ring and a V ring
+//   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
+//   warps 2-5   softmax for Q0 (one thread per query row / TMEM lane)
+//   warps 6-9   softmax for Q1
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [0,128) S0 = Q0 K^T   [128,256) S1 = Q1 K^T   [256,256+D) O0   [256+D,256+2D) O1
+// The probabilities P (16-bit) are written back over the first 64 columns of
+// their S tile and consumed from tensor memory by the P.V MMA.  MMA order per
+// key tile j:  PV0(j), S0(j+1), PV1(j), S1(j+1): while one softmax group works
+// on its scores the tensor core runs the other group's products.
+//
+// Running maximum: exact except that the O / l rescale is skipped while the
+// new tile maximum exceeds the reference maximum by at most 8 (base-2 units);
+// the reference then lags the true maximum by at most 8, so every exponent is
+// <= 2^8 and the final O = acc / l is the same quotient up to rounding.
+#include "common.cuh"
+#include "internal.h"
+
+namespace fa2 {
+namespace {
+
+constexpr int BM = 128;            // query rows per tile = TMEM lanes
+constexpr int BN = 128;            // keys per K/V tile
+constexpr int kQTiles = 2;         // query tiles per CTA
+constexpr int kThreads = 320;      // 10 warps
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int D>
+struct FwdCfg : Tile16<D> {
+    static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
+    static constexpr int kQTileBytes = BM * D * 2;
+    static constexpr int kKVTileBytes = BN * D * 2;
+    static constexpr int kSmemQ = 0;
+    static constexpr int kSmemK = kSmemQ + kQTiles * kQTileBytes;
+    static constexpr int kSmemV = kSmemK + kStages * kKVTileBytes;
+    static constexpr int kSmemBar = kSmemV + kStages * kKVTileBytes;
+    static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1;
+    static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
+    static constexpr int kSmemBytes = kSmemMisc + 16 + 1024;  // + slack to align the base to 1024
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(256 + 2 * D <= (int)kTmemCols, "tensor memory budget");
+};
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr, float* __restrict__ lse_ptr,
+                      int n_q, int n_k, float scale_log2, unsigned int* status) {
+    using C = FwdCfg<D>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_addr);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.y;
+    const int q0 = blockIdx.x * (BM * kQTiles);
+    const int n_kv = (n_k + BN - 1) / BN;
+
+    const uint32_t bars = base + C::kSmemBar;
+    const uint32_t B_Q = bars;
+    auto B_KF = [&](int s) { return bars + 8u * (1 + s); };
+    auto B_KE = [&](int s) { return bars + 8u * (1 + S + s); };
+    auto B_VF = [&](int s) { return bars + 8u * (1 + 2 * S + s); };
+    auto B_VE = [&](int s) { return bars + 8u * (1 + 3 * S + s); };
+    auto B_SF = [&](int t) { return bars + 8u * (1 + 4 * S + t); };
+    auto B_PF = [&](int t) { return bars + 8u * (3 + 4 * S + t); };
+    const uint32_t B_OD = bars + 8u * (5 + 4 * S);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 4);
+    const Watchdog wd{abort_flag, status};
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        mbar_init(B_Q, 1);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(B_KF(s), 1);
+            mbar_init(B_KE(s), 1);
+            mbar_init(B_VF(s), 1);
+            mbar_init(B_VE(s), 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(B_SF(t), 1);
+            mbar_init(B_PF(t), BM);
+        }
+        mbar_init(B_OD, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    const uint32_t q_smem = base + C::kSmemQ;
+    const uint32_t k_smem = base + C::kSmemK;
+    const uint32_t v_smem = base + C::kSmemV;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(B_Q, kQTiles * C::kQTileBytes);
+            for (int t = 0; t < kQTiles; ++t)
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(q_smem + t * C::kQTileBytes + a * BM * C::kAtomRowBytes, &tm_q, B_Q, a * C::kAtomCols,
+                                q0 + t * BM, bh);
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < n_kv; ++j) {
+                const int s = j % S;
+                const uint32_t release_parity = ((j / S) & 1) ^ 1;
+                if (j >= S && !(ok = mbar_wait(B_KE(s), release_parity, wd))) break;
+                mbar_arrive_expect_tx(B_KF(s), C::kKVTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(k_smem + s * C::kKVTileBytes + a * BN * C::kAtomRowBytes, &tm_k, B_KF(s),
+                                a * C::kAtomCols, j * BN, bh);
+                if (j >= S && !(ok = mbar_wait(B_VE(s), release_parity, wd))) {
+                    issued = 2 * j + 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(B_VF(s), C::kKVTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_3d(v_smem + s * C::kKVTileBytes + a * BN * C::kAtomRowBytes, &tm_v, B_VF(s),
+                                a * C::kAtomCols, j * BN, bh);
+                issued = 2 * j + 2;
+            }
+            if (!ok) {
+                // Drain the copies still in flight before the CTA's shared memory is released.
+                drain_wait(B_Q, 0);
+                for (int i = (issued > 2 * S ? issued - 2 * S : 0); i < issued; ++i) {
+                    const int j = i >> 1, s = j % S;
+                    drain_wait((i & 1) ? B_VF(s) : B_KF(s), (j / S) & 1);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16_f32acc(BM, BN, kBf16, false, false);
+            const uint32_t idesc_o = idesc_f16_f32acc(BM, D, kBf16, false, true);
+            auto issue_s = [&](int t, int s) {
+                const uint32_t d_tmem = tmem + (uint32_t)(t * BN);
+                const uint32_t qa = q_smem + t * C::kQTileBytes;
+                const uint32_t kb = k_smem + s * C::kKVTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(d_tmem, C::kmajor(qa, kk, BM), C::kmajor(kb, kk, BN), idesc_s, kk > 0 ? 1u : 0u);
+            };
+            auto issue_pv = [&](int t, int s, bool acc) {
+                const uint32_t d_tmem = tmem + 256u + (uint32_t)(t * D);
+                const uint32_t vb = v_smem + s * C::kKVTileBytes;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
+                           (acc || kk > 0) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(B_Q, 0, wd) && mbar_wait(B_KF(0), 0, wd);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                mma_commit(B_SF(0));
+                issue_s(1, 0);
+                mma_commit(B_SF(1));
+                mma_commit(B_KE(0));
+            }
+            for (int j = 0; ok && j < n_kv; ++j) {
+                const int s = j % S;
+                const int jn = j + 1;
+                const int sn = jn % S;
+                if (!(ok = mbar_wait(B_VF(s), (j / S) & 1, wd))) break;
+                for (int t = 0; t < kQTiles; ++t) {
+                    if (!(ok = mbar_wait(B_PF(t), j & 1, wd))) break;
+                    tc_fence_after();
+                    issue_pv(t, s, j > 0);
+                    if (t == kQTiles - 1) mma_commit(B_VE(s));
+                    if (jn < n_kv) {
+                        if (t == 0) {
+                            if (!(ok = mbar_wait(B_KF(sn), (jn / S) & 1, wd))) break;
+                            tc_fence_after();
+                        }
+                        issue_s(t, sn);
+                        mma_commit(B_SF(t));
+                        if (t == kQTiles - 1) mma_commit(B_KE(sn));
+                    }
+                }
+            }
+            // Completion of everything issued: the softmax groups read O after it,
+            // and tensor memory is released only after it.
+            mma_commit(B_OD);
+            drain_wait(B_OD, 0);
+        }
+    } else {
+        // ------------------------------------------------------------------ softmax groups
+        const int t = (warp - 2) >> 2;
+        const int quarter = warp & 3;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t s_addr = tmem + lane_off + (uint32_t)(t * BN);
+        const uint32_t o_addr = tmem + lane_off + 256u + (uint32_t)(t * D);
+        float m2 = -INFINITY;  // reference maximum, base-2 units (score * scale * log2 e)
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            if (!(ok = warp_wait(B_SF(t), j & 1, wd))) break;
+            tc_fence_after();
+            float s[BN];
+            tmem_ld128(s_addr, s);
+            const int valid = n_k - j * BN;
+            if (valid < BN) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    if (c >= valid) s[c] = -INFINITY;
+            }
+            float mx = s[0];
+#pragma unroll
+            for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
+            const float m_new = mx * scale_log2;
+            if (j == 0) {
+                m2 = m_new;
+            } else {
+                const bool need = m_new > m2 + kRescaleThreshold;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float alpha = need ? ex2_approx(m2 - m_new) : 1.f;
+                    if (need) {
+                        l *= alpha;
+                        m2 = m_new;
+                    }
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(o_addr + 32u * c, r);
+                        tmem_ld_wait();
+                        reg_fence(r);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+                        tmem_st32(o_addr + 32u * c, r);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            float rs = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * i], scale_log2, -m2));
+                    const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * i + 1], scale_log2, -m2));
+                    rs += p0 + p1;
+                    pk[i] = pack2<kBf16>(p0, p1);
+                }
+                tmem_st32(s_addr + 32u * h, pk);
+            }
+            l += rs;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(B_PF(t));
+        }
+        if (ok) ok = warp_wait(B_OD, 0, wd);
+        if (ok) {
+            tc_fence_after();
+            const int row = q0 + t * BM + quarter * 32 + lane;
+            const float inv_l = 1.f / l;
+            uint16_t* orow = reinterpret_cast<uint16_t*>(o_ptr) + ((size_t)bh * n_q + row) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(o_addr + 32u * c, r);
+                tmem_ld_wait();
+                reg_fence(r);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack2<kBf16>(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+                if (row < n_q) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                }
+            }
+            if (row < n_q) lse_ptr[(size_t)bh * n_q + row] = (m2 + lg2_approx(l)) * kLn2;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D, bool kBf16>
+cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
+    using C = FwdCfg<D>;
+    const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap tq, tk, tv;
+    if (!encode_tmap_3d(&tq, dt, 2, p.q, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BM, sw) ||
+        !encode_tmap_3d(&tk, dt, 2, p.k, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw) ||
+        !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw))
+        return cudaErrorInvalidValue;
+    auto kern = fa2_fwd_tc_kernel<D, kBf16>;
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)((p.n_q + BM * kQTiles - 1) / (BM * kQTiles)), (unsigned)p.bh, 1);
+    const float scale_log2 = p.scale * 1.4426950408889634f;
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p.o, p.lse, (int)p.n_q, (int)p.n_k, scale_log2, p.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream) {
+    const bool bf = p.dtype == kBf16;
+    switch (p.d) {
+        case 32: return bf ? launch_impl<32, true>(p, stream, 0) : launch_impl<32, false>(p, stream, 1);
+        case 64: return bf ? launch_impl<64, true>(p, stream, 2) : launch_impl<64, false>(p, stream, 3);
+        case 128: return bf ? launch_impl<128, true>(p, stream, 4) : launch_impl<128, false>(p, stream, 5);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa2

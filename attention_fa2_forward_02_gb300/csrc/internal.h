@@ -1,0 +1,72 @@
+// internal.h - host-side interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fa2 {
+
+enum Dtype : int { kF32 = 0, kF16 = 1, kBf16 = 2 };
+
+struct FwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* o;
+    float* lse;
+    int64_t bh, n_q, n_k;
+    int d;
+    int dtype;
+    float scale;
+    unsigned int* status;  // device watchdog word
+};
+
+struct BwdParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* o;
+    const void* d_o;
+    const float* lse;
+    void* dq;
+    void* dk;
+    void* dv;
+    float* delta;  // [bh, n_q_pad] row sums D (0 in the padding rows), inside the workspace
+    float* lse2;   // [bh, n_q_pad] LSE * log2(e) (+inf in the padding rows), inside the workspace
+    int64_t n_q_pad;
+    int64_t bh, n_q, n_k;
+    int d;
+    int dtype;
+    float scale;
+    unsigned int* status;
+};
+
+// One batched 2-D transpose: for z in [0, batches), dst block z ([cols, rows]
+// row-major) is the transpose of src block z ([rows, cols] row-major).  The
+// block base offsets (in elements) come from the psa map selected by `kind`.
+struct PsaParams {
+    const void* src0;
+    const void* src1;  // merge: hi (src0 = lo); pack: unused
+    void* dst;
+    int kind;          // 0 = pack, 1 = merge
+    int elem_bytes;    // 2 or 4
+    int64_t B, nh, kd, n, qkv_h, c;
+};
+
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_psa(const PsaParams& p, cudaStream_t stream);
+
+// Encodes a 3-D tiled tensor map over a contiguous [d2, d1, d0] tensor of
+// `elem_bytes` elements (d0 innermost), box {box0, box1, 1}.  Returns false on failure.
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t d0, uint64_t d1,
+                    uint64_t d2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
+
+// Raises the dynamic shared-memory limit of `func` on the current device once.
+cudaError_t ensure_smem_limit(const void* func, int bytes, int slot);
+
+}  // namespace fa2

@@ -78,7 +78,8 @@ fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, flo
 /*
  * fa2_backward_workspace_size - bytes of device workspace fa2_backward needs
  * for these sizes (0 if the sizes are invalid).  The workspace holds the row
- * sums D = rowsum(O * dO) in float32.
+ * sums D = rowsum(O * dO) and a base-2 copy of the LSE, both float32 and padded
+ * to a multiple of 128 rows per head: 2 * bh * ceil(n_q / 128) * 128 * 4 bytes.
  */
 size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype);
 

@@ -1,0 +1,108 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/fa2.h declares,
+and rejects invalid arguments on the host before any CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_fa2_forward_02_gb300 import binding
+from attention_fa2_forward_02_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, MISALIGNED, CUDA_ERR, TIMEOUT, WORKSPACE = range(7)
+F32, F16, BF16 = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return binding.library()
+
+
+def declared_functions():
+    names = []
+    for fname in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fname.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fname)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for n in ("fa2_forward", "fa2_backward", "fa2_backward_workspace_size", "psa_pack_qkv", "psa_merge_attn_nchw",
+              "fa2_status_string", "fa2_device_status"):
+        assert n in names
+    assert set(binding.EXPORTS) <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(binding.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(raw, name), f"{name} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        msg = lib.fa2_status_string(s).decode()
+        assert msg and msg != "unknown status"
+    assert lib.fa2_status_string(99).decode() == "unknown status"
+
+
+P = ctypes.c_void_p(0x1000)        # never dereferenced: every call below fails validation first
+PM = ctypes.c_void_p(0x1008)       # misaligned
+
+
+def fwd(lib, q=P, k=P, v=P, o=P, l=P, bh=2, nq=64, nk=64, d=64, dt=BF16, scale=0.125):
+    return lib.fa2_forward(q, k, v, o, l, bh, nq, nk, d, dt, scale, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    ({"q": None}, INVALID), ({"l": None}, INVALID), ({"bh": 0}, INVALID), ({"nq": 0}, INVALID), ({"nk": -1}, INVALID),
+    ({"d": 0}, INVALID), ({"dt": 7}, INVALID), ({"scale": 0.0}, INVALID), ({"scale": float("nan")}, INVALID),
+    ({"scale": float("inf")}, INVALID), ({"d": 16}, UNSUPPORTED), ({"d": 96}, UNSUPPORTED), ({"d": 7}, UNSUPPORTED),
+    ({"bh": 70000}, UNSUPPORTED), ({"q": PM}, MISALIGNED), ({"o": PM}, MISALIGNED),
+])
+def test_forward_validation(lib, kw, want):
+    assert fwd(lib, **kw) == want
+
+
+def test_backward_validation(lib):
+    args = [P] * 9
+    assert lib.fa2_backward(*args, P, 1 << 20, 2, 64, 64, 64, F32, 0.125, None) == UNSUPPORTED
+    assert lib.fa2_backward(*args, None, 1 << 20, 2, 64, 64, 64, BF16, 0.125, None) == WORKSPACE
+    assert lib.fa2_backward(*args, P, 16, 2, 64, 64, 64, BF16, 0.125, None) == WORKSPACE
+    assert lib.fa2_backward(*args, PM, 1 << 20, 2, 64, 64, 64, BF16, 0.125, None) == WORKSPACE
+    assert lib.fa2_backward(None, *args[1:], P, 1 << 20, 2, 64, 64, 64, BF16, 0.125, None) == INVALID
+    assert lib.fa2_backward(*args, P, 1 << 20, 2, 64, 64, 48, BF16, 0.125, None) == UNSUPPORTED
+    assert lib.fa2_backward(*args[:6], PM, *args[7:], P, 1 << 20, 2, 64, 64, 64, BF16, 0.125, None) == MISALIGNED
+
+
+def test_workspace_size(lib):
+    assert lib.fa2_backward_workspace_size(2, 100, 50, 64, BF16) >= 2 * 100 * 4
+    assert lib.fa2_backward_workspace_size(0, 100, 50, 64, BF16) == 0
+    assert lib.fa2_backward_workspace_size(2, 100, 50, 48, BF16) == 0
+
+
+def test_psa_validation(lib):
+    # qkv_h not a multiple of 4*num_heads
+    assert lib.psa_pack_qkv(P, P, 100, 20, 20, 8, 4, F16, None) == INVALID
+    assert lib.psa_pack_qkv(None, P, 512, 20, 20, 8, 4, F16, None) == INVALID
+    assert lib.psa_pack_qkv(P, P, 512, 0, 20, 8, 4, F16, None) == INVALID
+    assert lib.psa_pack_qkv(P, P, 512, 20, 20, 8, 4, 9, None) == INVALID
+    assert lib.psa_pack_qkv(PM, P, 512, 20, 20, 8, 4, F16, None) == MISALIGNED
+    assert lib.psa_merge_attn_nchw(P, P, P, 250, 20, 20, 8, 4, F16, None) == INVALID
+    assert lib.psa_merge_attn_nchw(P, None, P, 256, 20, 20, 8, 4, F16, None) == INVALID
+    assert lib.psa_merge_attn_nchw(P, P, PM, 256, 20, 20, 8, 4, F16, None) == MISALIGNED
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(binding.Fa2Error):
+        saved = binding._lib
+        try:
+            binding._lib = None
+            binding.library(str(tmp_path / "missing.so"))
+        finally:
+            binding._lib = saved

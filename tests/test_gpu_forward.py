@@ -1,0 +1,167 @@
+"""GPU parity of fa2_forward against the float64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+
+from attention_fa2_forward_02_gb300 import binding, synth
+from oracle import attention as A
+from tests import gpu_util as G
+from tests.golden.load import load
+from tests.tolerance import check_16bit, check_f32, check_lse
+
+pytestmark = pytest.mark.gpu
+
+
+def run_forward(q, k, v, dtype, scale):
+    torch = G.require_gpu()
+    bh, n_q, d = q.shape
+    qd, kd, vd = G.to_device(q, dtype), G.to_device(k, dtype), G.to_device(v, dtype)
+    o = G.empty((bh, n_q, d), dtype)
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    binding.fa2_device_status()
+    return G.to_f64(o), G.to_f64(lse)
+
+
+SHAPES = [
+    (2, 300, 400),    # ragged query and key tails, several tiles
+    (1, 1, 1),        # a single query and a single key
+    (3, 129, 129),    # one past a tile
+    (2, 256, 128),    # exactly two query tiles, one key tile
+    (1, 520, 77),     # key length below one tile
+    (2, 64, 1000),    # queries below one tile, many key tiles
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("bh,n_q,n_k", SHAPES)
+def test_forward_tensor_core_vs_oracle(dtype, d, bh, n_q, n_k):
+    q, k, v = G.inputs(f"fwd/{dtype}/{d}/{bh}/{n_q}/{n_k}", bh, n_q, n_k, d, dtype)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_forward(q, k, v, dtype, scale)
+    o_ref, lse_ref = A.forward(synth.widen(q, dtype), synth.widen(k, dtype), synth.widen(v, dtype), scale)
+    check_16bit(o, o_ref, "O")
+    check_lse(lse, lse_ref)
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("bh,n_q,n_k", [(2, 64, 64), (1, 37, 91), (1, 1, 1)])
+def test_forward_f32_vs_oracle(d, bh, n_q, n_k):
+    q, k, v = G.inputs(f"fwd32/{d}/{bh}/{n_q}/{n_k}", bh, n_q, n_k, d, "f32")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_forward(q, k, v, "f32", scale)
+    o_ref, lse_ref = A.forward(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), scale)
+    check_f32(o, o_ref, "O")
+    check_f32(lse, lse_ref, "LSE")
+
+
+def test_forward_tiny_fp32_config():
+    """BH=2 (B=1, H=2), N_q=N_k=64, HEAD_DIM=32, float32, scale 1/sqrt(32)."""
+    q, k, v = G.inputs("config/tiny_fp32", 2, 64, 64, 32, "f32")
+    o, lse = run_forward(q, k, v, "f32", 1 / math.sqrt(32))
+    o_ref, lse_ref = A.forward(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), 1 / math.sqrt(32))
+    check_f32(o, o_ref, "O")
+    check_f32(lse, lse_ref, "LSE")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_forward_page_worked_example(dtype):
+    """The single-key example of the vyre-libs unit tests, head_dim zero-padded to 32.
+
+    Zero columns add nothing to q.k, and zero V columns only add zero output
+    columns, so the first four outputs must be V itself and LSE = 12.5.
+    """
+    g = load("seq_len_one.txt")
+    pad = lambda x: np.pad(np.array(x, dtype=np.float64).reshape(1, 1, 4), ((0, 0), (0, 0), (0, 28)))
+    q, k, v = (synth.to_storage(pad(g[n]), dtype) for n in ("q", "k", "v"))
+    o, lse = run_forward(q, k, v, dtype, g["scale"])
+    assert np.array_equal(o[0, 0, :4], np.array(g["o"])) and np.all(o[0, 0, 4:] == 0)
+    assert abs(lse[0, 0] - g["lse"]) <= 1e-5
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_forward_constant_rows_example(dtype):
+    """The constant-input example (q=1, k=0.5, v=2) at GPU head_dim 32 and several tiles of rows."""
+    n, d = 300, 32
+    q = synth.to_storage(np.full((1, n, d), 1.0), dtype)
+    k = synth.to_storage(np.full((1, n, d), 0.5), dtype)
+    v = synth.to_storage(np.full((1, n, d), 2.0), dtype)
+    scale = 1 / math.sqrt(d)
+    o, lse = run_forward(q, k, v, dtype, scale)
+    assert np.all(o == 2.0)
+    assert np.max(np.abs(lse - (math.log(n) + d * 0.5 * scale))) <= 1e-4
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_forward_invariants(dtype):
+    """Constant V gives that constant; identical key rows give mean(V) and LSE = ln N_k + scale q.k."""
+    bh, n_q, n_k, d = 2, 200, 333, 64
+    q, k, v = G.inputs(f"inv/{dtype}", bh, n_q, n_k, d, dtype)
+    scale = 1 / math.sqrt(d)
+    vc = synth.to_storage(np.full((bh, n_k, d), -1.25), dtype)
+    o, _ = run_forward(q, k, vc, dtype, scale)
+    assert np.max(np.abs(o + 1.25)) <= 1e-2
+    krow = k[:, :1]
+    ks = np.repeat(krow, n_k, axis=1)
+    o, lse = run_forward(q, ks, v, dtype, scale)
+    check_16bit(o, np.broadcast_to(synth.widen(v, dtype).mean(axis=1, keepdims=True), o.shape), "O (identical keys)")
+    want = math.log(n_k) + scale * np.einsum("bid,bd->bi", synth.widen(q, dtype), synth.widen(krow, dtype)[:, 0])
+    check_lse(lse, want, "LSE (identical keys)")
+
+
+def test_forward_deterministic_and_in_bounds():
+    """Two runs agree bit for bit, and nothing is written outside O and LSE (guard bands)."""
+    torch = G.require_gpu()
+    bh, n_q, n_k, d = 3, 300, 200, 128
+    q, k, v = G.inputs("canary", bh, n_q, n_k, d, "bf16")
+    qd, kd, vd = (G.to_device(x, "bf16") for x in (q, k, v))
+    guard = 4096
+    o_buf = torch.full((bh * n_q * d + 2 * guard,), -7.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((bh * n_q + 2 * guard,), -7.0, dtype=torch.float32, device="cuda")
+    o = o_buf[guard:guard + bh * n_q * d].view(bh, n_q, d)
+    lse = l_buf[guard:guard + bh * n_q].view(bh, n_q)
+    binding.fa2_forward(qd, kd, vd, o, lse, 1 / math.sqrt(d))
+    first = (o.clone(), lse.clone())
+    binding.fa2_forward(qd, kd, vd, o, lse, 1 / math.sqrt(d))
+    binding.fa2_device_status()
+    assert torch.equal(first[0], o) and torch.equal(first[1], lse)
+    assert torch.all(o_buf[:guard] == -7.0) and torch.all(o_buf[-guard:] == -7.0)
+    assert torch.all(l_buf[:guard] == -7.0) and torch.all(l_buf[-guard:] == -7.0)
+
+
+def _sampled_rows(tag, bh, n_q, n_k, d, k_scale, bh_list, rows):
+    torch = G.require_gpu()
+    q, k, v = G.inputs(tag, bh, n_q, n_k, d, "bf16", k_scale=k_scale)
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd = (G.to_device(x, "bf16") for x in (q, k, v))
+    o = G.empty((bh, n_q, d), "bf16")
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    binding.fa2_device_status()
+    for b in bh_list:
+        o_ref, l_ref = A.forward_rows(synth.widen(q[b:b + 1], "bf16"), synth.widen(k[b:b + 1], "bf16"),
+                                      synth.widen(v[b:b + 1], "bf16"), scale, 0, rows)
+        check_16bit(G.to_f64(o[b, rows]), o_ref, f"O rows of head {b}")
+        check_lse(G.to_f64(lse[b, rows]), l_ref, f"LSE rows of head {b}")
+    return o, lse
+
+
+def test_forward_full_size_d64_sampled():
+    """Non-causal bf16 forward, B=4 H=16 (BH=64), N=4096, d=64: sampled rows against the oracle."""
+    rows = np.array([0, 1, 127, 128, 2047, 2048, 4094, 4095])
+    _sampled_rows("config/fwd_d64", 64, 4096, 4096, 64, 1.0, [0, 31, 63], rows)
+
+
+def test_forward_full_size_d128_sampled():
+    """bf16 forward, B=2 H=16 (BH=32), N=8192, d=128: sampled rows against the oracle."""
+    rows = np.array([0, 255, 256, 4000, 8191])
+    _sampled_rows("config/fwdbwd_d128", 32, 8192, 8192, 128, 1.0, [0, 17, 31], rows)
+
+
+def test_forward_cross_attention_peaked_sampled():
+    """B=1 H=32, N_q=1024 vs N_k=32768, d=128, K scaled by 8 (peaked rows): sampled rows."""
+    rows = np.array([0, 100, 511, 512, 1023])
+    o, lse = _sampled_rows("config/cross_k8", 32, 1024, 32768, 128, 8.0, [0, 31], rows)
+    assert np.all(np.isfinite(G.to_f64(o))) and np.all(np.isfinite(G.to_f64(lse)))

@@ -1,0 +1,96 @@
+"""GPU parity of the PSA rearrangement passes (bit-exact) and of the C2PSA attention pipeline."""
+import math
+
+import numpy as np
+import pytest
+
+from attention_fa2_forward_02_gb300 import binding, synth
+from oracle import attention as A
+from oracle import psa as P
+from tests import gpu_util as G
+from tests.tolerance import check_16bit
+
+pytestmark = pytest.mark.gpu
+
+
+def _raw_tensor(words, dtype):
+    """Raw words as a CUDA tensor whose bits are exactly `words`."""
+    import torch
+    if dtype == "f32":
+        return torch.from_numpy(words.view(np.int32).copy()).view(torch.float32).cuda()
+    t = torch.from_numpy(words.view(np.int16).copy())
+    return t.view(torch.bfloat16 if dtype == "bf16" else torch.float16).cuda()
+
+
+def _words(t, dtype):
+    import torch
+    if dtype == "f32":
+        return t.view(torch.int32).cpu().numpy().view(np.uint32)
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _patterns(tag, shape, dtype):
+    w16 = synth.counter_u16(tag, shape)
+    if dtype == "f32":
+        hi = synth.counter_u16(tag + "/hi", shape).astype(np.uint32)
+        return (hi << np.uint32(16)) | w16.astype(np.uint32)
+    return w16
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("B,nh,kd,H,W", [(8, 4, 32, 20, 20), (2, 2, 16, 5, 7), (1, 3, 8, 1, 1), (3, 1, 64, 9, 16)])
+def test_pack_merge_bit_exact(dtype, B, nh, kd, H, W):
+    G.require_gpu()
+    qkv = _patterns(f"psa/{dtype}/{B}/{nh}/{kd}/{H}/{W}", (B, nh * 4 * kd, H, W), dtype)
+    qkv_d = _raw_tensor(qkv, dtype)
+    packed = _raw_tensor(np.zeros(qkv.size, dtype=qkv.dtype), dtype)
+    binding.psa_pack_qkv(qkv_d, packed, nh)
+    got = _words(packed, dtype).reshape(4, B * nh, H * W, kd)
+    assert np.array_equal(got, P.pack_qkv(qkv, nh))
+    # merge the V_lo / V_hi sections back: the V channels of QKV, bit for bit
+    out = _raw_tensor(np.zeros((B, nh * 2 * kd, H, W), dtype=qkv.dtype), dtype).view(B, nh * 2 * kd, H, W)
+    sec = packed.view(4, B * nh, H * W, kd)
+    binding.psa_merge_attn_nchw(sec[2], sec[3], out, nh)
+    binding.fa2_device_status()
+    merged = _words(out, dtype).reshape(B, nh * 2 * kd, H, W)
+    assert np.array_equal(merged, P.merge_attn_nchw(got[2], got[3], B, nh, H, W))
+    assert np.array_equal(merged, P.extract_v_nchw(qkv, nh))
+
+
+def test_merge_independent_inputs():
+    G.require_gpu()
+    B, nh, kd, H, W = 2, 3, 32, 6, 10
+    lo = synth.counter_u16("merge/lo", (B * nh, H * W, kd))
+    hi = synth.counter_u16("merge/hi", (B * nh, H * W, kd))
+    out = _raw_tensor(np.zeros((B, nh * 2 * kd, H, W), dtype=np.uint16), "f16").view(B, nh * 2 * kd, H, W)
+    binding.psa_merge_attn_nchw(_raw_tensor(lo, "f16").view(B * nh, H * W, kd), _raw_tensor(hi, "f16").view(B * nh, H * W, kd), out, nh)
+    binding.fa2_device_status()
+    assert np.array_equal(_words(out, "f16").reshape(B, nh * 2 * kd, H, W), P.merge_attn_nchw(lo, hi, B, nh, H, W))
+
+
+def test_c2psa_pipeline():
+    """YOLO C2PSA block: QKV [8, 512, 20, 20] fp16, num_heads 4, KEY_DIM 32: pack, two
+    attention calls (V_lo, V_hi) with HEAD_DIM 32 on N = 400 tokens, merge to [8, 256, 20, 20]."""
+    torch = G.require_gpu()
+    B, nh, kd, H, W = 8, 4, 32, 20, 20
+    n, bh = H * W, B * nh
+    qkv = synth.tensor("config/c2psa/qkv", (B, nh * 4 * kd, H, W), "f16")
+    qkv_d = G.to_device(qkv, "f16")
+    packed = torch.empty((4, bh, n, kd), dtype=torch.float16, device="cuda")
+    binding.psa_pack_qkv(qkv_d, packed, nh)
+    o_lo = torch.empty((bh, n, kd), dtype=torch.float16, device="cuda")
+    o_hi = torch.empty_like(o_lo)
+    lse_lo = torch.empty((bh, n), dtype=torch.float32, device="cuda")
+    lse_hi = torch.empty_like(lse_lo)
+    scale = 1.0 / math.sqrt(kd)
+    binding.fa2_forward(packed[0], packed[1], packed[2], o_lo, lse_lo, scale)
+    binding.fa2_forward(packed[0], packed[1], packed[3], o_hi, lse_hi, scale)
+    out = torch.empty((B, nh * 2 * kd, H, W), dtype=torch.float16, device="cuda")
+    binding.psa_merge_attn_nchw(o_lo, o_hi, out, nh)
+    binding.fa2_device_status()
+    # oracle pipeline
+    pk = synth.widen(P.pack_qkv(qkv, nh), "f16")
+    r_lo, _ = A.forward(pk[0], pk[1], pk[2], scale)
+    r_hi, _ = A.forward(pk[0], pk[1], pk[3], scale)
+    ref = P.merge_attn_nchw(r_lo, r_hi, B, nh, H, W)
+    check_16bit(G.to_f64(out), ref, "merged attention output")

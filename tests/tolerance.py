@@ -1,0 +1,38 @@
+"""The parity bar for floating-point outputs, in one place.
+
+Attention outputs (O, dQ, dK, dV) computed from 16-bit inputs with float32
+accumulation must be within 2e-2 absolute of the float64 oracle AND within
+2e-2 * max|oracle| (the second bound keeps the check meaningful when the
+outputs themselves are ~1e-2, where a zero output would pass a bare 2e-2).
+The float32 path: 1e-4 absolute.  LSE: 1e-3 absolute.
+"""
+import numpy as np
+
+ABS_16 = 2e-2
+REL_16 = 2e-2
+ABS_F32 = 1e-4
+ABS_LSE = 1e-3
+
+
+def attention_error(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    scale = float(np.max(np.abs(ref))) if ref.size else 0.0
+    return err, scale
+
+
+def check_16bit(got, ref, what="output"):
+    err, scale = attention_error(got, ref)
+    ok = np.all(np.isfinite(got)) and err <= ABS_16 and err <= REL_16 * scale
+    assert ok, f"{what}: max|err| = {err:.3e}, max|ref| = {scale:.3e} (bounds {ABS_16} and {REL_16}*max|ref|)"
+
+
+def check_f32(got, ref, what="output"):
+    err, _ = attention_error(got, ref)
+    assert np.all(np.isfinite(got)) and err <= ABS_F32, f"{what}: max|err| = {err:.3e} > {ABS_F32}"
+
+
+def check_lse(got, ref, what="lse"):
+    err, _ = attention_error(got, ref)
+    assert np.all(np.isfinite(got)) and err <= ABS_LSE, f"{what}: max|err| = {err:.3e} > {ABS_LSE}"
