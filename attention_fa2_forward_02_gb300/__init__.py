@@ -9,7 +9,11 @@ Python or CPU compute path, and calls fail loudly if the library is missing.
 from .binding import (  # noqa: F401
     Fa2Error,
     fa2_backward,
+    fa2_backward_dkdv,
+    fa2_backward_dq,
+    fa2_backward_preprocess,
     fa2_backward_workspace_size,
+    fa2_device_status,
     fa2_forward,
     fa2_status_string,
     library,

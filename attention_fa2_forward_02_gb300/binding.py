@@ -24,6 +24,9 @@ EXPORTS = (
     "fa2_forward",
     "fa2_backward_workspace_size",
     "fa2_backward",
+    "fa2_backward_preprocess",
+    "fa2_backward_dkdv",
+    "fa2_backward_dq",
     "psa_pack_qkv",
     "psa_merge_attn_nchw",
     "fa2_device_status",
@@ -52,6 +55,11 @@ def _declare(lib):
         "fa2_forward": (ctypes.c_int, [_c_ptr] * 5 + [_i64, _i64, _i64, _i32, _i32, _f32, _c_ptr]),
         "fa2_backward_workspace_size": (ctypes.c_size_t, [_i64, _i64, _i64, _i32, _i32]),
         "fa2_backward": (ctypes.c_int, [_c_ptr] * 10 + [ctypes.c_size_t, _i64, _i64, _i64, _i32, _i32, _f32, _c_ptr]),
+        "fa2_backward_preprocess": (ctypes.c_int, [_c_ptr] * 4 + [ctypes.c_size_t, _i64, _i64, _i64, _i32, _i32, _c_ptr]),
+        "fa2_backward_dkdv": (ctypes.c_int, [_c_ptr] * 5 + [ctypes.c_size_t, _c_ptr, _c_ptr, _i64, _i64, _i64, _i32, _i32,
+                                                           _f32, _c_ptr]),
+        "fa2_backward_dq": (ctypes.c_int, [_c_ptr] * 5 + [ctypes.c_size_t, _c_ptr, _i64, _i64, _i64, _i32, _i32, _f32,
+                                                         _c_ptr]),
         "psa_pack_qkv": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "psa_merge_attn_nchw": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "fa2_device_status": (ctypes.c_int, [_c_ptr]),
@@ -149,6 +157,38 @@ def fa2_backward(q, k, v, o, d_o, lse, dq, dk, dv, workspace, softmax_scale: flo
                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                                 bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
     _check(st, "fa2_backward")
+
+
+def _bwd_sizes(q, k, workspace):
+    bh, n_q, d = q.shape
+    return bh, n_q, k.shape[1], d, workspace.numel() * workspace.element_size()
+
+
+def fa2_backward_preprocess(o, d_o, lse, workspace, n_k: int, stream=None) -> None:
+    """Stage 1 of fa2_backward: fills the workspace (row sums D and the base-2 LSE)."""
+    bh, n_q, d = o.shape
+    st = library().fa2_backward_preprocess(_dev(o, "o", 3), _dev(d_o, "d_o", 3), _dev(lse, "lse", 2),
+                                           _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                                           bh, n_q, n_k, d, _dtype_code(o), _stream(stream))
+    _check(st, "fa2_backward_preprocess")
+
+
+def fa2_backward_dkdv(q, k, v, d_o, workspace, dk, dv, softmax_scale: float, stream=None) -> None:
+    """Stage 2 of fa2_backward: dK and dV (the pass over key tiles)."""
+    bh, n_q, n_k, d, wsb = _bwd_sizes(q, k, workspace)
+    st = library().fa2_backward_dkdv(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(d_o, "d_o", 3),
+                                     _dev(workspace, "workspace"), wsb, _dev(dk, "dk", 3), _dev(dv, "dv", 3),
+                                     bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
+    _check(st, "fa2_backward_dkdv")
+
+
+def fa2_backward_dq(q, k, v, d_o, workspace, dq, softmax_scale: float, stream=None) -> None:
+    """Stage 3 of fa2_backward: dQ (the pass over query tiles)."""
+    bh, n_q, n_k, d, wsb = _bwd_sizes(q, k, workspace)
+    st = library().fa2_backward_dq(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(d_o, "d_o", 3),
+                                   _dev(workspace, "workspace"), wsb, _dev(dq, "dq", 3),
+                                   bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
+    _check(st, "fa2_backward_dq")
 
 
 def psa_pack_qkv(qkv, packed, num_heads: int, stream=None) -> None:

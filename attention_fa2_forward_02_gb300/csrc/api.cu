@@ -122,16 +122,21 @@ size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t
     return 2 * (size_t)(bh * n_q_pad) * sizeof(float);
 }
 
-fa2_status fa2_backward(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
-                        void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int64_t bh, int64_t n_q,
-                        int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
-    if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
+static fa2_status backward_common(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                                  size_t workspace_bytes, int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
+                                  fa2_dtype dtype, float softmax_scale, void* stream, int stages) {
+    // pointers each stage reads or writes; the others may be null
+    const bool pre = stages & kBwdPreprocess, dkdv = stages & kBwdDkDv, dqs = stages & kBwdDq;
+    if ((pre && (!o || !d_o || !lse)) || ((dkdv || dqs) && (!q || !k || !v || !d_o)) || (dkdv && (!dk || !dv)) ||
+        (dqs && !dq))
+        return FA2_ERR_INVALID_ARG;
     fa2_status st = check_attention_sizes(bh, n_q, n_k, head_dim, dtype, softmax_scale);
     if (st != FA2_OK) return st;
     if (dtype == FA2_DTYPE_F32) return FA2_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(d_o) || !aligned16(lse) ||
-        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-        return FA2_ERR_MISALIGNED;
+    const void* ptrs[] = {q, k, v, o, d_o, lse, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return FA2_ERR_MISALIGNED;
     const size_t need = fa2_backward_workspace_size(bh, n_q, n_k, head_dim, dtype);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA2_ERR_WORKSPACE;
     BwdParams p{};
@@ -142,7 +147,39 @@ fa2_status fa2_backward(const void* q, const void* k, const void* v, const void*
     p.lse2 = p.delta + bh * p.n_q_pad;
     p.bh = bh; p.n_q = n_q; p.n_k = n_k; p.d = head_dim; p.dtype = (int)dtype; p.scale = softmax_scale;
     if (!status_word(&p.status)) return FA2_ERR_CUDA;
-    return launch_bwd_tc(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+    return launch_bwd_tc(p, static_cast<cudaStream_t>(stream), stages) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+fa2_status fa2_backward(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                        void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int64_t bh, int64_t n_q,
+                        int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
+    if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
+    return backward_common(q, k, v, o, d_o, lse, dq, dk, dv, workspace, workspace_bytes, bh, n_q, n_k, head_dim, dtype,
+                           softmax_scale, stream, kBwdAll);
+}
+
+fa2_status fa2_backward_preprocess(const void* o, const void* d_o, const float* lse, void* workspace,
+                                   size_t workspace_bytes, int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
+                                   fa2_dtype dtype, void* stream) {
+    if (!o || !d_o || !lse) return FA2_ERR_INVALID_ARG;
+    return backward_common(nullptr, nullptr, nullptr, o, d_o, lse, nullptr, nullptr, nullptr, workspace,
+                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, 1.0f, stream, kBwdPreprocess);
+}
+
+fa2_status fa2_backward_dkdv(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
+                             size_t workspace_bytes, void* dk, void* dv, int64_t bh, int64_t n_q, int64_t n_k,
+                             int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
+    if (!q || !k || !v || !d_o || !dk || !dv) return FA2_ERR_INVALID_ARG;
+    return backward_common(q, k, v, nullptr, d_o, nullptr, nullptr, dk, dv, const_cast<void*>(workspace),
+                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDkDv);
+}
+
+fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
+                           size_t workspace_bytes, void* dq, int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
+                           fa2_dtype dtype, float softmax_scale, void* stream) {
+    if (!q || !k || !v || !d_o || !dq) return FA2_ERR_INVALID_ARG;
+    return backward_common(q, k, v, nullptr, d_o, nullptr, dq, nullptr, nullptr, const_cast<void*>(workspace),
+                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDq);
 }
 
 static fa2_status psa_common(int32_t H, int32_t W, int32_t B, int32_t num_heads, fa2_dtype dtype, int* elem_bytes) {

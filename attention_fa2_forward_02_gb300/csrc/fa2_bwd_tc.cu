@@ -456,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------------------ launch
 
 template <int D, bool kBf16>
-cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot) {
+cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int stages) {
     using C = BwdCfg<D>;
-    {
+    if (stages & kBwdPreprocess) {
         constexpr int RPC = 256 / (D / 8);
         const dim3 grid((unsigned)((p.n_q_pad + RPC - 1) / RPC), (unsigned)p.bh, 1);
         bwd_preprocess_kernel<D, kBf16><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(p.o),
@@ -467,6 +467,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    if (!(stages & (kBwdDkDv | kBwdDq))) return cudaSuccess;
     const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUtensorMap tq, tk, tv, tdo;
@@ -476,12 +477,17 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot) {
         !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
         return cudaErrorInvalidValue;
     const float scale_log2 = p.scale * kLog2e;
-    auto dkdv = bwd_dkdv_kernel<D, kBf16>;
-    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(dkdv), C::kSmemDkv, slot);
-    if (e != cudaSuccess) return e;
-    dkdv<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDkv, stream>>>(
-        tq, tk, tv, tdo, p.lse2, p.delta, p.dk, p.dv, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.scale, scale_log2, p.status);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (stages & kBwdDkDv) {
+        auto dkdv = bwd_dkdv_kernel<D, kBf16>;
+        e = ensure_smem_limit(reinterpret_cast<const void*>(dkdv), C::kSmemDkv, slot);
+        if (e != cudaSuccess) return e;
+        dkdv<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDkv, stream>>>(
+            tq, tk, tv, tdo, p.lse2, p.delta, p.dk, p.dv, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.scale, scale_log2,
+            p.status);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (!(stages & kBwdDq)) return cudaSuccess;
     auto dqk = bwd_dq_kernel<D, kBf16>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
     if (e != cudaSuccess) return e;
@@ -492,12 +498,12 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot) {
 
 }  // namespace
 
-cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream) {
+cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream, int stages) {
     const bool bf = p.dtype == kBf16;
     switch (p.d) {
-        case 32: return bf ? launch_impl<32, true>(p, stream, 16) : launch_impl<32, false>(p, stream, 18);
-        case 64: return bf ? launch_impl<64, true>(p, stream, 20) : launch_impl<64, false>(p, stream, 22);
-        case 128: return bf ? launch_impl<128, true>(p, stream, 24) : launch_impl<128, false>(p, stream, 26);
+        case 32: return bf ? launch_impl<32, true>(p, stream, 16, stages) : launch_impl<32, false>(p, stream, 18, stages);
+        case 64: return bf ? launch_impl<64, true>(p, stream, 20, stages) : launch_impl<64, false>(p, stream, 22, stages);
+        case 128: return bf ? launch_impl<128, true>(p, stream, 24, stages) : launch_impl<128, false>(p, stream, 26, stages);
         default: return cudaErrorInvalidValue;
     }
 }

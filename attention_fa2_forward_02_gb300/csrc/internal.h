@@ -58,7 +58,9 @@ struct PsaParams {
 
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream);
+// Backward stages, combinable as a bit mask.
+enum BwdStage : int { kBwdPreprocess = 1, kBwdDkDv = 2, kBwdDq = 4, kBwdAll = 7 };
+cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream, int stages);
 cudaError_t launch_psa(const PsaParams& p, cudaStream_t stream);
 
 // Encodes a 3-D tiled tensor map over a contiguous [d2, d1, d0] tensor of

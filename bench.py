@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Throughput of the attention hot path on GB300, one JSON line on stdout.
+
+One step is one pass of every step of the path over one batch of seeded
+synthetic inputs, all on one CUDA stream:
+
+* the YOLO C2PSA block: QKV [8, 512, 20, 20] fp16 -> psa_pack_qkv -> two
+  fa2_forward calls (HEAD_DIM 32 on Q, K with V_lo and with V_hi, N = 400)
+  -> psa_merge_attn_nchw -> [8, 256, 20, 20];
+* attention forward + backward, bf16, B=2 H=16 (BH = 32), N_q = N_k = 8192,
+  HEAD_DIM 128: fa2_forward, then fa2_backward_preprocess,
+  fa2_backward_dkdv and fa2_backward_dq (the three stages of fa2_backward).
+
+``value`` = algorithmic FLOPs of a step / device time of a step, in TFLOP/s:
+forward 4*BH*N_q*N_k*d, backward 2.5x the forward (recomputed products are not
+counted), for both attention problems of the step.  Inputs are resident in HBM
+when the timed region starts; the per-step working set (Q, K, V, dO, O, dQ, dK,
+dV: 512 MiB) is larger than the 129 MB L2, so no flush is inserted.
+
+``--impl reference`` times the float64 CPU oracle instead (on a bounded sample
+of the same workload per step); it is a deliberately slow baseline.
+
+Multi-GPU (torchrun, one process per GPU): each rank runs its own batch (weak
+scaling, no collective on the data path); the step time is the maximum over
+ranks and ``value`` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from attention_fa2_forward_02_gb300 import synth  # noqa: E402
+
+# ---------------------------------------------------------------------------- workload
+BH, N, D = 32, 8192, 128            # B=2, H=16
+PSA_B, PSA_NH, PSA_KD, PSA_H, PSA_W = 8, 4, 32, 20, 20
+PSA_N = PSA_H * PSA_W
+PSA_BH = PSA_B * PSA_NH
+FWD_FLOPS = 4.0 * BH * N * N * D
+BWD_FLOPS = 2.5 * FWD_FLOPS
+PSA_FLOPS = 2 * 4.0 * PSA_BH * PSA_N * PSA_N * PSA_KD
+STEP_FLOPS = FWD_FLOPS + BWD_FLOPS + PSA_FLOPS
+# algorithmic FLOPs of each timed kernel (per launch): the backward's 10*d per
+# (query, key) pair splits as S, dP, dV, dK (8*d) in the key pass and dQ (2*d)
+KERNEL_FLOPS = {"fa2_fwd": FWD_FLOPS, "fa2_bwd_dkdv": 0.8 * BWD_FLOPS, "fa2_bwd_dq": 0.2 * BWD_FLOPS}
+KERNEL_SOURCES = {
+    "fa2_fwd": ["fa2_fwd_tc.cu", "common.cuh"],
+    "fa2_bwd_dkdv": ["fa2_bwd_tc.cu", "common.cuh"],
+    "fa2_bwd_dq": ["fa2_bwd_tc.cu", "common.cuh"],
+}
+LAUNCHES_PER_STEP = 8  # pack, fwd lo, fwd hi, merge, fwd, preprocess, dkdv, dq
+WORKLOAD = ("C2PSA block (QKV [8,512,20,20] fp16, 4 heads, KEY_DIM 32) + attention fwd+bwd "
+            "bf16 B=2 H=16 N=8192 HEAD_DIM=128")
+METRIC = "FA2 fwd+bwd TFLOP/s (bf16, B=2 H=16 N=8192 d=128, with the C2PSA pack/attention/merge block)"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sustained": p["bf16_tflops_sustained"],
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMED = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device_id: str):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", device_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"unavailable": "nvidia-smi not found"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMED, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"unavailable": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ---------------------------------------------------------------------------- ncu traffic
+def _sources_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "attention_fa2_forward_02_gb300", "csrc", n), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_bf16_d128_n8192.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_t = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    m_h = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    if not m_t or not m_h or m_h.group(1) != _sources_hash(KERNEL_SOURCES[kernel]):
+        return None
+    return float(m_t.group(1))
+
+
+# ---------------------------------------------------------------------------- inputs
+def make_inputs(seed):
+    q = synth.tensor("bench/attn/q", (BH, N, D), "bf16", seed=seed)
+    k = synth.tensor("bench/attn/k", (BH, N, D), "bf16", seed=seed)
+    v = synth.tensor("bench/attn/v", (BH, N, D), "bf16", seed=seed)
+    d_o = synth.tensor("bench/attn/do", (BH, N, D), "bf16", seed=seed)
+    qkv = synth.tensor("bench/c2psa/qkv", (PSA_B, PSA_NH * 4 * PSA_KD, PSA_H, PSA_W), "f16", seed=seed)
+    return q, k, v, d_o, qkv
+
+
+def cpu_oracle_sample(q, k, v, d_o, budget_s: float, block_rows: int = 1024):
+    """The float64 oracle (as it stands) on blocks of query rows of head 0 until the budget is spent."""
+    from oracle import attention as A
+    w = synth.widen
+    kb, vb = w(k[0:1], "bf16"), w(v[0:1], "bf16")
+    scale = 1 / math.sqrt(D)
+    t0 = time.perf_counter()
+    blocks = 0
+    while True:
+        r0 = (blocks * block_rows) % N
+        A.backward(w(q[0:1, r0:r0 + block_rows], "bf16"), kb, vb, w(d_o[0:1, r0:r0 + block_rows], "bf16"), scale)
+        blocks += 1
+        if time.perf_counter() - t0 >= budget_s or blocks * block_rows >= N:
+            break
+    dt = time.perf_counter() - t0
+    flops = 3.5 * 4.0 * blocks * block_rows * N * D
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"{blocks} block(s) of {block_rows} query rows x {N} keys of one head, HEAD_DIM {D}: "
+                      f"forward+backward in float64 numpy ({dt:.1f} s); FLOPs counted as for the GPU step"}
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return 0
+    from oracle import attention as A
+    block = 256
+    heads = {n: synth.normal(synth.BASE_SEED, f"bench/attn/{n}", N * D).reshape(1, N, D) for n in ("q", "k", "v", "do")}
+    w = {n: synth.widen(synth.to_storage(x, "bf16"), "bf16") for n, x in heads.items()}
+    scale = 1 / math.sqrt(D)
+
+    def ref_step(i):
+        r0 = (i * block) % N
+        A.backward(w["q"][:, r0:r0 + block], w["k"], w["v"], w["do"][:, r0:r0 + block], scale)
+
+    for i in range(args.warmup):
+        ref_step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        ref_step(i)
+    dt = time.perf_counter() - t0
+    flops = 3.5 * 4.0 * block * N * D * args.steps
+    value = flops / dt / 1e12
+    sample = (f"each step: {block} query rows x {N} keys of one head (HEAD_DIM {D}), forward+backward in float64 "
+              f"numpy; the C2PSA block is not sampled")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    rank, world, local = env_rank()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from attention_fa2_forward_02_gb300 import binding as B
+    from attention_fa2_forward_02_gb300 import build as build_mod
+    build_mod.build()
+    B.library()
+
+    q_h, k_h, v_h, do_h, qkv_h = make_inputs(synth.BASE_SEED + rank)
+
+    def pinned(arr, dtype):
+        if dtype == torch.bfloat16:
+            t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(np.ascontiguousarray(arr))
+        return t.pin_memory()
+
+    hq, hk, hv, hdo = (pinned(x, torch.bfloat16) for x in (q_h, k_h, v_h, do_h))
+    hqkv = pinned(qkv_h, torch.float16)
+    dev = torch.device("cuda", local)
+    q, k, v, d_o = (x.to(dev) for x in (hq, hk, hv, hdo))
+    qkv = hqkv.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((BH, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(B.fa2_backward_workspace_size(BH, N, N, D, B.DTYPE_BF16), dtype=torch.uint8, device=dev)
+    packed = torch.empty((4, PSA_BH, PSA_N, PSA_KD), dtype=torch.float16, device=dev)
+    o_lo = torch.empty((PSA_BH, PSA_N, PSA_KD), dtype=torch.float16, device=dev)
+    o_hi = torch.empty_like(o_lo)
+    lse_lo = torch.empty((PSA_BH, PSA_N), dtype=torch.float32, device=dev)
+    lse_hi = torch.empty_like(lse_lo)
+    merged = torch.empty((PSA_B, PSA_NH * 2 * PSA_KD, PSA_H, PSA_W), dtype=torch.float16, device=dev)
+    s128, s32 = 1 / math.sqrt(D), 1 / math.sqrt(PSA_KD)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        B.psa_pack_qkv(qkv, packed, PSA_NH)
+        B.fa2_forward(packed[0], packed[1], packed[2], o_lo, lse_lo, s32)
+        B.fa2_forward(packed[0], packed[1], packed[3], o_hi, lse_hi, s32)
+        B.psa_merge_attn_nchw(o_lo, o_hi, merged, PSA_NH)
+        if ev is not None:
+            ev[1].record(stream)
+        B.fa2_forward(q, k, v, o, lse, s128)
+        if ev is not None:
+            ev[2].record(stream)
+        B.fa2_backward_preprocess(o, d_o, lse, ws, N)
+        if ev is not None:
+            ev[3].record(stream)
+        B.fa2_backward_dkdv(q, k, v, d_o, ws, dk, dv, s128)
+        if ev is not None:
+            ev[4].record(stream)
+        B.fa2_backward_dq(q, k, v, d_o, ws, dq, s128)
+        if ev is not None:
+            ev[5].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step()
+    B.fa2_device_status()
+    barrier()
+
+    # ------------------------------------------------------------------ timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    e_begin, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        dev_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:  # noqa: BLE001
+        dev_id = str(local)
+    sampler = ClockSampler(dev_id)
+    time.sleep(0.3)
+    e_begin.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(e_begin.elapsed_time(e_end))
+    B.fa2_device_status()
+    barrier()
+
+    ms_step = elapsed_ms / args.steps
+    value = world * STEP_FLOPS / (ms_step * 1e-3) / 1e12
+    names = ["c2psa_block", "fa2_fwd", "fa2_bwd_preprocess", "fa2_bwd_dkdv", "fa2_bwd_dq"]
+    per = {n: statistics.fmean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
+           for i, n in enumerate(names)}
+    pk = peaks()
+    dominant = max(KERNEL_FLOPS, key=lambda n: per[n])
+    achieved = KERNEL_FLOPS[dominant] / (per[dominant] * 1e-3) / 1e12
+    traffic = load_traffic(dominant)
+    roofline = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sustained"], "traffic": traffic,
+                "peak_kind": f"bf16 dense, sustained ({pk['source']})",
+                "flops_per_launch": KERNEL_FLOPS[dominant]}
+    bwd_ms = per["fa2_bwd_preprocess"] + per["fa2_bwd_dkdv"] + per["fa2_bwd_dq"]
+    components = {
+        "fa2_fwd_ms": per["fa2_fwd"], "fa2_fwd_tflops": FWD_FLOPS / per["fa2_fwd"] / 1e9,
+        "fa2_fwd_frac_burst_peak": FWD_FLOPS / per["fa2_fwd"] / 1e9 / pk["bf16"],
+        "fa2_bwd_ms": bwd_ms, "fa2_bwd_tflops": BWD_FLOPS / bwd_ms / 1e9,
+        "fa2_bwd_frac_burst_peak": BWD_FLOPS / bwd_ms / 1e9 / pk["bf16"],
+        "fa2_bwd_preprocess_ms": per["fa2_bwd_preprocess"], "fa2_bwd_dkdv_ms": per["fa2_bwd_dkdv"],
+        "fa2_bwd_dq_ms": per["fa2_bwd_dq"], "c2psa_block_us": per["c2psa_block"] * 1e3,
+        "peak_bf16_burst_tflops": pk["bf16"], "peak_source": pk["source"],
+    }
+
+    # ------------------------------------------------------------------ PSA pack / merge bandwidth
+    components.update(psa_bandwidth(torch, B, dev, pk))
+
+    # ------------------------------------------------------------------ end to end, host buffers
+    e2e_steps = max(3, args.steps // 10)
+    ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, dq, dk, dv))
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hmerged = torch.empty(merged.shape, dtype=merged.dtype).pin_memory()
+    ins = [(q, hq), (k, hk), (v, hv), (d_o, hdo), (qkv, hqkv)]
+    outs = [(ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv), (hmerged, merged)]
+    h2d = sum(h.numel() * h.element_size() for _, h in ins)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        for dst, src in ins:
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in outs:
+            dst.copy_(src, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b)) / e2e_steps
+    e2e = {"value": world * STEP_FLOPS / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
+    B.fa2_device_status()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "global_batch": world * BH, "seq_len": N, "head_dim": D,
+                   "parallelism": f"replicas x{world} (independent batches per GPU, no collective)",
+                   "l2": "inputs larger than L2 (512 MiB attention working set per step), no flush"},
+        "components": components, "roofline": roofline, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(q_h, k_h, v_h, do_h, budget_s=args.cpu_budget)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def psa_bandwidth(torch, B, dev, pk):
+    """psa_pack_qkv / psa_merge_attn_nchw GB/s: at the C2PSA shape (L2-resident) and at
+    B=1024 (419 MB per tensor, larger than L2)."""
+    out = {}
+    for label, b in (("c2psa", PSA_B), ("hbm_b1024", 1024)):
+        qkv = torch.randn((b, PSA_NH * 4 * PSA_KD, PSA_H, PSA_W), device=dev).to(torch.float16)
+        packed = torch.empty((4, b * PSA_NH, PSA_N, PSA_KD), dtype=torch.float16, device=dev)
+        merged = torch.empty((b, PSA_NH * 2 * PSA_KD, PSA_H, PSA_W), dtype=torch.float16, device=dev)
+        reps = 50 if b > PSA_B else 200
+        times = {"pack": [], "merge": []}
+        for _ in range(5):
+            B.psa_pack_qkv(qkv, packed, PSA_NH)
+            B.psa_merge_attn_nchw(packed[2], packed[3], merged, PSA_NH)
+        for _ in range(reps):
+            for name in ("pack", "merge"):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if name == "pack":
+                    B.psa_pack_qkv(qkv, packed, PSA_NH)
+                else:
+                    B.psa_merge_attn_nchw(packed[2], packed[3], merged, PSA_NH)
+                e1.record()
+                times[name].append((e0, e1))
+        torch.cuda.synchronize()
+        nbytes = {"pack": 2 * qkv.numel() * 2, "merge": 2 * merged.numel() * 2}
+        for name in ("pack", "merge"):
+            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in times[name])
+            out[f"psa_{name}_{label}_gbs"] = nbytes[name] / (ms * 1e-3) / 1e9
+            if label != "c2psa":
+                out[f"psa_{name}_{label}_frac_hbm"] = out[f"psa_{name}_{label}_gbs"] / pk["hbm_gbs"]
+        del qkv, packed, merged
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    return run_reference(args) if args.impl == "reference" else run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

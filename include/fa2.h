@@ -114,6 +114,32 @@ fa2_status fa2_backward(const void* q, const void* k, const void* v, const void*
                         fa2_dtype dtype, float softmax_scale, void* stream);
 
 /*
+ * The three stages of fa2_backward, callable one by one (fa2_backward is
+ * exactly these three, in this order, on one stream).  The pages keep the two
+ * main passes as separate kernels ("vision-rs 0.1.1 flash_attn2.rs",
+ * flash_attention2_backward_dq and flash_attention2_backward_dkv).  Arguments
+ * mean what they mean for fa2_backward; the workspace must be the same buffer
+ * across the three calls.
+ *
+ * fa2_backward_preprocess - fills the workspace from o, d_o and lse
+ *   (D_i = sum_d O_id dO_id, the row sum both passes subtract).
+ * fa2_backward_dkdv - dk and dv from q, k, v, d_o and a filled workspace
+ *   (the pass over key tiles).
+ * fa2_backward_dq - dq from q, k, v, d_o and a filled workspace (the pass over
+ *   query tiles).
+ * Errors as for fa2_backward.
+ */
+fa2_status fa2_backward_preprocess(const void* o, const void* d_o, const float* lse, void* workspace,
+                                   size_t workspace_bytes, int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
+                                   fa2_dtype dtype, void* stream);
+fa2_status fa2_backward_dkdv(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
+                             size_t workspace_bytes, void* dk, void* dv, int64_t bh, int64_t n_q, int64_t n_k,
+                             int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream);
+fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
+                           size_t workspace_bytes, void* dq, int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
+                           fa2_dtype dtype, float softmax_scale, void* stream);
+
+/*
  * psa_pack_qkv - NCHW QKV to the packed [4, B*num_heads, H*W, KEY_DIM] buffer.
  *
  * Defined by "vision_rs/models/yolo/kernels/attention/psa.rs", kernel

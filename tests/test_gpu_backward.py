@@ -1,0 +1,109 @@
+"""GPU parity of fa2_backward (dQ, dK, dV) against the float64 oracle, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+
+from attention_fa2_forward_02_gb300 import binding, synth
+from oracle import attention as A
+from tests import gpu_util as G
+from tests.tolerance import check_16bit
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd_bwd(q, k, v, d_o, dtype, scale):
+    """GPU forward (O, LSE), then GPU backward from them, as a training step would."""
+    torch = G.require_gpu()
+    bh, n_q, d = q.shape
+    n_k = k.shape[1]
+    qd, kd, vd, dod = (G.to_device(x, dtype) for x in (q, k, v, d_o))
+    o = G.empty((bh, n_q, d), dtype)
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    dq, dk, dv = G.empty((bh, n_q, d), dtype), G.empty((bh, n_k, d), dtype), G.empty((bh, n_k, d), dtype)
+    code = {"bf16": binding.DTYPE_BF16, "f16": binding.DTYPE_F16}[dtype]
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, code), dtype=torch.uint8, device="cuda")
+    binding.fa2_backward(qd, kd, vd, o, dod, lse, dq, dk, dv, ws, scale)
+    binding.fa2_device_status()
+    return G.to_f64(dq), G.to_f64(dk), G.to_f64(dv)
+
+
+SHAPES = [(2, 300, 400), (1, 1, 1), (3, 129, 129), (1, 520, 77), (2, 64, 1000), (1, 256, 256)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("bh,n_q,n_k", SHAPES)
+def test_backward_vs_oracle(dtype, d, bh, n_q, n_k):
+    tag = f"bwd/{dtype}/{d}/{bh}/{n_q}/{n_k}"
+    q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
+    d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, dtype, scale)
+    w = lambda x: synth.widen(x, dtype)
+    rq, rk, rv = A.backward(w(q), w(k), w(v), w(d_o), scale)
+    check_16bit(dq, rq, "dQ")
+    check_16bit(dk, rk, "dK")
+    check_16bit(dv, rv, "dV")
+
+
+def test_backward_gradient_identities():
+    """sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 (the rows of P sum to one) on the GPU result."""
+    bh, n, d = 2, 384, 64
+    q, k, v = G.inputs("bwd/identities", bh, n, n, d, "bf16")
+    d_o = synth.tensor("bwd/identities/do", (bh, n, d), "bf16")
+    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, "bf16", 1 / math.sqrt(d))
+    do64 = synth.widen(d_o, "bf16")
+    assert np.max(np.abs(dv.sum(axis=1) - do64.sum(axis=1))) <= 0.05 * np.max(np.abs(do64.sum(axis=1)))
+    assert np.max(np.abs(dk.sum(axis=1))) <= 0.02 * np.max(np.abs(dk)) * math.sqrt(n)
+
+
+def test_backward_full_size_sampled():
+    """bf16 forward+backward, B=2 H=16 (BH=32), N=8192, d=128: every dQ/dK/dV row of two heads
+    against the oracle's chunked per-head backward."""
+    bh, n, d = 32, 8192, 128
+    q, k, v = G.inputs("config/fwdbwd_d128", bh, n, n, d, "bf16")
+    d_o = synth.tensor("config/fwdbwd_d128/do", (bh, n, d), "bf16")
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, "bf16", scale)
+    w = lambda x: synth.widen(x, "bf16")
+    for b in (0, 31):
+        rq, rk, rv = A.backward_slice(w(q[b:b + 1]), w(k[b:b + 1]), w(v[b:b + 1]), w(d_o[b:b + 1]), scale, 0)
+        check_16bit(dq[b], rq, f"dQ head {b}")
+        check_16bit(dk[b], rk, f"dK head {b}")
+        check_16bit(dv[b], rv, f"dV head {b}")
+
+
+def test_backward_stages_equal_whole():
+    """fa2_backward_preprocess + _dkdv + _dq give exactly what fa2_backward gives."""
+    torch = G.require_gpu()
+    bh, n_q, n_k, d = 2, 333, 250, 64
+    q, k, v = G.inputs("bwd/stages", bh, n_q, n_k, d, "f16")
+    d_o = synth.tensor("bwd/stages/do", (bh, n_q, d), "f16")
+    qd, kd, vd, dod = (G.to_device(x, "f16") for x in (q, k, v, d_o))
+    scale = 1 / math.sqrt(d)
+    o = G.empty((bh, n_q, d), "f16")
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_F16), dtype=torch.uint8,
+                     device="cuda")
+    whole = [G.empty(x.shape, "f16") for x in (q, k, v)]
+    binding.fa2_backward(qd, kd, vd, o, dod, lse, *whole, ws, scale)
+    staged = [G.empty(x.shape, "f16") for x in (q, k, v)]
+    binding.fa2_backward_preprocess(o, dod, lse, ws, n_k)
+    binding.fa2_backward_dkdv(qd, kd, vd, dod, ws, staged[1], staged[2], scale)
+    binding.fa2_backward_dq(qd, kd, vd, dod, ws, staged[0], scale)
+    binding.fa2_device_status()
+    for a, b in zip(whole, staged):
+        assert torch.equal(a, b)
+
+
+def test_backward_deterministic():
+    bh, n, d = 2, 300, 128
+    q, k, v = G.inputs("bwd/det", bh, n, n, d, "bf16")
+    d_o = synth.tensor("bwd/det/do", (bh, n, d), "bf16")
+    a = run_fwd_bwd(q, k, v, d_o, "bf16", 1 / math.sqrt(d))
+    b = run_fwd_bwd(q, k, v, d_o, "bf16", 1 / math.sqrt(d))
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)

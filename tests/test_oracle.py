@@ -373,3 +373,16 @@ def test_bf16_rounding():
     # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: even mantissa wins (1.0); 1 + 3*2^-8 rounds up
     assert back[0] == 1.0 and back[1] == 1.0 and back[2] == 1.0 + 2 ** -6 and back[3] == -2.5
     assert np.all(np.abs(back[:4] - x[:4]) <= np.abs(x[:4]) * 2 ** -8)
+
+
+# --------------------------------------------------------------------------- the parity bar itself
+
+def test_tolerance_rejects_null_output():
+    """A zeroed output must fail the 16-bit bar even where |O| ~ 1e-2 (the full-size regime)."""
+    from tests.tolerance import check_16bit
+    ref = _rand((64, 32), 90, scale=1e-2)
+    with pytest.raises(AssertionError):
+        check_16bit(np.zeros_like(ref), ref)
+    with pytest.raises(AssertionError):
+        check_16bit(ref * 0.9, ref)
+    check_16bit(ref + 1e-5, ref)
