@@ -65,6 +65,19 @@ KERNEL_SOURCES = {
 LAUNCHES_PER_STEP = 8  # pack, fwd lo, fwd hi, merge, fwd, preprocess, dkdv, dq
 WORKLOAD = ("C2PSA block (QKV [8,512,20,20] fp16, 4 heads, KEY_DIM 32) + attention fwd+bwd "
             "bf16 B=2 H=16 N=8192 HEAD_DIM=128")
+
+
+def set_heads(bh: int):
+    """Resize the attention problem to `bh` (batch*head) slices; 32 (B=2, H=16) is the headline workload.
+    Smaller values serve profiler captures of the same complete step."""
+    global BH, FWD_FLOPS, BWD_FLOPS, STEP_FLOPS, KERNEL_FLOPS, WORKLOAD
+    BH = bh
+    FWD_FLOPS = 4.0 * BH * N * N * D
+    BWD_FLOPS = 2.5 * FWD_FLOPS
+    STEP_FLOPS = FWD_FLOPS + BWD_FLOPS + PSA_FLOPS
+    KERNEL_FLOPS = {"fa2_fwd": FWD_FLOPS, "fa2_bwd_dkdv": 0.8 * BWD_FLOPS, "fa2_bwd_dq": 0.2 * BWD_FLOPS}
+    if bh != 32:
+        WORKLOAD = WORKLOAD.replace("B=2 H=16", f"BH={bh}")
 METRIC = "FA2 fwd+bwd TFLOP/s (bf16, B=2 H=16 N=8192 d=128, with the C2PSA pack/attention/merge block)"
 
 
@@ -155,6 +168,8 @@ def _sources_hash(names):
 def load_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged since."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_bf16_d128_n8192.md")
+    if BH != 32:
+        return None
     try:
         text = open(path).read()
     except OSError:
@@ -184,16 +199,21 @@ def cpu_oracle_sample(q, k, v, d_o, budget_s: float, block_rows: int = 1024):
     scale = 1 / math.sqrt(D)
     t0 = time.perf_counter()
     blocks = 0
+    head = 0
     while True:
         r0 = (blocks * block_rows) % N
-        A.backward(w(q[0:1, r0:r0 + block_rows], "bf16"), kb, vb, w(d_o[0:1, r0:r0 + block_rows], "bf16"), scale)
+        if blocks and r0 == 0:  # next head once a head's query rows are all done
+            head = (head + 1) % BH
+            kb, vb = w(k[head:head + 1], "bf16"), w(v[head:head + 1], "bf16")
+        A.backward(w(q[head:head + 1, r0:r0 + block_rows], "bf16"), kb, vb,
+                   w(d_o[head:head + 1, r0:r0 + block_rows], "bf16"), scale)
         blocks += 1
-        if time.perf_counter() - t0 >= budget_s or blocks * block_rows >= N:
+        if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
     flops = 3.5 * 4.0 * blocks * block_rows * N * D
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-            "sample": f"{blocks} block(s) of {block_rows} query rows x {N} keys of one head, HEAD_DIM {D}: "
+            "sample": f"{blocks} block(s) of {block_rows} query rows x {N} keys (HEAD_DIM {D}, {head + 1} head(s)): "
                       f"forward+backward in float64 numpy ({dt:.1f} s); FLOPs counted as for the GPU step"}
 
 
@@ -441,13 +461,15 @@ def psa_bandwidth(torch, B, dev, pk):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--bh", type=int, default=32, help="attention batch*heads (32 = B=2 H=16, the headline workload)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
+    set_heads(args.bh)
     return run_reference(args) if args.impl == "reference" else run_ours(args)
 
 
