@@ -27,6 +27,7 @@ EXPORTS = (
     "fa2_backward_preprocess",
     "fa2_backward_dkdv",
     "fa2_backward_dq",
+    "fa2_backward_noalloc",
     "psa_pack_qkv",
     "psa_merge_attn_nchw",
     "fa2_device_status",
@@ -60,6 +61,7 @@ def _declare(lib):
                                                            _f32, _c_ptr]),
         "fa2_backward_dq": (ctypes.c_int, [_c_ptr] * 5 + [ctypes.c_size_t, _c_ptr, _i64, _i64, _i64, _i32, _i32, _f32,
                                                          _c_ptr]),
+        "fa2_backward_noalloc": (ctypes.c_int, [_c_ptr] * 9 + [_i64, _i64, _i64, _i32, _i32, _f32, _c_ptr]),
         "psa_pack_qkv": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "psa_merge_attn_nchw": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "fa2_device_status": (ctypes.c_int, [_c_ptr]),
@@ -84,7 +86,7 @@ def library(path: str | None = None):
 
 
 _MESSAGES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned pointer",
-             4: "CUDA error", 5: "device wait timed out", 6: "bad workspace"}
+             4: "CUDA error", 5: "device wait timed out", 6: "bad workspace", 7: "too large for the fixed scratch"}
 
 
 def fa2_status_string(status: int) -> str:
@@ -157,6 +159,21 @@ def fa2_backward(q, k, v, o, d_o, lse, dq, dk, dv, workspace, softmax_scale: flo
                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                                 bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
     _check(st, "fa2_backward")
+
+
+def fa2_backward_noalloc(q, k, v, o, d_o, lse, dq, dk, dv, softmax_scale: float, stream=None) -> None:
+    """fa2_backward for callers that cannot allocate device memory: the workspace is the
+    library's fixed device scratch (shared by all calls; overlapping calls race)."""
+    bh, n_q, d = q.shape
+    n_k = k.shape[1]
+    if (k.shape != (bh, n_k, d) or v.shape != k.shape or o.shape != q.shape or d_o.shape != q.shape
+            or lse.shape != (bh, n_q) or dq.shape != q.shape or dk.shape != k.shape or dv.shape != k.shape):
+        raise ValueError("inconsistent shapes")
+    st = library().fa2_backward_noalloc(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(o, "o", 3),
+                                        _dev(d_o, "d_o", 3), _dev(lse, "lse", 2), _dev(dq, "dq", 3),
+                                        _dev(dk, "dk", 3), _dev(dv, "dv", 3), bh, n_q, n_k, d, _dtype_code(q),
+                                        float(softmax_scale), _stream(stream))
+    _check(st, "fa2_backward_noalloc")
 
 
 def _bwd_sizes(q, k, workspace):

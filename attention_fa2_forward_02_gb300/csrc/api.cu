@@ -235,6 +235,7 @@ const char* fa2_status_string(fa2_status s) {
         case FA2_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
         case FA2_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (watchdog)";
         case FA2_ERR_WORKSPACE: return "workspace missing, misaligned or smaller than fa2_backward_workspace_size";
+        case FA2_ERR_SCRATCH_LIMIT: return "problem too large for fa2_backward_noalloc's fixed 8 MiB scratch";
         default: return "unknown status";
     }
 }

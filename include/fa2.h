@@ -39,7 +39,8 @@ typedef enum {
     FA2_ERR_MISALIGNED = 3,      /* a base pointer not 16-byte aligned */
     FA2_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed */
     FA2_ERR_DEVICE_TIMEOUT = 5,  /* a kernel gave up a bounded wait (reported by fa2_device_status) */
-    FA2_ERR_WORKSPACE = 6        /* workspace pointer null/misaligned or smaller than required */
+    FA2_ERR_WORKSPACE = 6,       /* workspace pointer null/misaligned or smaller than required */
+    FA2_ERR_SCRATCH_LIMIT = 7    /* the problem needs more than fa2_backward_noalloc's fixed scratch */
 } fa2_status;
 
 typedef enum {
@@ -138,6 +139,32 @@ fa2_status fa2_backward_dkdv(const void* q, const void* k, const void* v, const 
 fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
                            size_t workspace_bytes, void* dq, int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
                            fa2_dtype dtype, float softmax_scale, void* stream);
+
+/*
+ * fa2_backward_noalloc - fa2_backward without a caller-supplied workspace and
+ * without allocating any device memory.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory at call time - code whose device memory belongs
+ * to a host framework's pool (a raw cudaMalloc would bypass its accounting) and
+ * services that fix their memory budget at start-up and must not allocate, or
+ * risk running out of memory, while serving.  Arguments and results are those
+ * of fa2_backward minus the workspace; the caller still passes every input and
+ * output.  The workspace comes from one fixed 8 MiB device array inside the
+ * library (reserved on each GPU that loads the library until the process
+ * exits), which covers bh * ceil(n_q / 128) * 128 <= 1,048,576 query rows;
+ * larger problems return FA2_ERR_SCRATCH_LIMIT and launch nothing.
+ * The first call on a device looks up that array's device address, with the
+ * device current; make that first call before any stream capture.  All calls
+ * share the array, so calls whose GPU work overlaps (several streams or host
+ * threads on one device) race on it: serialise them.  Nothing in it needs to
+ * start at zero; each call rewrites what it reads.
+ * Errors: those of fa2_backward (except FA2_ERR_WORKSPACE), FA2_ERR_SCRATCH_LIMIT.
+ */
+fa2_status fa2_backward_noalloc(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                                const float* lse, void* dq, void* dk, void* dv,
+                                int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
+                                fa2_dtype dtype, float softmax_scale, void* stream);
 
 /*
  * psa_pack_qkv - NCHW QKV to the packed [4, B*num_heads, H*W, KEY_DIM] buffer.

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for s in range(7):
+    for s in range(8):
         msg = lib.fa2_status_string(s).decode()
         assert msg and msg != "unknown status"
     assert lib.fa2_status_string(99).decode() == "unknown status"

@@ -1,0 +1,76 @@
+"""fa2_backward_noalloc: the backward for callers that cannot allocate device memory.
+
+Such callers (code whose device memory belongs to a host framework's pool, or a
+service with a memory budget fixed at start-up) cannot hand fa2_backward a
+workspace; this entry point takes it from the library's fixed device scratch
+instead.  The test calls it through the C ABI twice in a row, on two different
+problems, and checks each result against fa2_backward with a caller-owned
+workspace, within the parity bar the other GPU tests use.  It also checks that
+a problem needing more than the fixed scratch is refused without a launch.
+
+The file name makes pytest collect it last.
+"""
+import ctypes
+import math
+
+import pytest
+
+from attention_fa2_forward_02_gb300 import binding, synth
+from tests import gpu_util as G
+from tests.tolerance import check_16bit
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_LIMIT = 7
+
+
+def _problem(tag, bh, n_q, n_k, d, dtype):
+    torch = G.require_gpu()
+    q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
+    d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)
+    qd, kd, vd, dod = (G.to_device(x, dtype) for x in (q, k, v, d_o))
+    scale = 1 / math.sqrt(d)
+    o = G.empty((bh, n_q, d), dtype)
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    return qd, kd, vd, o, dod, lse, scale
+
+
+def _with_workspace(qd, kd, vd, o, dod, lse, scale):
+    torch = G.require_gpu()
+    bh, n_q, d = qd.shape
+    code = binding.DTYPE_BF16 if qd.dtype == torch.bfloat16 else binding.DTYPE_F16
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, kd.shape[1], d, code), dtype=torch.uint8,
+                     device="cuda")
+    grads = [torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)]
+    binding.fa2_backward(qd, kd, vd, o, dod, lse, *grads, ws, scale)
+    return grads
+
+
+def test_noalloc_matches_backward_on_two_calls_in_a_row():
+    torch = G.require_gpu()
+    problems = [("noalloc/a", 3, 700, 520, 128, "bf16"), ("noalloc/b", 2, 129, 300, 64, "f16")]
+    results = []
+    for tag, bh, n_q, n_k, d, dtype in problems:
+        args = _problem(tag, bh, n_q, n_k, d, dtype)
+        got = [torch.empty_like(args[0]), torch.empty_like(args[1]), torch.empty_like(args[2])]
+        binding.fa2_backward_noalloc(*args[:6], *got, args[6])
+        results.append((args, got))
+    binding.fa2_device_status()
+    for args, got in results:
+        want = _with_workspace(*args)
+        torch.cuda.synchronize()
+        for name, a, b in zip(("dQ", "dK", "dV"), got, want):
+            check_16bit(G.to_f64(a), G.to_f64(b), f"fa2_backward_noalloc {name}")
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch():
+    torch = G.require_gpu()
+    t = torch.empty((1, 128, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 128), dtype=torch.float32, device="cuda")
+    p = ctypes.c_void_p(t.data_ptr())
+    # 64 heads x 32768 query rows need 16 MiB of workspace: refused before anything is launched
+    st = binding.library().fa2_backward_noalloc(p, p, p, p, p, ctypes.c_void_p(lse.data_ptr()), p, p, p,
+                                                64, 32768, 128, 128, binding.DTYPE_BF16, 0.088, None)
+    assert st == SCRATCH_LIMIT
+    binding.fa2_device_status()
