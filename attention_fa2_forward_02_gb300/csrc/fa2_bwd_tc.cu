@@ -14,10 +14,12 @@
 //      dV += P^T dO, dK += dS^T Q;
 //   3. dQ: one CTA per 128-query tile, looping over 128-key tiles:
 //      S = Q K^T, dP = dO V^T, dS elementwise, dQ += dS K.
+// In both passes the elementwise work is split in two steps with their own
+// barriers so that it overlaps the tensor core (see the MMA orders below).
 // The 16-bit P^T / dS^T / dS are written back into tensor memory over the
 // score columns they came from and consumed from there by the next MMA.
-// Warp roles (192 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue,
-// warps 2-5 elementwise (one thread per TMEM lane).
+// Warp roles (320 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue,
+// warps 2-9 elementwise (two warps per TMEM lane quarter).
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,7 +27,13 @@ namespace fa2 {
 namespace {
 
 constexpr int BT = 128;         // rows of every tile (keys or queries)
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 elementwise
+constexpr int kElemThreads = 256;
+// The 16-bit probabilities / dS of a 128-column fp32 score tile occupy 64 columns
+// starting at column 32 of that tile: the warp owning score columns [0, 64)
+// writes [32, 64) and the one owning [64, 128) writes [64, 96), so each warp only
+// overwrites columns it has itself already read.
+constexpr uint32_t kPackedCol = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -78,30 +86,38 @@ struct BwdCfg : Tile16<D> {
     static constexpr int kTile = BT * D * 2;
     // dK/dV kernel: K, V resident; per stage Q_i, dO_i, lse2_i, delta_i
     static constexpr int kStageDkv = 2 * kTile + 2 * BT * 4;
-    static constexpr int kDkvStages = kStages;
-    static constexpr int kDkvBar = 2 * kTile + kDkvStages * kStageDkv;
+    static constexpr int kDkvBar = 2 * kTile + kStages * kStageDkv;
     // dQ kernel: Q, dO resident; per stage K_j, V_j
     static constexpr int kStageDq = 2 * kTile;
     static constexpr int kDqBar = 2 * kTile + kStages * kStageDq;
-    static constexpr int kNumBars = 3 + 2 * kStages + 2;
+    static constexpr int kNumBars = 1 + 2 * kStages + 5;
     static constexpr int kSmemDkv = kDkvBar + kNumBars * 8 + 16 + 1024;
     static constexpr int kSmemDq = kDqBar + kNumBars * 8 + 16 + 1024;
     static_assert(kSmemDkv <= 227 * 1024 && kSmemDq <= 227 * 1024, "shared memory budget");
     static_assert(kStageDkv % 1024 == 0, "stage alignment");
 };
 
-// Barrier block layout shared by both kernels:
-//   0 resident tiles full, 1..S stage full, S+1..2S stage empty, 2S+1 scores done,
-//   2S+2 elementwise done, 2S+3 all MMAs done
+// Barriers shared by both kernels:
+//   resident  the tiles loaded once per CTA          (TMA transaction count)
+//   full[s]   stage s loaded                         (TMA transaction count)
+//   empty[s]  stage s no longer read by any MMA      (tcgen05.commit)
+//   s_full    the first score tile (S^T or S) is in TMEM   (tcgen05.commit)
+//   dp_full   the second score tile (dP^T or dP) is in TMEM (tcgen05.commit)
+//   e1        elementwise step 1 done: dK/dV pass - P^T is in TMEM;
+//             dQ pass - S has been read (256 arrivals)
+//   e2        elementwise step 2 done: dS^T / dS is in TMEM (256 arrivals)
+//   done      every MMA issued has completed (tcgen05.commit)
 struct Bars {
     uint32_t base;
     int S;
     __device__ uint32_t resident() const { return base; }
     __device__ uint32_t full(int s) const { return base + 8u * (1 + s); }
     __device__ uint32_t empty(int s) const { return base + 8u * (1 + S + s); }
-    __device__ uint32_t scores() const { return base + 8u * (1 + 2 * S); }
-    __device__ uint32_t elem() const { return base + 8u * (2 + 2 * S); }
-    __device__ uint32_t done() const { return base + 8u * (3 + 2 * S); }
+    __device__ uint32_t s_full() const { return base + 8u * (1 + 2 * S); }
+    __device__ uint32_t dp_full() const { return base + 8u * (2 + 2 * S); }
+    __device__ uint32_t e1() const { return base + 8u * (3 + 2 * S); }
+    __device__ uint32_t e2() const { return base + 8u * (4 + 2 * S); }
+    __device__ uint32_t done() const { return base + 8u * (5 + 2 * S); }
 };
 
 __device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_flag) {
@@ -111,8 +127,10 @@ __device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_fla
         mbar_init(b.full(s), 1);
         mbar_init(b.empty(s), 1);
     }
-    mbar_init(b.scores(), 1);
-    mbar_init(b.elem(), BT);
+    mbar_init(b.s_full(), 1);
+    mbar_init(b.dp_full(), 1);
+    mbar_init(b.e1(), kElemThreads);
+    mbar_init(b.e2(), kElemThreads);
     mbar_init(b.done(), 1);
     fence_barrier_init();
 }
@@ -130,7 +148,18 @@ __device__ __forceinline__ void store_row_chunk(void* base, size_t row, int D, i
     }
 }
 
+// The two 32-column chunks an elementwise warp owns, in the order that lets it
+// write 16-bit results at kPackedCol without overwriting a column it has not read.
+__device__ __forceinline__ int owned_chunk(int half, int cc) { return 2 * half + (half == 0 ? 1 - cc : cc); }
+
 // ------------------------------------------------------------------------------ dK / dV
+//
+// MMA order per query tile i (one thread issues, the tensor core executes in order):
+//   S^T(i) -> s_full, dP^T(i) -> dp_full, [e1(i)] dV += P^T(i) dO(i),
+//   S^T(i+1) -> s_full, [e2(i)] dK += dS^T(i) Q(i) -> empty, dP^T(i+1) -> dp_full, ...
+// so P^T(i) is computed while dP^T(i) runs, dS^T(i) while dV(i) and S^T(i+1) run.
+// S^T(i+1) overwrites the columns holding P^T(i) only after dV(i), which reads
+// them, was issued; dP^T(i+1) likewise follows dK(i).
 
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -140,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     void* __restrict__ dv, int n_q, int n_k, int n_q_pad, float scale, float scale_log2,
                     unsigned int* status) {
     using C = BwdCfg<D>;
-    constexpr int S = C::kDkvStages;
+    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -205,89 +234,140 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
             const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
-            bool ok = mbar_wait(bars.resident(), 0, wd);
-            for (int i = 0; ok && i < n_qt; ++i) {
-                const int s = i % S;
-                if (!(ok = mbar_wait(bars.full(s), (i / S) & 1, wd))) break;
-                tc_fence_after();
+            auto issue_st = [&](int s) {  // S^T = K Q^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem, C::kmajor(k_smem, kk, BT), C::kmajor(stage_q(s), kk, BT), idesc_s, kk > 0);
+            };
+            auto issue_dpt = [&](int s) {  // dP^T = V dO^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 128u, C::kmajor(v_smem, kk, BT), C::kmajor(stage_do(s), kk, BT), idesc_s, kk > 0);
-                mma_commit(bars.scores());
-                if (!(ok = mbar_wait(bars.elem(), i & 1, wd))) break;
+            };
+            bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
+            if (ok) {
+                tc_fence_after();
+                issue_st(0);
+                mma_commit(bars.s_full());
+                issue_dpt(0);
+                mma_commit(bars.dp_full());
+            }
+            for (int i = 0; ok && i < n_qt; ++i) {
+                const int s = i % S;
+                const int sn = (i + 1) % S;
+                const bool more = i + 1 < n_qt;
+                if (!(ok = mbar_wait(bars.e1(), i & 1, wd))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk)
-                    mma_ts(tmem + 256u, tmem + (uint32_t)(kk * 8), C::mnmajor(stage_do(s), kk, BT), idesc_g, (i > 0 || kk > 0));
-#pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk)
-                    mma_ts(tmem + 256u + D, tmem + 128u + (uint32_t)(kk * 8), C::mnmajor(stage_q(s), kk, BT), idesc_g,
+                for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
+                    mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_do(s), kk, BT), idesc_g,
                            (i > 0 || kk > 0));
+                if (more) {
+                    if (!(ok = mbar_wait(bars.full(sn), ((i + 1) / S) & 1, wd))) break;
+                    tc_fence_after();
+                    issue_st(sn);
+                    mma_commit(bars.s_full());
+                }
+                if (!(ok = mbar_wait(bars.e2(), i & 1, wd))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
+                    mma_ts(tmem + 256u + D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_q(s), kk, BT),
+                           idesc_g, (i > 0 || kk > 0));
                 mma_commit(bars.empty(s));
+                if (more) {
+                    issue_dpt(sn);
+                    mma_commit(bars.dp_full());
+                }
             }
             mma_commit(bars.done());
             drain_wait(bars.done(), 0);
         }
     } else {
+        // Two warps per TMEM lane quarter; warp `half` owns query columns [64*half, 64*half + 64).
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
+        const float2 scale2 = make_float2(scale_log2, scale_log2);
         bool ok = true;
         for (int i = 0; i < n_qt; ++i) {
             const int s = i % S;
-            if (!(ok = warp_wait(bars.scores(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) break;
+            if (!(ok = warp_wait(bars.s_full(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) break;
             tc_fence_after();
             const float* l2 = reinterpret_cast<const float*>(smem + (stage_l2(s) - base));
             const float* dl = reinterpret_cast<const float*>(smem + (stage_dl(s) - base));
-#pragma unroll
-            for (int c = 0; c < BT / 32; ++c) {
-                uint32_t rs[32], rp[32];
-                tmem_ld32(t_s + 32u * c, rs);
-                tmem_ld32(t_dp + 32u * c, rp);
+            // step 1: P^T = 2^(S^T * scale * log2e - LSE2) for both owned chunks
+            float2 p[2][16];
+            {
+                uint32_t ra[32], rb[32];
+                tmem_ld32(t_s + 32u * owned_chunk(half, 0), ra);
+                tmem_ld32(t_s + 32u * owned_chunk(half, 1), rb);
                 tmem_ld_wait();
-                reg_fence(rs);
-                reg_fence(rp);
-                uint32_t pk_p[16], pk_ds[16];
+                reg_fence(ra);
+                reg_fence(rb);
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const int col = 32 * c + 2 * x;
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(rs[2 * x]), scale_log2, -l2[col]));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(rs[2 * x + 1]), scale_log2, -l2[col + 1]));
-                    const float d0 = p0 * (__uint_as_float(rp[2 * x]) - dl[col]);
-                    const float d1 = p1 * (__uint_as_float(rp[2 * x + 1]) - dl[col + 1]);
-                    pk_p[x] = pack2<kBf16>(p0, p1);
-                    pk_ds[x] = pack2<kBf16>(d0, d1);
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = owned_chunk(half, cc);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const uint32_t* r = cc == 0 ? ra : rb;
+                        const float2 lse = *reinterpret_cast<const float2*>(l2 + 32 * c + 2 * x);
+                        float2 v = __ffma2_rn(make_float2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])),
+                                              scale2, make_float2(-lse.x, -lse.y));
+                        v.x = ex2_approx(v.x);
+                        v.y = ex2_approx(v.y);
+                        p[cc][x] = v;
+                        pk[x] = pack2<kBf16>(v.x, v.y);
+                    }
+                    tmem_st16(t_s + kPackedCol + 16u * c, pk);
                 }
-                tmem_st16(t_s + 16u * c, pk_p);
-                tmem_st16(t_dp + 16u * c, pk_ds);
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bars.elem());
+            mbar_arrive(bars.e1());
+            // step 2: dS^T = P^T * (dP^T - D), chunk by chunk in write-safe order
+            if (!(ok = warp_wait(bars.dp_full(), i & 1, wd))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = owned_chunk(half, cc);
+                uint32_t rp[32];
+                tmem_ld32(t_dp + 32u * c, rp);
+                tmem_ld_wait();
+                reg_fence(rp);
+                uint32_t pk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const float2 dd = *reinterpret_cast<const float2*>(dl + 32 * c + 2 * x);
+                    const float2 ds = __fmul2_rn(p[cc][x], __fadd2_rn(make_float2(__uint_as_float(rp[2 * x]),
+                                                                                  __uint_as_float(rp[2 * x + 1])),
+                                                                      make_float2(-dd.x, -dd.y)));
+                    pk[x] = pack2<kBf16>(ds.x, ds.y);
+                }
+                tmem_st16(t_dp + kPackedCol + 16u * c, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bars.e2());
         }
         if (ok) ok = warp_wait(bars.done(), 0, wd);
         if (ok) {
             tc_fence_after();
             const int key = k0 + quarter * 32 + lane;
             const size_t row = (size_t)bh * n_k + key;
+            // half 0 writes dV, half 1 writes dK (scaled)
+            const uint32_t src = tmem + lane_off + 256u + (half ? (uint32_t)D : 0u);
+            void* dst = half ? dk : dv;
+            const float mul = half ? scale : 1.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + lane_off + 256u + 32u * c, r);
+                tmem_ld32(src + 32u * c, r);
                 tmem_ld_wait();
                 reg_fence(r);
-                store_row_chunk<kBf16>(dv, row, D, c, r, 1.f, key < n_k);
-            }
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + lane_off + 256u + D + 32u * c, r);
-                tmem_ld_wait();
-                reg_fence(r);
-                store_row_chunk<kBf16>(dk, row, D, c, r, scale, key < n_k);
+                store_row_chunk<kBf16>(dst, row, D, c, r, mul, key < n_k);
             }
         }
     }
@@ -301,6 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------ dQ
+//
+// MMA order per key tile j:
+//   S(j) -> s_full, dP(j) -> dp_full, [e1(j): S(j) read] S(j+1) -> s_full,
+//   [e2(j)] dQ += dS(j) K(j) -> empty, dP(j+1) -> dp_full, ...
+// dS lives in the dP columns, so dP(j+1) follows dQ(j); the S columns hold only
+// scores, so S(j+1) needs nothing but the elementwise warps having read S(j).
 
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -369,73 +455,123 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
             const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
-            bool ok = mbar_wait(bars.resident(), 0, wd);
-            for (int j = 0; ok && j < n_kt; ++j) {
-                const int s = j % S;
-                if (!(ok = mbar_wait(bars.full(s), (j / S) & 1, wd))) break;
-                tc_fence_after();
+            auto issue_s = [&](int s) {  // S = Q K^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem, C::kmajor(q_smem, kk, BT), C::kmajor(stage_k(s), kk, BT), idesc_s, kk > 0);
+            };
+            auto issue_dp = [&](int s) {  // dP = dO V^T
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem + 128u, C::kmajor(do_smem, kk, BT), C::kmajor(stage_v(s), kk, BT), idesc_s, kk > 0);
-                mma_commit(bars.scores());
-                if (!(ok = mbar_wait(bars.elem(), j & 1, wd))) break;
+            };
+            bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+                mma_commit(bars.s_full());
+                issue_dp(0);
+                mma_commit(bars.dp_full());
+            }
+            for (int j = 0; ok && j < n_kt; ++j) {
+                const int s = j % S;
+                const int sn = (j + 1) % S;
+                const bool more = j + 1 < n_kt;
+                if (more) {
+                    if (!(ok = mbar_wait(bars.e1(), j & 1, wd) && mbar_wait(bars.full(sn), ((j + 1) / S) & 1, wd))) break;
+                    tc_fence_after();
+                    issue_s(sn);
+                    mma_commit(bars.s_full());
+                }
+                if (!(ok = mbar_wait(bars.e2(), j & 1, wd))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk)
-                    mma_ts(tmem + 256u, tmem + 128u + (uint32_t)(kk * 8), C::mnmajor(stage_k(s), kk, BT), idesc_g,
-                           (j > 0 || kk > 0));
+                for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
+                    mma_ts(tmem + 256u, tmem + 128u + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_k(s), kk, BT),
+                           idesc_g, (j > 0 || kk > 0));
                 mma_commit(bars.empty(s));
+                if (more) {
+                    issue_dp(sn);
+                    mma_commit(bars.dp_full());
+                }
             }
             mma_commit(bars.done());
             drain_wait(bars.done(), 0);
         }
     } else {
+        // Two warps per TMEM lane quarter; warp `half` owns key columns [64*half, 64*half + 64).
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
         const int row = q0 + quarter * 32 + lane;
         const size_t w = (size_t)bh * n_q_pad + row;  // row < n_q_pad always
         const float my_l2 = lse2[w];
         const float my_d = delta[w];
+        const float2 scale2 = make_float2(scale_log2, scale_log2);
+        const float2 neg_l2 = make_float2(-my_l2, -my_l2), neg_d = make_float2(-my_d, -my_d);
         bool ok = true;
         for (int j = 0; j < n_kt; ++j) {
-            if (!(ok = warp_wait(bars.scores(), j & 1, wd))) break;
+            if (!(ok = warp_wait(bars.s_full(), j & 1, wd))) break;
             tc_fence_after();
             const int valid = n_k - j * BT;
+            // step 1: P = 2^(S * scale * log2e - LSE2) in registers; then S may be overwritten
+            float2 p[2][16];
+            {
+                uint32_t ra[32], rb[32];
+                tmem_ld32(t_s + 32u * owned_chunk(half, 0), ra);
+                tmem_ld32(t_s + 32u * owned_chunk(half, 1), rb);
+                tmem_ld_wait();
+                reg_fence(ra);
+                reg_fence(rb);
+                tc_fence_before();
+                mbar_arrive(bars.e1());
 #pragma unroll
-            for (int c = 0; c < BT / 32; ++c) {
-                uint32_t rs[32], rp[32];
-                tmem_ld32(t_s + 32u * c, rs);
+                for (int cc = 0; cc < 2; ++cc) {
+                    const uint32_t* r = cc == 0 ? ra : rb;
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        float2 v = __ffma2_rn(make_float2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])), scale2,
+                                              neg_l2);
+                        v.x = ex2_approx(v.x);
+                        v.y = ex2_approx(v.y);
+                        p[cc][x] = v;
+                    }
+                }
+            }
+            // step 2: dS = P * (dP - D), zero past the last key, chunk by chunk in write-safe order
+            if (!(ok = warp_wait(bars.dp_full(), j & 1, wd))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = owned_chunk(half, cc);
+                uint32_t rp[32];
                 tmem_ld32(t_dp + 32u * c, rp);
                 tmem_ld_wait();
-                reg_fence(rs);
                 reg_fence(rp);
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
                     const int col = 32 * c + 2 * x;
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(rs[2 * x]), scale_log2, -my_l2));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(rs[2 * x + 1]), scale_log2, -my_l2));
-                    float d0 = p0 * (__uint_as_float(rp[2 * x]) - my_d);
-                    float d1 = p1 * (__uint_as_float(rp[2 * x + 1]) - my_d);
-                    if (col >= valid) d0 = 0.f;
-                    if (col + 1 >= valid) d1 = 0.f;
-                    pk[x] = pack2<kBf16>(d0, d1);
+                    float2 ds = __fmul2_rn(
+                        p[cc][x], __fadd2_rn(make_float2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), neg_d));
+                    if (col >= valid) ds.x = 0.f;
+                    if (col + 1 >= valid) ds.y = 0.f;
+                    pk[x] = pack2<kBf16>(ds.x, ds.y);
                 }
-                tmem_st16(t_dp + 16u * c, pk);
+                tmem_st16(t_dp + kPackedCol + 16u * c, pk);
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bars.elem());
+            mbar_arrive(bars.e2());
         }
         if (ok) ok = warp_wait(bars.done(), 0, wd);
         if (ok) {
             tc_fence_after();
+            // the two warps of a quarter split the dQ columns: 32-column chunks alternate
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
+                if ((c & 1) != half) continue;
                 uint32_t r[32];
                 tmem_ld32(tmem + lane_off + 256u + 32u * c, r);
                 tmem_ld_wait();

@@ -220,20 +220,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m2 = -INFINITY;  // reference maximum, base-2 units (score * scale * log2 e)
         float l = 0.f;
         bool ok = true;
+        const float2 scale2 = make_float2(scale_log2, scale_log2);
         for (int j = 0; j < n_kv; ++j) {
             if (!(ok = warp_wait(B_SF(t), j & 1, wd))) break;
             tc_fence_after();
-            float s[BN];
-            tmem_ld128(s_addr, s);
+            // Only the last key tile can be partial; its columns >= valid are masked to -inf.
             const int valid = n_k - j * BN;
-            if (valid < BN) {
+            const bool tail = valid < BN;
+            // Pass 1 over the score row: its maximum (8 independent chains).
+            float mx;
+            {
+                float m8[8];
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
-                    if (c >= valid) s[c] = -INFINITY;
+                for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t a[32], b[32];
+                    tmem_ld32(s_addr + 64u * h, a);
+                    tmem_ld32(s_addr + 64u * h + 32u, b);
+                    tmem_ld_wait();
+                    reg_fence(a);
+                    reg_fence(b);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x = __uint_as_float(a[i]), y = __uint_as_float(b[i]);
+                        if (tail) {
+                            if (64 * h + i >= valid) x = -INFINITY;
+                            if (64 * h + 32 + i >= valid) y = -INFINITY;
+                        }
+                        m8[i & 7] = fmaxf(m8[i & 7], fmaxf(x, y));
+                    }
+                }
+                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
             const float m_new = mx * scale_log2;
             if (j == 0) {
                 m2 = m_new;
@@ -258,20 +277,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st_wait();
                 }
             }
-            float rs = 0.f;
+            // Pass 2: p = 2^(s*scale*log2e - m2) per 32-column chunk (the next chunk's
+            // load in flight meanwhile), row sum in four partial sums, P packed to
+            // 16 bits and stored over the score columns already consumed.
+            {
+                const float2 negm2 = make_float2(-m2, -m2);
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+                uint32_t cur[32], nxt[32];
+                tmem_ld32(s_addr, cur);
+                tmem_ld_wait();
+                reg_fence(cur);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pk[32];
+                for (int c = 0; c < BN / 32; ++c) {
+                    if (c + 1 < BN / 32) tmem_ld32(s_addr + 32u * (c + 1), nxt);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * i], scale_log2, -m2));
-                    const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * i + 1], scale_log2, -m2));
-                    rs += p0 + p1;
-                    pk[i] = pack2<kBf16>(p0, p1);
+                    for (int i = 0; i < 16; ++i) {
+                        float2 x = make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
+                        if (tail) {
+                            if (32 * c + 2 * i >= valid) x.x = -INFINITY;
+                            if (32 * c + 2 * i + 1 >= valid) x.y = -INFINITY;
+                        }
+                        float2 y = __ffma2_rn(x, scale2, negm2);
+                        y.x = ex2_approx(y.x);
+                        y.y = ex2_approx(y.y);
+                        if (i & 1) acc1 = __fadd2_rn(acc1, y);
+                        else acc0 = __fadd2_rn(acc0, y);
+                        pk[i] = pack2<kBf16>(y.x, y.y);
+                    }
+                    tmem_st16(s_addr + 16u * c, pk);
+                    if (c + 1 < BN / 32) {
+                        tmem_ld_wait();
+                        reg_fence(nxt);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
+                    }
                 }
-                tmem_st32(s_addr + 32u * h, pk);
+                l += (acc0.x + acc1.x) + (acc0.y + acc1.y);
             }
-            l += rs;
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(B_PF(t));
