@@ -30,7 +30,13 @@ EXPORTS = (
     "fa2_backward_noalloc",
     "psa_pack_qkv",
     "psa_merge_attn_nchw",
+    "psa_fa2_forward",
+    "psa_extract_v_nchw",
+    "psa_pack_qkv_backward",
+    "psa_merge_attn_backward",
+    "psa_extract_v_backward",
     "fa2_device_status",
+    "fa2_watchdog_selftest",
     "fa2_status_string",
 )
 
@@ -64,7 +70,13 @@ def _declare(lib):
         "fa2_backward_noalloc": (ctypes.c_int, [_c_ptr] * 9 + [_i64, _i64, _i64, _i32, _i32, _f32, _c_ptr]),
         "psa_pack_qkv": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "psa_merge_attn_nchw": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
+        "psa_fa2_forward": (ctypes.c_int, [_c_ptr] * 4 + [_i64, _i64, _i32, _i32, _f32, _c_ptr]),
+        "psa_extract_v_nchw": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 7 + [_c_ptr]),
+        "psa_pack_qkv_backward": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
+        "psa_merge_attn_backward": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
+        "psa_extract_v_backward": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 7 + [_c_ptr]),
         "fa2_device_status": (ctypes.c_int, [_c_ptr]),
+        "fa2_watchdog_selftest": (ctypes.c_int, [_c_ptr]),
         "fa2_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -228,6 +240,63 @@ def psa_merge_attn_nchw(lo, hi, out, num_heads: int, stream=None) -> None:
     _check(st, "psa_merge_attn_nchw")
 
 
+def psa_fa2_forward(packed, o_lo, o_hi, lse, softmax_scale: float, stream=None) -> None:
+    """packed [4, BH, N, KD] -> O_lo, O_hi [BH, N, KD] and the shared LSE [BH, N] in one pass."""
+    import torch
+    _, bh, n, kd = packed.shape
+    if o_lo.shape != (bh, n, kd) or o_hi.shape != o_lo.shape or lse.shape != (bh, n) or lse.dtype != torch.float32:
+        raise ValueError("o_lo / o_hi are [BH, N, KD]; lse is float32 [BH, N]")
+    st = library().psa_fa2_forward(_dev(packed, "packed", 4), _dev(o_lo, "o_lo", 3), _dev(o_hi, "o_hi", 3),
+                                   _dev(lse, "lse", 2), bh, n, kd, _dtype_code(packed), float(softmax_scale),
+                                   _stream(stream))
+    _check(st, "psa_fa2_forward")
+
+
+def psa_extract_v_nchw(qkv, v, num_heads: int, stream=None) -> None:
+    """qkv NCHW [B, qkv_h, H, W] -> v NCHW [B, qkv_h/2, H, W] (the V_lo / V_hi channels)."""
+    b, qkv_h, h, w = qkv.shape
+    if v.shape != (b, qkv_h // 2, h, w) or v.dtype != qkv.dtype:
+        raise ValueError("v must be [B, qkv_h/2, H, W] of qkv's dtype")
+    st = library().psa_extract_v_nchw(_dev(qkv, "qkv", 4), _dev(v, "v", 4), qkv_h, v.shape[1], h, w, b, num_heads,
+                                      _dtype_code(qkv), _stream(stream))
+    _check(st, "psa_extract_v_nchw")
+
+
+def psa_pack_qkv_backward(d_packed, d_qkv, num_heads: int, stream=None) -> None:
+    """d_packed [4, B*num_heads, H*W, KD] -> d_qkv NCHW [B, qkv_h, H, W] (every element written)."""
+    b, qkv_h, h, w = d_qkv.shape
+    if d_packed.numel() != d_qkv.numel() or d_packed.dtype != d_qkv.dtype:
+        raise ValueError("d_packed must hold as many elements as d_qkv, same dtype")
+    st = library().psa_pack_qkv_backward(_dev(d_packed, "d_packed"), _dev(d_qkv, "d_qkv", 4), qkv_h, h, w, b, num_heads,
+                                         _dtype_code(d_qkv), _stream(stream))
+    _check(st, "psa_pack_qkv_backward")
+
+
+def psa_merge_attn_backward(d_merged, d_lo, d_hi, num_heads: int, stream=None) -> None:
+    """d_merged NCHW [B, c, H, W] -> d_lo, d_hi [B*num_heads, H*W, c/(2*num_heads)]."""
+    b, c, h, w = d_merged.shape
+    if d_lo.shape != d_hi.shape or d_lo.numel() * 2 != d_merged.numel():
+        raise ValueError("d_lo and d_hi must together hold d_merged's elements")
+    st = library().psa_merge_attn_backward(_dev(d_merged, "d_merged", 4), _dev(d_lo, "d_lo"), _dev(d_hi, "d_hi"), c, h,
+                                           w, b, num_heads, _dtype_code(d_merged), _stream(stream))
+    _check(st, "psa_merge_attn_backward")
+
+
+def psa_extract_v_backward(d_v, d_qkv, num_heads: int, stream=None) -> None:
+    """d_qkv[:, V channels] += d_v (float32 add, one rounding to the storage dtype)."""
+    b, qkv_h, h, w = d_qkv.shape
+    if d_v.shape != (b, qkv_h // 2, h, w) or d_v.dtype != d_qkv.dtype:
+        raise ValueError("d_v must be [B, qkv_h/2, H, W] of d_qkv's dtype")
+    st = library().psa_extract_v_backward(_dev(d_v, "d_v", 4), _dev(d_qkv, "d_qkv", 4), qkv_h, d_v.shape[1], h, w, b,
+                                          num_heads, _dtype_code(d_qkv), _stream(stream))
+    _check(st, "psa_extract_v_backward")
+
+
 def fa2_device_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel gave up a bounded wait."""
     _check(library().fa2_device_status(_stream(stream)), "fa2_device_status")
+
+
+def fa2_watchdog_selftest(stream=None) -> None:
+    """Launch the bounded-wait self-test (a wait that gives up after about a second)."""
+    _check(library().fa2_watchdog_selftest(_stream(stream)), "fa2_watchdog_selftest")

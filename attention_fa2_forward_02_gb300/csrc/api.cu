@@ -85,6 +85,8 @@ bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, co
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool watchdog_word(unsigned int** out) { return status_word(out); }
+
 cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -114,6 +116,23 @@ fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, flo
     const cudaError_t e = dtype == FA2_DTYPE_F32 ? launch_fwd_f32(p, static_cast<cudaStream_t>(stream))
                                                  : launch_fwd_tc(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* lse, int64_t bh, int64_t n,
+                           int32_t key_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
+    if (!packed || !o_lo || !o_hi || !lse) return FA2_ERR_INVALID_ARG;
+    fa2_status st = check_attention_sizes(bh, n, n, key_dim, dtype, softmax_scale);
+    if (st != FA2_OK) return st;
+    if (dtype == FA2_DTYPE_F32 || key_dim == 128) return FA2_ERR_UNSUPPORTED;
+    if (!aligned16(packed) || !aligned16(o_lo) || !aligned16(o_hi) || !aligned16(lse)) return FA2_ERR_MISALIGNED;
+    // sections of the packed buffer, as FlashAttn2PsaRuntimeOp addresses them: base + s * BH * N * KEY_DIM
+    const size_t section = (size_t)bh * (size_t)n * (size_t)key_dim * 2;
+    const char* base = static_cast<const char*>(packed);
+    FwdParams p{base, base + section, base + 2 * section, o_lo, lse, bh, n, n, key_dim, (int)dtype, softmax_scale, nullptr};
+    p.v2 = base + 3 * section;
+    p.o2 = o_hi;
+    if (!status_word(&p.status)) return FA2_ERR_CUDA;
+    return launch_fwd_tc_dual_v(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
 size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype) {
@@ -213,6 +232,65 @@ fa2_status psa_merge_attn_nchw(const void* lo, const void* hi, void* out, int32_
     if (!aligned16(lo) || !aligned16(hi) || !aligned16(out)) return FA2_ERR_MISALIGNED;
     if (2LL * B * num_heads > kMaxGridY) return FA2_ERR_UNSUPPORTED;
     PsaParams p{lo, hi, out, 1, eb, B, num_heads, c / (2 * num_heads), (int64_t)H * W, 0, c};
+    return launch_psa(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+// Shared checks of the V extraction and the adjoints: sizes, channel counts
+// (qkv_h = num_heads * 4 * KD, c = num_heads * 2 * KD), alignment, grid limits.
+static fa2_status psa_checks(const void* const* ptrs, int nptrs, int32_t qkv_h, int32_t c, int32_t H, int32_t W,
+                             int32_t B, int32_t num_heads, fa2_dtype dtype, int* eb, int sections) {
+    for (int i = 0; i < nptrs; ++i)
+        if (!ptrs[i]) return FA2_ERR_INVALID_ARG;
+    fa2_status st = psa_common(H, W, B, num_heads, dtype, eb);
+    if (st != FA2_OK) return st;
+    if (qkv_h <= 0 || qkv_h % (4 * num_heads) != 0) return FA2_ERR_INVALID_ARG;
+    if (c >= 0 && c != qkv_h / 2) return FA2_ERR_INVALID_ARG;
+    for (int i = 0; i < nptrs; ++i)
+        if (!aligned16(ptrs[i])) return FA2_ERR_MISALIGNED;
+    if ((int64_t)sections * B * num_heads > kMaxGridY) return FA2_ERR_UNSUPPORTED;
+    return FA2_OK;
+}
+
+fa2_status psa_extract_v_nchw(const void* qkv, void* v, int32_t qkv_h, int32_t c, int32_t H, int32_t W, int32_t B,
+                              int32_t num_heads, fa2_dtype dtype, void* stream) {
+    const void* ptrs[] = {qkv, v};
+    int eb = 0;
+    fa2_status st = psa_checks(ptrs, 2, qkv_h, c, H, W, B, num_heads, dtype, &eb, 1);
+    if (st != FA2_OK) return st;
+    PsaParams p{qkv, nullptr, v, kPsaExtractV, eb, B, num_heads, qkv_h / (4 * num_heads), (int64_t)H * W, qkv_h, c};
+    return launch_psa(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+fa2_status psa_pack_qkv_backward(const void* d_packed, void* d_qkv, int32_t qkv_h, int32_t H, int32_t W, int32_t B,
+                                 int32_t num_heads, fa2_dtype dtype, void* stream) {
+    const void* ptrs[] = {d_packed, d_qkv};
+    int eb = 0;
+    fa2_status st = psa_checks(ptrs, 2, qkv_h, -1, H, W, B, num_heads, dtype, &eb, 4);
+    if (st != FA2_OK) return st;
+    PsaParams p{d_packed, nullptr, d_qkv, kPsaPackBwd, eb, B, num_heads, qkv_h / (4 * num_heads), (int64_t)H * W, qkv_h, 0};
+    return launch_psa(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+fa2_status psa_merge_attn_backward(const void* d_merged, void* d_lo, void* d_hi, int32_t c, int32_t H, int32_t W,
+                                   int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream) {
+    const void* ptrs[] = {d_merged, d_lo, d_hi};
+    int eb = 0;
+    if (c <= 0) return FA2_ERR_INVALID_ARG;
+    fa2_status st = psa_checks(ptrs, 3, 2 * c, c, H, W, B, num_heads, dtype, &eb, 2);
+    if (st != FA2_OK) return st;
+    PsaParams p{d_merged, nullptr, d_lo, kPsaMergeBwd, eb, B, num_heads, c / (2 * num_heads), (int64_t)H * W, 2 * c, c};
+    p.dst1 = d_hi;
+    return launch_psa(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+fa2_status psa_extract_v_backward(const void* d_v, void* d_qkv, int32_t qkv_h, int32_t c, int32_t H, int32_t W,
+                                  int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream) {
+    const void* ptrs[] = {d_v, d_qkv};
+    int eb = 0;
+    fa2_status st = psa_checks(ptrs, 2, qkv_h, c, H, W, B, num_heads, dtype, &eb, 1);
+    if (st != FA2_OK) return st;
+    PsaParams p{d_v, nullptr, d_qkv, kPsaExtractVBwd, eb, B, num_heads, qkv_h / (4 * num_heads), (int64_t)H * W, qkv_h, c};
+    p.dtype = (int)dtype;
     return launch_psa(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 

@@ -38,28 +38,32 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
 
-template <int D>
+// kNV = number of value tensors sharing the scores: 1 (plain attention) or 2
+// (the PSA V_lo / V_hi pair, whose probabilities are identical).
+template <int D, int kNV>
 struct FwdCfg : Tile16<D> {
     static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
     static constexpr int kQTileBytes = BM * D * 2;
     static constexpr int kKVTileBytes = BN * D * 2;
+    static constexpr int kVStageBytes = kNV * kKVTileBytes;
     static constexpr int kSmemQ = 0;
     static constexpr int kSmemK = kSmemQ + kQTiles * kQTileBytes;
     static constexpr int kSmemV = kSmemK + kStages * kKVTileBytes;
-    static constexpr int kSmemBar = kSmemV + kStages * kKVTileBytes;
+    static constexpr int kSmemBar = kSmemV + kStages * kVStageBytes;
     static constexpr int kNumBars = 1 + 4 * kStages + 2 + 2 + 1;
     static constexpr int kSmemMisc = kSmemBar + kNumBars * 8;
     static constexpr int kSmemBytes = kSmemMisc + 16 + 1024;  // + slack to align the base to 1024
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-    static_assert(256 + 2 * D <= (int)kTmemCols, "tensor memory budget");
+    static_assert(256 + 2 * kNV * D <= (int)kTmemCols, "tensor memory budget");
 };
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_ptr, float* __restrict__ lse_ptr,
-                      int n_q, int n_k, float scale_log2, unsigned int* status) {
-    using C = FwdCfg<D>;
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v2,
+                      void* __restrict__ o_ptr, void* __restrict__ o2_ptr, float* __restrict__ lse_ptr, int n_q, int n_k,
+                      float scale_log2, unsigned int* status) {
+    using C = FwdCfg<D, kNV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -120,6 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
+            if (kNV == 2) prefetch_tmap(&tm_v2);
             mbar_arrive_expect_tx(B_Q, kQTiles * C::kQTileBytes);
             for (int t = 0; t < kQTiles; ++t)
                 for (int a = 0; a < C::kAtoms; ++a)
@@ -139,10 +144,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     issued = 2 * j + 1;
                     break;
                 }
-                mbar_arrive_expect_tx(B_VF(s), C::kKVTileBytes);
-                for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_3d(v_smem + s * C::kKVTileBytes + a * BN * C::kAtomRowBytes, &tm_v, B_VF(s),
-                                a * C::kAtomCols, j * BN, bh);
+                mbar_arrive_expect_tx(B_VF(s), C::kVStageBytes);
+                for (int v = 0; v < kNV; ++v)
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_3d(v_smem + s * C::kVStageBytes + v * C::kKVTileBytes + a * BN * C::kAtomRowBytes,
+                                    v ? &tm_v2 : &tm_v, B_VF(s), a * C::kAtomCols, j * BN, bh);
                 issued = 2 * j + 2;
             }
             if (!ok) {
@@ -168,12 +174,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(d_tmem, C::kmajor(qa, kk, BM), C::kmajor(kb, kk, BN), idesc_s, kk > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int t, int s, bool acc) {
-                const uint32_t d_tmem = tmem + 256u + (uint32_t)(t * D);
-                const uint32_t vb = v_smem + s * C::kKVTileBytes;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
-                           (acc || kk > 0) ? 1u : 0u);
+                for (int v = 0; v < kNV; ++v) {
+                    const uint32_t d_tmem = tmem + 256u + (uint32_t)((t * kNV + v) * D);
+                    const uint32_t vb = v_smem + s * C::kVStageBytes + v * C::kKVTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
+                               (acc || kk > 0) ? 1u : 0u);
+                }
             };
             bool ok = mbar_wait(B_Q, 0, wd) && mbar_wait(B_KF(0), 0, wd);
             if (ok) {
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t s_addr = tmem + lane_off + (uint32_t)(t * BN);
-        const uint32_t o_addr = tmem + lane_off + 256u + (uint32_t)(t * D);
+        const uint32_t o_addr = tmem + lane_off + 256u + (uint32_t)(t * kNV * D);  // kNV accumulators of D columns
         float m2 = -INFINITY;  // reference maximum, base-2 units (score * scale * log2 e)
         float l = 0.f;
         bool ok = true;
@@ -265,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m2 = m_new;
                     }
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < kNV * D / 32; ++c) {
                         uint32_t r[32];
                         tmem_ld32(o_addr + 32u * c, r);
                         tmem_ld_wait();
@@ -324,21 +333,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int row = q0 + t * BM + quarter * 32 + lane;
             const float inv_l = 1.f / l;
-            uint16_t* orow = reinterpret_cast<uint16_t*>(o_ptr) + ((size_t)bh * n_q + row) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(o_addr + 32u * c, r);
-                tmem_ld_wait();
-                reg_fence(r);
-                uint32_t pk[16];
+            for (int v = 0; v < kNV; ++v) {
+                uint16_t* orow = reinterpret_cast<uint16_t*>(v ? o2_ptr : o_ptr) + ((size_t)bh * n_q + row) * D;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<kBf16>(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
-                if (row < n_q) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(o_addr + (uint32_t)(v * D) + 32u * c, r);
+                    tmem_ld_wait();
+                    reg_fence(r);
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack2<kBf16>(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+                    if (row < n_q) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+                            dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                    }
                 }
             }
             if (row < n_q) lse_ptr[(size_t)bh * n_q + row] = (m2 + lg2_approx(l)) * kLn2;
@@ -353,22 +366,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, int kNV>
 cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, kNV>;
     const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, tv2;
     if (!encode_tmap_3d(&tq, dt, 2, p.q, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BM, sw) ||
         !encode_tmap_3d(&tk, dt, 2, p.k, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw) ||
-        !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw))
+        !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw) ||
+        !encode_tmap_3d(&tv2, dt, 2, kNV == 2 ? p.v2 : p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw))
         return cudaErrorInvalidValue;
-    auto kern = fa2_fwd_tc_kernel<D, kBf16>;
+    auto kern = fa2_fwd_tc_kernel<D, kBf16, kNV>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((p.n_q + BM * kQTiles - 1) / (BM * kQTiles)), (unsigned)p.bh, 1);
     const float scale_log2 = p.scale * 1.4426950408889634f;
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p.o, p.lse, (int)p.n_q, (int)p.n_k, scale_log2, p.status);
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k, scale_log2,
+                                                    p.status);
     return cudaGetLastError();
 }
 
@@ -377,9 +392,18 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream) {
     const bool bf = p.dtype == kBf16;
     switch (p.d) {
-        case 32: return bf ? launch_impl<32, true>(p, stream, 0) : launch_impl<32, false>(p, stream, 1);
-        case 64: return bf ? launch_impl<64, true>(p, stream, 2) : launch_impl<64, false>(p, stream, 3);
-        case 128: return bf ? launch_impl<128, true>(p, stream, 4) : launch_impl<128, false>(p, stream, 5);
+        case 32: return bf ? launch_impl<32, true, 1>(p, stream, 0) : launch_impl<32, false, 1>(p, stream, 1);
+        case 64: return bf ? launch_impl<64, true, 1>(p, stream, 2) : launch_impl<64, false, 1>(p, stream, 3);
+        case 128: return bf ? launch_impl<128, true, 1>(p, stream, 4) : launch_impl<128, false, 1>(p, stream, 5);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_fwd_tc_dual_v(const FwdParams& p, cudaStream_t stream) {
+    const bool bf = p.dtype == kBf16;
+    switch (p.d) {
+        case 32: return bf ? launch_impl<32, true, 2>(p, stream, 6) : launch_impl<32, false, 2>(p, stream, 7);
+        case 64: return bf ? launch_impl<64, true, 2>(p, stream, 8) : launch_impl<64, false, 2>(p, stream, 9);
         default: return cudaErrorInvalidValue;
     }
 }

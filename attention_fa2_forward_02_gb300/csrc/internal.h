@@ -22,6 +22,8 @@ struct FwdParams {
     int dtype;
     float scale;
     unsigned int* status;  // device watchdog word
+    const void* v2 = nullptr;  // second value tensor (PSA V_hi) for launch_fwd_tc_dual_v
+    void* o2 = nullptr;        // its output
 };
 
 struct BwdParams {
@@ -44,20 +46,27 @@ struct BwdParams {
     unsigned int* status;
 };
 
-// One batched 2-D transpose: for z in [0, batches), dst block z ([cols, rows]
-// row-major) is the transpose of src block z ([rows, cols] row-major).  The
-// block base offsets (in elements) come from the psa map selected by `kind`.
+// The PSA rearrangements.  Pack / merge and their adjoints are batched 2-D
+// transposes (dst block z, [cols, rows] row-major, is the transpose of src block
+// z, [rows, cols] row-major) whose block offsets come from the map `kind`
+// selects; the V extraction and its adjoint copy / accumulate contiguous runs.
+enum PsaKind : int { kPsaPack = 0, kPsaMerge = 1, kPsaExtractV = 2, kPsaPackBwd = 3, kPsaMergeBwd = 4, kPsaExtractVBwd = 5 };
+
 struct PsaParams {
     const void* src0;
-    const void* src1;  // merge: hi (src0 = lo); pack: unused
+    const void* src1;  // merge: hi (src0 = lo); otherwise unused
     void* dst;
-    int kind;          // 0 = pack, 1 = merge
+    int kind;          // PsaKind
     int elem_bytes;    // 2 or 4
     int64_t B, nh, kd, n, qkv_h, c;
+    void* dst1 = nullptr;  // merge backward: d_hi (dst = d_lo)
+    int dtype = 0;         // Dtype, for the accumulating adjoint
 };
 
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream);
+// One pass over the scores applied to two value tensors (v, v2) with outputs (o, o2).
+cudaError_t launch_fwd_tc_dual_v(const FwdParams& p, cudaStream_t stream);
 // Backward stages, combinable as a bit mask.
 enum BwdStage : int { kBwdPreprocess = 1, kBwdDkDv = 2, kBwdDq = 4, kBwdAll = 7 };
 cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream, int stages);
@@ -67,6 +76,9 @@ cudaError_t launch_psa(const PsaParams& p, cudaStream_t stream);
 // `elem_bytes` elements (d0 innermost), box {box0, box1, 1}.  Returns false on failure.
 bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t d0, uint64_t d1,
                     uint64_t d2, uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle);
+
+// Device address of the watchdog word on the current device (looked up once per device).
+bool watchdog_word(unsigned int** out);
 
 // Raises the dynamic shared-memory limit of `func` on the current device once.
 cudaError_t ensure_smem_limit(const void* func, int bytes, int slot);

@@ -1,15 +1,21 @@
-// psa.cu - the PSA (YOLO C2PSA) rearrangement passes as coalesced tiled transposes.
+// psa.cu - the PSA (YOLO C2PSA) rearrangement passes and their adjoints.
 //
 // "vision_rs/models/yolo/kernels/attention/psa.rs":
-//   psa_pack_qkv:        packed[s, b*nh + h, n, dd] = qkv[b, h*4*KD + s*KD + dd, n]
-//   psa_merge_attn_nchw: out[b, h*2*KD + dd, n] = lo[b*nh + h, n, dd],
-//                        out[b, h*2*KD + KD + dd, n] = hi[b*nh + h, n, dd]
-// Both are batches of 2-D transposes between a channel-major block [KD, N]
-// (NCHW, spatial positions contiguous) and a token-major block [N, KD].  The
-// page's kernels read (pack) or write (merge) with a stride of H*W elements;
-// here each CTA stages a tile in shared memory so that both the global reads
-// and the global writes are contiguous 16-byte vectors.  Words are moved, never
-// interpreted, so any bit pattern (NaN payloads included) survives unchanged.
+//   psa_pack_qkv:           packed[s, b*nh + h, n, dd] = qkv[b, h*4*KD + s*KD + dd, n]
+//   psa_merge_attn_nchw:    out[b, h*2*KD + dd, n] = lo[b*nh + h, n, dd],
+//                           out[b, h*2*KD + KD + dd, n] = hi[b*nh + h, n, dd]
+//   psa_extract_v_nchw:     v[b, h*2*KD + t, n] = qkv[b, h*4*KD + 2*KD + t, n], t < 2*KD
+//   psa_merge_attn_backward, psa_pack_qkv_backward: the same index maps read the
+//                           other way round (plain stores: no two writes overlap)
+//   psa_extract_v_backward: d_qkv[b, h*4*KD + 2*KD + t, n] += d_v[b, h*2*KD + t, n]
+// pack / merge and their adjoints are batches of 2-D transposes between a
+// channel-major block [KD, N] (NCHW, positions contiguous) and a token-major
+// block [N, KD].  The page's kernels read or write with a stride of H*W
+// elements; here each CTA stages a tile in shared memory so that both the
+// global reads and the global writes are contiguous 16-byte vectors.  The V
+// extraction and its adjoint move contiguous runs of 2*KD*N elements per head.
+// Copies move words without interpreting them (any bit pattern survives); the
+// accumulating adjoint adds in float32 and rounds once to the storage type.
 #include "common.cuh"
 #include "internal.h"
 
@@ -18,23 +24,41 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Element offsets of block z for the two maps.
-struct PackMap {
+// Block z of a transpose: which source / destination buffer and the element
+// offsets of the block in them.
+struct BlockRef {
+    int64_t src_off, dst_off;
+    int src_sel, dst_sel;
+};
+
+// channel-major [KD, N] -> token-major [N, KD]
+struct PackMap {  // qkv -> packed, z = (s, bh)
     int64_t bnh, nh, kd, n, qkv_h;
-    __device__ void operator()(int64_t z, int64_t& src_off, int64_t& dst_off, int& which) const {
+    __device__ BlockRef operator()(int64_t z) const {
         const int64_t s = z / bnh, bh = z % bnh, b = bh / nh, h = bh % nh;
-        src_off = (b * qkv_h + h * 4 * kd + s * kd) * n;
-        dst_off = (s * bnh + bh) * n * kd;
-        which = 0;
+        return {(b * qkv_h + h * 4 * kd + s * kd) * n, (s * bnh + bh) * n * kd, 0, 0};
     }
 };
-struct MergeMap {
+struct MergeBwdMap {  // d_merged -> d_lo / d_hi, z = (half, bh)
     int64_t bnh, nh, kd, n, c;
-    __device__ void operator()(int64_t z, int64_t& src_off, int64_t& dst_off, int& which) const {
+    __device__ BlockRef operator()(int64_t z) const {
         const int64_t half = z / bnh, bh = z % bnh, b = bh / nh, h = bh % nh;
-        src_off = bh * n * kd;
-        dst_off = (b * c + h * 2 * kd + half * kd) * n;
-        which = (int)half;
+        return {(b * c + h * 2 * kd + half * kd) * n, bh * n * kd, 0, (int)half};
+    }
+};
+// token-major [N, KD] -> channel-major [KD, N]
+struct MergeMap {  // lo / hi -> out, z = (half, bh)
+    int64_t bnh, nh, kd, n, c;
+    __device__ BlockRef operator()(int64_t z) const {
+        const int64_t half = z / bnh, bh = z % bnh, b = bh / nh, h = bh % nh;
+        return {bh * n * kd, (b * c + h * 2 * kd + half * kd) * n, (int)half, 0};
+    }
+};
+struct PackBwdMap {  // d_packed -> d_qkv, z = (s, bh)
+    int64_t bnh, nh, kd, n, qkv_h;
+    __device__ BlockRef operator()(int64_t z) const {
+        const int64_t s = z / bnh, bh = z % bnh, b = bh / nh, h = bh % nh;
+        return {(s * bnh + bh) * n * kd, (b * qkv_h + h * 4 * kd + s * kd) * n, 0, 0};
     }
 };
 
@@ -48,15 +72,13 @@ struct Vec16 {
 // are aligned to it.
 template <typename W, int TR, int TC, bool kVec, typename Map>
 __global__ void __launch_bounds__(kThreads)
-    psa_transpose_kernel(const W* __restrict__ src0, const W* __restrict__ src1, W* __restrict__ dst, int64_t R,
-                         int64_t C, Map map) {
+    psa_transpose_kernel(const W* __restrict__ src0, const W* __restrict__ src1, W* __restrict__ dst0,
+                         W* __restrict__ dst1, int64_t R, int64_t C, Map map) {
     constexpr int V = kVec ? Vec16<W>::N : 1;
     __shared__ __align__(16) W tile[TR][TC + Vec16<W>::N];
-    int64_t src_off, dst_off;
-    int which;
-    map((int64_t)blockIdx.z, src_off, dst_off, which);
-    const W* src = (which ? src1 : src0) + src_off;
-    W* out = dst + dst_off;
+    const BlockRef blk = map((int64_t)blockIdx.z);
+    const W* src = (blk.src_sel ? src1 : src0) + blk.src_off;
+    W* out = (blk.dst_sel ? dst1 : dst0) + blk.dst_off;
     const int64_t r0 = (int64_t)blockIdx.y * TR;
     const int64_t c0 = (int64_t)blockIdx.x * TC;
 
@@ -98,11 +120,97 @@ cudaError_t launch_t(const PsaParams& p, int64_t R, int64_t C, int64_t batches, 
     const dim3 grid((unsigned)((C + TC - 1) / TC), (unsigned)((R + TR - 1) / TR), (unsigned)batches);
     const W* s0 = static_cast<const W*>(p.src0);
     const W* s1 = static_cast<const W*>(p.src1 ? p.src1 : p.src0);
-    W* d = static_cast<W*>(p.dst);
+    W* d0 = static_cast<W*>(p.dst);
+    W* d1 = static_cast<W*>(p.dst1 ? p.dst1 : p.dst);
     if (vec)
-        psa_transpose_kernel<W, TR, TC, true, Map><<<grid, kThreads, 0, stream>>>(s0, s1, d, R, C, map);
+        psa_transpose_kernel<W, TR, TC, true, Map><<<grid, kThreads, 0, stream>>>(s0, s1, d0, d1, R, C, map);
     else
-        psa_transpose_kernel<W, TR, TC, false, Map><<<grid, kThreads, 0, stream>>>(s0, s1, d, R, C, map);
+        psa_transpose_kernel<W, TR, TC, false, Map><<<grid, kThreads, 0, stream>>>(s0, s1, d0, d1, R, C, map);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- V extraction and its adjoint
+//
+// Per head the V_lo and V_hi channels of QKV (channels h*4*KD + 2*KD .. h*4*KD + 4*KD)
+// and of V (h*2*KD .. h*2*KD + 2*KD) are contiguous runs of len = 2*KD*N elements.
+
+template <typename W>
+__device__ __forceinline__ float widen(W x, int dtype) {
+    if constexpr (sizeof(W) == 4) {
+        return __uint_as_float(x);
+    } else {
+        if (dtype == kBf16) return __uint_as_float(((uint32_t)x) << 16);
+        return __half2float(__ushort_as_half(x));
+    }
+}
+
+template <typename W>
+__device__ __forceinline__ W narrow(float x, int dtype) {
+    if constexpr (sizeof(W) == 4) {
+        return __float_as_uint(x);
+    } else {
+        if (dtype == kBf16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+        return __half_as_ushort(__float2half_rn(x));
+    }
+}
+
+// kAdd = false: qkv (src) -> v (dst) copy.  kAdd = true: d_qkv (dst) += d_v (src).
+template <typename W, bool kAdd, bool kVec>
+__global__ void __launch_bounds__(kThreads)
+    psa_v_runs_kernel(const W* __restrict__ src, W* __restrict__ dst, int64_t len, int64_t nh, int64_t kd, int64_t n,
+                      int64_t qkv_h, int64_t c, int dtype) {
+    constexpr int V = kVec ? Vec16<W>::N : 1;
+    const int64_t bh = blockIdx.y, b = bh / nh, h = bh % nh;
+    const int64_t qkv_off = (b * qkv_h + h * 4 * kd + 2 * kd) * n;
+    const int64_t v_off = (b * c + h * 2 * kd) * n;
+    const W* s = src + (kAdd ? v_off : qkv_off);
+    W* d = dst + (kAdd ? qkv_off : v_off);
+    for (int64_t i = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * V; i < len; i += (int64_t)gridDim.x * kThreads * V) {
+        if constexpr (kVec) {
+            union {
+                uint4 u;
+                W w[Vec16<W>::N];
+            } a;
+            a.u = *reinterpret_cast<const uint4*>(s + i);
+            if constexpr (kAdd) {
+                union {
+                    uint4 u;
+                    W w[Vec16<W>::N];
+                } o;
+                o.u = *reinterpret_cast<const uint4*>(d + i);
+#pragma unroll
+                for (int t = 0; t < V; ++t) o.w[t] = narrow<W>(widen<W>(o.w[t], dtype) + widen<W>(a.w[t], dtype), dtype);
+                *reinterpret_cast<uint4*>(d + i) = o.u;
+            } else {
+                *reinterpret_cast<uint4*>(d + i) = a.u;
+            }
+        } else {
+            if constexpr (kAdd)
+                d[i] = narrow<W>(widen<W>(d[i], dtype) + widen<W>(s[i], dtype), dtype);
+            else
+                d[i] = s[i];
+        }
+    }
+}
+
+template <typename W>
+cudaError_t launch_v_runs(const PsaParams& p, bool add, cudaStream_t stream) {
+    constexpr int V = Vec16<W>::N;
+    const int64_t len = 2 * p.kd * p.n;
+    const bool vec = (p.kd % V == 0) || (p.n % V == 0);
+    const int64_t per_block = (int64_t)kThreads * (vec ? V : 1);
+    const unsigned gx = (unsigned)std::min<int64_t>((len + per_block - 1) / per_block, 1024);
+    const dim3 grid(gx, (unsigned)(p.B * p.nh), 1);
+    const W* s = static_cast<const W*>(p.src0);
+    W* d = static_cast<W*>(p.dst);
+#define FA2_V_RUNS(ADD, VEC) \
+    psa_v_runs_kernel<W, ADD, VEC><<<grid, kThreads, 0, stream>>>(s, d, len, p.nh, p.kd, p.n, p.qkv_h, p.c, p.dtype)
+    if (add) {
+        if (vec) FA2_V_RUNS(true, true); else FA2_V_RUNS(true, false);
+    } else {
+        if (vec) FA2_V_RUNS(false, true); else FA2_V_RUNS(false, false);
+    }
+#undef FA2_V_RUNS
     return cudaGetLastError();
 }
 
@@ -111,14 +219,22 @@ cudaError_t launch_w(const PsaParams& p, cudaStream_t stream) {
     constexpr int V = Vec16<W>::N;
     const bool vec = (p.kd % V == 0) && (p.n % V == 0);
     const int64_t bnh = p.B * p.nh;
-    if (p.kind == 0) {
-        // block [KD channels, N positions] -> [N, KD]
-        const PackMap m{bnh, p.nh, p.kd, p.n, p.qkv_h};
-        return launch_t<W, 32, 64>(p, p.kd, p.n, 4 * bnh, m, vec, stream);
+    switch (p.kind) {
+        case kPsaPack:  // block [KD channels, N positions] -> [N, KD]
+            return launch_t<W, 32, 64>(p, p.kd, p.n, 4 * bnh, PackMap{bnh, p.nh, p.kd, p.n, p.qkv_h}, vec, stream);
+        case kPsaMergeBwd:
+            return launch_t<W, 32, 64>(p, p.kd, p.n, 2 * bnh, MergeBwdMap{bnh, p.nh, p.kd, p.n, p.c}, vec, stream);
+        case kPsaMerge:  // block [N positions, KD] -> [KD channels, N]
+            return launch_t<W, 64, 32>(p, p.n, p.kd, 2 * bnh, MergeMap{bnh, p.nh, p.kd, p.n, p.c}, vec, stream);
+        case kPsaPackBwd:
+            return launch_t<W, 64, 32>(p, p.n, p.kd, 4 * bnh, PackBwdMap{bnh, p.nh, p.kd, p.n, p.qkv_h}, vec, stream);
+        case kPsaExtractV:
+            return launch_v_runs<W>(p, false, stream);
+        case kPsaExtractVBwd:
+            return launch_v_runs<W>(p, true, stream);
+        default:
+            return cudaErrorInvalidValue;
     }
-    // block [N positions, KD] -> [KD channels, N]
-    const MergeMap m{bnh, p.nh, p.kd, p.n, p.c};
-    return launch_t<W, 64, 32>(p, p.n, p.kd, 2 * bnh, m, vec, stream);
 }
 
 }  // namespace

@@ -4,9 +4,9 @@
 One step is one pass of every step of the path over one batch of seeded
 synthetic inputs, all on one CUDA stream:
 
-* the YOLO C2PSA block: QKV [8, 512, 20, 20] fp16 -> psa_pack_qkv -> two
-  fa2_forward calls (HEAD_DIM 32 on Q, K with V_lo and with V_hi, N = 400)
-  -> psa_merge_attn_nchw -> [8, 256, 20, 20];
+* the YOLO C2PSA block: QKV [8, 512, 20, 20] fp16 -> psa_pack_qkv ->
+  psa_fa2_forward (HEAD_DIM 32 on Q, K with V_lo and with V_hi, N = 400, one
+  pass over the scores for both) -> psa_merge_attn_nchw -> [8, 256, 20, 20];
 * attention forward + backward, bf16, B=2 H=16 (BH = 32), N_q = N_k = 8192,
   HEAD_DIM 128: fa2_forward, then fa2_backward_preprocess,
   fa2_backward_dkdv and fa2_backward_dq (the three stages of fa2_backward).
@@ -62,7 +62,7 @@ KERNEL_SOURCES = {
     "fa2_bwd_dkdv": ["fa2_bwd_tc.cu", "common.cuh"],
     "fa2_bwd_dq": ["fa2_bwd_tc.cu", "common.cuh"],
 }
-LAUNCHES_PER_STEP = 8  # pack, fwd lo, fwd hi, merge, fwd, preprocess, dkdv, dq
+LAUNCHES_PER_STEP = 7  # pack, fused PSA fwd (V_lo and V_hi), merge, fwd, preprocess, dkdv, dq
 WORKLOAD = ("C2PSA block (QKV [8,512,20,20] fp16, 4 heads, KEY_DIM 32) + attention fwd+bwd "
             "bf16 B=2 H=16 N=8192 HEAD_DIM=128")
 
@@ -253,6 +253,21 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------- our arm
+def reduce_max(x: float, dist=None, device=None) -> float:
+    """The maximum of `x` over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, step_flops: float, ms_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own batch (weak scaling) in the max-over-ranks step time."""
+    return world * step_flops / (ms_step * 1e-3) / 1e12
+
+
 def run_ours(args):
     import torch
     rank, world, local = env_rank()
@@ -275,43 +290,48 @@ def run_ours(args):
             t = torch.from_numpy(np.ascontiguousarray(arr))
         return t.pin_memory()
 
-    hq, hk, hv, hdo = (pinned(x, torch.bfloat16) for x in (q_h, k_h, v_h, do_h))
-    hqkv = pinned(qkv_h, torch.float16)
+    host_in = {"q": pinned(q_h, torch.bfloat16), "k": pinned(k_h, torch.bfloat16), "v": pinned(v_h, torch.bfloat16),
+               "do": pinned(do_h, torch.bfloat16), "qkv": pinned(qkv_h, torch.float16)}
     dev = torch.device("cuda", local)
-    q, k, v, d_o = (x.to(dev) for x in (hq, hk, hv, hdo))
-    qkv = hqkv.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((BH, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(B.fa2_backward_workspace_size(BH, N, N, D, B.DTYPE_BF16), dtype=torch.uint8, device=dev)
-    packed = torch.empty((4, PSA_BH, PSA_N, PSA_KD), dtype=torch.float16, device=dev)
-    o_lo = torch.empty((PSA_BH, PSA_N, PSA_KD), dtype=torch.float16, device=dev)
-    o_hi = torch.empty_like(o_lo)
-    lse_lo = torch.empty((PSA_BH, PSA_N), dtype=torch.float32, device=dev)
-    lse_hi = torch.empty_like(lse_lo)
-    merged = torch.empty((PSA_B, PSA_NH * 2 * PSA_KD, PSA_H, PSA_W), dtype=torch.float16, device=dev)
+
+    def alloc_set(fill: bool):
+        """One set of device buffers for a step: inputs (copied from the host when `fill`) and outputs."""
+        b = {n: (h.to(dev) if fill else torch.empty(h.shape, dtype=h.dtype, device=dev)) for n, h in host_in.items()}
+        b["o"] = torch.empty_like(b["q"])
+        b["lse"] = torch.empty((BH, N), dtype=torch.float32, device=dev)
+        b["dq"], b["dk"], b["dv"] = torch.empty_like(b["q"]), torch.empty_like(b["k"]), torch.empty_like(b["v"])
+        b["ws"] = torch.empty(B.fa2_backward_workspace_size(BH, N, N, D, B.DTYPE_BF16), dtype=torch.uint8, device=dev)
+        b["packed"] = torch.empty((4, PSA_BH, PSA_N, PSA_KD), dtype=torch.float16, device=dev)
+        b["o_lo"] = torch.empty((PSA_BH, PSA_N, PSA_KD), dtype=torch.float16, device=dev)
+        b["o_hi"] = torch.empty_like(b["o_lo"])
+        b["lse_lo"] = torch.empty((PSA_BH, PSA_N), dtype=torch.float32, device=dev)
+        b["lse_hi"] = torch.empty_like(b["lse_lo"])
+        b["merged"] = torch.empty((PSA_B, PSA_NH * 2 * PSA_KD, PSA_H, PSA_W), dtype=torch.float16, device=dev)
+        return b
+
+    sets = [alloc_set(True)]
     s128, s32 = 1 / math.sqrt(D), 1 / math.sqrt(PSA_KD)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
+    def step(b=None, ev=None):
+        b = b or sets[0]
         if ev is not None:
             ev[0].record(stream)
-        B.psa_pack_qkv(qkv, packed, PSA_NH)
-        B.fa2_forward(packed[0], packed[1], packed[2], o_lo, lse_lo, s32)
-        B.fa2_forward(packed[0], packed[1], packed[3], o_hi, lse_hi, s32)
-        B.psa_merge_attn_nchw(o_lo, o_hi, merged, PSA_NH)
+        B.psa_pack_qkv(b["qkv"], b["packed"], PSA_NH)
+        B.psa_fa2_forward(b["packed"], b["o_lo"], b["o_hi"], b["lse_lo"], s32)
+        B.psa_merge_attn_nchw(b["o_lo"], b["o_hi"], b["merged"], PSA_NH)
         if ev is not None:
             ev[1].record(stream)
-        B.fa2_forward(q, k, v, o, lse, s128)
+        B.fa2_forward(b["q"], b["k"], b["v"], b["o"], b["lse"], s128)
         if ev is not None:
             ev[2].record(stream)
-        B.fa2_backward_preprocess(o, d_o, lse, ws, N)
+        B.fa2_backward_preprocess(b["o"], b["do"], b["lse"], b["ws"], N)
         if ev is not None:
             ev[3].record(stream)
-        B.fa2_backward_dkdv(q, k, v, d_o, ws, dk, dv, s128)
+        B.fa2_backward_dkdv(b["q"], b["k"], b["v"], b["do"], b["ws"], b["dk"], b["dv"], s128)
         if ev is not None:
             ev[4].record(stream)
-        B.fa2_backward_dq(q, k, v, d_o, ws, dq, s128)
+        B.fa2_backward_dq(b["q"], b["k"], b["v"], b["do"], b["ws"], b["dq"], s128)
         if ev is not None:
             ev[5].record(stream)
 
@@ -322,11 +342,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
     def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dist, dev)
 
     for _ in range(args.warmup):
         step()
@@ -344,7 +360,7 @@ def run_ours(args):
     time.sleep(0.3)
     e_begin.record(stream)
     for s in range(args.steps):
-        step(evs[s])
+        step(ev=evs[s])
     e_end.record(stream)
     torch.cuda.synchronize()
     clocks = sampler.stop()
@@ -353,7 +369,7 @@ def run_ours(args):
     barrier()
 
     ms_step = elapsed_ms / args.steps
-    value = world * STEP_FLOPS / (ms_step * 1e-3) / 1e12
+    value = job_throughput(world, STEP_FLOPS, ms_step)
     names = ["c2psa_block", "fa2_fwd", "fa2_bwd_preprocess", "fa2_bwd_dkdv", "fa2_bwd_dq"]
     per = {n: statistics.fmean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
            for i, n in enumerate(names)}
@@ -380,28 +396,53 @@ def run_ours(args):
     components.update(psa_bandwidth(torch, B, dev, pk))
 
     # ------------------------------------------------------------------ end to end, host buffers
-    e2e_steps = max(3, args.steps // 10)
-    ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, dq, dk, dv))
-    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    hmerged = torch.empty(merged.shape, dtype=merged.dtype).pin_memory()
-    ins = [(q, hq), (k, hk), (v, hv), (d_o, hdo), (qkv, hqkv)]
-    outs = [(ho, o), (hlse, lse), (hdq, dq), (hdk, dk), (hdv, dv), (hmerged, merged)]
-    h2d = sum(h.numel() * h.element_size() for _, h in ins)
-    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+    # Every step copies its inputs in from pinned host memory and all of its
+    # results (O, LSE, dQ, dK, dV, the merged C2PSA output) back.  Two buffer sets
+    # and two copy streams let the copies of steps s+2 (in) and s (out) run while
+    # step s+1 computes.
+    e2e_steps = max(4, args.steps // 10)
+    sets.append(alloc_set(False))
+    out_names = ["o", "lse", "dq", "dk", "dv", "merged"]
+    host_out = {n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory() for n in out_names}
+    h2d = sum(h.numel() * h.element_size() for h in host_in.values())
+    d2h = sum(h.numel() * h.element_size() for h in host_out.values())
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    out_read = [torch.cuda.Event() for _ in range(2)]
     barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        for dst, src in ins:
-            dst.copy_(src, non_blocking=True)
-        step()
-        for dst, src in outs:
-            dst.copy_(src, non_blocking=True)
-    b.record(stream)
+    a.record(h2d_stream)
+
+    def copy_in(i):
+        with torch.cuda.stream(h2d_stream):
+            for n, h in host_in.items():
+                sets[i][n].copy_(h, non_blocking=True)
+            in_ready[i].record(h2d_stream)
+
+    copy_in(0)
+    copy_in(1)
+    for s in range(e2e_steps):
+        i = s % 2
+        stream.wait_event(in_ready[i])
+        if s >= 2:
+            stream.wait_event(out_read[i])  # outputs of step s-2 copied out before they are overwritten
+        step(sets[i])
+        computed[i].record(stream)
+        d2h_stream.wait_event(computed[i])
+        with torch.cuda.stream(d2h_stream):
+            for n in out_names:
+                host_out[n].copy_(sets[i][n], non_blocking=True)
+            out_read[i].record(d2h_stream)
+        if s + 2 < e2e_steps:
+            h2d_stream.wait_event(computed[i])  # step s has finished reading set i's inputs
+            copy_in(i)
+    b.record(d2h_stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(a.elapsed_time(b)) / e2e_steps
-    e2e = {"value": world * STEP_FLOPS / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps}
+    e2e = {"value": job_throughput(world, STEP_FLOPS, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
+           "copies": "pinned host buffers, H2D and D2H on two copy streams overlapping the neighbouring steps"}
     B.fa2_device_status()
 
     line = {

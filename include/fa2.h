@@ -203,6 +203,91 @@ fa2_status psa_merge_attn_nchw(const void* lo, const void* hi, void* out, int32_
                                int32_t W, int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream);
 
 /*
+ * psa_fa2_forward - both PSA attention calls (V_lo and V_hi) in one pass.
+ *
+ * Defined by "vision_rs/models/yolo/kernels/attention/psa.rs",
+ * FlashAttn2PsaRuntimeOp::new_lo / new_hi: attention with HEAD_DIM = KEY_DIM on
+ * Q = section 0, K = section 1 of the packed buffer and V = section 2 (V_lo) or
+ * section 3 (V_hi), softmax_scale = 1/sqrt(KEY_DIM) as that op passes it.  The
+ * two calls share Q and K, hence their scores, probabilities and LSE; this call
+ * computes them once and applies them to both value sections, writing exactly
+ * what two fa2_forward calls on (Q, K, V_lo) and (Q, K, V_hi) would write up to
+ * rounding order (the module comment's "V split trick", without the second pass).
+ *
+ *   packed      [4, bh, n, key_dim]   dtype, device, read (as written by psa_pack_qkv)
+ *   o_lo, o_hi  [bh, n, key_dim]      dtype, device, written
+ *   lse         [bh, n]               float32, device, written (shared by both)
+ *
+ * dtype F16 / BF16, key_dim in {32, 64}; FA2_ERR_UNSUPPORTED otherwise.
+ * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED, FA2_ERR_CUDA.
+ */
+fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* lse, int64_t bh, int64_t n,
+                           int32_t key_dim, fa2_dtype dtype, float softmax_scale, void* stream);
+
+/*
+ * psa_extract_v_nchw - the V_lo / V_hi channels of QKV as an NCHW tensor.
+ *
+ * Defined by "vision_rs/models/yolo/kernels/attention/psa.rs", kernel
+ * psa_extract_v_nchw (same argument order, B explicit): with
+ * KEY_DIM = qkv_h / (4 * num_heads), v[b, h*2*KEY_DIM + t, n] =
+ * qkv[b, h*4*KEY_DIM + 2*KEY_DIM + t, n] for t < 2*KEY_DIM.
+ *
+ *   qkv  [B, qkv_h, H, W]  dtype, device, read
+ *   v    [B, c, H, W]      dtype, device, written; c must equal qkv_h / 2
+ *
+ * Bit-exact copy.  Errors: FA2_ERR_INVALID_ARG, FA2_ERR_MISALIGNED, FA2_ERR_UNSUPPORTED, FA2_ERR_CUDA.
+ */
+fa2_status psa_extract_v_nchw(const void* qkv, void* v, int32_t qkv_h, int32_t c, int32_t H, int32_t W,
+                              int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream);
+
+/*
+ * psa_pack_qkv_backward - the adjoint of psa_pack_qkv: d_packed back to NCHW.
+ *
+ * "vision_rs/models/yolo/kernels/attention/psa.rs", kernel psa_pack_qkv_backward
+ * (same argument order): d_qkv[b, h*4*KEY_DIM + s*KEY_DIM + dd, n] =
+ * d_packed[s, b*num_heads + h, n, dd].  The page accumulates with atomics into
+ * a zeroed d_qkv because psa_extract_v_backward also adds into the V channels;
+ * here this call WRITES every element of d_qkv (no zeroing needed, bit-exact,
+ * deterministic) and psa_extract_v_backward, called after it on the same
+ * stream, adds its part.
+ *
+ *   d_packed [4, B*num_heads, H*W, KEY_DIM]  dtype, device, read
+ *   d_qkv    [B, qkv_h, H, W]                dtype, device, written
+ */
+fa2_status psa_pack_qkv_backward(const void* d_packed, void* d_qkv, int32_t qkv_h, int32_t H, int32_t W,
+                                 int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream);
+
+/*
+ * psa_merge_attn_backward - the adjoint of psa_merge_attn_nchw.
+ *
+ * "vision_rs/models/yolo/kernels/attention/psa.rs", kernel psa_merge_attn_backward
+ * (same argument order, B explicit): d_lo[b*num_heads + h, n, dd] =
+ * d_merged[b, h*2*KEY_DIM + dd, n], d_hi[...] = d_merged[b, h*2*KEY_DIM + KEY_DIM + dd, n]
+ * with KEY_DIM = c / (2 * num_heads).  Plain stores, bit-exact.
+ *
+ *   d_merged   [B, c, H, W]                   dtype, device, read
+ *   d_lo, d_hi [B*num_heads, H*W, KEY_DIM]    dtype, device, written
+ */
+fa2_status psa_merge_attn_backward(const void* d_merged, void* d_lo, void* d_hi, int32_t c, int32_t H, int32_t W,
+                                   int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream);
+
+/*
+ * psa_extract_v_backward - the adjoint of psa_extract_v_nchw, accumulated.
+ *
+ * "vision_rs/models/yolo/kernels/attention/psa.rs", kernel psa_extract_v_backward
+ * (same argument order, B explicit): d_qkv[b, h*4*KEY_DIM + 2*KEY_DIM + t, n] +=
+ * d_v[b, h*2*KEY_DIM + t, n] for t < 2*KEY_DIM.  The page uses atomic_add; here
+ * each element is read, added in float32 and rounded once (RNE) to dtype, in a
+ * single deterministic pass.  Call it after psa_pack_qkv_backward on the same
+ * stream.  Other channels of d_qkv are left as they are.
+ *
+ *   d_v    [B, c, H, W]      dtype, device, read; c must equal qkv_h / 2
+ *   d_qkv  [B, qkv_h, H, W]  dtype, device, read and written
+ */
+fa2_status psa_extract_v_backward(const void* d_v, void* d_qkv, int32_t qkv_h, int32_t c, int32_t H, int32_t W,
+                                  int32_t B, int32_t num_heads, fa2_dtype dtype, void* stream);
+
+/*
  * fa2_device_status - the watchdog word of the library's kernels.
  *
  * Every wait inside the library's kernels is bounded in time.  A kernel that
@@ -212,6 +297,20 @@ fa2_status psa_merge_attn_nchw(const void* lo, const void* hi, void* out, int32_
  * FA2_OK or FA2_ERR_DEVICE_TIMEOUT (FA2_ERR_CUDA if the synchronisation failed).
  */
 fa2_status fa2_device_status(void* stream);
+
+/*
+ * fa2_watchdog_selftest - drives the bounded-wait path on purpose.
+ *
+ * Launches one thread on `stream` that waits on a shared-memory barrier no one
+ * will complete, with the same time-bounded wait the pipeline kernels use.  The
+ * wait gives up after about one second, records the timeout in the watchdog
+ * word and returns; nothing faults or hangs.  A following fa2_device_status()
+ * returns FA2_ERR_DEVICE_TIMEOUT (and clears the word).  For tests of the
+ * failure-detection path; the pages have no counterpart (their invalid-size
+ * path is a trap program, which this library never emits on a device).
+ * Errors: FA2_ERR_CUDA if the launch fails.
+ */
+fa2_status fa2_watchdog_selftest(void* stream);
 
 /* fa2_status_string - a static, human-readable message for a status code. */
 const char* fa2_status_string(fa2_status s);

@@ -74,16 +74,60 @@ def extract_v_nchw(qkv: np.ndarray, num_heads: int) -> np.ndarray:
 
 
 def pack_qkv_backward(d_packed: np.ndarray, batch: int, num_heads: int, height: int, width: int) -> np.ndarray:
-    """psa.rs ``psa_pack_qkv_backward``: the adjoint of pack (a scatter; no overlaps)."""
+    """psa.rs ``psa_pack_qkv_backward``: the adjoint of pack.
+
+    Every element of d_qkv receives exactly one element of d_packed (the pack map
+    is a bijection), so the page's scatter-add into a zeroed d_qkv equals this
+    assignment; the dtype (even raw 16-bit words) is preserved.
+    """
     _, bh, n, kd = d_packed.shape
     qkv_h = num_heads * 4 * kd
-    out = np.zeros((batch, qkv_h, n), dtype=np.float64)
+    out = np.empty((batch, qkv_h, n), dtype=d_packed.dtype)
     for s in range(4):
         for b in range(batch):
             for h in range(num_heads):
                 c0 = h * 4 * kd + s * kd
-                out[b, c0:c0 + kd, :] += np.asarray(d_packed[s, b * num_heads + h], dtype=np.float64).T
+                out[b, c0:c0 + kd, :] = d_packed[s, b * num_heads + h].T
     return out.reshape(batch, qkv_h, height, width)
+
+
+def _words_to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact float64 values of stored words: 'bf16' (uint16 bit patterns), 'f16', 'f32'."""
+    if dtype == "bf16":
+        return (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return np.asarray(x).astype(np.float64)
+
+
+def _round_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 values once-per-format to the storage type (RNE).
+
+    bf16: to float32 first, then to the nearest bfloat16 (ties to even) on the
+    float32 bit pattern; the float32 step is exact for the sums formed here (a
+    sum of two bfloat16 values needs at most 24 significant bits unless the
+    smaller addend lies below half an ulp of the larger, in which case both
+    orders of rounding give the larger).
+    """
+    if dtype == "bf16":
+        b = x.astype(np.float32).view(np.uint32)
+        lsb = (b >> np.uint32(16)) & np.uint32(1)
+        return ((b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+    return x.astype(np.float16 if dtype == "f16" else np.float32)
+
+
+def extract_v_backward(d_v: np.ndarray, d_qkv: np.ndarray, num_heads: int, dtype: str) -> np.ndarray:
+    """psa.rs ``psa_extract_v_backward``: d_qkv with its V_lo / V_hi channels increased by d_v.
+
+    The addition is exact (float64) and rounded once to the storage dtype; the
+    other channels are returned unchanged.
+    """
+    b_, qkv_h, h_, w_ = d_qkv.shape
+    kd = key_dim(qkv_h, num_heads)
+    out = d_qkv.copy()
+    for h in range(num_heads):
+        src = slice(h * 2 * kd, (h + 1) * 2 * kd)
+        dst = slice(h * 4 * kd + 2 * kd, (h + 1) * 4 * kd)
+        out[:, dst] = _round_f64(_words_to_f64(d_qkv[:, dst], dtype) + _words_to_f64(d_v[:, src], dtype), dtype)
+    return out
 
 
 def merge_attn_backward(d_merged: np.ndarray, num_heads: int):

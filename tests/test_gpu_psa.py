@@ -94,3 +94,85 @@ def test_c2psa_pipeline():
     r_hi, _ = A.forward(pk[0], pk[1], pk[3], scale)
     ref = P.merge_attn_nchw(r_lo, r_hi, B, nh, H, W)
     check_16bit(G.to_f64(out), ref, "merged attention output")
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("B,nh,kd,H,W", [(8, 4, 32, 20, 20), (2, 2, 16, 5, 7), (1, 3, 2, 1, 3)])
+def test_extract_v_and_adjoints_bit_exact(dtype, B, nh, kd, H, W):
+    """psa_extract_v_nchw, psa_pack_qkv_backward and psa_merge_attn_backward move words exactly."""
+    import torch
+    G.require_gpu()
+    tag = f"psa_adj/{dtype}/{B}/{nh}/{kd}/{H}/{W}"
+    qkv = _patterns(tag + "/qkv", (B, nh * 4 * kd, H, W), dtype)
+    v = _raw_tensor(np.zeros((B, nh * 2 * kd, H, W), dtype=qkv.dtype), dtype).view(B, nh * 2 * kd, H, W)
+    binding.psa_extract_v_nchw(_raw_tensor(qkv, dtype).view(qkv.shape), v, nh)
+    d_packed = _patterns(tag + "/dpacked", (4, B * nh, H * W, kd), dtype)
+    d_qkv = _raw_tensor(np.zeros(qkv.shape, dtype=qkv.dtype), dtype).view(qkv.shape)
+    binding.psa_pack_qkv_backward(_raw_tensor(d_packed, dtype), d_qkv, nh)
+    d_merged = _patterns(tag + "/dmerged", (B, nh * 2 * kd, H, W), dtype)
+    d_lo = _raw_tensor(np.zeros((B * nh, H * W, kd), dtype=qkv.dtype), dtype).view(B * nh, H * W, kd)
+    d_hi = torch.empty_like(d_lo)
+    binding.psa_merge_attn_backward(_raw_tensor(d_merged, dtype).view(d_merged.shape), d_lo, d_hi, nh)
+    binding.fa2_device_status()
+    assert np.array_equal(_words(v, dtype).reshape(v.shape), P.extract_v_nchw(qkv, nh))
+    assert np.array_equal(_words(d_qkv, dtype).reshape(qkv.shape), P.pack_qkv_backward(d_packed, B, nh, H, W))
+    want_lo, want_hi = P.merge_attn_backward(d_merged, nh)
+    assert np.array_equal(_words(d_lo, dtype).reshape(want_lo.shape), want_lo)
+    assert np.array_equal(_words(d_hi, dtype).reshape(want_hi.shape), want_hi)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("B,nh,kd,H,W", [(8, 4, 32, 20, 20), (3, 1, 8, 3, 5)])
+def test_extract_v_backward_accumulates_exactly(dtype, B, nh, kd, H, W):
+    """d_qkv from psa_pack_qkv_backward, then psa_extract_v_backward adds d_v into its V channels:
+    bit-exact against the oracle's exact sum rounded once to the storage type."""
+    G.require_gpu()
+    tag = f"psa_evb/{dtype}/{B}/{nh}/{kd}"
+    d_packed = synth.tensor(tag + "/dpacked", (4, B * nh, H * W, kd), dtype)
+    d_v = synth.tensor(tag + "/dv", (B, nh * 2 * kd, H, W), dtype)
+    d_qkv = G.empty((B, nh * 4 * kd, H, W), dtype)
+    binding.psa_pack_qkv_backward(G.to_device(d_packed, dtype), d_qkv, nh)
+    binding.psa_extract_v_backward(G.to_device(d_v, dtype), d_qkv, nh)
+    binding.fa2_device_status()
+    want = P.extract_v_backward(d_v, P.pack_qkv_backward(d_packed, B, nh, H, W), nh, dtype)
+    assert np.array_equal(_words(d_qkv, dtype).reshape(want.shape), want.view(np.uint32 if dtype == "f32" else np.uint16))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("bh,n,kd", [(32, 400, 32), (3, 129, 32), (2, 300, 64), (1, 1, 32), (2, 520, 64)])
+def test_psa_fa2_forward_vs_oracle(dtype, bh, n, kd):
+    """One pass over the scores, applied to V_lo and V_hi: each output against the oracle's attention."""
+    torch = G.require_gpu()
+    packed = synth.tensor(f"psa_fused/{dtype}/{bh}/{n}/{kd}", (4, bh, n, kd), dtype)
+    pd = G.to_device(packed, dtype)
+    o_lo, o_hi = G.empty((bh, n, kd), dtype), G.empty((bh, n, kd), dtype)
+    lse = torch.empty((bh, n), dtype=torch.float32, device="cuda")
+    scale = 1 / math.sqrt(kd)
+    binding.psa_fa2_forward(pd, o_lo, o_hi, lse, scale)
+    binding.fa2_device_status()
+    w = synth.widen(packed, dtype)
+    r_lo, r_lse = A.forward(w[0], w[1], w[2], scale)
+    r_hi, _ = A.forward(w[0], w[1], w[3], scale)
+    check_16bit(G.to_f64(o_lo), r_lo, "O_lo")
+    check_16bit(G.to_f64(o_hi), r_hi, "O_hi")
+    from tests.tolerance import check_lse
+    check_lse(G.to_f64(lse), r_lse)
+
+
+def test_psa_fa2_forward_equals_two_calls():
+    """The fused call and the two separate fa2_forward calls agree to rounding (same scores, same P)."""
+    torch = G.require_gpu()
+    bh, n, kd = 32, 400, 32
+    packed = synth.tensor("psa_fused/two_calls", (4, bh, n, kd), "f16")
+    pd = G.to_device(packed, "f16")
+    fo = [G.empty((bh, n, kd), "f16") for _ in range(2)]
+    lse = torch.empty((bh, n), dtype=torch.float32, device="cuda")
+    binding.psa_fa2_forward(pd, fo[0], fo[1], lse, 1 / math.sqrt(kd))
+    so = [G.empty((bh, n, kd), "f16") for _ in range(2)]
+    sl = torch.empty_like(lse)
+    for i, sec in enumerate((2, 3)):
+        binding.fa2_forward(pd[0], pd[1], pd[sec], so[i], sl, 1 / math.sqrt(kd))
+    binding.fa2_device_status()
+    for a, b in zip(fo, so):
+        assert float((a.float() - b.float()).abs().max()) <= 2e-3
+    assert float((lse - sl).abs().max()) <= 1e-5

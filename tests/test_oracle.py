@@ -349,6 +349,56 @@ def test_psa_adjoints():
     assert np.isclose(np.sum(P.merge_attn_nchw(lo, hi, b_, nh, hh, ww) * g), np.sum(lo * dlo) + np.sum(hi * dhi), rtol=1e-12)
 
 
+def test_psa_adjoint_maps_brute():
+    """pack^T and merge^T as element loops on raw 16-bit words; extract_v^T on exact values."""
+    b_, nh, kd, hh, ww = 2, 2, 4, 3, 5
+    n = hh * ww
+    d_packed = synth.counter_u16("pin/dpacked", (4, b_ * nh, n, kd))
+    got = P.pack_qkv_backward(d_packed, b_, nh, hh, ww)
+    assert got.dtype == np.uint16
+    for s in range(4):
+        for bh in range(b_ * nh):
+            b, h = divmod(bh, nh)
+            for t in range(n):
+                for dd in range(kd):
+                    assert got[b, h * 4 * kd + s * kd + dd, t // ww, t % ww] == d_packed[s, bh, t, dd]
+    d_merged = synth.counter_u16("pin/dmerged", (b_, nh * 2 * kd, hh, ww))
+    d_lo, d_hi = P.merge_attn_backward(d_merged, nh)
+    for bh in range(b_ * nh):
+        b, h = divmod(bh, nh)
+        for t in range(n):
+            for dd in range(kd):
+                assert d_lo[bh, t, dd] == d_merged[b, h * 2 * kd + dd, t // ww, t % ww]
+                assert d_hi[bh, t, dd] == d_merged[b, h * 2 * kd + kd + dd, t // ww, t % ww]
+    # extract_v^T: exact sums of small integers survive every rounding, other channels untouched
+    qkv = np.arange(b_ * nh * 4 * kd * n, dtype=np.float64).reshape(b_, nh * 4 * kd, hh, ww) % 7
+    dv = (np.arange(b_ * nh * 2 * kd * n, dtype=np.float64).reshape(b_, nh * 2 * kd, hh, ww) % 5) - 2
+    for dt in ("f32", "f16", "bf16"):
+        store = (lambda x: P._round_f64(x, dt))
+        out = P._words_to_f64(P.extract_v_backward(store(dv), store(qkv), nh, dt), dt)
+        want = qkv.copy()
+        for b in range(b_):
+            for h in range(nh):
+                for t in range(2 * kd):
+                    want[b, h * 4 * kd + 2 * kd + t] += dv[b, h * 2 * kd + t]
+        assert np.array_equal(out, want)
+
+
+def test_psa_extract_v_backward_is_the_adjoint():
+    """<extract_v(x), y> = <x, extract_v^T(y)> on exact values (extract_v^T applied to a zero d_qkv)."""
+    b_, nh, kd, hh, ww = 2, 3, 2, 2, 3
+    x = _rand((b_, nh * 4 * kd, hh, ww), 80)
+    y = _rand((b_, nh * 2 * kd, hh, ww), 81)
+    lhs = np.sum(P.extract_v_nchw(x, nh) * y)
+    back = np.zeros_like(x)
+    for h in range(nh):
+        back[:, h * 4 * kd + 2 * kd:(h + 1) * 4 * kd] += y[:, h * 2 * kd:(h + 1) * 2 * kd]
+    assert np.isclose(lhs, np.sum(x * back), rtol=1e-12)
+    # the oracle's accumulating adjoint in float32 storage agrees to float32 rounding
+    got = P.extract_v_backward(y.astype(np.float32), np.zeros_like(x, dtype=np.float32), nh, "f32")
+    assert np.allclose(got, back, atol=1e-6)
+
+
 def test_psa_rejects_bad_channels():
     with pytest.raises(ValueError):
         P.pack_qkv(np.zeros((1, 10, 2, 2), np.uint16), 1)
