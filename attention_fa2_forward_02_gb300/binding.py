@@ -31,6 +31,7 @@ EXPORTS = (
     "psa_pack_qkv",
     "psa_merge_attn_nchw",
     "psa_fa2_forward",
+    "psa_fa2_backward",
     "psa_extract_v_nchw",
     "psa_pack_qkv_backward",
     "psa_merge_attn_backward",
@@ -71,6 +72,7 @@ def _declare(lib):
         "psa_pack_qkv": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "psa_merge_attn_nchw": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "psa_fa2_forward": (ctypes.c_int, [_c_ptr] * 4 + [_i64, _i64, _i32, _i32, _f32, _c_ptr]),
+        "psa_fa2_backward": (ctypes.c_int, [_c_ptr] * 8 + [ctypes.c_size_t, _i64, _i64, _i32, _i32, _f32, _c_ptr]),
         "psa_extract_v_nchw": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 7 + [_c_ptr]),
         "psa_pack_qkv_backward": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "psa_merge_attn_backward": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
@@ -250,6 +252,24 @@ def psa_fa2_forward(packed, o_lo, o_hi, lse, softmax_scale: float, stream=None) 
                                    _dev(lse, "lse", 2), bh, n, kd, _dtype_code(packed), float(softmax_scale),
                                    _stream(stream))
     _check(st, "psa_fa2_forward")
+
+
+def psa_fa2_backward(packed, o_lo, o_hi, d_o_lo, d_o_hi, lse, d_packed, workspace, softmax_scale: float,
+                     stream=None) -> None:
+    """Gradients of both PSA attention calls into d_packed [4, BH, N, KD]:
+    (dQ_lo + dQ_hi, dK_lo + dK_hi, dV_lo, dV_hi)."""
+    _, bh, n, kd = packed.shape
+    for name, t in (("o_lo", o_lo), ("o_hi", o_hi), ("d_o_lo", d_o_lo), ("d_o_hi", d_o_hi)):
+        if t.shape != (bh, n, kd):
+            raise ValueError(f"{name} must be [BH, N, KD]")
+    if d_packed.shape != packed.shape or lse.shape != (bh, n):
+        raise ValueError("d_packed like packed; lse [BH, N]")
+    st = library().psa_fa2_backward(_dev(packed, "packed", 4), _dev(o_lo, "o_lo", 3), _dev(o_hi, "o_hi", 3),
+                                    _dev(d_o_lo, "d_o_lo", 3), _dev(d_o_hi, "d_o_hi", 3), _dev(lse, "lse", 2),
+                                    _dev(d_packed, "d_packed", 4), _dev(workspace, "workspace"),
+                                    workspace.numel() * workspace.element_size(), bh, n, kd, _dtype_code(packed),
+                                    float(softmax_scale), _stream(stream))
+    _check(st, "psa_fa2_backward")
 
 
 def psa_extract_v_nchw(qkv, v, num_heads: int, stream=None) -> None:

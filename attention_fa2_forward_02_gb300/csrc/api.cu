@@ -201,6 +201,35 @@ fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const vo
                            workspace_bytes, bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDq);
 }
 
+fa2_status psa_fa2_backward(const void* packed, const void* o_lo, const void* o_hi, const void* d_o_lo,
+                            const void* d_o_hi, const float* lse, void* d_packed, void* workspace,
+                            size_t workspace_bytes, int64_t bh, int64_t n, int32_t key_dim, fa2_dtype dtype,
+                            float softmax_scale, void* stream) {
+    if (!packed || !o_lo || !o_hi || !d_o_lo || !d_o_hi || !lse || !d_packed) return FA2_ERR_INVALID_ARG;
+    fa2_status st = check_attention_sizes(bh, n, n, key_dim, dtype, softmax_scale);
+    if (st != FA2_OK) return st;
+    if (dtype == FA2_DTYPE_F32 || key_dim == 128) return FA2_ERR_UNSUPPORTED;
+    const void* ptrs[] = {packed, o_lo, o_hi, d_o_lo, d_o_hi, lse, d_packed};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return FA2_ERR_MISALIGNED;
+    const size_t need = fa2_backward_workspace_size(bh, n, n, key_dim, dtype);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA2_ERR_WORKSPACE;
+    // sections of the packed buffers: base + s * BH * N * KEY_DIM (FlashAttn2PsaRuntimeOp's pointer arithmetic)
+    const size_t section = (size_t)bh * (size_t)n * (size_t)key_dim * 2;
+    const char* in = static_cast<const char*>(packed);
+    char* out = static_cast<char*>(d_packed);
+    BwdParams p{};
+    p.q = in; p.k = in + section; p.v = in + 2 * section; p.v2 = in + 3 * section;
+    p.o = o_lo; p.o2 = o_hi; p.d_o = d_o_lo; p.d_o2 = d_o_hi; p.lse = lse;
+    p.dq = out; p.dk = out + section; p.dv = out + 2 * section; p.dv2 = out + 3 * section;
+    p.n_q_pad = (n + 127) / 128 * 128;
+    p.delta = static_cast<float*>(workspace);
+    p.lse2 = p.delta + bh * p.n_q_pad;
+    p.bh = bh; p.n_q = n; p.n_k = n; p.d = key_dim; p.dtype = (int)dtype; p.scale = softmax_scale;
+    if (!status_word(&p.status)) return FA2_ERR_CUDA;
+    return launch_bwd_tc_dual_v(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
 static fa2_status psa_common(int32_t H, int32_t W, int32_t B, int32_t num_heads, fa2_dtype dtype, int* elem_bytes) {
     if (H <= 0 || W <= 0 || B <= 0 || num_heads <= 0) return FA2_ERR_INVALID_ARG;
     if (!valid_dtype(dtype)) return FA2_ERR_INVALID_ARG;

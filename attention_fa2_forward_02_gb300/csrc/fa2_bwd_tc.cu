@@ -39,9 +39,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------------------ preprocess
 
+// D_i = sum_d O_id dO_id (summed over the (O, dO) pairs when o2 / d_o2 are given).
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(256)
-    bwd_preprocess_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o, const float* __restrict__ lse,
+    bwd_preprocess_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o,
+                          const uint16_t* __restrict__ o2, const uint16_t* __restrict__ d_o2, const float* __restrict__ lse,
                           float* __restrict__ delta, float* __restrict__ lse2, int n_q, int n_q_pad) {
     constexpr int TPR = D / 8;             // threads per row, 8 elements (16 bytes) each
     constexpr int RPC = 256 / TPR;         // rows per CTA
@@ -51,22 +53,24 @@ __global__ void __launch_bounds__(256)
     float acc = 0.f;
     if (r < n_q) {
         const size_t off = ((size_t)bh * n_q + r) * D + part * 8;
-        const uint4 a = *reinterpret_cast<const uint4*>(o + off);
-        const uint4 b = *reinterpret_cast<const uint4*>(d_o + off);
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-        const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+        for (int pair = 0; pair < (o2 ? 2 : 1); ++pair) {
+            const uint4 a = *reinterpret_cast<const uint4*>((pair ? o2 : o) + off);
+            const uint4 b = *reinterpret_cast<const uint4*>((pair ? d_o2 : d_o) + off);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 fa, fb;
-            if constexpr (kBf16) {
-                fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[i]));
-                fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[i]));
-            } else {
-                fa = __half22float2(*reinterpret_cast<const __half2*>(&aw[i]));
-                fb = __half22float2(*reinterpret_cast<const __half2*>(&bw[i]));
+            for (int i = 0; i < 4; ++i) {
+                float2 fa, fb;
+                if constexpr (kBf16) {
+                    fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[i]));
+                    fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[i]));
+                } else {
+                    fa = __half22float2(*reinterpret_cast<const __half2*>(&aw[i]));
+                    fb = __half22float2(*reinterpret_cast<const __half2*>(&bw[i]));
+                }
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
             }
-            acc = fmaf(fa.x, fb.x, acc);
-            acc = fmaf(fa.y, fb.y, acc);
         }
     }
 #pragma unroll
@@ -80,16 +84,19 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------------------------ shared pieces
 
-template <int D>
+// kNV = number of (V, dO) pairs sharing the probabilities: 1 (plain attention) or
+// 2 (the PSA V_lo / V_hi pair: dP = dO_lo V_lo^T + dO_hi V_hi^T, one dV per pair).
+template <int D, int kNV>
 struct BwdCfg : Tile16<D> {
     static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
     static constexpr int kTile = BT * D * 2;
-    // dK/dV kernel: K, V resident; per stage Q_i, dO_i, lse2_i, delta_i
-    static constexpr int kStageDkv = 2 * kTile + 2 * BT * 4;
-    static constexpr int kDkvBar = 2 * kTile + kStages * kStageDkv;
-    // dQ kernel: Q, dO resident; per stage K_j, V_j
-    static constexpr int kStageDq = 2 * kTile;
-    static constexpr int kDqBar = 2 * kTile + kStages * kStageDq;
+    static_assert(256 + (kNV + 1) * D <= (int)kTmemCols, "tensor memory budget");
+    // dK/dV kernel: K, V (and V2) resident; per stage Q_i, dO_i (and dO2_i), lse2_i, delta_i
+    static constexpr int kStageDkv = (1 + kNV) * kTile + 2 * BT * 4;
+    static constexpr int kDkvBar = (1 + kNV) * kTile + kStages * kStageDkv;
+    // dQ kernel: Q, dO (and dO2) resident; per stage K_j, V_j (and V2_j)
+    static constexpr int kStageDq = (1 + kNV) * kTile;
+    static constexpr int kDqBar = (1 + kNV) * kTile + kStages * kStageDq;
     static constexpr int kNumBars = 1 + 2 * kStages + 5;
     static constexpr int kSmemDkv = kDkvBar + kNumBars * 8 + 16 + 1024;
     static constexpr int kSmemDq = kDqBar + kNumBars * 8 + 16 + 1024;
@@ -161,14 +168,15 @@ __device__ __forceinline__ int owned_chunk(int half, int cc) { return 2 * half +
 // S^T(i+1) overwrites the columns holding P^T(i) only after dV(i), which reads
 // them, was issued; dP^T(i+1) likewise follows dK(i).
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
                     const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dk,
-                    void* __restrict__ dv, int n_q, int n_k, int n_q_pad, float scale, float scale_log2,
-                    unsigned int* status) {
-    using C = BwdCfg<D>;
+                    void* __restrict__ dv, void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, float scale,
+                    float scale_log2, unsigned int* status) {
+    using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -183,11 +191,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kDkvBar + C::kNumBars * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kDkvBar + C::kNumBars * 8 + 4);
     const Watchdog wd{abort_flag, status};
-    const uint32_t k_smem = base, v_smem = base + C::kTile;
-    auto stage_q = [&](int s) { return base + 2 * C::kTile + s * C::kStageDkv; };
-    auto stage_do = [&](int s) { return stage_q(s) + C::kTile; };
-    auto stage_l2 = [&](int s) { return stage_q(s) + 2 * C::kTile; };
-    auto stage_dl = [&](int s) { return stage_q(s) + 2 * C::kTile + BT * 4; };
+    const uint32_t k_smem = base;
+    auto v_smem = [&](int v) { return base + (1 + v) * C::kTile; };  // V, V2 resident after K
+    auto stage_q = [&](int s) { return base + (1 + kNV) * C::kTile + s * C::kStageDkv; };
+    auto stage_do = [&](int s, int v) { return stage_q(s) + (1 + v) * C::kTile; };
+    auto stage_l2 = [&](int s) { return stage_q(s) + (1 + kNV) * C::kTile; };
+    auto stage_dl = [&](int s) { return stage_l2(s) + BT * 4; };
 
     if (threadIdx.x == 0) init_bars(bars, abort_flag);
     if (warp == 1) {
@@ -205,20 +214,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            mbar_arrive_expect_tx(bars.resident(), 2 * C::kTile);
+            mbar_arrive_expect_tx(bars.resident(), (1 + kNV) * C::kTile);
             for (int a = 0; a < C::kAtoms; ++a) {
                 tma_load_3d(k_smem + a * BT * C::kAtomRowBytes, &tm_k, bars.resident(), a * C::kAtomCols, k0, bh);
-                tma_load_3d(v_smem + a * BT * C::kAtomRowBytes, &tm_v, bars.resident(), a * C::kAtomCols, k0, bh);
+                for (int v = 0; v < kNV; ++v)
+                    tma_load_3d(v_smem(v) + a * BT * C::kAtomRowBytes, v ? &tm_v2 : &tm_v, bars.resident(),
+                                a * C::kAtomCols, k0, bh);
             }
             int issued = 0;
             bool ok = true;
             for (int i = 0; i < n_qt; ++i) {
                 const int s = i % S;
                 if (i >= S && !(ok = mbar_wait(bars.empty(s), ((i / S) & 1) ^ 1, wd))) break;
-                mbar_arrive_expect_tx(bars.full(s), 2 * C::kTile + 2 * BT * 4);
+                mbar_arrive_expect_tx(bars.full(s), (1 + kNV) * C::kTile + 2 * BT * 4);
                 for (int a = 0; a < C::kAtoms; ++a) {
                     tma_load_3d(stage_q(s) + a * BT * C::kAtomRowBytes, &tm_q, bars.full(s), a * C::kAtomCols, i * BT, bh);
-                    tma_load_3d(stage_do(s) + a * BT * C::kAtomRowBytes, &tm_do, bars.full(s), a * C::kAtomCols, i * BT, bh);
+                    for (int v = 0; v < kNV; ++v)
+                        tma_load_3d(stage_do(s, v) + a * BT * C::kAtomRowBytes, v ? &tm_do2 : &tm_do, bars.full(s),
+                                    a * C::kAtomCols, i * BT, bh);
                 }
                 const size_t w = (size_t)bh * n_q_pad + (size_t)i * BT;
                 bulk_load(stage_l2(s), lse2 + w, BT * 4, bars.full(s));
@@ -239,10 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem, C::kmajor(k_smem, kk, BT), C::kmajor(stage_q(s), kk, BT), idesc_s, kk > 0);
             };
-            auto issue_dpt = [&](int s) {  // dP^T = V dO^T
+            auto issue_dpt = [&](int s) {  // dP^T = sum over pairs of V dO^T
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128u, C::kmajor(v_smem, kk, BT), C::kmajor(stage_do(s), kk, BT), idesc_s, kk > 0);
+                for (int v = 0; v < kNV; ++v)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + 128u, C::kmajor(v_smem(v), kk, BT), C::kmajor(stage_do(s, v), kk, BT), idesc_s,
+                               (v > 0 || kk > 0));
             };
             bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
             if (ok) {
@@ -259,9 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!(ok = mbar_wait(bars.e1(), i & 1, wd))) break;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
-                    mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_do(s), kk, BT), idesc_g,
-                           (i > 0 || kk > 0));
+                for (int v = 0; v < kNV; ++v)
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO (one accumulator per pair)
+                        mma_ts(tmem + 256u + (uint32_t)(v * D), tmem + kPackedCol + (uint32_t)(kk * 8),
+                               C::mnmajor(stage_do(s, v), kk, BT), idesc_g, (i > 0 || kk > 0));
                 if (more) {
                     if (!(ok = mbar_wait(bars.full(sn), ((i + 1) / S) & 1, wd))) break;
                     tc_fence_after();
@@ -272,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
-                    mma_ts(tmem + 256u + D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_q(s), kk, BT),
-                           idesc_g, (i > 0 || kk > 0));
+                    mma_ts(tmem + 256u + (uint32_t)(kNV * D), tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
+                           C::mnmajor(stage_q(s), kk, BT), idesc_g, (i > 0 || kk > 0));
                 mma_commit(bars.empty(s));
                 if (more) {
                     issue_dpt(sn);
@@ -357,17 +375,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int key = k0 + quarter * 32 + lane;
             const size_t row = (size_t)bh * n_k + key;
-            // half 0 writes dV, half 1 writes dK (scaled)
-            const uint32_t src = tmem + lane_off + 256u + (half ? (uint32_t)D : 0u);
-            void* dst = half ? dk : dv;
-            const float mul = half ? scale : 1.f;
+            // half 0 writes dV (each pair's), half 1 writes dK (scaled)
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(src + 32u * c, r);
-                tmem_ld_wait();
-                reg_fence(r);
-                store_row_chunk<kBf16>(dst, row, D, c, r, mul, key < n_k);
+            for (int v = 0; v < (half ? 1 : kNV); ++v) {
+                const uint32_t src = tmem + lane_off + 256u + (uint32_t)((half ? kNV : v) * D);
+                void* dst = half ? dk : (v ? dv2 : dv);
+                const float mul = half ? scale : 1.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(src + 32u * c, r);
+                    tmem_ld_wait();
+                    reg_fence(r);
+                    store_row_chunk<kBf16>(dst, row, D, c, r, mul, key < n_k);
+                }
             }
         }
     }
@@ -388,13 +409,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // dS lives in the dP columns, so dP(j+1) follows dQ(j); the S columns hold only
 // scores, so S(j+1) needs nothing but the elementwise warps having read S(j).
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
                   const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dq, int n_q,
                   int n_k, int n_q_pad, float scale, float scale_log2, unsigned int* status) {
-    using C = BwdCfg<D>;
+    using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -409,9 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kDqBar + C::kNumBars * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kDqBar + C::kNumBars * 8 + 4);
     const Watchdog wd{abort_flag, status};
-    const uint32_t q_smem = base, do_smem = base + C::kTile;
-    auto stage_k = [&](int s) { return base + 2 * C::kTile + s * C::kStageDq; };
-    auto stage_v = [&](int s) { return stage_k(s) + C::kTile; };
+    const uint32_t q_smem = base;
+    auto do_smem = [&](int v) { return base + (1 + v) * C::kTile; };  // dO, dO2 resident after Q
+    auto stage_k = [&](int s) { return base + (1 + kNV) * C::kTile + s * C::kStageDq; };
+    auto stage_v = [&](int s, int v) { return stage_k(s) + (1 + v) * C::kTile; };
 
     if (threadIdx.x == 0) init_bars(bars, abort_flag);
     if (warp == 1) {
@@ -429,20 +452,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            mbar_arrive_expect_tx(bars.resident(), 2 * C::kTile);
+            mbar_arrive_expect_tx(bars.resident(), (1 + kNV) * C::kTile);
             for (int a = 0; a < C::kAtoms; ++a) {
                 tma_load_3d(q_smem + a * BT * C::kAtomRowBytes, &tm_q, bars.resident(), a * C::kAtomCols, q0, bh);
-                tma_load_3d(do_smem + a * BT * C::kAtomRowBytes, &tm_do, bars.resident(), a * C::kAtomCols, q0, bh);
+                for (int v = 0; v < kNV; ++v)
+                    tma_load_3d(do_smem(v) + a * BT * C::kAtomRowBytes, v ? &tm_do2 : &tm_do, bars.resident(),
+                                a * C::kAtomCols, q0, bh);
             }
             int issued = 0;
             bool ok = true;
             for (int j = 0; j < n_kt; ++j) {
                 const int s = j % S;
                 if (j >= S && !(ok = mbar_wait(bars.empty(s), ((j / S) & 1) ^ 1, wd))) break;
-                mbar_arrive_expect_tx(bars.full(s), 2 * C::kTile);
+                mbar_arrive_expect_tx(bars.full(s), (1 + kNV) * C::kTile);
                 for (int a = 0; a < C::kAtoms; ++a) {
                     tma_load_3d(stage_k(s) + a * BT * C::kAtomRowBytes, &tm_k, bars.full(s), a * C::kAtomCols, j * BT, bh);
-                    tma_load_3d(stage_v(s) + a * BT * C::kAtomRowBytes, &tm_v, bars.full(s), a * C::kAtomCols, j * BT, bh);
+                    for (int v = 0; v < kNV; ++v)
+                        tma_load_3d(stage_v(s, v) + a * BT * C::kAtomRowBytes, v ? &tm_v2 : &tm_v, bars.full(s),
+                                    a * C::kAtomCols, j * BT, bh);
                 }
                 issued = j + 1;
             }
@@ -460,10 +487,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem, C::kmajor(q_smem, kk, BT), C::kmajor(stage_k(s), kk, BT), idesc_s, kk > 0);
             };
-            auto issue_dp = [&](int s) {  // dP = dO V^T
+            auto issue_dp = [&](int s) {  // dP = sum over pairs of dO V^T
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128u, C::kmajor(do_smem, kk, BT), C::kmajor(stage_v(s), kk, BT), idesc_s, kk > 0);
+                for (int v = 0; v < kNV; ++v)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem + 128u, C::kmajor(do_smem(v), kk, BT), C::kmajor(stage_v(s, v), kk, BT), idesc_s,
+                               (v > 0 || kk > 0));
             };
             bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
             if (ok) {
@@ -591,44 +621,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------------------ launch
 
-template <int D, bool kBf16>
+template <int D, bool kBf16, int kNV>
 cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int stages) {
-    using C = BwdCfg<D>;
+    using C = BwdCfg<D, kNV>;
     if (stages & kBwdPreprocess) {
         constexpr int RPC = 256 / (D / 8);
         const dim3 grid((unsigned)((p.n_q_pad + RPC - 1) / RPC), (unsigned)p.bh, 1);
-        bwd_preprocess_kernel<D, kBf16><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(p.o),
-                                                                 static_cast<const uint16_t*>(p.d_o), p.lse, p.delta,
-                                                                 p.lse2, (int)p.n_q, (int)p.n_q_pad);
+        bwd_preprocess_kernel<D, kBf16><<<grid, 256, 0, stream>>>(
+            static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.d_o),
+            kNV == 2 ? static_cast<const uint16_t*>(p.o2) : nullptr, kNV == 2 ? static_cast<const uint16_t*>(p.d_o2) : nullptr,
+            p.lse, p.delta, p.lse2, (int)p.n_q, (int)p.n_q_pad);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     if (!(stages & (kBwdDkDv | kBwdDq))) return cudaSuccess;
     const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tv2, tdo2;
+    const void* v2 = kNV == 2 ? p.v2 : p.v;
+    const void* do2 = kNV == 2 ? p.d_o2 : p.d_o;
     if (!encode_tmap_3d(&tq, dt, 2, p.q, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
         !encode_tmap_3d(&tdo, dt, 2, p.d_o, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tdo2, dt, 2, do2, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
         !encode_tmap_3d(&tk, dt, 2, p.k, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
-        !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
+        !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tv2, dt, 2, v2, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
         return cudaErrorInvalidValue;
     const float scale_log2 = p.scale * kLog2e;
     cudaError_t e = cudaSuccess;
     if (stages & kBwdDkDv) {
-        auto dkdv = bwd_dkdv_kernel<D, kBf16>;
+        auto dkdv = bwd_dkdv_kernel<D, kBf16, kNV>;
         e = ensure_smem_limit(reinterpret_cast<const void*>(dkdv), C::kSmemDkv, slot);
         if (e != cudaSuccess) return e;
         dkdv<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDkv, stream>>>(
-            tq, tk, tv, tdo, p.lse2, p.delta, p.dk, p.dv, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.scale, scale_log2,
-            p.status);
+            tq, tk, tv, tdo, tv2, tdo2, p.lse2, p.delta, p.dk, p.dv, p.dv2, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad,
+            p.scale, scale_log2, p.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (!(stages & kBwdDq)) return cudaSuccess;
-    auto dqk = bwd_dq_kernel<D, kBf16>;
+    auto dqk = bwd_dq_kernel<D, kBf16, kNV>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
     if (e != cudaSuccess) return e;
     dqk<<<dim3((unsigned)((p.n_q + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDq, stream>>>(
-        tq, tk, tv, tdo, p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.scale, scale_log2, p.status);
+        tq, tk, tv, tdo, tv2, tdo2, p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.scale, scale_log2,
+        p.status);
     return cudaGetLastError();
 }
 
@@ -637,9 +673,19 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
 cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream, int stages) {
     const bool bf = p.dtype == kBf16;
     switch (p.d) {
-        case 32: return bf ? launch_impl<32, true>(p, stream, 16, stages) : launch_impl<32, false>(p, stream, 18, stages);
-        case 64: return bf ? launch_impl<64, true>(p, stream, 20, stages) : launch_impl<64, false>(p, stream, 22, stages);
-        case 128: return bf ? launch_impl<128, true>(p, stream, 24, stages) : launch_impl<128, false>(p, stream, 26, stages);
+        case 32: return bf ? launch_impl<32, true, 1>(p, stream, 16, stages) : launch_impl<32, false, 1>(p, stream, 18, stages);
+        case 64: return bf ? launch_impl<64, true, 1>(p, stream, 20, stages) : launch_impl<64, false, 1>(p, stream, 22, stages);
+        case 128:
+            return bf ? launch_impl<128, true, 1>(p, stream, 24, stages) : launch_impl<128, false, 1>(p, stream, 26, stages);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_bwd_tc_dual_v(const BwdParams& p, cudaStream_t stream) {
+    const bool bf = p.dtype == kBf16;
+    switch (p.d) {
+        case 32: return bf ? launch_impl<32, true, 2>(p, stream, 28, kBwdAll) : launch_impl<32, false, 2>(p, stream, 30, kBwdAll);
+        case 64: return bf ? launch_impl<64, true, 2>(p, stream, 32, kBwdAll) : launch_impl<64, false, 2>(p, stream, 34, kBwdAll);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -44,6 +44,11 @@ struct BwdParams {
     int dtype;
     float scale;
     unsigned int* status;
+    // second (V, O, dO) triple sharing the probabilities, for launch_bwd_tc_dual_v
+    const void* v2 = nullptr;
+    const void* o2 = nullptr;
+    const void* d_o2 = nullptr;
+    void* dv2 = nullptr;
 };
 
 // The PSA rearrangements.  Pack / merge and their adjoints are batched 2-D
@@ -70,6 +75,9 @@ cudaError_t launch_fwd_tc_dual_v(const FwdParams& p, cudaStream_t stream);
 // Backward stages, combinable as a bit mask.
 enum BwdStage : int { kBwdPreprocess = 1, kBwdDkDv = 2, kBwdDq = 4, kBwdAll = 7 };
 cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream, int stages);
+// All three stages for two (V, O, dO) triples sharing Q, K and the probabilities:
+// dQ, dK from the summed dS; dV and dV2 per triple.
+cudaError_t launch_bwd_tc_dual_v(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_psa(const PsaParams& p, cudaStream_t stream);
 
 // Encodes a 3-D tiled tensor map over a contiguous [d2, d1, d0] tensor of

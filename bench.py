@@ -394,6 +394,7 @@ def run_ours(args):
 
     # ------------------------------------------------------------------ PSA pack / merge bandwidth
     components.update(psa_bandwidth(torch, B, dev, pk))
+    components.update(c2psa_graph_timings(torch, B, dev))
 
     # ------------------------------------------------------------------ end to end, host buffers
     # Every step copies its inputs in from pinned host memory and all of its
@@ -463,6 +464,68 @@ def run_ours(args):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def c2psa_graph_timings(torch, B, dev):
+    """GPU time of the C2PSA block (QKV [8, 512, 20, 20] fp16) as CUDA graphs, replayed 200 times:
+    the forward (pack, fused attention, merge) and the training step (forward, then merge^T, fused
+    attention backward, pack^T, and extract_v / extract_v^T for the V path).  At this size every
+    kernel takes a few microseconds, so a graph removes the per-launch host cost."""
+    nh, kd, n, bh = PSA_NH, PSA_KD, PSA_N, PSA_BH
+    c = nh * 2 * kd
+    qkv = torch.randn((PSA_B, nh * 4 * kd, PSA_H, PSA_W), device=dev).to(torch.float16)
+    d_out = torch.randn((PSA_B, c, PSA_H, PSA_W), device=dev).to(torch.float16)
+    d_vpe = torch.randn_like(d_out)
+    packed = torch.empty((4, bh, n, kd), dtype=torch.float16, device=dev)
+    o_lo, o_hi = torch.empty((bh, n, kd), dtype=torch.float16, device=dev), torch.empty((bh, n, kd), dtype=torch.float16, device=dev)
+    lse = torch.empty((bh, n), dtype=torch.float32, device=dev)
+    merged, v_nchw = torch.empty_like(d_out), torch.empty_like(d_out)
+    d_lo, d_hi = torch.empty_like(o_lo), torch.empty_like(o_hi)
+    d_packed = torch.empty_like(packed)
+    d_qkv = torch.empty_like(qkv)
+    ws = torch.empty(B.fa2_backward_workspace_size(bh, n, n, kd, B.DTYPE_F16), dtype=torch.uint8, device=dev)
+    s32 = 1 / math.sqrt(kd)
+
+    def fwd():
+        B.psa_pack_qkv(qkv, packed, nh)
+        B.psa_fa2_forward(packed, o_lo, o_hi, lse, s32)
+        B.psa_merge_attn_nchw(o_lo, o_hi, merged, nh)
+
+    def train():
+        fwd()
+        B.psa_extract_v_nchw(qkv, v_nchw, nh)
+        B.psa_merge_attn_backward(d_out, d_lo, d_hi, nh)
+        B.psa_fa2_backward(packed, o_lo, o_hi, d_lo, d_hi, lse, d_packed, ws, s32)
+        B.psa_pack_qkv_backward(d_packed, d_qkv, nh)
+        B.psa_extract_v_backward(d_vpe, d_qkv, nh)
+
+    out = {}
+    for name, fn, launches in (("c2psa_fwd_graph_us", fwd, 3), ("c2psa_train_graph_us", train, 8)):
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    fn()  # warm-up outside capture: first-call set-up (smem limits, symbol lookups)
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            for _ in range(5):
+                g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(200):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            out[name] = e0.elapsed_time(e1) / 200 * 1e3
+            out[name.replace("_us", "_kernels")] = launches
+        except Exception as exc:  # noqa: BLE001
+            out[name] = f"unavailable: {type(exc).__name__}: {exc}"[:200]
+    B.fa2_device_status()
+    return out
 
 
 def psa_bandwidth(torch, B, dev, pk):

@@ -225,6 +225,32 @@ fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* ls
                            int32_t key_dim, fa2_dtype dtype, float softmax_scale, void* stream);
 
 /*
+ * psa_fa2_backward - the backward of both PSA attention calls into d_packed.
+ *
+ * Defined by "vision_rs/models/yolo/kernels/attention/psa.rs", kernel
+ * psa_fa2_backward as FlashAttn2PsaRuntimeOp wires it for the V_lo and V_hi
+ * calls: section 0 of d_packed receives dQ_lo + dQ_hi, section 1 dK_lo + dK_hi
+ * (the page adds them with atomics), section 2 dV_lo and section 3 dV_hi.
+ * The two calls share Q, K, the scores and the probabilities P, so
+ * dS = P * (dO_lo V_lo^T + dO_hi V_hi^T - D_lo - D_hi) gives both sums at once;
+ * one pass over key tiles (dK, dV_lo, dV_hi) and one over query tiles (dQ),
+ * with plain stores: deterministic, no zeroing of d_packed needed.
+ *
+ *   packed          [4, bh, n, key_dim]  dtype, device, read (Q, K, V_lo, V_hi)
+ *   o_lo, o_hi      [bh, n, key_dim]     dtype, device, read (as written by psa_fa2_forward)
+ *   d_o_lo, d_o_hi  [bh, n, key_dim]     dtype, device, read (gradients of o_lo, o_hi)
+ *   lse             [bh, n]              float32, device, read (from psa_fa2_forward)
+ *   d_packed        [4, bh, n, key_dim]  dtype, device, written (every element)
+ *   workspace       at least fa2_backward_workspace_size(bh, n, n, key_dim, dtype) bytes
+ *
+ * dtype F16 / BF16, key_dim in {32, 64}.  Errors as for fa2_backward.
+ */
+fa2_status psa_fa2_backward(const void* packed, const void* o_lo, const void* o_hi, const void* d_o_lo,
+                            const void* d_o_hi, const float* lse, void* d_packed, void* workspace,
+                            size_t workspace_bytes, int64_t bh, int64_t n, int32_t key_dim, fa2_dtype dtype,
+                            float softmax_scale, void* stream);
+
+/*
  * psa_extract_v_nchw - the V_lo / V_hi channels of QKV as an NCHW tensor.
  *
  * Defined by "vision_rs/models/yolo/kernels/attention/psa.rs", kernel

@@ -131,6 +131,19 @@ def backward_slice(q, k, v, d_o, scale: float, bh: int, row_chunk: int = 1024):
     return dq, dk, dv
 
 
+def psa_backward(packed: np.ndarray, d_o_lo: np.ndarray, d_o_hi: np.ndarray, scale: float) -> np.ndarray:
+    """Gradient of the PSA packed buffer [4, BH, N, KD] through both attention calls.
+
+    psa.rs ``psa_fa2_backward`` as ``FlashAttn2PsaRuntimeOp`` wires it for the V_lo
+    (section 2) and V_hi (section 3) calls: sections 0 and 1 receive the sums of the
+    two calls' dQ and dK, sections 2 and 3 each call's dV.
+    """
+    q, k, v_lo, v_hi = (np.asarray(packed[s], dtype=np.float64) for s in range(4))
+    dq_lo, dk_lo, dv_lo = backward(q, k, v_lo, d_o_lo, scale)
+    dq_hi, dk_hi, dv_hi = backward(q, k, v_hi, d_o_hi, scale)
+    return np.stack([dq_lo + dq_hi, dk_lo + dk_hi, dv_lo, dv_hi])
+
+
 def bwd_preprocess(o: np.ndarray, d_o: np.ndarray) -> np.ndarray:
     """D_i = sum_d O_id dO_id  (flash_attn2.rs backward, ``D_q = rowsum(O_q * dO_q)``)."""
     return np.sum(np.asarray(o, dtype=np.float64) * np.asarray(d_o, dtype=np.float64), axis=-1)

@@ -176,3 +176,71 @@ def test_psa_fa2_forward_equals_two_calls():
     for a, b in zip(fo, so):
         assert float((a.float() - b.float()).abs().max()) <= 2e-3
     assert float((lse - sl).abs().max()) <= 1e-5
+
+
+def _psa_fwd_bwd(packed, d_lo, d_hi, dtype, scale):
+    torch = G.require_gpu()
+    _, bh, n, kd = packed.shape
+    pd = G.to_device(packed, dtype)
+    o_lo, o_hi = G.empty((bh, n, kd), dtype), G.empty((bh, n, kd), dtype)
+    lse = torch.empty((bh, n), dtype=torch.float32, device="cuda")
+    binding.psa_fa2_forward(pd, o_lo, o_hi, lse, scale)
+    d_packed = G.empty(packed.shape, dtype)
+    code = {"bf16": binding.DTYPE_BF16, "f16": binding.DTYPE_F16}[dtype]
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n, n, kd, code), dtype=torch.uint8, device="cuda")
+    binding.psa_fa2_backward(pd, o_lo, o_hi, G.to_device(d_lo, dtype), G.to_device(d_hi, dtype), lse, d_packed, ws, scale)
+    binding.fa2_device_status()
+    return d_packed
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("bh,n,kd", [(32, 400, 32), (3, 129, 32), (2, 300, 64), (1, 1, 32)])
+def test_psa_fa2_backward_vs_oracle(dtype, bh, n, kd):
+    """Sections of d_packed: dQ_lo + dQ_hi, dK_lo + dK_hi, dV_lo, dV_hi against the oracle."""
+    tag = f"psa_bwd/{dtype}/{bh}/{n}/{kd}"
+    packed = synth.tensor(tag + "/packed", (4, bh, n, kd), dtype)
+    d_lo = synth.tensor(tag + "/dlo", (bh, n, kd), dtype)
+    d_hi = synth.tensor(tag + "/dhi", (bh, n, kd), dtype)
+    scale = 1 / math.sqrt(kd)
+    got = G.to_f64(_psa_fwd_bwd(packed, d_lo, d_hi, dtype, scale))
+    w = lambda x: synth.widen(x, dtype)  # noqa: E731
+    want = A.psa_backward(w(packed), w(d_lo), w(d_hi), scale)
+    for s, name in enumerate(("dQ_lo+dQ_hi", "dK_lo+dK_hi", "dV_lo", "dV_hi")):
+        check_16bit(got[s], want[s], name)
+
+
+def test_c2psa_training_chain():
+    """The whole C2PSA attention step and its gradient, fp16, QKV [8, 512, 20, 20], 4 heads, KEY_DIM 32:
+    pack -> fused attention -> merge; then merge^T -> fused attention backward -> pack^T, plus a
+    gradient arriving at the extracted V (extract_v^T adds it into d_qkv)."""
+    torch = G.require_gpu()
+    B, nh, kd, H, W = 8, 4, 32, 20, 20
+    n, bh, c = H * W, B * nh, nh * 2 * kd
+    qkv = synth.tensor("c2psa_train/qkv", (B, nh * 4 * kd, H, W), "f16")
+    d_out = synth.tensor("c2psa_train/dout", (B, c, H, W), "f16")
+    d_vpe = synth.tensor("c2psa_train/dvpe", (B, c, H, W), "f16")
+    scale = 1 / math.sqrt(kd)
+    qkv_d = G.to_device(qkv, "f16")
+    packed = G.empty((4, bh, n, kd), "f16")
+    binding.psa_pack_qkv(qkv_d, packed, nh)
+    o_lo, o_hi = G.empty((bh, n, kd), "f16"), G.empty((bh, n, kd), "f16")
+    lse = torch.empty((bh, n), dtype=torch.float32, device="cuda")
+    binding.psa_fa2_forward(packed, o_lo, o_hi, lse, scale)
+    d_lo, d_hi = G.empty((bh, n, kd), "f16"), G.empty((bh, n, kd), "f16")
+    binding.psa_merge_attn_backward(G.to_device(d_out, "f16"), d_lo, d_hi, nh)
+    d_packed = G.empty((4, bh, n, kd), "f16")
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n, n, kd, binding.DTYPE_F16), dtype=torch.uint8,
+                     device="cuda")
+    binding.psa_fa2_backward(packed, o_lo, o_hi, d_lo, d_hi, lse, d_packed, ws, scale)
+    d_qkv = G.empty(qkv.shape, "f16")
+    binding.psa_pack_qkv_backward(d_packed, d_qkv, nh)
+    binding.psa_extract_v_backward(G.to_device(d_vpe, "f16"), d_qkv, nh)
+    binding.fa2_device_status()
+    # oracle chain in float64
+    pk = synth.widen(P.pack_qkv(qkv, nh), "f16")
+    g_lo, g_hi = P.merge_attn_backward(synth.widen(d_out, "f16"), nh)
+    g_packed = A.psa_backward(pk, g_lo, g_hi, scale)
+    want = P.pack_qkv_backward(g_packed, B, nh, H, W)
+    for h in range(nh):
+        want[:, h * 4 * kd + 2 * kd:(h + 1) * 4 * kd] += synth.widen(d_vpe, "f16")[:, h * 2 * kd:(h + 1) * 2 * kd]
+    check_16bit(G.to_f64(d_qkv), want, "d_qkv")

@@ -223,6 +223,31 @@ def test_backward_slice_pinned():
     assert pin_gradient_closed_forms(sliced)
 
 
+def test_psa_backward_finite_differences():
+    """Gradient of L = sum(O_lo * dO_lo) + sum(O_hi * dO_hi) w.r.t. every element of the packed buffer."""
+    packed = _rand((4, 1, 4, 3), 95)
+    d_lo, d_hi = _rand((1, 4, 3), 96), _rand((1, 4, 3), 97)
+    scale = 0.6
+
+    def loss(pk):
+        o_lo, _ = A.forward(pk[0], pk[1], pk[2], scale)
+        o_hi, _ = A.forward(pk[0], pk[1], pk[3], scale)
+        return float(np.sum(o_lo * d_lo) + np.sum(o_hi * d_hi))
+
+    g = A.psa_backward(packed, d_lo, d_hi, scale)
+    h = 1e-6
+    num = np.zeros_like(packed)
+    for idx in np.ndindex(packed.shape):
+        old = packed[idx]
+        packed[idx] = old + h
+        fp = loss(packed)
+        packed[idx] = old - h
+        fm = loss(packed)
+        packed[idx] = old
+        num[idx] = (fp - fm) / (2 * h)
+    assert np.allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
 def test_preprocess_loop():
     o, d_o = _rand((2, 3, 5), 60), _rand((2, 3, 5), 61)
     want = np.array([[math.fsum(o[b, i, t] * d_o[b, i, t] for t in range(5)) for i in range(3)] for b in range(2)])
