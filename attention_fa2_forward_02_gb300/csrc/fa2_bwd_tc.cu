@@ -94,10 +94,15 @@ struct BwdCfg : Tile16<D> {
     // dK/dV kernel: K, V (and V2) resident; per stage Q_i, dO_i (and dO2_i), lse2_i, delta_i
     static constexpr int kStageDkv = (1 + kNV) * kTile + 2 * BT * 4;
     static constexpr int kDkvBar = (1 + kNV) * kTile + kStages * kStageDkv;
-    // dQ kernel: Q, dO (and dO2) resident; per stage K_j, V_j (and V2_j)
+    // dQ kernel: Q, dO (and dO2) live in tensor memory (copied once per CTA); per
+    // stage K_j, V_j (and V2_j) in shared memory
+    static constexpr int kStagesDq = D == 128 ? 3 : 4;
     static constexpr int kStageDq = (1 + kNV) * kTile;
-    static constexpr int kDqBar = (1 + kNV) * kTile + kStages * kStageDq;
-    static constexpr int kNumBars = 1 + 2 * kStages + 5;
+    static constexpr int kDqBar = kStagesDq * kStageDq;
+    static constexpr int kQCol = 256 + D;                              // Q as 16-bit pairs: D/2 columns
+    static constexpr int kDoCol = 256 + D + D / 2;                     // dO (then dO2): D/2 columns each
+    static_assert(kDoCol + kNV * D / 2 <= (int)kTmemCols, "tensor memory budget of the dQ pass");
+    static constexpr int kNumBars = 1 + 2 * (kStagesDq > kStages ? kStagesDq : kStages) + 5;
     static constexpr int kSmemDkv = kDkvBar + kNumBars * 8 + 16 + 1024;
     static constexpr int kSmemDq = kDqBar + kNumBars * 8 + 16 + 1024;
     static_assert(kSmemDkv <= 227 * 1024 && kSmemDq <= 227 * 1024, "shared memory budget");
@@ -105,7 +110,8 @@ struct BwdCfg : Tile16<D> {
 };
 
 // Barriers shared by both kernels:
-//   resident  the tiles loaded once per CTA          (TMA transaction count)
+//   resident  dK/dV pass: K, V loaded once per CTA   (TMA transaction count);
+//             dQ pass: Q, dO copied into tensor memory (256 arrivals)
 //   full[s]   stage s loaded                         (TMA transaction count)
 //   empty[s]  stage s no longer read by any MMA      (tcgen05.commit)
 //   s_full    the first score tile (S^T or S) is in TMEM   (tcgen05.commit)
@@ -127,9 +133,9 @@ struct Bars {
     __device__ uint32_t done() const { return base + 8u * (5 + 2 * S); }
 };
 
-__device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_flag) {
+__device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_flag, uint32_t resident_count) {
     *abort_flag = 0;
-    mbar_init(b.resident(), 1);
+    mbar_init(b.resident(), resident_count);
     for (int s = 0; s < b.S; ++s) {
         mbar_init(b.full(s), 1);
         mbar_init(b.empty(s), 1);
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage_l2 = [&](int s) { return stage_q(s) + (1 + kNV) * C::kTile; };
     auto stage_dl = [&](int s) { return stage_l2(s) + BT * 4; };
 
-    if (threadIdx.x == 0) init_bars(bars, abort_flag);
+    if (threadIdx.x == 0) init_bars(bars, abort_flag, 1);
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
         tmem_relinquish();
@@ -408,16 +414,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   [e2(j)] dQ += dS(j) K(j) -> empty, dP(j+1) -> dp_full, ...
 // dS lives in the dP columns, so dP(j+1) follows dQ(j); the S columns hold only
 // scores, so S(j+1) needs nothing but the elementwise warps having read S(j).
+// Q and dO are the same for every key tile: the elementwise warps copy them once
+// into tensor memory (16-bit pairs, the layout an MMA reads its A operand in), so
+// S and dP read only K and V from shared memory.
 
 template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_v2, const uint16_t* __restrict__ q_ptr,
+                  const uint16_t* __restrict__ do_ptr, const uint16_t* __restrict__ do2_ptr,
                   const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dq, int n_q,
                   int n_k, int n_q_pad, float scale, float scale_log2, unsigned int* status) {
     using C = BwdCfg<D, kNV>;
-    constexpr int S = C::kStages;
+    constexpr int S = C::kStagesDq;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -431,12 +440,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kDqBar + C::kNumBars * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kDqBar + C::kNumBars * 8 + 4);
     const Watchdog wd{abort_flag, status};
-    const uint32_t q_smem = base;
-    auto do_smem = [&](int v) { return base + (1 + v) * C::kTile; };  // dO, dO2 resident after Q
-    auto stage_k = [&](int s) { return base + (1 + kNV) * C::kTile + s * C::kStageDq; };
+    auto stage_k = [&](int s) { return base + s * C::kStageDq; };
     auto stage_v = [&](int s, int v) { return stage_k(s) + (1 + v) * C::kTile; };
 
-    if (threadIdx.x == 0) init_bars(bars, abort_flag);
+    if (threadIdx.x == 0) init_bars(bars, abort_flag, kElemThreads);
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_holder), kTmemCols);
         tmem_relinquish();
@@ -448,17 +455,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            prefetch_tmap(&tm_do);
-            mbar_arrive_expect_tx(bars.resident(), (1 + kNV) * C::kTile);
-            for (int a = 0; a < C::kAtoms; ++a) {
-                tma_load_3d(q_smem + a * BT * C::kAtomRowBytes, &tm_q, bars.resident(), a * C::kAtomCols, q0, bh);
-                for (int v = 0; v < kNV; ++v)
-                    tma_load_3d(do_smem(v) + a * BT * C::kAtomRowBytes, v ? &tm_do2 : &tm_do, bars.resident(),
-                                a * C::kAtomCols, q0, bh);
-            }
+            if (kNV == 2) prefetch_tmap(&tm_v2);
             int issued = 0;
             bool ok = true;
             for (int j = 0; j < n_kt; ++j) {
@@ -474,7 +473,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 issued = j + 1;
             }
             if (!ok) {
-                drain_wait(bars.resident(), 0);
                 for (int j = (issued > S ? issued - S : 0); j < issued; ++j) drain_wait(bars.full(j % S), (j / S) & 1);
             }
         }
@@ -482,18 +480,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
             const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
-            auto issue_s = [&](int s) {  // S = Q K^T
+            auto issue_s = [&](int s) {  // S = Q K^T, Q from tensor memory
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem, C::kmajor(q_smem, kk, BT), C::kmajor(stage_k(s), kk, BT), idesc_s, kk > 0);
+                    mma_ts(tmem, tmem + (uint32_t)(C::kQCol + kk * 8), C::kmajor(stage_k(s), kk, BT), idesc_s, kk > 0);
             };
-            auto issue_dp = [&](int s) {  // dP = sum over pairs of dO V^T
+            auto issue_dp = [&](int s) {  // dP = sum over pairs of dO V^T, dO from tensor memory
 #pragma unroll
                 for (int v = 0; v < kNV; ++v)
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + 128u, C::kmajor(do_smem(v), kk, BT), C::kmajor(stage_v(s, v), kk, BT), idesc_s,
-                               (v > 0 || kk > 0));
+                        mma_ts(tmem + 128u, tmem + (uint32_t)(C::kDoCol + v * D / 2 + kk * 8),
+                               C::kmajor(stage_v(s, v), kk, BT), idesc_s, (v > 0 || kk > 0));
             };
             bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
             if (ok) {
@@ -538,6 +536,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t w = (size_t)bh * n_q_pad + row;  // row < n_q_pad always
         const float my_l2 = lse2[w];
         const float my_d = delta[w];
+        // This thread's row of Q (half 0) or of dO / dO2 (half 1) into tensor memory,
+        // zeros past the last query; pairs of 16-bit elements per 32-bit column.
+        {
+            const bool valid = row < n_q;
+            for (int t = 0; t < (half ? kNV : 1); ++t) {
+                const uint16_t* src = half ? (t ? do2_ptr : do_ptr) : q_ptr;
+                const uint32_t col = half ? (uint32_t)(C::kDoCol + t * D / 2) : (uint32_t)C::kQCol;
+                const uint4* rowp = reinterpret_cast<const uint4*>(src + ((size_t)bh * n_q + (valid ? row : 0)) * D);
+                if constexpr (D >= 64) {
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        uint32_t wv[32];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const uint4 x = valid ? rowp[c * 8 + u] : make_uint4(0u, 0u, 0u, 0u);
+                            wv[4 * u] = x.x;
+                            wv[4 * u + 1] = x.y;
+                            wv[4 * u + 2] = x.z;
+                            wv[4 * u + 3] = x.w;
+                        }
+                        tmem_st32(tmem + lane_off + col + 32u * c, wv);
+                    }
+                } else {
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint4 x = valid ? rowp[u] : make_uint4(0u, 0u, 0u, 0u);
+                        wv[4 * u] = x.x;
+                        wv[4 * u + 1] = x.y;
+                        wv[4 * u + 2] = x.z;
+                        wv[4 * u + 3] = x.w;
+                    }
+                    tmem_st16(tmem + lane_off + col, wv);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bars.resident());
+        }
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         const float2 neg_l2 = make_float2(-my_l2, -my_l2), neg_d = make_float2(-my_d, -my_d);
         bool ok = true;
@@ -663,8 +700,9 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
     if (e != cudaSuccess) return e;
     dqk<<<dim3((unsigned)((p.n_q + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDq, stream>>>(
-        tq, tk, tv, tdo, tv2, tdo2, p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.scale, scale_log2,
-        p.status);
+        tk, tv, tv2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
+        static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k,
+        (int)p.n_q_pad, p.scale, scale_log2, p.status);
     return cudaGetLastError();
 }
 
