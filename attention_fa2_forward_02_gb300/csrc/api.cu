@@ -56,7 +56,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool valid_dtype(fa2_dtype d) { return d == FA2_DTYPE_F32 || d == FA2_DTYPE_F16 || d == FA2_DTYPE_BF16; }
 
-bool supported_head_dim(int32_t d) { return d == 32 || d == 64 || d == 128; }
+// Any multiple of 8 up to 128: the kernels run at the next of 32, 64, 128 with the
+// extra columns read as zeros (TMA fills past the tensor edge) and never stored.
+bool supported_head_dim(int32_t d) { return d >= 8 && d <= 128 && d % 8 == 0; }
 
 constexpr int64_t kMaxGridY = 65535;
 constexpr int64_t kMaxSeq = (int64_t)1 << 30;
@@ -123,7 +125,7 @@ fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* ls
     if (!packed || !o_lo || !o_hi || !lse) return FA2_ERR_INVALID_ARG;
     fa2_status st = check_attention_sizes(bh, n, n, key_dim, dtype, softmax_scale);
     if (st != FA2_OK) return st;
-    if (dtype == FA2_DTYPE_F32 || key_dim == 128) return FA2_ERR_UNSUPPORTED;
+    if (dtype == FA2_DTYPE_F32 || key_dim > 64) return FA2_ERR_UNSUPPORTED;
     if (!aligned16(packed) || !aligned16(o_lo) || !aligned16(o_hi) || !aligned16(lse)) return FA2_ERR_MISALIGNED;
     // sections of the packed buffer, as FlashAttn2PsaRuntimeOp addresses them: base + s * BH * N * KEY_DIM
     const size_t section = (size_t)bh * (size_t)n * (size_t)key_dim * 2;
@@ -208,7 +210,7 @@ fa2_status psa_fa2_backward(const void* packed, const void* o_lo, const void* o_
     if (!packed || !o_lo || !o_hi || !d_o_lo || !d_o_hi || !lse || !d_packed) return FA2_ERR_INVALID_ARG;
     fa2_status st = check_attention_sizes(bh, n, n, key_dim, dtype, softmax_scale);
     if (st != FA2_OK) return st;
-    if (dtype == FA2_DTYPE_F32 || key_dim == 128) return FA2_ERR_UNSUPPORTED;
+    if (dtype == FA2_DTYPE_F32 || key_dim > 64) return FA2_ERR_UNSUPPORTED;
     const void* ptrs[] = {packed, o_lo, o_hi, d_o_lo, d_o_hi, lse, d_packed};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return FA2_ERR_MISALIGNED;
@@ -337,7 +339,7 @@ const char* fa2_status_string(fa2_status s) {
     switch (s) {
         case FA2_OK: return "ok";
         case FA2_ERR_INVALID_ARG: return "invalid argument (null pointer, size <= 0, inconsistent shape or bad scale)";
-        case FA2_ERR_UNSUPPORTED: return "unsupported (head_dim not in {32, 64, 128}, dtype, or a size beyond the kernels' limits)";
+        case FA2_ERR_UNSUPPORTED: return "unsupported (head_dim not a multiple of 8 in [8, 128], dtype, or a size beyond the kernels' limits)";
         case FA2_ERR_MISALIGNED: return "a tensor base pointer is not 16-byte aligned";
         case FA2_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
         case FA2_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (watchdog)";

@@ -44,15 +44,15 @@ template <int D, bool kBf16>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o,
                           const uint16_t* __restrict__ o2, const uint16_t* __restrict__ d_o2, const float* __restrict__ lse,
-                          float* __restrict__ delta, float* __restrict__ lse2, int n_q, int n_q_pad) {
+                          float* __restrict__ delta, float* __restrict__ lse2, int n_q, int n_q_pad, int d_act) {
     constexpr int TPR = D / 8;             // threads per row, 8 elements (16 bytes) each
     constexpr int RPC = 256 / TPR;         // rows per CTA
     const int bh = blockIdx.y;
     const int r = blockIdx.x * RPC + threadIdx.x / TPR;
     const int part = threadIdx.x % TPR;
     float acc = 0.f;
-    if (r < n_q) {
-        const size_t off = ((size_t)bh * n_q + r) * D + part * 8;
+    if (r < n_q && part * 8 < d_act) {  // rows of d_act <= D elements
+        const size_t off = ((size_t)bh * n_q + r) * d_act + part * 8;
         for (int pair = 0; pair < (o2 ? 2 : 1); ++pair) {
             const uint4 a = *reinterpret_cast<const uint4*>((pair ? o2 : o) + off);
             const uint4 b = *reinterpret_cast<const uint4*>((pair ? d_o2 : d_o) + off);
@@ -148,16 +148,19 @@ __device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_fla
     fence_barrier_init();
 }
 
+// Stores columns [32c, 32c + 32) of a row of d_act elements (16-byte pieces past
+// d_act, zeros of the padded tile, are skipped).
 template <bool kBf16>
-__device__ __forceinline__ void store_row_chunk(void* base, size_t row, int D, int c, const uint32_t (&r)[32], float mul,
-                                                bool valid) {
+__device__ __forceinline__ void store_row_chunk(void* base, size_t row, int d_act, int c, const uint32_t (&r)[32],
+                                                float mul, bool valid) {
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) pk[i] = pack2<kBf16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
     if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + row * D + 32 * c);
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + row * d_act + 32 * c);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int v = 0; v < 4; ++v)
+            if (32 * c + 8 * v < d_act) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
     }
 }
 
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
                     const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dk,
-                    void* __restrict__ dv, void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, float scale,
+                    void* __restrict__ dv, void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale,
                     float scale_log2, unsigned int* status) {
     using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStages;
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(src + 32u * c, r);
                     tmem_ld_wait();
                     reg_fence(r);
-                    store_row_chunk<kBf16>(dst, row, D, c, r, mul, key < n_k);
+                    store_row_chunk<kBf16>(dst, row, d_act, c, r, mul, key < n_k);
                 }
             }
         }
@@ -424,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v2, const uint16_t* __restrict__ q_ptr,
                   const uint16_t* __restrict__ do_ptr, const uint16_t* __restrict__ do2_ptr,
                   const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dq, int n_q,
-                  int n_k, int n_q_pad, float scale, float scale_log2, unsigned int* status) {
+                  int n_k, int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status) {
     using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStagesDq;
     extern __shared__ uint8_t smem_raw[];
@@ -543,14 +546,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < (half ? kNV : 1); ++t) {
                 const uint16_t* src = half ? (t ? do2_ptr : do_ptr) : q_ptr;
                 const uint32_t col = half ? (uint32_t)(C::kDoCol + t * D / 2) : (uint32_t)C::kQCol;
-                const uint4* rowp = reinterpret_cast<const uint4*>(src + ((size_t)bh * n_q + (valid ? row : 0)) * D);
+                const uint4* rowp = reinterpret_cast<const uint4*>(src + ((size_t)bh * n_q + (valid ? row : 0)) * d_act);
                 if constexpr (D >= 64) {
 #pragma unroll
                     for (int c = 0; c < D / 64; ++c) {
                         uint32_t wv[32];
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
-                            const uint4 x = valid ? rowp[c * 8 + u] : make_uint4(0u, 0u, 0u, 0u);
+                            const uint4 x = (valid && (c * 8 + u) * 8 < d_act) ? rowp[c * 8 + u] : make_uint4(0u, 0u, 0u, 0u);
                             wv[4 * u] = x.x;
                             wv[4 * u + 1] = x.y;
                             wv[4 * u + 2] = x.z;
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t wv[16];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const uint4 x = valid ? rowp[u] : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 x = (valid && u * 8 < d_act) ? rowp[u] : make_uint4(0u, 0u, 0u, 0u);
                         wv[4 * u] = x.x;
                         wv[4 * u + 1] = x.y;
                         wv[4 * u + 2] = x.z;
@@ -643,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + lane_off + 256u + 32u * c, r);
                 tmem_ld_wait();
                 reg_fence(r);
-                store_row_chunk<kBf16>(dq, (size_t)bh * n_q + row, D, c, r, scale, row < n_q);
+                store_row_chunk<kBf16>(dq, (size_t)bh * n_q + row, d_act, c, r, scale, row < n_q);
             }
         }
     }
@@ -667,7 +670,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         bwd_preprocess_kernel<D, kBf16><<<grid, 256, 0, stream>>>(
             static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.d_o),
             kNV == 2 ? static_cast<const uint16_t*>(p.o2) : nullptr, kNV == 2 ? static_cast<const uint16_t*>(p.d_o2) : nullptr,
-            p.lse, p.delta, p.lse2, (int)p.n_q, (int)p.n_q_pad);
+            p.lse, p.delta, p.lse2, (int)p.n_q, (int)p.n_q_pad, p.d);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -677,12 +680,14 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     CUtensorMap tq, tk, tv, tdo, tv2, tdo2;
     const void* v2 = kNV == 2 ? p.v2 : p.v;
     const void* do2 = kNV == 2 ? p.d_o2 : p.d_o;
-    if (!encode_tmap_3d(&tq, dt, 2, p.q, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
-        !encode_tmap_3d(&tdo, dt, 2, p.d_o, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
-        !encode_tmap_3d(&tdo2, dt, 2, do2, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
-        !encode_tmap_3d(&tk, dt, 2, p.k, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
-        !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
-        !encode_tmap_3d(&tv2, dt, 2, v2, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
+    // maps over the true head dimension p.d <= D: TMA fills the box columns past it with zeros
+    const uint64_t d = (uint64_t)p.d;
+    if (!encode_tmap_3d(&tq, dt, 2, p.q, d, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tdo, dt, 2, p.d_o, d, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tdo2, dt, 2, do2, d, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tk, dt, 2, p.k, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tv, dt, 2, p.v, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tv2, dt, 2, v2, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
         return cudaErrorInvalidValue;
     const float scale_log2 = p.scale * kLog2e;
     cudaError_t e = cudaSuccess;
@@ -692,7 +697,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         if (e != cudaSuccess) return e;
         dkdv<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDkv, stream>>>(
             tq, tk, tv, tdo, tv2, tdo2, p.lse2, p.delta, p.dk, p.dv, p.dv2, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad,
-            p.scale, scale_log2, p.status);
+            p.d, p.scale, scale_log2, p.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (!(stages & kBwdDq)) return cudaSuccess;
@@ -702,7 +707,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     dqk<<<dim3((unsigned)((p.n_q + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDq, stream>>>(
         tk, tv, tv2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
         static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k,
-        (int)p.n_q_pad, p.scale, scale_log2, p.status);
+        (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status);
     return cudaGetLastError();
 }
 
@@ -710,7 +715,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
 
 cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream, int stages) {
     const bool bf = p.dtype == kBf16;
-    switch (p.d) {
+    switch (pad_head_dim(p.d)) {
         case 32: return bf ? launch_impl<32, true, 1>(p, stream, 16, stages) : launch_impl<32, false, 1>(p, stream, 18, stages);
         case 64: return bf ? launch_impl<64, true, 1>(p, stream, 20, stages) : launch_impl<64, false, 1>(p, stream, 22, stages);
         case 128:
@@ -721,7 +726,7 @@ cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream, int stages) {
 
 cudaError_t launch_bwd_tc_dual_v(const BwdParams& p, cudaStream_t stream) {
     const bool bf = p.dtype == kBf16;
-    switch (p.d) {
+    switch (pad_head_dim(p.d)) {
         case 32: return bf ? launch_impl<32, true, 2>(p, stream, 28, kBwdAll) : launch_impl<32, false, 2>(p, stream, 30, kBwdAll);
         case 64: return bf ? launch_impl<64, true, 2>(p, stream, 32, kBwdAll) : launch_impl<64, false, 2>(p, stream, 34, kBwdAll);
         default: return cudaErrorInvalidValue;

@@ -19,7 +19,7 @@ constexpr int kKeyTile = 32;  // keys per shared-memory tile
 template <int D>
 __global__ void __launch_bounds__(kRows * 32)
     fa2_fwd_f32_kernel(const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
-                       float* __restrict__ o, float* __restrict__ lse, int n_q, int n_k, float scale) {
+                       float* __restrict__ o, float* __restrict__ lse, int n_q, int n_k, int d_act, float scale) {
     constexpr int E = D / 32;  // elements per lane
     __shared__ float ks[kKeyTile][D];
     __shared__ float vs[kKeyTile][D];
@@ -32,18 +32,22 @@ __global__ void __launch_bounds__(kRows * 32)
     float qr[E], acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        qr[e] = active ? q[((size_t)bh * n_q + row) * D + lane + 32 * e] : 0.f;
+        // elements past the true head dimension d_act <= D are zero
+        const bool in = active && lane + 32 * e < d_act;
+        qr[e] = in ? q[((size_t)bh * n_q + row) * d_act + lane + 32 * e] : 0.f;
         acc[e] = 0.f;
     }
     float m = -INFINITY, l = 0.f;
-    const float* kb = k + (size_t)bh * n_k * D;
-    const float* vb = v + (size_t)bh * n_k * D;
+    const float* kb = k + (size_t)bh * n_k * d_act;
+    const float* vb = v + (size_t)bh * n_k * d_act;
     for (int j0 = 0; j0 < n_k; j0 += kKeyTile) {
         const int nt = min(kKeyTile, n_k - j0);
         __syncthreads();
         for (int i = threadIdx.x; i < nt * D; i += blockDim.x) {
-            ks[i / D][i % D] = kb[(size_t)j0 * D + i];
-            vs[i / D][i % D] = vb[(size_t)j0 * D + i];
+            const int r = i / D, cidx = i % D;
+            const bool in = cidx < d_act;
+            ks[r][cidx] = in ? kb[(size_t)(j0 + r) * d_act + cidx] : 0.f;
+            vs[r][cidx] = in ? vb[(size_t)(j0 + r) * d_act + cidx] : 0.f;
         }
         __syncthreads();
         for (int j = 0; j < nt; ++j) {
@@ -64,7 +68,8 @@ __global__ void __launch_bounds__(kRows * 32)
     }
     if (active) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[((size_t)bh * n_q + row) * D + lane + 32 * e] = acc[e] / l;
+        for (int e = 0; e < E; ++e)
+            if (lane + 32 * e < d_act) o[((size_t)bh * n_q + row) * d_act + lane + 32 * e] = acc[e] / l;
         if (lane == 0) lse[(size_t)bh * n_q + row] = m + logf(l);
     }
 }
@@ -74,14 +79,14 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream) {
     const dim3 grid((unsigned)((p.n_q + kRows - 1) / kRows), (unsigned)p.bh, 1);
     fa2_fwd_f32_kernel<D><<<grid, kRows * 32, 0, stream>>>(static_cast<const float*>(p.q), static_cast<const float*>(p.k),
                                                           static_cast<const float*>(p.v), static_cast<float*>(p.o), p.lse,
-                                                          (int)p.n_q, (int)p.n_k, p.scale);
+                                                          (int)p.n_q, (int)p.n_k, p.d, p.scale);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd_f32(const FwdParams& p, cudaStream_t stream) {
-    switch (p.d) {
+    switch (pad_head_dim(p.d)) {
         case 32: return launch_impl<32>(p, stream);
         case 64: return launch_impl<64>(p, stream);
         case 128: return launch_impl<128>(p, stream);

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v2,
                       void* __restrict__ o_ptr, void* __restrict__ o2_ptr, float* __restrict__ lse_ptr, int n_q, int n_k,
-                      float scale_log2, unsigned int* status) {
+                      int d_act, float scale_log2, unsigned int* status) {
     using C = FwdCfg<D, kNV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -335,7 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = 1.f / l;
 #pragma unroll
             for (int v = 0; v < kNV; ++v) {
-                uint16_t* orow = reinterpret_cast<uint16_t*>(v ? o2_ptr : o_ptr) + ((size_t)bh * n_q + row) * D;
+                // rows of d_act <= D elements: the columns past d_act (zeros from the padded
+                // tiles) are never stored
+                uint16_t* orow = reinterpret_cast<uint16_t*>(v ? o2_ptr : o_ptr) + ((size_t)bh * n_q + row) * d_act;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t r[32];
@@ -350,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
                         for (int w = 0; w < 4; ++w)
-                            dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+                            if (32 * c + 8 * w < d_act)
+                                dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
                     }
                 }
             }
@@ -372,18 +375,20 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
     const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUtensorMap tq, tk, tv, tv2;
-    if (!encode_tmap_3d(&tq, dt, 2, p.q, D, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BM, sw) ||
-        !encode_tmap_3d(&tk, dt, 2, p.k, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw) ||
-        !encode_tmap_3d(&tv, dt, 2, p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw) ||
-        !encode_tmap_3d(&tv2, dt, 2, kNV == 2 ? p.v2 : p.v, D, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw))
+    // maps over the true head dimension p.d <= D: TMA fills the box columns past it with zeros
+    const uint64_t d = (uint64_t)p.d;
+    if (!encode_tmap_3d(&tq, dt, 2, p.q, d, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BM, sw) ||
+        !encode_tmap_3d(&tk, dt, 2, p.k, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw) ||
+        !encode_tmap_3d(&tv, dt, 2, p.v, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw) ||
+        !encode_tmap_3d(&tv2, dt, 2, kNV == 2 ? p.v2 : p.v, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BN, sw))
         return cudaErrorInvalidValue;
     auto kern = fa2_fwd_tc_kernel<D, kBf16, kNV>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((p.n_q + BM * kQTiles - 1) / (BM * kQTiles)), (unsigned)p.bh, 1);
     const float scale_log2 = p.scale * 1.4426950408889634f;
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k, scale_log2,
-                                                    p.status);
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k, p.d,
+                                                    scale_log2, p.status);
     return cudaGetLastError();
 }
 
@@ -391,7 +396,7 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
 
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream) {
     const bool bf = p.dtype == kBf16;
-    switch (p.d) {
+    switch (pad_head_dim(p.d)) {
         case 32: return bf ? launch_impl<32, true, 1>(p, stream, 0) : launch_impl<32, false, 1>(p, stream, 1);
         case 64: return bf ? launch_impl<64, true, 1>(p, stream, 2) : launch_impl<64, false, 1>(p, stream, 3);
         case 128: return bf ? launch_impl<128, true, 1>(p, stream, 4) : launch_impl<128, false, 1>(p, stream, 5);
@@ -401,7 +406,7 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream) {
 
 cudaError_t launch_fwd_tc_dual_v(const FwdParams& p, cudaStream_t stream) {
     const bool bf = p.dtype == kBf16;
-    switch (p.d) {
+    switch (pad_head_dim(p.d)) {
         case 32: return bf ? launch_impl<32, true, 2>(p, stream, 6) : launch_impl<32, false, 2>(p, stream, 7);
         case 64: return bf ? launch_impl<64, true, 2>(p, stream, 8) : launch_impl<64, false, 2>(p, stream, 9);
         default: return cudaErrorInvalidValue;

@@ -11,6 +11,9 @@ namespace fa2 {
 
 enum Dtype : int { kF32 = 0, kF16 = 1, kBf16 = 2 };
 
+// The kernel size a head dimension runs at (head_dim is a multiple of 8, <= 128).
+inline int pad_head_dim(int d) { return d <= 32 ? 32 : (d <= 64 ? 64 : 128); }
+
 struct FwdParams {
     const void* q;
     const void* k;

@@ -21,6 +21,11 @@
  *  - Layout of attention tensors: [BH, N, HEAD_DIM] with BH = BATCH * N_HEADS
  *    ("vision-rs 0.1.1 flash_attn2.rs", module comment: all tensors stored as
  *    [BATCH * N_HEADS, N_CTX, HEAD_DIM] row-major, contiguous).
+ *  - HEAD_DIM: any multiple of 8 from 8 to 128 (rows must be whole 16-byte
+ *    units for the tensor-memory copies).  The kernels run at the next of 32,
+ *    64, 128; the columns beyond HEAD_DIM are read as zeros and never written.
+ *    The pages' builders take any head dimension; one that is not a multiple
+ *    of 8 returns FA2_ERR_UNSUPPORTED.
  */
 #ifndef FA2_GB300_H
 #define FA2_GB300_H
@@ -66,9 +71,9 @@ typedef enum {
  *                              dtype; this library always stores float32)
  *   softmax_scale              > 0 and finite; callers normally pass 1/sqrt(head_dim)
  *
- * dtype BF16 / F16: head_dim in {32, 64, 128}; tensor-core kernel, float32
+ * dtype BF16 / F16: head_dim a multiple of 8 in [8, 128]; tensor-core kernel, float32
  * accumulation, the probabilities rounded to dtype before the P.V product.
- * dtype F32: head_dim in {32, 64, 128}; a float32 CUDA-core kernel (meant for
+ * dtype F32: head_dim a multiple of 8 in [8, 128]; a float32 CUDA-core kernel (meant for
  * small problems; float32 products and sums throughout).
  * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED, FA2_ERR_CUDA.
  */
@@ -103,7 +108,7 @@ size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t
  *               fa2_backward_workspace_size(...) bytes, 16-byte aligned; its
  *               contents on entry do not matter; the call overwrites it.
  *
- * dtype BF16 / F16 with head_dim in {32, 64, 128}; float32 accumulation.
+ * dtype BF16 / F16 with head_dim a multiple of 8 in [8, 128]; float32 accumulation.
  * dtype F32 returns FA2_ERR_UNSUPPORTED.
  * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED,
  *         FA2_ERR_WORKSPACE, FA2_ERR_CUDA.
@@ -218,7 +223,7 @@ fa2_status psa_merge_attn_nchw(const void* lo, const void* hi, void* out, int32_
  *   o_lo, o_hi  [bh, n, key_dim]      dtype, device, written
  *   lse         [bh, n]               float32, device, written (shared by both)
  *
- * dtype F16 / BF16, key_dim in {32, 64}; FA2_ERR_UNSUPPORTED otherwise.
+ * dtype F16 / BF16, key_dim a multiple of 8 in [8, 64]; FA2_ERR_UNSUPPORTED otherwise.
  * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED, FA2_ERR_CUDA.
  */
 fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* lse, int64_t bh, int64_t n,
@@ -243,7 +248,7 @@ fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* ls
  *   d_packed        [4, bh, n, key_dim]  dtype, device, written (every element)
  *   workspace       at least fa2_backward_workspace_size(bh, n, n, key_dim, dtype) bytes
  *
- * dtype F16 / BF16, key_dim in {32, 64}.  Errors as for fa2_backward.
+ * dtype F16 / BF16, key_dim a multiple of 8 in [8, 64].  Errors as for fa2_backward.
  */
 fa2_status psa_fa2_backward(const void* packed, const void* o_lo, const void* o_hi, const void* d_o_lo,
                             const void* d_o_hi, const float* lse, void* d_packed, void* workspace,

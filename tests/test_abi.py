@@ -62,7 +62,7 @@ def fwd(lib, q=P, k=P, v=P, o=P, l=P, bh=2, nq=64, nk=64, d=64, dt=BF16, scale=0
 @pytest.mark.parametrize("kw,want", [
     ({"q": None}, INVALID), ({"l": None}, INVALID), ({"bh": 0}, INVALID), ({"nq": 0}, INVALID), ({"nk": -1}, INVALID),
     ({"d": 0}, INVALID), ({"dt": 7}, INVALID), ({"scale": 0.0}, INVALID), ({"scale": float("nan")}, INVALID),
-    ({"scale": float("inf")}, INVALID), ({"d": 16}, UNSUPPORTED), ({"d": 96}, UNSUPPORTED), ({"d": 7}, UNSUPPORTED),
+    ({"scale": float("inf")}, INVALID), ({"d": 12}, UNSUPPORTED), ({"d": 136}, UNSUPPORTED), ({"d": 7}, UNSUPPORTED),
     ({"bh": 70000}, UNSUPPORTED), ({"q": PM}, MISALIGNED), ({"o": PM}, MISALIGNED),
 ])
 def test_forward_validation(lib, kw, want):
@@ -76,14 +76,15 @@ def test_backward_validation(lib):
     assert lib.fa2_backward(*args, P, 16, 2, 64, 64, 64, BF16, 0.125, None) == WORKSPACE
     assert lib.fa2_backward(*args, PM, 1 << 20, 2, 64, 64, 64, BF16, 0.125, None) == WORKSPACE
     assert lib.fa2_backward(None, *args[1:], P, 1 << 20, 2, 64, 64, 64, BF16, 0.125, None) == INVALID
-    assert lib.fa2_backward(*args, P, 1 << 20, 2, 64, 64, 48, BF16, 0.125, None) == UNSUPPORTED
+    assert lib.fa2_backward(*args, P, 1 << 20, 2, 64, 64, 44, BF16, 0.125, None) == UNSUPPORTED
     assert lib.fa2_backward(*args[:6], PM, *args[7:], P, 1 << 20, 2, 64, 64, 64, BF16, 0.125, None) == MISALIGNED
 
 
 def test_workspace_size(lib):
     assert lib.fa2_backward_workspace_size(2, 100, 50, 64, BF16) >= 2 * 100 * 4
     assert lib.fa2_backward_workspace_size(0, 100, 50, 64, BF16) == 0
-    assert lib.fa2_backward_workspace_size(2, 100, 50, 48, BF16) == 0
+    assert lib.fa2_backward_workspace_size(2, 100, 50, 44, BF16) == 0
+    assert lib.fa2_backward_workspace_size(2, 100, 50, 48, BF16) >= 2 * 100 * 4
 
 
 def test_psa_validation(lib):
