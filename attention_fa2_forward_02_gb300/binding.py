@@ -196,7 +196,7 @@ def _bwd_sizes(q, k, workspace):
 
 
 def fa2_backward_preprocess(o, d_o, lse, workspace, n_k: int, stream=None) -> None:
-    """Stage 1 of fa2_backward: fills the workspace (row sums D and the base-2 LSE)."""
+    """Stage 1 of the two-pass backward: fills the workspace (row sums D and the base-2 LSE)."""
     bh, n_q, d = o.shape
     st = library().fa2_backward_preprocess(_dev(o, "o", 3), _dev(d_o, "d_o", 3), _dev(lse, "lse", 2),
                                            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
@@ -205,7 +205,7 @@ def fa2_backward_preprocess(o, d_o, lse, workspace, n_k: int, stream=None) -> No
 
 
 def fa2_backward_dkdv(q, k, v, d_o, workspace, dk, dv, softmax_scale: float, stream=None) -> None:
-    """Stage 2 of fa2_backward: dK and dV (the pass over key tiles)."""
+    """Stage 2 of the two-pass backward: dK and dV (the pass over key tiles)."""
     bh, n_q, n_k, d, wsb = _bwd_sizes(q, k, workspace)
     st = library().fa2_backward_dkdv(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(d_o, "d_o", 3),
                                      _dev(workspace, "workspace"), wsb, _dev(dk, "dk", 3), _dev(dv, "dv", 3),
@@ -214,7 +214,7 @@ def fa2_backward_dkdv(q, k, v, d_o, workspace, dk, dv, softmax_scale: float, str
 
 
 def fa2_backward_dq(q, k, v, d_o, workspace, dq, softmax_scale: float, stream=None) -> None:
-    """Stage 3 of fa2_backward: dQ (the pass over query tiles)."""
+    """Stage 3 of the two-pass backward: dQ (the pass over query tiles)."""
     bh, n_q, n_k, d, wsb = _bwd_sizes(q, k, workspace)
     st = library().fa2_backward_dq(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(d_o, "d_o", 3),
                                    _dev(workspace, "workspace"), wsb, _dev(dq, "dq", 3),

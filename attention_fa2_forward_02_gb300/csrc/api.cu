@@ -101,6 +101,71 @@ cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
     return e;
 }
 
+// fa2_backward runs the one-pass kernel (dQ through float32 reductions) for
+// kernel head sizes up to 64 and the two-pass kernels above.  Measured on GB300
+// at BH = 32, N = 8192: head size 32 / 64: 1.62 / 1.79 ms one-pass against
+// 2.05 / 2.25 ms two-pass; head size 128: 2.99 ms against 2.78 ms, where the
+// reductions (4 bytes per query row, key tile and head column) reach the L2's
+// reduction throughput.
+static bool use_one_pass(int32_t head_dim) { return pad_head_dim(head_dim) <= 64; }
+
+// Workspace of the two-pass backward (the stage entry points, the PSA backward):
+// D and LSE2, float32, padded to a multiple of 128 rows per head.
+size_t two_pass_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype) {
+    if (check_attention_sizes(bh, n_q, n_k, head_dim, dtype, 1.0f) != FA2_OK) return 0;
+    const int64_t n_q_pad = (n_q + 127) / 128 * 128;
+    return 2 * (size_t)(bh * n_q_pad) * sizeof(float);
+}
+
+namespace {
+
+// stages = kBwdAll with one_pass, for a head size the one-pass kernel serves: the one-pass
+// backward (fa2_backward_workspace_size bytes); otherwise the given stages of the two-pass
+// backward (two_pass_workspace_size bytes).
+fa2_status backward_common(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
+                           void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int64_t bh,
+                           int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale,
+                           void* stream, int stages, bool one_pass) {
+    // pointers each stage reads or writes; the others may be null
+    const bool pre = stages & kBwdPreprocess, dkdv = stages & kBwdDkDv, dqs = stages & kBwdDq;
+    if ((pre && (!o || !d_o || !lse)) || ((dkdv || dqs) && (!q || !k || !v || !d_o)) || (dkdv && (!dk || !dv)) ||
+        (dqs && !dq))
+        return FA2_ERR_INVALID_ARG;
+    fa2_status st = check_attention_sizes(bh, n_q, n_k, head_dim, dtype, softmax_scale);
+    if (st != FA2_OK) return st;
+    if (dtype == FA2_DTYPE_F32) return FA2_ERR_UNSUPPORTED;
+    const void* ptrs[] = {q, k, v, o, d_o, lse, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return FA2_ERR_MISALIGNED;
+    one_pass = one_pass && stages == kBwdAll && use_one_pass(head_dim);
+    const size_t need = one_pass ? fa2_backward_workspace_size(bh, n_q, n_k, head_dim, dtype)
+                                 : two_pass_workspace_size(bh, n_q, n_k, head_dim, dtype);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA2_ERR_WORKSPACE;
+    BwdParams p{};
+    p.q = q; p.k = k; p.v = v; p.o = o; p.d_o = d_o; p.lse = lse;
+    p.dq = dq; p.dk = dk; p.dv = dv;
+    p.n_q_pad = (n_q + 127) / 128 * 128;
+    p.delta = static_cast<float*>(workspace);
+    p.lse2 = p.delta + bh * p.n_q_pad;
+    if (one_pass) p.dq_acc = p.lse2 + bh * p.n_q_pad;  // 16-byte aligned: n_q_pad is a multiple of 128
+    p.bh = bh; p.n_q = n_q; p.n_k = n_k; p.d = head_dim; p.dtype = (int)dtype; p.scale = softmax_scale;
+    if (!status_word(&p.status)) return FA2_ERR_CUDA;
+    const cudaError_t e = one_pass ? launch_bwd_fused(p, static_cast<cudaStream_t>(stream))
+                                   : launch_bwd_tc(p, static_cast<cudaStream_t>(stream), stages);
+    return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+}  // namespace
+
+fa2_status backward_two_pass(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                             const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype,
+                             float softmax_scale, void* stream) {
+    if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
+    return backward_common(q, k, v, o, d_o, lse, dq, dk, dv, workspace, workspace_bytes, bh, n_q, n_k, head_dim, dtype,
+                           softmax_scale, stream, kBwdAll, false);
+}
+
 }  // namespace fa2
 
 using namespace fa2;
@@ -137,38 +202,12 @@ fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* ls
     return launch_fwd_tc_dual_v(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
 }
 
+// The one-pass backward adds the float32 dQ accumulator, [bh, n_q_pad, pad_head_dim(head_dim)].
 size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype) {
-    if (check_attention_sizes(bh, n_q, n_k, head_dim, dtype, 1.0f) != FA2_OK) return 0;
+    const size_t two_pass = two_pass_workspace_size(bh, n_q, n_k, head_dim, dtype);
+    if (two_pass == 0 || !use_one_pass(head_dim)) return two_pass;
     const int64_t n_q_pad = (n_q + 127) / 128 * 128;
-    return 2 * (size_t)(bh * n_q_pad) * sizeof(float);
-}
-
-static fa2_status backward_common(const void* q, const void* k, const void* v, const void* o, const void* d_o,
-                                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
-                                  size_t workspace_bytes, int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
-                                  fa2_dtype dtype, float softmax_scale, void* stream, int stages) {
-    // pointers each stage reads or writes; the others may be null
-    const bool pre = stages & kBwdPreprocess, dkdv = stages & kBwdDkDv, dqs = stages & kBwdDq;
-    if ((pre && (!o || !d_o || !lse)) || ((dkdv || dqs) && (!q || !k || !v || !d_o)) || (dkdv && (!dk || !dv)) ||
-        (dqs && !dq))
-        return FA2_ERR_INVALID_ARG;
-    fa2_status st = check_attention_sizes(bh, n_q, n_k, head_dim, dtype, softmax_scale);
-    if (st != FA2_OK) return st;
-    if (dtype == FA2_DTYPE_F32) return FA2_ERR_UNSUPPORTED;
-    const void* ptrs[] = {q, k, v, o, d_o, lse, dq, dk, dv};
-    for (const void* ptr : ptrs)
-        if (ptr && !aligned16(ptr)) return FA2_ERR_MISALIGNED;
-    const size_t need = fa2_backward_workspace_size(bh, n_q, n_k, head_dim, dtype);
-    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA2_ERR_WORKSPACE;
-    BwdParams p{};
-    p.q = q; p.k = k; p.v = v; p.o = o; p.d_o = d_o; p.lse = lse;
-    p.dq = dq; p.dk = dk; p.dv = dv;
-    p.n_q_pad = (n_q + 127) / 128 * 128;
-    p.delta = static_cast<float*>(workspace);
-    p.lse2 = p.delta + bh * p.n_q_pad;
-    p.bh = bh; p.n_q = n_q; p.n_k = n_k; p.d = head_dim; p.dtype = (int)dtype; p.scale = softmax_scale;
-    if (!status_word(&p.status)) return FA2_ERR_CUDA;
-    return launch_bwd_tc(p, static_cast<cudaStream_t>(stream), stages) == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+    return two_pass + (size_t)(bh * n_q_pad) * (size_t)pad_head_dim(head_dim) * sizeof(float);
 }
 
 fa2_status fa2_backward(const void* q, const void* k, const void* v, const void* o, const void* d_o, const float* lse,
@@ -176,7 +215,7 @@ fa2_status fa2_backward(const void* q, const void* k, const void* v, const void*
                         int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
     if (!q || !k || !v || !o || !d_o || !lse || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
     return backward_common(q, k, v, o, d_o, lse, dq, dk, dv, workspace, workspace_bytes, bh, n_q, n_k, head_dim, dtype,
-                           softmax_scale, stream, kBwdAll);
+                           softmax_scale, stream, kBwdAll, true);
 }
 
 fa2_status fa2_backward_preprocess(const void* o, const void* d_o, const float* lse, void* workspace,
@@ -184,7 +223,7 @@ fa2_status fa2_backward_preprocess(const void* o, const void* d_o, const float* 
                                    fa2_dtype dtype, void* stream) {
     if (!o || !d_o || !lse) return FA2_ERR_INVALID_ARG;
     return backward_common(nullptr, nullptr, nullptr, o, d_o, lse, nullptr, nullptr, nullptr, workspace,
-                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, 1.0f, stream, kBwdPreprocess);
+                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, 1.0f, stream, kBwdPreprocess, false);
 }
 
 fa2_status fa2_backward_dkdv(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
@@ -192,7 +231,7 @@ fa2_status fa2_backward_dkdv(const void* q, const void* k, const void* v, const 
                              int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
     if (!q || !k || !v || !d_o || !dk || !dv) return FA2_ERR_INVALID_ARG;
     return backward_common(q, k, v, nullptr, d_o, nullptr, nullptr, dk, dv, const_cast<void*>(workspace),
-                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDkDv);
+                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDkDv, false);
 }
 
 fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
@@ -200,7 +239,7 @@ fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const vo
                            fa2_dtype dtype, float softmax_scale, void* stream) {
     if (!q || !k || !v || !d_o || !dq) return FA2_ERR_INVALID_ARG;
     return backward_common(q, k, v, nullptr, d_o, nullptr, dq, nullptr, nullptr, const_cast<void*>(workspace),
-                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDq);
+                           workspace_bytes, bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDq, false);
 }
 
 fa2_status psa_fa2_backward(const void* packed, const void* o_lo, const void* o_hi, const void* d_o_lo,
@@ -214,7 +253,7 @@ fa2_status psa_fa2_backward(const void* packed, const void* o_lo, const void* o_
     const void* ptrs[] = {packed, o_lo, o_hi, d_o_lo, d_o_hi, lse, d_packed};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return FA2_ERR_MISALIGNED;
-    const size_t need = fa2_backward_workspace_size(bh, n, n, key_dim, dtype);
+    const size_t need = two_pass_workspace_size(bh, n, n, key_dim, dtype);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA2_ERR_WORKSPACE;
     // sections of the packed buffers: base + s * BH * N * KEY_DIM (FlashAttn2PsaRuntimeOp's pointer arithmetic)
     const size_t section = (size_t)bh * (size_t)n * (size_t)key_dim * 2;

@@ -1,0 +1,407 @@
+// fa2_bwd_fused.cu - attention backward in one pass over key tiles, on the
+// sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// What it computes: the gradients of "vision-rs 0.1.1 flash_attn2.rs", kernels
+// flash_attention2_backward_dq and flash_attention2_backward_dkv:
+//   P_ij = exp(s_ij - LSE_i),  dV_j = sum_i P_ij dO_i,  dS_ij = P_ij (dO_i . v_j - D_i),
+//   dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
+// That page computes dQ in a pass of its own over query rows, which forms S and
+// dP a second time.  Here the pass over key tiles also forms the product
+// dS_(i,j) K_j of the query tile i it is visiting and adds it, with float32
+// vector reductions, into a dQ accumulator in the workspace; a last small
+// kernel scales the sums and rounds them into dq.  Each dQ element is then a
+// float32 sum of per-key-tile float32 partial sums, added in whatever order the
+// CTAs reach it (not bit-reproducible from run to run).
+//
+// Per CTA: one 128-key tile (K, V resident in shared memory), looping over the
+// query tiles of its head starting at tile (key tile index mod n_qt), so that the
+// CTAs of a head add into different query tiles at any one time.
+// Tensor memory (512 columns x 128 lanes):
+//   [0, 128)      S^T = K Q^T; then P^T, 16-bit, in columns [32, 96)
+//   [128, 256)    dP^T = V dO^T; then dS^T, 16-bit, in [160, 224); then dQ_i (D columns)
+//   [256, 256+D)  dV      [256+D, 256+2D)  dK
+// dS itself (queries x keys, the A operand of the dQ product) is written by the
+// elementwise warps into shared memory: over the dO tile of the stage (D = 128:
+// dV and dP^T, the only readers of dO, have completed by then) or into a
+// buffer of its own (D < 128, where a dO tile is too small).
+//
+// MMA order per query tile i (one thread issues, the tensor core runs in order):
+//   [e1(i)] dV += P^T(i) dO(i);  [dq_read(i-1)] dP^T(i) -> dp_full;
+//   S^T(i+1) -> s_full;  [e2(i)] dK += dS^T(i) Q(i);  dQ_i = dS(i) K -> dq_full, empty
+// Elementwise warps per query tile i:
+//   [s_full] P^T(i) -> e1;  [dq_full(i-1)] read dQ_(i-1), reduce into the
+//   accumulator -> dq_read;  [dp_full] dS^T(i) into TMEM, dS(i) into shared memory -> e2
+// so the warps compute P under dK / dQ, reduce dQ under dV and compute dS under
+// S^T, while the tensor core runs dV, dP^T, S^T, dK, dQ back to back.
+// In-order execution of the tensor core is what makes the column reuse safe: an
+// MMA that overwrites columns another reads (S^T(i+1) over P^T(i), dQ_i over
+// dS^T(i)) is always issued after the MMA that reads them.
+#include "bwd_common.cuh"
+#include "internal.h"
+
+namespace fa2 {
+namespace {
+
+template <int D>
+struct FusedCfg : Tile16<D> {
+    static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
+    static constexpr int kTile = BT * D * 2;
+    static constexpr int kDsBytes = BT * BT * 2;
+    static constexpr bool kDsInDo = kTile == kDsBytes;  // D = 128: dS over the stage's dO tile
+    // K, V resident; per stage Q_i, dO_i, lse2_i, delta_i; then (D < 128) the dS buffer; barriers
+    static constexpr int kStage = 2 * kTile + 2 * BT * 4;
+    static constexpr int kSmemStages = 2 * kTile;
+    static constexpr int kSmemDs = kSmemStages + kStages * kStage;
+    static constexpr int kSmemBar = kSmemDs + (kDsInDo ? 0 : kDsBytes);
+    static constexpr int kNumBars = 2 * kStages + kBwdBars;
+    static constexpr int kSmemBytes = kSmemBar + kNumBars * 8 + 16 + 1024;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kStage % 1024 == 0 && kSmemDs % 1024 == 0, "operand alignment");
+    static_assert(256 + 2 * D <= (int)kBwdTmemCols, "tensor memory budget");
+};
+
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const float* __restrict__ lse2, const float* __restrict__ delta, float* __restrict__ dq_acc,
+                     void* __restrict__ dk, void* __restrict__ dv, int n_q, int n_k, int n_q_pad, int d_act, float scale,
+                     float scale_log2, unsigned int* status) {
+    using C = FusedCfg<D>;
+    using DsTile = Tile16<BT>;  // dS as a [keys, queries] tile: MN-major A operand of the dQ product
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* smem = smem_raw + (base - raw_addr);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int bh = blockIdx.y;
+    const int k0 = blockIdx.x * BT;
+    const int n_qt = (n_q + BT - 1) / BT;
+    const int qt_first = blockIdx.x % n_qt;
+    auto qtile = [&](int i) { return (i + qt_first) % n_qt; };
+
+    const Bars bars{base + C::kSmemBar, S};
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kSmemBar + C::kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kSmemBar + C::kNumBars * 8 + 4);
+    const Watchdog wd{abort_flag, status};
+    const uint32_t k_smem = base;
+    const uint32_t v_smem = base + C::kTile;
+    auto stage_q = [&](int s) { return base + C::kSmemStages + s * C::kStage; };
+    auto stage_do = [&](int s) { return stage_q(s) + C::kTile; };
+    auto stage_l2 = [&](int s) { return stage_q(s) + 2 * C::kTile; };
+    auto stage_dl = [&](int s) { return stage_l2(s) + BT * 4; };
+    auto ds_smem = [&](int s) { return C::kDsInDo ? stage_do(s) : base + C::kSmemDs; };
+
+    if (threadIdx.x == 0) init_bars(bars, abort_flag, 1);
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_holder), kBwdTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            prefetch_tmap(&tm_do);
+            mbar_arrive_expect_tx(bars.resident(), 2 * C::kTile);
+            for (int a = 0; a < C::kAtoms; ++a) {
+                tma_load_3d(k_smem + a * BT * C::kAtomRowBytes, &tm_k, bars.resident(), a * C::kAtomCols, k0, bh);
+                tma_load_3d(v_smem + a * BT * C::kAtomRowBytes, &tm_v, bars.resident(), a * C::kAtomCols, k0, bh);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int i = 0; i < n_qt; ++i) {
+                const int s = i % S;
+                const int qt = qtile(i);
+                if (i >= S && !(ok = mbar_wait(bars.empty(s), ((i / S) & 1) ^ 1, wd))) break;
+                mbar_arrive_expect_tx(bars.full(s), 2 * C::kTile + 2 * BT * 4);
+                for (int a = 0; a < C::kAtoms; ++a) {
+                    tma_load_3d(stage_q(s) + a * BT * C::kAtomRowBytes, &tm_q, bars.full(s), a * C::kAtomCols, qt * BT, bh);
+                    tma_load_3d(stage_do(s) + a * BT * C::kAtomRowBytes, &tm_do, bars.full(s), a * C::kAtomCols, qt * BT,
+                                bh);
+                }
+                const size_t w = (size_t)bh * n_q_pad + (size_t)qt * BT;
+                bulk_load(stage_l2(s), lse2 + w, BT * 4, bars.full(s));
+                bulk_load(stage_dl(s), delta + w, BT * 4, bars.full(s));
+                issued = i + 1;
+            }
+            if (!ok) {
+                drain_wait(bars.resident(), 0);
+                for (int i = (issued > S ? issued - S : 0); i < issued; ++i) drain_wait(bars.full(i % S), (i / S) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);  // S^T, dP^T
+            const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);    // dV, dK: A from TMEM
+            const uint32_t idesc_q = idesc_f16_f32acc(BT, D, kBf16, true, true);     // dQ: both MN-major
+            auto issue_st = [&](int s) {  // S^T = K Q^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem, C::kmajor(k_smem, kk, BT), C::kmajor(stage_q(s), kk, BT), idesc_s, kk > 0);
+            };
+            bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
+            if (ok) {
+                tc_fence_after();
+                issue_st(0);
+                mma_commit(bars.s_full());
+            }
+            for (int i = 0; ok && i < n_qt; ++i) {
+                const int s = i % S;
+                const int sn = (i + 1) % S;
+                const bool more = i + 1 < n_qt;
+                if (!(ok = mbar_wait(bars.e1(), i & 1, wd))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
+                    mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_do(s), kk, BT), idesc_g,
+                           (i > 0 || kk > 0));
+                if (i > 0) {  // dP^T overwrites the columns of dQ_(i-1)
+                    if (!(ok = mbar_wait(bars.dq_read(), (i - 1) & 1, wd))) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO^T
+                    mma_ss(tmem + 128u, C::kmajor(v_smem, kk, BT), C::kmajor(stage_do(s), kk, BT), idesc_s, kk > 0);
+                mma_commit(bars.dp_full());
+                if (more) {
+                    if (!(ok = mbar_wait(bars.full(sn), ((i + 1) / S) & 1, wd))) break;
+                    tc_fence_after();
+                    issue_st(sn);
+                    mma_commit(bars.s_full());
+                }
+                if (!(ok = mbar_wait(bars.e2(), i & 1, wd))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
+                    mma_ts(tmem + 256u + (uint32_t)D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
+                           C::mnmajor(stage_q(s), kk, BT), idesc_g, (i > 0 || kk > 0));
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk)  // dQ_i = dS K (keys are the reduction dimension)
+                    mma_ss(tmem + 128u, DsTile::mnmajor(ds_smem(s), kk, BT), C::mnmajor(k_smem, kk, BT), idesc_q, kk > 0);
+                mma_commit(bars.dq_full());
+                mma_commit(bars.empty(s));
+            }
+            mma_commit(bars.done());
+            drain_wait(bars.done(), 0);
+        }
+    } else {
+        // ------------------------------------------------------------------ elementwise warps
+        // Two warps per TMEM lane quarter; warp `half` owns query columns [64*half, 64*half + 64)
+        // of the score tiles and dQ columns [half*D/2, half*D/2 + D/2).
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
+        const int r = quarter * 32 + lane;  // key row (score tiles) and query row (dQ tile) of this thread
+        const float2 scale2 = make_float2(scale_log2, scale_log2);
+        // Reads dQ of the i-th visited query tile out of TMEM and adds it into the
+        // accumulator, laid out per (bh, query tile) as [D/4][128 rows][4] floats so
+        // that a warp's 16-byte reductions cover 512 contiguous bytes.
+        auto reduce_dq = [&](int i) -> bool {
+            if (!warp_wait(bars.dq_full(), i & 1, wd)) return false;
+            tc_fence_after();
+            float4* tile = reinterpret_cast<float4*>(dq_acc) + ((size_t)bh * n_qt + qtile(i)) * (size_t)(D / 4) * BT + r;
+            if constexpr (D >= 64) {
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    const int col0 = half * (D / 2) + 32 * c;
+                    uint32_t v[32];
+                    tmem_ld32(t_dp + (uint32_t)col0, v);
+                    tmem_ld_wait();
+                    reg_fence(v);
+#pragma unroll
+                    for (int g = 0; g < 8; ++g)
+                        atomicAdd(tile + (size_t)(col0 / 4 + g) * BT,
+                                  make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                              __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
+                }
+            } else {
+                const int col0 = half * (D / 2);
+                uint32_t v[16];
+                tmem_ld16(t_dp + (uint32_t)col0, v);
+                tmem_ld_wait();
+                reg_fence(v);
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    atomicAdd(tile + (size_t)(col0 / 4 + g) * BT,
+                              make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
+                                          __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
+            }
+            tc_fence_before();
+            mbar_arrive(bars.dq_read());
+            return true;
+        };
+        bool ok = true;
+        for (int i = 0; i < n_qt; ++i) {
+            const int s = i % S;
+            if (!(ok = warp_wait(bars.s_full(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) break;
+            tc_fence_after();
+            const float* l2 = reinterpret_cast<const float*>(smem + (stage_l2(s) - base));
+            const float* dl = reinterpret_cast<const float*>(smem + (stage_dl(s) - base));
+            // step 1: P^T = 2^(S^T * scale * log2e - LSE2) for both owned chunks
+            float2 p[2][16];
+            {
+                uint32_t ra[32], rb[32];
+                tmem_ld32(t_s + 32u * owned_chunk(half, 0), ra);
+                tmem_ld32(t_s + 32u * owned_chunk(half, 1), rb);
+                tmem_ld_wait();
+                reg_fence(ra);
+                reg_fence(rb);
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = owned_chunk(half, cc);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const uint32_t* rr = cc == 0 ? ra : rb;
+                        const float2 lse = *reinterpret_cast<const float2*>(l2 + 32 * c + 2 * x);
+                        float2 v = __ffma2_rn(make_float2(__uint_as_float(rr[2 * x]), __uint_as_float(rr[2 * x + 1])),
+                                              scale2, make_float2(-lse.x, -lse.y));
+                        v.x = ex2_approx(v.x);
+                        v.y = ex2_approx(v.y);
+                        p[cc][x] = v;
+                        pk[x] = pack2<kBf16>(v.x, v.y);
+                    }
+                    tmem_st16(t_s + kPackedCol + 16u * c, pk);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(bars.e1());
+            // the previous query tile's dQ, while dV(i) runs
+            if (i > 0 && !(ok = reduce_dq(i - 1))) break;
+            // step 2: dS^T = P^T * (dP^T - D), chunk by chunk in write-safe order, into
+            // TMEM (for dK) and as dS into shared memory (for dQ)
+            if (!(ok = warp_wait(bars.dp_full(), i & 1, wd))) break;
+            tc_fence_after();
+            const uint32_t ds_row = ds_smem(s) + (uint32_t)r * 128u;  // row r of the [keys, queries] tile
+            const uint32_t swz = (uint32_t)(r & 7);                   // 128-byte swizzle of that row
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = owned_chunk(half, cc);
+                uint32_t rp[32];
+                tmem_ld32(t_dp + 32u * c, rp);
+                tmem_ld_wait();
+                reg_fence(rp);
+                uint32_t pk[16];
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const float2 dd = *reinterpret_cast<const float2*>(dl + 32 * c + 2 * x);
+                    const float2 ds = __fmul2_rn(p[cc][x], __fadd2_rn(make_float2(__uint_as_float(rp[2 * x]),
+                                                                                  __uint_as_float(rp[2 * x + 1])),
+                                                                      make_float2(-dd.x, -dd.y)));
+                    pk[x] = pack2<kBf16>(ds.x, ds.y);
+                }
+                tmem_st16(t_dp + kPackedCol + 16u * c, pk);
+                // queries [32c, 32c + 32): 64-column atom c / 2, 16-byte chunks 4 (c % 2) .. + 3
+                const uint32_t atom = ds_row + (uint32_t)(c >> 1) * (uint32_t)(BT * 128);
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    st_shared_v4(atom + (((uint32_t)((c & 1) * 4 + w) ^ swz) << 4), pk[4 * w], pk[4 * w + 1],
+                                 pk[4 * w + 2], pk[4 * w + 3]);
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bars.e2());
+        }
+        if (ok && n_qt > 0) ok = reduce_dq(n_qt - 1);
+        if (ok) ok = warp_wait(bars.done(), 0, wd);
+        if (ok) {
+            tc_fence_after();
+            const int key = k0 + r;
+            const size_t row = (size_t)bh * n_k + key;
+            // half 0 writes dV, half 1 writes dK (scaled)
+            const uint32_t src = tmem + lane_off + 256u + (uint32_t)(half * D);
+            void* dst = half ? dk : dv;
+            const float mul = half ? scale : 1.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(src + 32u * c, v);
+                tmem_ld_wait();
+                reg_fence(v);
+                store_row_chunk<kBf16>(dst, row, d_act, c, v, mul, key < n_k);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kBwdTmemCols);
+    }
+}
+
+// dq[bh, row, :d_act] = scale * the accumulated sums, rounded to the 16-bit dtype.
+// One thread per query row; a warp's loads cover 512 contiguous bytes.
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(BT)
+    bwd_dq_round_kernel(const float4* __restrict__ dq_acc, void* __restrict__ dq, int n_q, int d_act, float scale) {
+    const int qt = blockIdx.x, bh = blockIdx.y, r = threadIdx.x;
+    const int row = qt * BT + r;
+    if (row >= n_q) return;
+    const int n_qt = gridDim.x;
+    const float4* tile = dq_acc + ((size_t)bh * n_qt + qt) * (size_t)(D / 4) * BT + r;
+    uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dq) + ((size_t)bh * n_q + row) * d_act);
+#pragma unroll
+    for (int g = 0; g < D / 8; ++g) {
+        if (8 * g >= d_act) break;
+        const float4 a = tile[(size_t)(2 * g) * BT], b = tile[(size_t)(2 * g + 1) * BT];
+        out[g] = make_uint4(pack2<kBf16>(a.x * scale, a.y * scale), pack2<kBf16>(a.z * scale, a.w * scale),
+                            pack2<kBf16>(b.x * scale, b.y * scale), pack2<kBf16>(b.z * scale, b.w * scale));
+    }
+}
+
+template <int D, bool kBf16>
+cudaError_t fused_impl(const BwdParams& p, cudaStream_t stream, int slot) {
+    using C = FusedCfg<D>;
+    if (!p.dq_acc) return cudaErrorInvalidValue;
+    cudaError_t e = launch_bwd_tc(p, stream, kBwdPreprocess);  // D, LSE2, zeroed accumulator
+    if (e != cudaSuccess) return e;
+    const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap tq, tk, tv, tdo;
+    // maps over the true head dimension p.d <= D: TMA fills the box columns past it with zeros
+    const uint64_t d = (uint64_t)p.d;
+    if (!encode_tmap_3d(&tq, dt, 2, p.q, d, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tdo, dt, 2, p.d_o, d, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tk, dt, 2, p.k, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tv, dt, 2, p.v, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
+        return cudaErrorInvalidValue;
+    auto kern = bwd_fused_kernel<D, kBf16>;
+    e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot);
+    if (e != cudaSuccess) return e;
+    const int n_qt = (int)((p.n_q + BT - 1) / BT);
+    kern<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kBwdThreads, C::kSmemBytes, stream>>>(
+        tq, tk, tv, tdo, p.lse2, p.delta, p.dq_acc, p.dk, p.dv, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.d, p.scale,
+        p.scale * kLog2e, p.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_dq_round_kernel<D, kBf16><<<dim3((unsigned)n_qt, (unsigned)p.bh, 1), BT, 0, stream>>>(
+        reinterpret_cast<const float4*>(p.dq_acc), p.dq, (int)p.n_q, p.d, p.scale);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_fused(const BwdParams& p, cudaStream_t stream) {
+    const bool bf = p.dtype == kBf16;
+    switch (pad_head_dim(p.d)) {
+        case 32: return bf ? fused_impl<32, true>(p, stream, 36) : fused_impl<32, false>(p, stream, 37);
+        case 64: return bf ? fused_impl<64, true>(p, stream, 38) : fused_impl<64, false>(p, stream, 39);
+        case 128: return bf ? fused_impl<128, true>(p, stream, 40) : fused_impl<128, false>(p, stream, 41);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa2

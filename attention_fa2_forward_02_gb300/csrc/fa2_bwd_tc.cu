@@ -20,36 +20,34 @@
 // score columns they came from and consumed from there by the next MMA.
 // Warp roles (320 threads): warp 0 TMA, warp 1 TMEM allocation + MMA issue,
 // warps 2-9 elementwise (two warps per TMEM lane quarter).
-#include "common.cuh"
+#include "bwd_common.cuh"
 #include "internal.h"
 
 namespace fa2 {
 namespace {
 
-constexpr int BT = 128;         // rows of every tile (keys or queries)
-constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 elementwise
-constexpr int kElemThreads = 256;
-// The 16-bit probabilities / dS of a 128-column fp32 score tile occupy 64 columns
-// starting at column 32 of that tile: the warp owning score columns [0, 64)
-// writes [32, 64) and the one owning [64, 128) writes [64, 96), so each warp only
-// overwrites columns it has itself already read.
-constexpr uint32_t kPackedCol = 32;
-constexpr uint32_t kTmemCols = 512;
-constexpr float kLog2e = 1.4426950408889634f;
-
 // ------------------------------------------------------------------------------ preprocess
 
 // D_i = sum_d O_id dO_id (summed over the (O, dO) pairs when o2 / d_o2 are given).
+// With dq_acc given, also zeroes the float32 dQ accumulator of the one-pass
+// backward ([bh, n_q_pad, D] floats, D the kernel head size): each thread clears
+// the 8 floats of its own row and part, so the grid clears all of it.
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(256)
     bwd_preprocess_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o,
                           const uint16_t* __restrict__ o2, const uint16_t* __restrict__ d_o2, const float* __restrict__ lse,
-                          float* __restrict__ delta, float* __restrict__ lse2, int n_q, int n_q_pad, int d_act) {
+                          float* __restrict__ delta, float* __restrict__ lse2, float* __restrict__ dq_acc, int n_q,
+                          int n_q_pad, int d_act) {
     constexpr int TPR = D / 8;             // threads per row, 8 elements (16 bytes) each
     constexpr int RPC = 256 / TPR;         // rows per CTA
     const int bh = blockIdx.y;
     const int r = blockIdx.x * RPC + threadIdx.x / TPR;
     const int part = threadIdx.x % TPR;
+    if (dq_acc && r < n_q_pad) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * n_q_pad + r) * D + part * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     float acc = 0.f;
     if (r < n_q && part * 8 < d_act) {  // rows of d_act <= D elements
         const size_t off = ((size_t)bh * n_q + r) * d_act + part * 8;
@@ -90,7 +88,7 @@ template <int D, int kNV>
 struct BwdCfg : Tile16<D> {
     static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
     static constexpr int kTile = BT * D * 2;
-    static_assert(256 + (kNV + 1) * D <= (int)kTmemCols, "tensor memory budget");
+    static_assert(256 + (kNV + 1) * D <= (int)kBwdTmemCols, "tensor memory budget");
     // dK/dV kernel: K, V (and V2) resident; per stage Q_i, dO_i (and dO2_i), lse2_i, delta_i
     static constexpr int kStageDkv = (1 + kNV) * kTile + 2 * BT * 4;
     static constexpr int kDkvBar = (1 + kNV) * kTile + kStages * kStageDkv;
@@ -101,72 +99,13 @@ struct BwdCfg : Tile16<D> {
     static constexpr int kDqBar = kStagesDq * kStageDq;
     static constexpr int kQCol = 256 + D;                              // Q as 16-bit pairs: D/2 columns
     static constexpr int kDoCol = 256 + D + D / 2;                     // dO (then dO2): D/2 columns each
-    static_assert(kDoCol + kNV * D / 2 <= (int)kTmemCols, "tensor memory budget of the dQ pass");
-    static constexpr int kNumBars = 1 + 2 * (kStagesDq > kStages ? kStagesDq : kStages) + 5;
+    static_assert(kDoCol + kNV * D / 2 <= (int)kBwdTmemCols, "tensor memory budget of the dQ pass");
+    static constexpr int kNumBars = 2 * (kStagesDq > kStages ? kStagesDq : kStages) + kBwdBars;
     static constexpr int kSmemDkv = kDkvBar + kNumBars * 8 + 16 + 1024;
     static constexpr int kSmemDq = kDqBar + kNumBars * 8 + 16 + 1024;
     static_assert(kSmemDkv <= 227 * 1024 && kSmemDq <= 227 * 1024, "shared memory budget");
     static_assert(kStageDkv % 1024 == 0, "stage alignment");
 };
-
-// Barriers shared by both kernels:
-//   resident  dK/dV pass: K, V loaded once per CTA   (TMA transaction count);
-//             dQ pass: Q, dO copied into tensor memory (256 arrivals)
-//   full[s]   stage s loaded                         (TMA transaction count)
-//   empty[s]  stage s no longer read by any MMA      (tcgen05.commit)
-//   s_full    the first score tile (S^T or S) is in TMEM   (tcgen05.commit)
-//   dp_full   the second score tile (dP^T or dP) is in TMEM (tcgen05.commit)
-//   e1        elementwise step 1 done: dK/dV pass - P^T is in TMEM;
-//             dQ pass - S has been read (256 arrivals)
-//   e2        elementwise step 2 done: dS^T / dS is in TMEM (256 arrivals)
-//   done      every MMA issued has completed (tcgen05.commit)
-struct Bars {
-    uint32_t base;
-    int S;
-    __device__ uint32_t resident() const { return base; }
-    __device__ uint32_t full(int s) const { return base + 8u * (1 + s); }
-    __device__ uint32_t empty(int s) const { return base + 8u * (1 + S + s); }
-    __device__ uint32_t s_full() const { return base + 8u * (1 + 2 * S); }
-    __device__ uint32_t dp_full() const { return base + 8u * (2 + 2 * S); }
-    __device__ uint32_t e1() const { return base + 8u * (3 + 2 * S); }
-    __device__ uint32_t e2() const { return base + 8u * (4 + 2 * S); }
-    __device__ uint32_t done() const { return base + 8u * (5 + 2 * S); }
-};
-
-__device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_flag, uint32_t resident_count) {
-    *abort_flag = 0;
-    mbar_init(b.resident(), resident_count);
-    for (int s = 0; s < b.S; ++s) {
-        mbar_init(b.full(s), 1);
-        mbar_init(b.empty(s), 1);
-    }
-    mbar_init(b.s_full(), 1);
-    mbar_init(b.dp_full(), 1);
-    mbar_init(b.e1(), kElemThreads);
-    mbar_init(b.e2(), kElemThreads);
-    mbar_init(b.done(), 1);
-    fence_barrier_init();
-}
-
-// Stores columns [32c, 32c + 32) of a row of d_act elements (16-byte pieces past
-// d_act, zeros of the padded tile, are skipped).
-template <bool kBf16>
-__device__ __forceinline__ void store_row_chunk(void* base, size_t row, int d_act, int c, const uint32_t (&r)[32],
-                                                float mul, bool valid) {
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack2<kBf16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
-    if (valid) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(base) + row * d_act + 32 * c);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-            if (32 * c + 8 * v < d_act) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-    }
-}
-
-// The two 32-column chunks an elementwise warp owns, in the order that lets it
-// write 16-bit results at kPackedCol without overwriting a column it has not read.
-__device__ __forceinline__ int owned_chunk(int half, int cc) { return 2 * half + (half == 0 ? 1 - cc : cc); }
 
 // ------------------------------------------------------------------------------ dK / dV
 //
@@ -178,7 +117,7 @@ __device__ __forceinline__ int owned_chunk(int half, int cc) { return 2 * half +
 // them, was issued; dP^T(i+1) likewise follows dK(i).
 
 template <int D, bool kBf16, int kNV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
@@ -209,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) init_bars(bars, abort_flag, 1);
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_alloc(smem_u32(tmem_holder), kBwdTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -406,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, kBwdTmemCols);
     }
 }
 
@@ -422,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // S and dP read only K and V from shared memory.
 
 template <int D, bool kBf16, int kNV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_v2, const uint16_t* __restrict__ q_ptr,
                   const uint16_t* __restrict__ do_ptr, const uint16_t* __restrict__ do2_ptr,
@@ -448,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) init_bars(bars, abort_flag, kElemThreads);
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+        tmem_alloc(smem_u32(tmem_holder), kBwdTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -655,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, kBwdTmemCols);
     }
 }
 
@@ -670,7 +609,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         bwd_preprocess_kernel<D, kBf16><<<grid, 256, 0, stream>>>(
             static_cast<const uint16_t*>(p.o), static_cast<const uint16_t*>(p.d_o),
             kNV == 2 ? static_cast<const uint16_t*>(p.o2) : nullptr, kNV == 2 ? static_cast<const uint16_t*>(p.d_o2) : nullptr,
-            p.lse, p.delta, p.lse2, (int)p.n_q, (int)p.n_q_pad, p.d);
+            p.lse, p.delta, p.lse2, p.dq_acc, (int)p.n_q, (int)p.n_q_pad, p.d);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -695,7 +634,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         auto dkdv = bwd_dkdv_kernel<D, kBf16, kNV>;
         e = ensure_smem_limit(reinterpret_cast<const void*>(dkdv), C::kSmemDkv, slot);
         if (e != cudaSuccess) return e;
-        dkdv<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDkv, stream>>>(
+        dkdv<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kBwdThreads, C::kSmemDkv, stream>>>(
             tq, tk, tv, tdo, tv2, tdo2, p.lse2, p.delta, p.dk, p.dv, p.dv2, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad,
             p.d, p.scale, scale_log2, p.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -704,7 +643,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     auto dqk = bwd_dq_kernel<D, kBf16, kNV>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
     if (e != cudaSuccess) return e;
-    dqk<<<dim3((unsigned)((p.n_q + BT - 1) / BT), (unsigned)p.bh, 1), kThreads, C::kSmemDq, stream>>>(
+    dqk<<<dim3((unsigned)((p.n_q + BT - 1) / BT), (unsigned)p.bh, 1), kBwdThreads, C::kSmemDq, stream>>>(
         tk, tv, tv2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
         static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k,
         (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status);

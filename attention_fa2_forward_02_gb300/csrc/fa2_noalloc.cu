@@ -1,7 +1,7 @@
 // fa2_noalloc.cu - fa2_backward for callers that cannot allocate device memory.
 //
-// fa2_backward needs a device workspace (the row sums D and a base-2 copy of
-// the LSE).  Some callers cannot hand one over: code whose device memory is
+// fa2_backward needs a device workspace (the row sums D, a base-2 copy of the
+// LSE and a float32 dQ accumulator).  Some callers cannot hand one over: code whose device memory is
 // owned by a host framework's pool or arena (a raw cudaMalloc there would
 // bypass the pool's accounting), and services that fix their memory budget at
 // start-up and must not allocate - or risk running out of memory - while
@@ -23,8 +23,10 @@
 
 namespace fa2 {
 
-// 8 MiB: the workspace of fa2_backward is 8 bytes per query row (rounded up to
-// 128 rows per head), so this covers BH * ceil(n_q / 128) * 128 <= 1,048,576.
+// 8 MiB: the two-pass backward needs 8 bytes of workspace per query row (rounded
+// up to 128 rows per head), so this covers BH * ceil(n_q / 128) * 128 <= 1,048,576;
+// the one-pass backward (4 * head size bytes more per row, the dQ accumulator)
+// runs when it fits too.
 constexpr size_t kNoallocScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
@@ -59,7 +61,7 @@ extern "C" fa2_status fa2_backward_noalloc(const void* q, const void* k, const v
                                            const float* lse, void* dq, void* dk, void* dv, int64_t bh, int64_t n_q,
                                            int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale,
                                            void* stream) {
-    const size_t need = fa2_backward_workspace_size(bh, n_q, n_k, head_dim, dtype);
+    const size_t need = fa2::two_pass_workspace_size(bh, n_q, n_k, head_dim, dtype);
     if (need == 0)  // invalid sizes: the regular entry point names the offending argument, launching nothing
         return fa2_backward(q, k, v, o, d_o, lse, dq, dk, dv, nullptr, 0, bh, n_q, n_k, head_dim, dtype,
                             softmax_scale, stream);
@@ -67,6 +69,10 @@ extern "C" fa2_status fa2_backward_noalloc(const void* q, const void* k, const v
     void* scratch = nullptr;
     const fa2_status st = fa2::scratch_address(&scratch);
     if (st != FA2_OK) return st;
-    return fa2_backward(q, k, v, o, d_o, lse, dq, dk, dv, scratch, fa2::kNoallocScratchBytes, bh, n_q, n_k, head_dim,
-                        dtype, softmax_scale, stream);
+    // the one-pass backward when its dQ accumulator fits as well, else the two-pass one
+    if (fa2_backward_workspace_size(bh, n_q, n_k, head_dim, dtype) <= fa2::kNoallocScratchBytes)
+        return fa2_backward(q, k, v, o, d_o, lse, dq, dk, dv, scratch, fa2::kNoallocScratchBytes, bh, n_q, n_k,
+                            head_dim, dtype, softmax_scale, stream);
+    return fa2::backward_two_pass(q, k, v, o, d_o, lse, dq, dk, dv, scratch, fa2::kNoallocScratchBytes, bh, n_q, n_k,
+                                  head_dim, dtype, softmax_scale, stream);
 }

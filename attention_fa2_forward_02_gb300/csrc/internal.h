@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "fa2.h"
+
 namespace fa2 {
 
 enum Dtype : int { kF32 = 0, kF16 = 1, kBf16 = 2 };
@@ -52,6 +54,9 @@ struct BwdParams {
     const void* o2 = nullptr;
     const void* d_o2 = nullptr;
     void* dv2 = nullptr;
+    // float32 dQ accumulator of the one-pass backward, [bh, n_q_pad, pad_head_dim(d)],
+    // inside the workspace; zeroed by the preprocess stage when set
+    float* dq_acc = nullptr;
 };
 
 // The PSA rearrangements.  Pack / merge and their adjoints are batched 2-D
@@ -81,7 +86,19 @@ cudaError_t launch_bwd_tc(const BwdParams& p, cudaStream_t stream, int stages);
 // All three stages for two (V, O, dO) triples sharing Q, K and the probabilities:
 // dQ, dK from the summed dS; dV and dV2 per triple.
 cudaError_t launch_bwd_tc_dual_v(const BwdParams& p, cudaStream_t stream);
+// The whole backward in three launches: preprocess (also zeroing p.dq_acc), one
+// pass over key tiles producing dK, dV and the dQ sums, and the dQ rounding pass.
+cudaError_t launch_bwd_fused(const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_psa(const PsaParams& p, cudaStream_t stream);
+
+// Workspace bytes of the two-pass backward (D and LSE2 only); 0 for invalid sizes.
+size_t two_pass_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype);
+// fa2_backward through the two-pass kernels (preprocess, dK/dV pass, dQ pass):
+// needs only two_pass_workspace_size bytes of workspace.
+fa2_status backward_two_pass(const void* q, const void* k, const void* v, const void* o, const void* d_o,
+                             const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype,
+                             float softmax_scale, void* stream);
 
 // Encodes a 3-D tiled tensor map over a contiguous [d2, d1, d0] tensor of
 // `elem_bytes` elements (d0 innermost), box {box0, box1, 1}.  Returns false on failure.

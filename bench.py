@@ -9,7 +9,8 @@ synthetic inputs, all on one CUDA stream:
   pass over the scores for both) -> psa_merge_attn_nchw -> [8, 256, 20, 20];
 * attention forward + backward, bf16, B=2 H=16 (BH = 32), N_q = N_k = 8192,
   HEAD_DIM 128: fa2_forward, then fa2_backward_preprocess,
-  fa2_backward_dkdv and fa2_backward_dq (the three stages of fa2_backward).
+  fa2_backward_dkdv and fa2_backward_dq (the three stages fa2_backward runs at
+  this head size).
 
 ``value`` = algorithmic FLOPs of a step / device time of a step, in TFLOP/s:
 forward 4*BH*N_q*N_k*d, backward 2.5x the forward (recomputed products are not
@@ -59,8 +60,8 @@ STEP_FLOPS = FWD_FLOPS + BWD_FLOPS + PSA_FLOPS
 KERNEL_FLOPS = {"fa2_fwd": FWD_FLOPS, "fa2_bwd_dkdv": 0.8 * BWD_FLOPS, "fa2_bwd_dq": 0.2 * BWD_FLOPS}
 KERNEL_SOURCES = {
     "fa2_fwd": ["fa2_fwd_tc.cu", "common.cuh"],
-    "fa2_bwd_dkdv": ["fa2_bwd_tc.cu", "common.cuh"],
-    "fa2_bwd_dq": ["fa2_bwd_tc.cu", "common.cuh"],
+    "fa2_bwd_dkdv": ["fa2_bwd_tc.cu", "bwd_common.cuh", "common.cuh"],
+    "fa2_bwd_dq": ["fa2_bwd_tc.cu", "bwd_common.cuh", "common.cuh"],
 }
 LAUNCHES_PER_STEP = 7  # pack, fused PSA fwd (V_lo and V_hi), merge, fwd, preprocess, dkdv, dq
 WORKLOAD = ("C2PSA block (QKV [8,512,20,20] fp16, 4 heads, KEY_DIM 32) + attention fwd+bwd "

@@ -83,9 +83,14 @@ fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, flo
 
 /*
  * fa2_backward_workspace_size - bytes of device workspace fa2_backward needs
- * for these sizes (0 if the sizes are invalid).  The workspace holds the row
- * sums D = rowsum(O * dO) and a base-2 copy of the LSE, both float32 and padded
- * to a multiple of 128 rows per head: 2 * bh * ceil(n_q / 128) * 128 * 4 bytes.
+ * for these sizes (0 if the sizes are invalid).  With n_q_pad = ceil(n_q / 128) * 128
+ * and hd = head_dim rounded up to 32, 64 or 128, the workspace holds
+ *   the row sums D = rowsum(O * dO), float32 [bh, n_q_pad]      (4 * bh * n_q_pad bytes),
+ *   a base-2 copy of the LSE, float32 [bh, n_q_pad]             (4 * bh * n_q_pad bytes),
+ *   for head_dim <= 64 only (the one-pass backward), the float32 dQ accumulator
+ *   [bh, n_q_pad, hd]                                           (4 * bh * n_q_pad * hd bytes).
+ * The three stage entry points below need only the first two parts
+ * (8 * bh * n_q_pad bytes); a buffer of this size serves them as well.
  */
 size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype);
 
@@ -96,8 +101,16 @@ size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t
  * flash_attention2_backward_dq and flash_attention2_backward_dkv:
  * D_i = sum_d O_id dO_id;  P_ij = exp(s_ij - LSE_i);  dV_j = sum_i P_ij dO_i;
  * dS_ij = P_ij (dO_i . v_j - D_i);  dQ_i = scale sum_j dS_ij k_j;
- * dK_j = scale sum_i dS_ij q_i.  Structure as on that page: a pass over key
- * tiles (dK, dV) and a pass over query tiles (dQ), plus a row-sum pass for D.
+ * dK_j = scale sum_i dS_ij q_i.  Three launches either way:
+ *  - head_dim > 64: the page's structure, a pass over key tiles (dK, dV) and a
+ *    pass over query tiles (dQ), plus the row sums D first (the three stage
+ *    entry points below, in order);
+ *  - head_dim <= 64: the row sums D (and a reset of the dQ accumulator), one
+ *    pass over key tiles that also adds each tile's share of dQ into a float32
+ *    accumulator in the workspace with reductions, and a rounding pass for dq.
+ *    The page's dQ pass recomputes S and dP; at these head sizes that costs more
+ *    than the reductions.  The reductions land in any order, so dq is not
+ *    bit-reproducible from run to run here (dk and dv are).
  *
  *   q, o, d_o   [bh, n_q, head_dim]  dtype, device, read (o and lse as written by fa2_forward)
  *   k, v        [bh, n_k, head_dim]  dtype, device, read
@@ -120,12 +133,14 @@ fa2_status fa2_backward(const void* q, const void* k, const void* v, const void*
                         fa2_dtype dtype, float softmax_scale, void* stream);
 
 /*
- * The three stages of fa2_backward, callable one by one (fa2_backward is
- * exactly these three, in this order, on one stream).  The pages keep the two
- * main passes as separate kernels ("vision-rs 0.1.1 flash_attn2.rs",
- * flash_attention2_backward_dq and flash_attention2_backward_dkv).  Arguments
- * mean what they mean for fa2_backward; the workspace must be the same buffer
- * across the three calls.
+ * The two-pass backward as three stages, callable one by one: the structure of
+ * the pages, whose two main passes are separate kernels ("vision-rs 0.1.1
+ * flash_attn2.rs", flash_attention2_backward_dq and flash_attention2_backward_dkv).
+ * The three calls in this order on one stream are fa2_backward for head_dim > 64;
+ * for head_dim <= 64 they give the same gradients without the one-pass kernel's
+ * reductions (dq bit-reproducible).  They need a workspace of
+ * 8 * bh * ceil(n_q / 128) * 128 bytes; fa2_backward_workspace_size bytes also do.  Arguments mean what they mean for fa2_backward; the workspace must be
+ * the same buffer across the three calls.
  *
  * fa2_backward_preprocess - fills the workspace from o, d_o and lse
  *   (D_i = sum_d O_id dO_id, the row sum both passes subtract).
@@ -157,8 +172,10 @@ fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const vo
  * of fa2_backward minus the workspace; the caller still passes every input and
  * output.  The workspace comes from one fixed 8 MiB device array inside the
  * library (reserved on each GPU that loads the library until the process
- * exits), which covers bh * ceil(n_q / 128) * 128 <= 1,048,576 query rows;
- * larger problems return FA2_ERR_SCRATCH_LIMIT and launch nothing.
+ * exits).  Problems whose fa2_backward_workspace_size fits in it run as
+ * fa2_backward runs them; others run the two-pass stages, which need 8 bytes
+ * per padded query row and so cover bh * ceil(n_q / 128) * 128 <= 1,048,576
+ * query rows; larger problems return FA2_ERR_SCRATCH_LIMIT and launch nothing.
  * The first call on a device looks up that array's device address, with the
  * device current; make that first call before any stream capture.  All calls
  * share the array, so calls whose GPU work overlaps (several streams or host
@@ -246,7 +263,8 @@ fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* ls
  *   d_o_lo, d_o_hi  [bh, n, key_dim]     dtype, device, read (gradients of o_lo, o_hi)
  *   lse             [bh, n]              float32, device, read (from psa_fa2_forward)
  *   d_packed        [4, bh, n, key_dim]  dtype, device, written (every element)
- *   workspace       at least fa2_backward_workspace_size(bh, n, n, key_dim, dtype) bytes
+ *   workspace       16-byte aligned, at least 8 * bh * ceil(n / 128) * 128 bytes (D and the
+ *                   base-2 LSE of the two-pass stages; fa2_backward_workspace_size bytes also do)
  *
  * dtype F16 / BF16, key_dim a multiple of 8 in [8, 64].  Errors as for fa2_backward.
  */

@@ -64,6 +64,22 @@ def test_noalloc_matches_backward_on_two_calls_in_a_row():
             check_16bit(G.to_f64(a), G.to_f64(b), f"fa2_backward_noalloc {name}")
 
 
+def test_noalloc_two_pass_when_the_accumulator_does_not_fit():
+    """8 heads x 4096 query rows, head_dim 64: the one-pass workspace (8.65 MB with its dQ
+    accumulator) exceeds the fixed 8 MiB scratch, the two-pass one (256 KiB) fits."""
+    torch = G.require_gpu()
+    bh, n_q, n_k, d = 8, 4096, 512, 64
+    assert binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_BF16) > 8 << 20
+    args = _problem("noalloc/c", bh, n_q, n_k, d, "bf16")
+    got = [torch.empty_like(args[0]), torch.empty_like(args[1]), torch.empty_like(args[2])]
+    binding.fa2_backward_noalloc(*args[:6], *got, args[6])
+    binding.fa2_device_status()
+    want = _with_workspace(*args)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("dQ", "dK", "dV"), got, want):
+        check_16bit(G.to_f64(a), G.to_f64(b), f"fa2_backward_noalloc (two-pass) {name}")
+
+
 def test_noalloc_refuses_problems_beyond_its_scratch():
     torch = G.require_gpu()
     t = torch.empty((1, 128, 128), dtype=torch.bfloat16, device="cuda")
