@@ -259,17 +259,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = owned_chunk(half, cc);
+                    const uint32_t* rr = cc == 0 ? ra : rb;
                     uint32_t pk[16];
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const uint32_t* rr = cc == 0 ? ra : rb;
-                        const float2 lse = *reinterpret_cast<const float2*>(l2 + 32 * c + 2 * x);
-                        float2 v = __ffma2_rn(make_float2(__uint_as_float(rr[2 * x]), __uint_as_float(rr[2 * x + 1])),
-                                              scale2, make_float2(-lse.x, -lse.y));
-                        v.x = ex2_approx(v.x);
-                        v.y = ex2_approx(v.y);
-                        p[cc][x] = v;
-                        pk[x] = pack2<kBf16>(v.x, v.y);
+                    for (int x = 0; x < 16; x += 2) {
+                        const float4 nl = *reinterpret_cast<const float4*>(l2 + 32 * c + 2 * x);  // -LSE2, 4 queries
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            float2 v = __ffma2_rn(make_float2(__uint_as_float(rr[2 * (x + u)]), __uint_as_float(rr[2 * (x + u) + 1])),
+                                                  scale2, u ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y));
+                            v.x = ex2_approx(v.x);
+                            v.y = ex2_approx(v.y);
+                            p[cc][x + u] = v;
+                            pk[x + u] = pack2<kBf16>(v.x, v.y);
+                        }
                     }
                     tmem_st16(t_s + kPackedCol + 16u * c, pk);
                 }
@@ -294,12 +297,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 reg_fence(rp);
                 uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const float2 dd = *reinterpret_cast<const float2*>(dl + 32 * c + 2 * x);
-                    const float2 ds = __fmul2_rn(p[cc][x], __fadd2_rn(make_float2(__uint_as_float(rp[2 * x]),
-                                                                                  __uint_as_float(rp[2 * x + 1])),
-                                                                      make_float2(-dd.x, -dd.y)));
-                    pk[x] = pack2<kBf16>(ds.x, ds.y);
+                for (int x = 0; x < 16; x += 2) {
+                    const float4 nd = *reinterpret_cast<const float4*>(dl + 32 * c + 2 * x);  // -D, 4 queries
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float2 ds = __fmul2_rn(
+                            p[cc][x + u], __fadd2_rn(make_float2(__uint_as_float(rp[2 * (x + u)]), __uint_as_float(rp[2 * (x + u) + 1])),
+                                                     u ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y)));
+                        pk[x + u] = pack2<kBf16>(ds.x, ds.y);
+                    }
                 }
                 tmem_st16(t_dp + kPackedCol + 16u * c, pk);
                 // queries [32c, 32c + 32): 64-column atom c / 2, 16-byte chunks 4 (c % 2) .. + 3

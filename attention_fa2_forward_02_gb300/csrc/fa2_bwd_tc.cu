@@ -75,8 +75,9 @@ __global__ void __launch_bounds__(256)
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, TPR);
     if (part == 0 && r < n_q_pad) {
         const size_t w = (size_t)bh * n_q_pad + r;
-        delta[w] = r < n_q ? acc : 0.f;
-        lse2[w] = r < n_q ? lse[(size_t)bh * n_q + r] * kLog2e : INFINITY;
+        // stored negated: the passes add them (-inf in the padding rows makes their P zero)
+        delta[w] = r < n_q ? -acc : 0.f;
+        lse2[w] = r < n_q ? -lse[(size_t)bh * n_q + r] * kLog2e : -INFINITY;
     }
 }
 
@@ -275,17 +276,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = owned_chunk(half, cc);
+                    const uint32_t* r = cc == 0 ? ra : rb;
                     uint32_t pk[16];
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const uint32_t* r = cc == 0 ? ra : rb;
-                        const float2 lse = *reinterpret_cast<const float2*>(l2 + 32 * c + 2 * x);
-                        float2 v = __ffma2_rn(make_float2(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])),
-                                              scale2, make_float2(-lse.x, -lse.y));
-                        v.x = ex2_approx(v.x);
-                        v.y = ex2_approx(v.y);
-                        p[cc][x] = v;
-                        pk[x] = pack2<kBf16>(v.x, v.y);
+                    for (int x = 0; x < 16; x += 2) {
+                        const float4 nl = *reinterpret_cast<const float4*>(l2 + 32 * c + 2 * x);  // -LSE2, 4 queries
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            float2 v = __ffma2_rn(make_float2(__uint_as_float(r[2 * (x + u)]), __uint_as_float(r[2 * (x + u) + 1])),
+                                                  scale2, u ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y));
+                            v.x = ex2_approx(v.x);
+                            v.y = ex2_approx(v.y);
+                            p[cc][x + u] = v;
+                            pk[x + u] = pack2<kBf16>(v.x, v.y);
+                        }
                     }
                     tmem_st16(t_s + kPackedCol + 16u * c, pk);
                 }
@@ -305,12 +309,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 reg_fence(rp);
                 uint32_t pk[16];
 #pragma unroll
-                for (int x = 0; x < 16; ++x) {
-                    const float2 dd = *reinterpret_cast<const float2*>(dl + 32 * c + 2 * x);
-                    const float2 ds = __fmul2_rn(p[cc][x], __fadd2_rn(make_float2(__uint_as_float(rp[2 * x]),
-                                                                                  __uint_as_float(rp[2 * x + 1])),
-                                                                      make_float2(-dd.x, -dd.y)));
-                    pk[x] = pack2<kBf16>(ds.x, ds.y);
+                for (int x = 0; x < 16; x += 2) {
+                    const float4 nd = *reinterpret_cast<const float4*>(dl + 32 * c + 2 * x);  // -D, 4 queries
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float2 ds = __fmul2_rn(
+                            p[cc][x + u], __fadd2_rn(make_float2(__uint_as_float(rp[2 * (x + u)]), __uint_as_float(rp[2 * (x + u) + 1])),
+                                                     u ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y)));
+                        pk[x + u] = pack2<kBf16>(ds.x, ds.y);
+                    }
                 }
                 tmem_st16(t_dp + kPackedCol + 16u * c, pk);
             }
@@ -476,8 +483,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
         const int row = q0 + quarter * 32 + lane;
         const size_t w = (size_t)bh * n_q_pad + row;  // row < n_q_pad always
-        const float my_l2 = lse2[w];
-        const float my_d = delta[w];
+        const float my_nl2 = lse2[w];  // -LSE * log2(e)
+        const float my_nd = delta[w];   // -D
         // This thread's row of Q (half 0) or of dO / dO2 (half 1) into tensor memory,
         // zeros past the last query; pairs of 16-bit elements per 32-bit column.
         {
@@ -518,7 +525,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(bars.resident());
         }
         const float2 scale2 = make_float2(scale_log2, scale_log2);
-        const float2 neg_l2 = make_float2(-my_l2, -my_l2), neg_d = make_float2(-my_d, -my_d);
+        const float2 neg_l2 = make_float2(my_nl2, my_nl2), neg_d = make_float2(my_nd, my_nd);
         bool ok = true;
         for (int j = 0; j < n_kt; ++j) {
             if (!(ok = warp_wait(bars.s_full(), j & 1, wd))) break;

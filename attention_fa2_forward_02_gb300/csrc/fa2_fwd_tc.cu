@@ -236,7 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Only the last key tile can be partial; its columns >= valid are masked to -inf.
             const int valid = n_k - j * BN;
             const bool tail = valid < BN;
-            // Pass 1 over the score row: its maximum (8 independent chains).
+            // Pass 1 over the score row: its maximum (8 independent chains of three-input
+            // maxima; the masking of a partial last tile kept out of the full-tile path).
             float mx;
             {
                 float m8[8];
@@ -250,17 +251,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     reg_fence(a);
                     reg_fence(b);
+                    if (tail) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = __uint_as_float(a[i]), y = __uint_as_float(b[i]);
-                        if (tail) {
-                            if (64 * h + i >= valid) x = -INFINITY;
-                            if (64 * h + 32 + i >= valid) y = -INFINITY;
+                        for (int i = 0; i < 32; ++i) {
+                            if (64 * h + i >= valid) a[i] = __float_as_uint(-INFINITY);
+                            if (64 * h + 32 + i >= valid) b[i] = __float_as_uint(-INFINITY);
                         }
-                        m8[i & 7] = fmaxf(m8[i & 7], fmaxf(x, y));
                     }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) m8[i & 7] = fmax3(m8[i & 7], __uint_as_float(a[i]), __uint_as_float(b[i]));
                 }
-                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             }
             const float m_new = mx * scale_log2;
             if (j == 0) {
@@ -300,13 +301,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < BN / 32; ++c) {
                     if (c + 1 < BN / 32) tmem_ld32(s_addr + 32u * (c + 1), nxt);
                     uint32_t pk[16];
+                    if (tail) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= valid) cur[i] = __float_as_uint(-INFINITY);
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        float2 x = make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
-                        if (tail) {
-                            if (32 * c + 2 * i >= valid) x.x = -INFINITY;
-                            if (32 * c + 2 * i + 1 >= valid) x.y = -INFINITY;
-                        }
+                        const float2 x = make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
                         float2 y = __ffma2_rn(x, scale2, negm2);
                         y.x = ex2_approx(y.x);
                         y.y = ex2_approx(y.y);

@@ -41,8 +41,8 @@ struct BwdParams {
     void* dq;
     void* dk;
     void* dv;
-    float* delta;  // [bh, n_q_pad] row sums D (0 in the padding rows), inside the workspace
-    float* lse2;   // [bh, n_q_pad] LSE * log2(e) (+inf in the padding rows), inside the workspace
+    float* delta;  // [bh, n_q_pad] minus the row sums D (0 in the padding rows), inside the workspace
+    float* lse2;   // [bh, n_q_pad] -LSE * log2(e) (-inf in the padding rows), inside the workspace
     int64_t n_q_pad;
     int64_t bh, n_q, n_k;
     int d;
