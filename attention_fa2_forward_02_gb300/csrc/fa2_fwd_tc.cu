@@ -233,82 +233,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n_kv; ++j) {
             if (!(ok = warp_wait(B_SF(t), j & 1, wd))) break;
             tc_fence_after();
-            // Only the last key tile can be partial; its columns >= valid are masked to -inf.
+            // The score row (128 columns) into registers: one read of the S tile per key tile.
+            uint32_t sr[BN / 32][32];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + 32u * c, sr[c]);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
+            // Only the last key tile can be partial: its columns past the last key become
+            // -inf, which drops them from the maximum and gives them probability 0.
             const int valid = n_k - j * BN;
-            const bool tail = valid < BN;
-            // Pass 1 over the score row: its maximum (8 independent chains of three-input
-            // maxima; the masking of a partial last tile kept out of the full-tile path).
+            if (valid < BN) {
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (32 * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
+            }
+            // The row maximum: 8 independent chains of three-input maxima.
             float mx;
             {
                 float m8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t a[32], b[32];
-                    tmem_ld32(s_addr + 64u * h, a);
-                    tmem_ld32(s_addr + 64u * h + 32u, b);
-                    tmem_ld_wait();
-                    reg_fence(a);
-                    reg_fence(b);
-                    if (tail) {
+                for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            if (64 * h + i >= valid) a[i] = __float_as_uint(-INFINITY);
-                            if (64 * h + 32 + i >= valid) b[i] = __float_as_uint(-INFINITY);
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) m8[i & 7] = fmax3(m8[i & 7], __uint_as_float(a[i]), __uint_as_float(b[i]));
-                }
+                    for (int i = 0; i < 16; ++i)
+                        m8[i & 7] = fmax3(m8[i & 7], __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
                 mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
             }
             const float m_new = mx * scale_log2;
+            float alpha = 1.f;   // factor for O and l when the reference maximum moves
+            bool rescale = false;
             if (j == 0) {
                 m2 = m_new;
             } else {
                 const bool need = m_new > m2 + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, need)) {
-                    const float alpha = need ? ex2_approx(m2 - m_new) : 1.f;
-                    if (need) {
-                        l *= alpha;
-                        m2 = m_new;
-                    }
-#pragma unroll
-                    for (int c = 0; c < kNV * D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(o_addr + 32u * c, r);
-                        tmem_ld_wait();
-                        reg_fence(r);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(o_addr + 32u * c, r);
-                    }
-                    tmem_st_wait();
+                rescale = __any_sync(0xffffffffu, need);
+                if (need) {
+                    alpha = ex2_approx(m2 - m_new);
+                    l *= alpha;
+                    m2 = m_new;
                 }
             }
-            // Pass 2: p = 2^(s*scale*log2e - m2) per 32-column chunk (the next chunk's
-            // load in flight meanwhile), row sum in four partial sums, P packed to
-            // 16 bits and stored over the score columns already consumed.
+            // p = 2^(s*scale*log2e - m2) from the registers, row sum in two packed partial
+            // sums, P packed to 16 bits and stored over the score columns (all already read).
             {
                 const float2 negm2 = make_float2(-m2, -m2);
                 float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-                uint32_t cur[32], nxt[32];
-                tmem_ld32(s_addr, cur);
-                tmem_ld_wait();
-                reg_fence(cur);
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
-                    if (c + 1 < BN / 32) tmem_ld32(s_addr + 32u * (c + 1), nxt);
                     uint32_t pk[16];
-                    if (tail) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (32 * c + i >= valid) cur[i] = __float_as_uint(-INFINITY);
-                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float2 x = make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1]));
+                        const float2 x = make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
                         float2 y = __ffma2_rn(x, scale2, negm2);
                         y.x = ex2_approx(y.x);
                         y.y = ex2_approx(y.y);
@@ -317,14 +296,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[i] = pack2<kBf16>(y.x, y.y);
                     }
                     tmem_st16(s_addr + 16u * c, pk);
-                    if (c + 1 < BN / 32) {
-                        tmem_ld_wait();
-                        reg_fence(nxt);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
-                    }
                 }
                 l += (acc0.x + acc1.x) + (acc0.y + acc1.y);
+            }
+            // The O rescale, when some row's reference maximum moved: before P is released
+            // to the P.V product (which is issued only after the arrival below), and after
+            // the previous P.V product (whose completion preceded this S tile's).
+            if (rescale) {
+#pragma unroll
+                for (int c = 0; c < kNV * D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(o_addr + 32u * c, o);
+                    tmem_ld_wait();
+                    reg_fence(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    tmem_st32(o_addr + 32u * c, o);
+                }
             }
             tmem_st_wait();
             tc_fence_before();
