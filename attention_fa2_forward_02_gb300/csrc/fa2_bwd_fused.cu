@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
         const int r = quarter * 32 + lane;  // key row (score tiles) and query row (dQ tile) of this thread
+        const bool key_valid = k0 + r < n_k;
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         // Reads dQ of the i-th visited query tile out of TMEM and adds it into the
         // accumulator, laid out per (bh, query tile) as [D/4][128 rows][4] floats so
@@ -282,19 +283,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(bars.e1());
             // the previous query tile's dQ, while dV(i) runs
             if (i > 0 && !(ok = reduce_dq(i - 1))) break;
-            // step 2: dS^T = P^T * (dP^T - D), chunk by chunk in write-safe order, into
-            // TMEM (for dK) and as dS into shared memory (for dQ)
+            // step 2: dS^T = P^T * (dP^T - D) into TMEM (for dK) and as dS into shared memory
+            // (for dQ); both owned chunks read before either is overwritten.  Rows of keys
+            // past the last one (zero K rows, where P may even overflow) get dS = 0.
             if (!(ok = warp_wait(bars.dp_full(), i & 1, wd))) break;
             tc_fence_after();
             const uint32_t ds_row = ds_smem(s) + (uint32_t)r * 128u;  // row r of the [keys, queries] tile
             const uint32_t swz = (uint32_t)(r & 7);                   // 128-byte swizzle of that row
+            uint32_t rp[2][32];
+            tmem_ld32(t_dp + 32u * owned_chunk(half, 0), rp[0]);
+            tmem_ld32(t_dp + 32u * owned_chunk(half, 1), rp[1]);
+            tmem_ld_wait();
+            reg_fence(rp[0]);
+            reg_fence(rp[1]);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = owned_chunk(half, cc);
-                uint32_t rp[32];
-                tmem_ld32(t_dp + 32u * c, rp);
-                tmem_ld_wait();
-                reg_fence(rp);
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; x += 2) {
@@ -302,9 +306,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const float2 ds = __fmul2_rn(
-                            p[cc][x + u], __fadd2_rn(make_float2(__uint_as_float(rp[2 * (x + u)]), __uint_as_float(rp[2 * (x + u) + 1])),
+                            p[cc][x + u], __fadd2_rn(make_float2(__uint_as_float(rp[cc][2 * (x + u)]), __uint_as_float(rp[cc][2 * (x + u) + 1])),
                                                      u ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y)));
-                        pk[x + u] = pack2<kBf16>(ds.x, ds.y);
+                        pk[x + u] = key_valid ? pack2<kBf16>(ds.x, ds.y) : 0u;
                     }
                 }
                 tmem_st16(t_dp + kPackedCol + 16u * c, pk);

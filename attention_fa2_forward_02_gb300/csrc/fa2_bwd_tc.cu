@@ -555,25 +555,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                 }
             }
-            // step 2: dS = P * (dP - D), zero past the last key, chunk by chunk in write-safe order
+            // step 2: dS = P * (dP - D), zero past the last key (where P may even overflow);
+            // both owned chunks read before either is overwritten by its 16-bit result
             if (!(ok = warp_wait(bars.dp_full(), j & 1, wd))) break;
             tc_fence_after();
+            uint32_t rp[2][32];
+            tmem_ld32(t_dp + 32u * owned_chunk(half, 0), rp[0]);
+            tmem_ld32(t_dp + 32u * owned_chunk(half, 1), rp[1]);
+            tmem_ld_wait();
+            reg_fence(rp[0]);
+            reg_fence(rp[1]);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = owned_chunk(half, cc);
-                uint32_t rp[32];
-                tmem_ld32(t_dp + 32u * c, rp);
-                tmem_ld_wait();
-                reg_fence(rp);
                 uint32_t pk[16];
 #pragma unroll
                 for (int x = 0; x < 16; ++x) {
-                    const int col = 32 * c + 2 * x;
-                    float2 ds = __fmul2_rn(
-                        p[cc][x], __fadd2_rn(make_float2(__uint_as_float(rp[2 * x]), __uint_as_float(rp[2 * x + 1])), neg_d));
-                    if (col >= valid) ds.x = 0.f;
-                    if (col + 1 >= valid) ds.y = 0.f;
+                    const float2 ds = __fmul2_rn(
+                        p[cc][x], __fadd2_rn(make_float2(__uint_as_float(rp[cc][2 * x]), __uint_as_float(rp[cc][2 * x + 1])), neg_d));
                     pk[x] = pack2<kBf16>(ds.x, ds.y);
+                }
+                if (valid < BT) {
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const int col = 32 * c + 2 * x;
+                        if (col >= valid) pk[x] &= 0xFFFF0000u;
+                        if (col + 1 >= valid) pk[x] &= 0x0000FFFFu;
+                    }
                 }
                 tmem_st16(t_dp + kPackedCol + 16u * c, pk);
             }
