@@ -134,3 +134,28 @@ def test_backward_reproducibility(d):
         assert np.array_equal(a[0], b[0])
     ulp = np.maximum(np.abs(a[0]), np.abs(b[0])) * 2.0 ** -7
     assert np.all(np.abs(a[0] - b[0]) <= ulp + 1e-30)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_far_negative_scores_with_a_partial_key_tile(d):
+    """Every score near -110 (LSE near -105): a padded key of the last, partial key tile has
+    score 0 and probability exp(0 - LSE), beyond float32; the kernels must keep it out of
+    dQ (one-pass head size 64, two-pass 128) and stay finite."""
+    bh, n_q, n_k = 1, 150, 200
+    scale = 1 / math.sqrt(d)
+    q = synth.to_storage(np.full((bh, n_q, d), 2.0), "bf16")
+    k_base = -110.0 / (2.0 * d * scale)
+    k = synth.to_storage(k_base + 0.5 * synth.normal(synth.BASE_SEED, f"bwd/farneg/{d}/k", bh * n_k * d).reshape(bh, n_k, d),
+                         "bf16")
+    v = synth.tensor(f"bwd/farneg/{d}/v", (bh, n_k, d), "bf16")
+    d_o = synth.tensor(f"bwd/farneg/{d}/do", (bh, n_q, d), "bf16")
+    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, "bf16", scale)
+    for x in (dq, dk, dv):
+        assert np.all(np.isfinite(x))
+    w = lambda x: synth.widen(x, "bf16")
+    rq, rk, rv = A.backward(w(q), w(k), w(v), w(d_o), scale)
+    _, lse = A.forward(w(q), w(k), w(v), scale)
+    assert np.max(lse) < -89  # exp(-LSE) overflows float32: the regime this test is about
+    check_16bit(dq, rq, "dQ")
+    check_16bit(dk, rk, "dK")
+    check_16bit(dv, rv, "dV")
