@@ -27,6 +27,7 @@ EXPORTS = (
     "fa2_backward_preprocess",
     "fa2_backward_dkdv",
     "fa2_backward_dq",
+    "fa2_backward_passes",
     "fa2_backward_noalloc",
     "psa_pack_qkv",
     "psa_merge_attn_nchw",
@@ -68,6 +69,8 @@ def _declare(lib):
                                                            _f32, _c_ptr]),
         "fa2_backward_dq": (ctypes.c_int, [_c_ptr] * 5 + [ctypes.c_size_t, _c_ptr, _i64, _i64, _i64, _i32, _i32, _f32,
                                                          _c_ptr]),
+        "fa2_backward_passes": (ctypes.c_int, [_c_ptr] * 5 + [ctypes.c_size_t, _c_ptr, _c_ptr, _c_ptr, _i64, _i64, _i64,
+                                                             _i32, _i32, _f32, _c_ptr]),
         "fa2_backward_noalloc": (ctypes.c_int, [_c_ptr] * 9 + [_i64, _i64, _i64, _i32, _i32, _f32, _c_ptr]),
         "psa_pack_qkv": (ctypes.c_int, [_c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
         "psa_merge_attn_nchw": (ctypes.c_int, [_c_ptr, _c_ptr, _c_ptr] + [_i32] * 6 + [_c_ptr]),
@@ -220,6 +223,16 @@ def fa2_backward_dq(q, k, v, d_o, workspace, dq, softmax_scale: float, stream=No
                                    _dev(workspace, "workspace"), wsb, _dev(dq, "dq", 3),
                                    bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
     _check(st, "fa2_backward_dq")
+
+
+def fa2_backward_passes(q, k, v, d_o, workspace, dq, dk, dv, softmax_scale: float, stream=None) -> None:
+    """Stages 2 and 3 of the two-pass backward in one launch: dQ, dK and dV from a filled workspace."""
+    bh, n_q, n_k, d, wsb = _bwd_sizes(q, k, workspace)
+    st = library().fa2_backward_passes(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(d_o, "d_o", 3),
+                                       _dev(workspace, "workspace"), wsb, _dev(dq, "dq", 3), _dev(dk, "dk", 3),
+                                       _dev(dv, "dv", 3), bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale),
+                                       _stream(stream))
+    _check(st, "fa2_backward_passes")
 
 
 def psa_pack_qkv(qkv, packed, num_heads: int, stream=None) -> None:

@@ -242,6 +242,14 @@ fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const vo
                            workspace_bytes, bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDq, false);
 }
 
+fa2_status fa2_backward_passes(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
+                               size_t workspace_bytes, void* dq, void* dk, void* dv, int64_t bh, int64_t n_q,
+                               int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream) {
+    if (!q || !k || !v || !d_o || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
+    return backward_common(q, k, v, nullptr, d_o, nullptr, dq, dk, dv, const_cast<void*>(workspace), workspace_bytes,
+                           bh, n_q, n_k, head_dim, dtype, softmax_scale, stream, kBwdDkDv | kBwdDq, false);
+}
+
 fa2_status psa_fa2_backward(const void* packed, const void* o_lo, const void* o_hi, const void* d_o_lo,
                             const void* d_o_hi, const float* lse, void* d_packed, void* workspace,
                             size_t workspace_bytes, int64_t bh, int64_t n, int32_t key_dim, fa2_dtype dtype,

@@ -117,14 +117,15 @@ struct BwdCfg : Tile16<D> {
 // S^T(i+1) overwrites the columns holding P^T(i) only after dV(i), which reads
 // them, was issued; dP^T(i+1) likewise follows dK(i).
 
+// One CTA of the dK/dV pass: key tile kt of head bh.  The tensor maps are the
+// kernel's own __grid_constant__ parameters (TMA reads them from parameter space).
 template <int D, bool kBf16, int kNV>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
-                    const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dk,
-                    void* __restrict__ dv, void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale,
-                    float scale_log2, unsigned int* status) {
+__device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                         const CUtensorMap& tm_do, const CUtensorMap& tm_v2, const CUtensorMap& tm_do2,
+                                         const float* __restrict__ lse2, const float* __restrict__ delta,
+                                         void* __restrict__ dk, void* __restrict__ dv, void* __restrict__ dv2, int n_q,
+                                         int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
+                                         unsigned int* status, int kt, int bh) {
     using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -132,8 +133,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_addr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.y;
-    const int k0 = blockIdx.x * BT;
+    const int k0 = kt * BT;
     const int n_qt = (n_q + BT - 1) / BT;
 
     const Bars bars{base + C::kDkvBar, S};
@@ -367,13 +367,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // into tensor memory (16-bit pairs, the layout an MMA reads its A operand in), so
 // S and dP read only K and V from shared memory.
 
+// One CTA of the dQ pass: query tile qt of head bh.
 template <int D, bool kBf16, int kNV>
-__global__ void __launch_bounds__(kBwdThreads, 1)
-    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_v2, const uint16_t* __restrict__ q_ptr,
-                  const uint16_t* __restrict__ do_ptr, const uint16_t* __restrict__ do2_ptr,
-                  const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dq, int n_q,
-                  int n_k, int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status) {
+__device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_v2,
+                                       const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
+                                       const uint16_t* __restrict__ do2_ptr, const float* __restrict__ lse2,
+                                       const float* __restrict__ delta, void* __restrict__ dq, int n_q, int n_k,
+                                       int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status,
+                                       int qt, int bh) {
     using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStagesDq;
     extern __shared__ uint8_t smem_raw[];
@@ -381,8 +382,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_addr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int bh = blockIdx.y;
-    const int q0 = blockIdx.x * BT;
+    const int q0 = qt * BT;
     const int n_kt = (n_k + BT - 1) / BT;
 
     const Bars bars{base + C::kDqBar, S};
@@ -613,6 +613,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// ------------------------------------------------------------------------------ kernels
+
+template <int D, bool kBf16, int kNV>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
+                    const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dk,
+                    void* __restrict__ dv, void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale,
+                    float scale_log2, unsigned int* status) {
+    dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, lse2, delta, dk, dv, dv2, n_q, n_k, n_q_pad, d_act,
+                            scale, scale_log2, status, blockIdx.x, blockIdx.y);
+}
+
+template <int D, bool kBf16, int kNV>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_v2, const uint16_t* __restrict__ q_ptr,
+                  const uint16_t* __restrict__ do_ptr, const uint16_t* __restrict__ do2_ptr,
+                  const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dq, int n_q,
+                  int n_k, int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status) {
+    dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act, scale,
+                          scale_log2, status, blockIdx.x, blockIdx.y);
+}
+
+// Both passes in one launch: per head (grid y), CTAs x < n_kt run the dK/dV pass for
+// key tile x, the others the dQ pass for query tile x - n_kt.  The passes are
+// independent once D and LSE2 are in the workspace; one grid lets the CTAs of one
+// fill the SMs the other leaves idle in its last wave.
+template <int D, bool kBf16, int kNV>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_passes_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
+                      const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
+                      const uint16_t* __restrict__ do2_ptr, const float* __restrict__ lse2,
+                      const float* __restrict__ delta, void* __restrict__ dq, void* __restrict__ dk, void* __restrict__ dv,
+                      void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
+                      unsigned int* status) {
+    const int n_kt = (n_k + BT - 1) / BT;
+    if ((int)blockIdx.x < n_kt)
+        dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, lse2, delta, dk, dv, dv2, n_q, n_k, n_q_pad,
+                                d_act, scale, scale_log2, status, blockIdx.x, blockIdx.y);
+    else
+        dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act,
+                              scale, scale_log2, status, blockIdx.x - n_kt, blockIdx.y);
+}
+
 // ------------------------------------------------------------------------------ launch
 
 template <int D, bool kBf16, int kNV>
@@ -645,11 +693,23 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         return cudaErrorInvalidValue;
     const float scale_log2 = p.scale * kLog2e;
     cudaError_t e = cudaSuccess;
+    const int n_kt = (int)((p.n_k + BT - 1) / BT), n_qt = (int)((p.n_q + BT - 1) / BT);
+    if ((stages & (kBwdDkDv | kBwdDq)) == (kBwdDkDv | kBwdDq)) {
+        auto both = bwd_passes_kernel<D, kBf16, kNV>;
+        constexpr int smem = C::kSmemDkv > C::kSmemDq ? C::kSmemDkv : C::kSmemDq;
+        e = ensure_smem_limit(reinterpret_cast<const void*>(both), smem, 42 + (slot - 16) / 2);  // slots 42..51
+        if (e != cudaSuccess) return e;
+        both<<<dim3((unsigned)(n_kt + n_qt), (unsigned)p.bh, 1), kBwdThreads, smem, stream>>>(
+            tq, tk, tv, tdo, tv2, tdo2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
+            static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, p.dk, p.dv, p.dv2, (int)p.n_q,
+            (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status);
+        return cudaGetLastError();
+    }
     if (stages & kBwdDkDv) {
         auto dkdv = bwd_dkdv_kernel<D, kBf16, kNV>;
         e = ensure_smem_limit(reinterpret_cast<const void*>(dkdv), C::kSmemDkv, slot);
         if (e != cudaSuccess) return e;
-        dkdv<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kBwdThreads, C::kSmemDkv, stream>>>(
+        dkdv<<<dim3((unsigned)n_kt, (unsigned)p.bh, 1), kBwdThreads, C::kSmemDkv, stream>>>(
             tq, tk, tv, tdo, tv2, tdo2, p.lse2, p.delta, p.dk, p.dv, p.dv2, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad,
             p.d, p.scale, scale_log2, p.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -658,7 +718,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     auto dqk = bwd_dq_kernel<D, kBf16, kNV>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
     if (e != cudaSuccess) return e;
-    dqk<<<dim3((unsigned)((p.n_q + BT - 1) / BT), (unsigned)p.bh, 1), kBwdThreads, C::kSmemDq, stream>>>(
+    dqk<<<dim3((unsigned)n_qt, (unsigned)p.bh, 1), kBwdThreads, C::kSmemDq, stream>>>(
         tk, tv, tv2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
         static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k,
         (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status);

@@ -8,9 +8,9 @@ synthetic inputs, all on one CUDA stream:
   psa_fa2_forward (HEAD_DIM 32 on Q, K with V_lo and with V_hi, N = 400, one
   pass over the scores for both) -> psa_merge_attn_nchw -> [8, 256, 20, 20];
 * attention forward + backward, bf16, B=2 H=16 (BH = 32), N_q = N_k = 8192,
-  HEAD_DIM 128: fa2_forward, then fa2_backward_preprocess,
-  fa2_backward_dkdv and fa2_backward_dq (the three stages fa2_backward runs at
-  this head size).
+  HEAD_DIM 128: fa2_forward, then fa2_backward_preprocess (the row sums D) and
+  fa2_backward_passes (the dK/dV and dQ passes in one grid) - the two launches
+  fa2_backward makes at this head size, called as stages so that each is timed.
 
 ``value`` = algorithmic FLOPs of a step / device time of a step, in TFLOP/s:
 forward 4*BH*N_q*N_k*d, backward 2.5x the forward (recomputed products are not
@@ -55,15 +55,15 @@ FWD_FLOPS = 4.0 * BH * N * N * D
 BWD_FLOPS = 2.5 * FWD_FLOPS
 PSA_FLOPS = 2 * 4.0 * PSA_BH * PSA_N * PSA_N * PSA_KD
 STEP_FLOPS = FWD_FLOPS + BWD_FLOPS + PSA_FLOPS
-# algorithmic FLOPs of each timed kernel (per launch): the backward's 10*d per
-# (query, key) pair splits as S, dP, dV, dK (8*d) in the key pass and dQ (2*d)
-KERNEL_FLOPS = {"fa2_fwd": FWD_FLOPS, "fa2_bwd_dkdv": 0.8 * BWD_FLOPS, "fa2_bwd_dq": 0.2 * BWD_FLOPS}
+# algorithmic FLOPs of each timed call: the backward's 10*d per (query, key) pair is
+# S, dP, dV, dK (8*d, the key-tile pass) and dQ (2*d; the dQ pass's recomputed S and
+# dP are not counted)
+KERNEL_FLOPS = {"fa2_fwd": FWD_FLOPS, "fa2_bwd_passes": BWD_FLOPS}
 KERNEL_SOURCES = {
     "fa2_fwd": ["fa2_fwd_tc.cu", "common.cuh"],
-    "fa2_bwd_dkdv": ["fa2_bwd_tc.cu", "bwd_common.cuh", "common.cuh"],
-    "fa2_bwd_dq": ["fa2_bwd_tc.cu", "bwd_common.cuh", "common.cuh"],
+    "fa2_bwd_passes": ["fa2_bwd_tc.cu", "bwd_common.cuh", "common.cuh"],
 }
-LAUNCHES_PER_STEP = 7  # pack, fused PSA fwd (V_lo and V_hi), merge, fwd, preprocess, dkdv, dq
+LAUNCHES_PER_STEP = 6  # pack, fused PSA fwd (V_lo and V_hi), merge, fwd, bwd preprocess, bwd passes
 WORKLOAD = ("C2PSA block (QKV [8,512,20,20] fp16, 4 heads, KEY_DIM 32) + attention fwd+bwd "
             "bf16 B=2 H=16 N=8192 HEAD_DIM=128")
 
@@ -76,7 +76,7 @@ def set_heads(bh: int):
     FWD_FLOPS = 4.0 * BH * N * N * D
     BWD_FLOPS = 2.5 * FWD_FLOPS
     STEP_FLOPS = FWD_FLOPS + BWD_FLOPS + PSA_FLOPS
-    KERNEL_FLOPS = {"fa2_fwd": FWD_FLOPS, "fa2_bwd_dkdv": 0.8 * BWD_FLOPS, "fa2_bwd_dq": 0.2 * BWD_FLOPS}
+    KERNEL_FLOPS = {"fa2_fwd": FWD_FLOPS, "fa2_bwd_passes": BWD_FLOPS}
     if bh != 32:
         WORKLOAD = WORKLOAD.replace("B=2 H=16", f"BH={bh}")
 METRIC = "FA2 fwd+bwd TFLOP/s (bf16, B=2 H=16 N=8192 d=128, with the C2PSA pack/attention/merge block)"
@@ -329,12 +329,9 @@ def run_ours(args):
         B.fa2_backward_preprocess(b["o"], b["do"], b["lse"], b["ws"], N)
         if ev is not None:
             ev[3].record(stream)
-        B.fa2_backward_dkdv(b["q"], b["k"], b["v"], b["do"], b["ws"], b["dk"], b["dv"], s128)
+        B.fa2_backward_passes(b["q"], b["k"], b["v"], b["do"], b["ws"], b["dq"], b["dk"], b["dv"], s128)
         if ev is not None:
             ev[4].record(stream)
-        B.fa2_backward_dq(b["q"], b["k"], b["v"], b["do"], b["ws"], b["dq"], s128)
-        if ev is not None:
-            ev[5].record(stream)
 
     def barrier():
         torch.cuda.synchronize()
@@ -351,7 +348,7 @@ def run_ours(args):
     barrier()
 
     # ------------------------------------------------------------------ timed region
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     e_begin, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     try:
         dev_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -371,7 +368,7 @@ def run_ours(args):
 
     ms_step = elapsed_ms / args.steps
     value = job_throughput(world, STEP_FLOPS, ms_step)
-    names = ["c2psa_block", "fa2_fwd", "fa2_bwd_preprocess", "fa2_bwd_dkdv", "fa2_bwd_dq"]
+    names = ["c2psa_block", "fa2_fwd", "fa2_bwd_preprocess", "fa2_bwd_passes"]
     per = {n: statistics.fmean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
            for i, n in enumerate(names)}
     pk = peaks()
@@ -382,16 +379,17 @@ def run_ours(args):
                 "unit": "TFLOP/s", "frac": achieved / pk["bf16_sustained"], "traffic": traffic,
                 "peak_kind": f"bf16 dense, sustained ({pk['source']})",
                 "flops_per_launch": KERNEL_FLOPS[dominant]}
-    bwd_ms = per["fa2_bwd_preprocess"] + per["fa2_bwd_dkdv"] + per["fa2_bwd_dq"]
+    bwd_ms = per["fa2_bwd_preprocess"] + per["fa2_bwd_passes"]
     components = {
         "fa2_fwd_ms": per["fa2_fwd"], "fa2_fwd_tflops": FWD_FLOPS / per["fa2_fwd"] / 1e9,
         "fa2_fwd_frac_burst_peak": FWD_FLOPS / per["fa2_fwd"] / 1e9 / pk["bf16"],
         "fa2_bwd_ms": bwd_ms, "fa2_bwd_tflops": BWD_FLOPS / bwd_ms / 1e9,
         "fa2_bwd_frac_burst_peak": BWD_FLOPS / bwd_ms / 1e9 / pk["bf16"],
-        "fa2_bwd_preprocess_ms": per["fa2_bwd_preprocess"], "fa2_bwd_dkdv_ms": per["fa2_bwd_dkdv"],
-        "fa2_bwd_dq_ms": per["fa2_bwd_dq"], "c2psa_block_us": per["c2psa_block"] * 1e3,
+        "fa2_bwd_preprocess_ms": per["fa2_bwd_preprocess"], "fa2_bwd_passes_ms": per["fa2_bwd_passes"],
+        "c2psa_block_us": per["c2psa_block"] * 1e3,
         "peak_bf16_burst_tflops": pk["bf16"], "peak_source": pk["source"],
     }
+    components.update(separate_passes(torch, B, sets[0], stream, s128))
 
     # ------------------------------------------------------------------ PSA pack / merge bandwidth
     components.update(psa_bandwidth(torch, B, dev, pk))
@@ -465,6 +463,25 @@ def run_ours(args):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def separate_passes(torch, B, b, stream, scale, reps=20):
+    """The backward's stages launched one by one (fa2_backward_preprocess, _dkdv, _dq), outside
+    the timed region: how the one-grid fa2_backward_passes splits between the passes."""
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+    for r in range(reps):
+        evs[r][0].record(stream)
+        B.fa2_backward_preprocess(b["o"], b["do"], b["lse"], b["ws"], N)
+        evs[r][1].record(stream)
+        B.fa2_backward_dkdv(b["q"], b["k"], b["v"], b["do"], b["ws"], b["dk"], b["dv"], scale)
+        evs[r][2].record(stream)
+        B.fa2_backward_dq(b["q"], b["k"], b["v"], b["do"], b["ws"], b["dq"], scale)
+        evs[r][3].record(stream)
+    torch.cuda.synchronize()
+    t = [statistics.fmean(evs[r][j].elapsed_time(evs[r][j + 1]) for r in range(reps)) for j in range(3)]
+    B.fa2_device_status()
+    return {"bwd_stages_separately_ms": sum(t), "bwd_preprocess_ms": t[0], "bwd_dkdv_pass_ms": t[1],
+            "bwd_dq_pass_ms": t[2], "bwd_dkdv_pass_tflops": 0.8 * BWD_FLOPS / t[1] / 1e9}
 
 
 def c2psa_graph_timings(torch, B, dev):

@@ -101,10 +101,10 @@ size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t
  * flash_attention2_backward_dq and flash_attention2_backward_dkv:
  * D_i = sum_d O_id dO_id;  P_ij = exp(s_ij - LSE_i);  dV_j = sum_i P_ij dO_i;
  * dS_ij = P_ij (dO_i . v_j - D_i);  dQ_i = scale sum_j dS_ij k_j;
- * dK_j = scale sum_i dS_ij q_i.  Three launches either way:
+ * dK_j = scale sum_i dS_ij q_i.
  *  - head_dim > 64: the page's structure, a pass over key tiles (dK, dV) and a
- *    pass over query tiles (dQ), plus the row sums D first (the three stage
- *    entry points below, in order);
+ *    pass over query tiles (dQ), after the row sums D: two launches (the stage
+ *    entry points fa2_backward_preprocess and fa2_backward_passes below);
  *  - head_dim <= 64: the row sums D (and a reset of the dQ accumulator), one
  *    pass over key tiles that also adds each tile's share of dQ into a float32
  *    accumulator in the workspace with reductions, and a rounding pass for dq.
@@ -136,11 +136,13 @@ fa2_status fa2_backward(const void* q, const void* k, const void* v, const void*
  * The two-pass backward as three stages, callable one by one: the structure of
  * the pages, whose two main passes are separate kernels ("vision-rs 0.1.1
  * flash_attn2.rs", flash_attention2_backward_dq and flash_attention2_backward_dkv).
- * The three calls in this order on one stream are fa2_backward for head_dim > 64;
- * for head_dim <= 64 they give the same gradients without the one-pass kernel's
- * reductions (dq bit-reproducible).  They need a workspace of
- * 8 * bh * ceil(n_q / 128) * 128 bytes; fa2_backward_workspace_size bytes also do.  Arguments mean what they mean for fa2_backward; the workspace must be
- * the same buffer across the three calls.
+ * fa2_backward_preprocess followed by fa2_backward_passes (or by _dkdv and _dq, in
+ * either order) on one stream gives, bit for bit, what fa2_backward gives for
+ * head_dim > 64; for head_dim <= 64 the same gradients without the one-pass
+ * kernel's reductions (dq bit-reproducible).  The stages need a workspace of
+ * 8 * bh * ceil(n_q / 128) * 128 bytes; fa2_backward_workspace_size bytes also
+ * do.  Arguments mean what they mean for fa2_backward; the workspace must be the
+ * same buffer across the calls.
  *
  * fa2_backward_preprocess - fills the workspace from o, d_o and lse
  *   (D_i = sum_d O_id dO_id, the row sum both passes subtract).
@@ -148,6 +150,9 @@ fa2_status fa2_backward(const void* q, const void* k, const void* v, const void*
  *   (the pass over key tiles).
  * fa2_backward_dq - dq from q, k, v, d_o and a filled workspace (the pass over
  *   query tiles).
+ * fa2_backward_passes - dq, dk and dv from a filled workspace: both passes in
+ *   one launch, whose CTAs for the two passes share the GPU (what fa2_backward
+ *   runs after the preprocess for head_dim > 64).
  * Errors as for fa2_backward.
  */
 fa2_status fa2_backward_preprocess(const void* o, const void* d_o, const float* lse, void* workspace,
@@ -159,6 +164,9 @@ fa2_status fa2_backward_dkdv(const void* q, const void* k, const void* v, const 
 fa2_status fa2_backward_dq(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
                            size_t workspace_bytes, void* dq, int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim,
                            fa2_dtype dtype, float softmax_scale, void* stream);
+fa2_status fa2_backward_passes(const void* q, const void* k, const void* v, const void* d_o, const void* workspace,
+                               size_t workspace_bytes, void* dq, void* dk, void* dv, int64_t bh, int64_t n_q,
+                               int64_t n_k, int32_t head_dim, fa2_dtype dtype, float softmax_scale, void* stream);
 
 /*
  * fa2_backward_noalloc - fa2_backward without a caller-supplied workspace and

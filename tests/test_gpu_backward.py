@@ -106,7 +106,12 @@ def test_backward_stages_vs_oracle_and_whole(d, dtype):
     small = torch.empty(8 * bh * 384, dtype=torch.uint8, device="cuda")  # D and LSE2 only
     staged = _stages(qd, kd, vd, o, dod, lse, scale, small, dtype)
     again = _stages(qd, kd, vd, o, dod, lse, scale, small, dtype)
+    one_grid = [G.empty(tuple(x.shape), dtype) for x in (qd, kd, vd)]
+    binding.fa2_backward_preprocess(o, dod, lse, small, n_k)
+    binding.fa2_backward_passes(qd, kd, vd, dod, small, *one_grid, scale)
     binding.fa2_device_status()
+    for name, a, b in zip(("dQ", "dK", "dV"), staged, one_grid):
+        assert torch.equal(a, b), f"fa2_backward_passes {name} differs from _dkdv + _dq"
     w = lambda x: synth.widen(x, dtype)
     ref = A.backward(w(q), w(k), w(v), w(d_o), scale)
     for name, a, b, c, r in zip(("dQ", "dK", "dV"), staged, whole, again, ref):
