@@ -638,10 +638,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                           scale_log2, status, blockIdx.x, blockIdx.y);
 }
 
-// Both passes in one launch: per head (grid y), CTAs x < n_kt run the dK/dV pass for
-// key tile x, the others the dQ pass for query tile x - n_kt.  The passes are
-// independent once D and LSE2 are in the workspace; one grid lets the CTAs of one
-// fill the SMs the other leaves idle in its last wave.
+// Both passes in one launch.  The passes are independent once D and LSE2 are in
+// the workspace; one grid lets the CTAs of one fill the SMs the other leaves idle
+// in its last wave.  Order of the CTAs (x fastest, then the head y):
+//   dq_first == 0: per head, x < n_kt runs the dK/dV pass for key tile x and the
+//     rest the dQ pass for query tile x - n_kt, so that a head's two sets of CTAs
+//     run together and share its Q, K, V, dO in L2;
+//   dq_first == 1: the dQ CTAs of all heads first, then all dK/dV CTAs - for
+//     shapes whose dQ CTAs (n_kt key tiles each) are much longer than the dK/dV
+//     CTAs (n_qt query tiles each): started first, they do not end in a tail.
 template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_passes_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -651,14 +656,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       const uint16_t* __restrict__ do2_ptr, const float* __restrict__ lse2,
                       const float* __restrict__ delta, void* __restrict__ dq, void* __restrict__ dk, void* __restrict__ dv,
                       void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
-                      unsigned int* status) {
-    const int n_kt = (n_k + BT - 1) / BT;
-    if ((int)blockIdx.x < n_kt)
+                      unsigned int* status, int dq_first) {
+    const int n_kt = (n_k + BT - 1) / BT, n_qt = (n_q + BT - 1) / BT;
+    int dkdv_tile = -1, dq_tile = -1, bh;
+    if (!dq_first) {
+        bh = blockIdx.y;
+        if ((int)blockIdx.x < n_kt) dkdv_tile = blockIdx.x;
+        else dq_tile = blockIdx.x - n_kt;
+    } else {
+        const int lin = blockIdx.y * gridDim.x + blockIdx.x, n_dq = (int)gridDim.y * n_qt;
+        if (lin < n_dq) {
+            bh = lin / n_qt;
+            dq_tile = lin % n_qt;
+        } else {
+            bh = (lin - n_dq) / n_kt;
+            dkdv_tile = (lin - n_dq) % n_kt;
+        }
+    }
+    if (dkdv_tile >= 0)
         dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, lse2, delta, dk, dv, dv2, n_q, n_k, n_q_pad,
-                                d_act, scale, scale_log2, status, blockIdx.x, blockIdx.y);
+                                d_act, scale, scale_log2, status, dkdv_tile, bh);
     else
         dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act,
-                              scale, scale_log2, status, blockIdx.x - n_kt, blockIdx.y);
+                              scale, scale_log2, status, dq_tile, bh);
 }
 
 // ------------------------------------------------------------------------------ launch
@@ -702,7 +722,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         both<<<dim3((unsigned)(n_kt + n_qt), (unsigned)p.bh, 1), kBwdThreads, smem, stream>>>(
             tq, tk, tv, tdo, tv2, tdo2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
             static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, p.dk, p.dv, p.dv2, (int)p.n_q,
-            (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status);
+            (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, n_kt >= 4 * n_qt ? 1 : 0);
         return cudaGetLastError();
     }
     if (stages & kBwdDkDv) {
