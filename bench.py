@@ -390,6 +390,7 @@ def run_ours(args):
         "peak_bf16_burst_tflops": pk["bf16"], "peak_source": pk["source"],
     }
     components.update(separate_passes(torch, B, sets[0], stream, s128))
+    components.update(other_configs(torch, B, dev, pk))
 
     # ------------------------------------------------------------------ PSA pack / merge bandwidth
     components.update(psa_bandwidth(torch, B, dev, pk))
@@ -482,6 +483,53 @@ def separate_passes(torch, B, b, stream, scale, reps=20):
     B.fa2_device_status()
     return {"bwd_stages_separately_ms": sum(t), "bwd_preprocess_ms": t[0], "bwd_dkdv_pass_ms": t[1],
             "bwd_dq_pass_ms": t[2], "bwd_dkdv_pass_tflops": 0.8 * BWD_FLOPS / t[1] / 1e9}
+
+
+def other_configs(torch, B, dev, pk, reps=20):
+    """The other attention shapes of the workload list, timed after the main region (seeded
+    N(0,1) inputs; each call timed alone with CUDA events, median of `reps`):
+    forward B=4 H=16 N=4096 d=64, and cross attention B=1 H=32 N_q=1024 N_k=32768 d=128
+    with K scaled by 8 (peaked rows), forward and backward."""
+    out = {}
+    for tag, bh, nq, nk, d, kscale, with_bwd in (("fwd_b4h16_n4096_d64", 64, 4096, 4096, 64, 1.0, True),
+                                                 ("cross_b1h32_nq1024_nk32768_d128", 32, 1024, 32768, 128, 8.0, True)):
+        g = torch.Generator(device=dev).manual_seed(synth.BASE_SEED)
+        q = torch.randn((bh, nq, d), device=dev, generator=g).to(torch.bfloat16)
+        k = (kscale * torch.randn((bh, nk, d), device=dev, generator=g)).to(torch.bfloat16)
+        v = torch.randn((bh, nk, d), device=dev, generator=g).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty((bh, nq), dtype=torch.float32, device=dev)
+        scale = 1 / math.sqrt(d)
+        fl = 4.0 * bh * nq * nk * d
+
+        def med(fn):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                fn()
+                b.record()
+                b.synchronize()
+                ts.append(a.elapsed_time(b))
+            return statistics.median(ts)
+        f_ms = med(lambda: B.fa2_forward(q, k, v, o, lse, scale))
+        out[f"{tag}_fwd_ms"] = f_ms
+        out[f"{tag}_fwd_tflops"] = fl / f_ms / 1e9
+        out[f"{tag}_fwd_frac_burst_peak"] = fl / f_ms / 1e9 / pk["bf16"]
+        if with_bwd:
+            d_o = torch.randn((bh, nq, d), device=dev, generator=g).to(torch.bfloat16)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            ws = torch.empty(B.fa2_backward_workspace_size(bh, nq, nk, d, B.DTYPE_BF16), dtype=torch.uint8, device=dev)
+            b_ms = med(lambda: B.fa2_backward(q, k, v, o, d_o, lse, dq, dk, dv, ws, scale))
+            out[f"{tag}_bwd_ms"] = b_ms
+            out[f"{tag}_bwd_tflops"] = 2.5 * fl / b_ms / 1e9
+            out[f"{tag}_bwd_frac_burst_peak"] = 2.5 * fl / b_ms / 1e9 / pk["bf16"]
+        B.fa2_device_status()
+        del q, k, v, o, lse
+    torch.cuda.empty_cache()
+    return out
 
 
 def c2psa_graph_timings(torch, B, dev):
