@@ -16,6 +16,7 @@
 // extraction and its adjoint move contiguous runs of 2*KD*N elements per head.
 // Copies move words without interpreting them (any bit pattern survives); the
 // accumulating adjoint adds in float32 and rounds once to the storage type.
+#include <atomic>
 #include "common.cuh"
 #include "internal.h"
 
@@ -115,6 +116,59 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// 16-bit data with R and C multiples of 8: each thread moves one 8 x 8 block of
+// block z.  It loads the block's 8 rows as 16-byte vectors, transposes it in
+// registers - word m of output row j pairs elements (2m, j) and (2m + 1, j), one
+// byte permute per word - and stores 8 vectors along R.  No shared memory, no bank
+// conflicts, 8 loads in flight.  Neighbouring lanes take neighbouring blocks along
+// the dimension with fewer blocks (kRowFast: along R), so that both sides are
+// contiguous runs: the loads of a row, and the stores of a destination row.
+template <typename Map, bool kRowFast>
+__global__ void __launch_bounds__(kThreads)
+    psa_transpose8_kernel(const uint16_t* __restrict__ src0, const uint16_t* __restrict__ src1,
+                          uint16_t* __restrict__ dst0, uint16_t* __restrict__ dst1, int64_t R, int64_t C,
+                          int64_t batches, Map map) {
+    const int64_t rb_n = R / 8, cb_n = C / 8, blocks = rb_n * cb_n;
+    const int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (t >= batches * blocks) return;
+    const int64_t z = t / blocks, rem = t % blocks;
+    const int64_t rb = kRowFast ? rem % rb_n : rem / cb_n, cb = kRowFast ? rem / rb_n : rem % cb_n;
+    const BlockRef blk = map(z);
+    const uint16_t* src = (blk.src_sel ? src1 : src0) + blk.src_off + (rb * 8) * C + cb * 8;
+    uint16_t* out = (blk.dst_sel ? dst1 : dst0) + blk.dst_off + (cb * 8) * R + rb * 8;
+    uint32_t w[8][4];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + k * C);
+        w[k][0] = v.x;
+        w[k][1] = v.y;
+        w[k][2] = v.z;
+        w[k][3] = v.w;
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            lo[m] = __byte_perm(w[2 * m][p], w[2 * m + 1][p], 0x5410);  // elements (2m, 2p), (2m+1, 2p)
+            hi[m] = __byte_perm(w[2 * m][p], w[2 * m + 1][p], 0x7632);  // elements (2m, 2p+1), (2m+1, 2p+1)
+        }
+        *reinterpret_cast<uint4*>(out + (2 * p) * R) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(out + (2 * p + 1) * R) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    }
+}
+
+// SMs of the current device, looked up once per device (0 if the query fails).
+inline int sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int sms = cache[dev].load(std::memory_order_relaxed);
+    if (sms == 0 && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+        cache[dev].store(sms, std::memory_order_relaxed);
+    return sms;
+}
+
 template <typename W, int TR, int TC, typename Map>
 cudaError_t launch_t(const PsaParams& p, int64_t R, int64_t C, int64_t batches, Map map, bool vec, cudaStream_t stream) {
     const dim3 grid((unsigned)((C + TC - 1) / TC), (unsigned)((R + TR - 1) / TR), (unsigned)batches);
@@ -122,6 +176,20 @@ cudaError_t launch_t(const PsaParams& p, int64_t R, int64_t C, int64_t batches, 
     const W* s1 = static_cast<const W*>(p.src1 ? p.src1 : p.src0);
     W* d0 = static_cast<W*>(p.dst);
     W* d1 = static_cast<W*>(p.dst1 ? p.dst1 : p.dst);
+    if constexpr (sizeof(W) == 2) {
+        // One thread per 64 elements: worth it only while the grid still gives every SM
+        // several blocks; smaller tensors keep the tiled kernel's finer grid.
+        const bool fills = batches * (R / 8) * (C / 8) >= (int64_t)4 * sm_count() * kThreads;
+        if (vec && R % 8 == 0 && C % 8 == 0 && fills) {
+            const int64_t threads = batches * (R / 8) * (C / 8);
+            const unsigned grid = (unsigned)((threads + kThreads - 1) / kThreads);
+            if (R < C)
+                psa_transpose8_kernel<Map, true><<<grid, kThreads, 0, stream>>>(s0, s1, d0, d1, R, C, batches, map);
+            else
+                psa_transpose8_kernel<Map, false><<<grid, kThreads, 0, stream>>>(s0, s1, d0, d1, R, C, batches, map);
+            return cudaGetLastError();
+        }
+    }
     if (vec)
         psa_transpose_kernel<W, TR, TC, true, Map><<<grid, kThreads, 0, stream>>>(s0, s1, d0, d1, R, C, map);
     else

@@ -594,37 +594,68 @@ def c2psa_graph_timings(torch, B, dev):
     return out
 
 
+def _graph_ms_per_call(torch, fn, calls=50, replays=20):
+    """Device time of one fn() call: `calls` back-to-back calls captured in a CUDA graph,
+    replayed `replays` times between two events (no per-launch host cost in the figure)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    for _ in range(3):
+        g.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (calls * replays)
+
+
 def psa_bandwidth(torch, B, dev, pk):
-    """psa_pack_qkv / psa_merge_attn_nchw GB/s: at the C2PSA shape (L2-resident) and at
-    B=1024 (419 MB per tensor, larger than L2)."""
+    """psa_pack_qkv / psa_merge_attn_nchw GB/s: at the C2PSA shape (3.3 MB per tensor,
+    L2-resident; a CUDA graph of 50 back-to-back calls, so that the few-microsecond kernels
+    and not the host's launch cost are timed) and at B=1024 (419 MB per tensor, larger than
+    L2: every call reads from and writes to HBM; median of per-call events)."""
     out = {}
     for label, b in (("c2psa", PSA_B), ("hbm_b1024", 1024)):
         qkv = torch.randn((b, PSA_NH * 4 * PSA_KD, PSA_H, PSA_W), device=dev).to(torch.float16)
         packed = torch.empty((4, b * PSA_NH, PSA_N, PSA_KD), dtype=torch.float16, device=dev)
         merged = torch.empty((b, PSA_NH * 2 * PSA_KD, PSA_H, PSA_W), dtype=torch.float16, device=dev)
-        reps = 50 if b > PSA_B else 200
-        times = {"pack": [], "merge": []}
-        for _ in range(5):
-            B.psa_pack_qkv(qkv, packed, PSA_NH)
-            B.psa_merge_attn_nchw(packed[2], packed[3], merged, PSA_NH)
-        for _ in range(reps):
-            for name in ("pack", "merge"):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                if name == "pack":
-                    B.psa_pack_qkv(qkv, packed, PSA_NH)
-                else:
-                    B.psa_merge_attn_nchw(packed[2], packed[3], merged, PSA_NH)
-                e1.record()
-                times[name].append((e0, e1))
-        torch.cuda.synchronize()
+        calls = {"pack": lambda: B.psa_pack_qkv(qkv, packed, PSA_NH),
+                 "merge": lambda: B.psa_merge_attn_nchw(packed[2], packed[3], merged, PSA_NH)}
+        ms = {}
+        if label == "c2psa":
+            for name, fn in calls.items():
+                ms[name] = _graph_ms_per_call(torch, fn)
+        else:
+            times = {"pack": [], "merge": []}
+            for _ in range(5):
+                for fn in calls.values():
+                    fn()
+            for _ in range(50):
+                for name, fn in calls.items():
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    fn()
+                    e1.record()
+                    times[name].append((e0, e1))
+            torch.cuda.synchronize()
+            ms = {name: statistics.median(e0.elapsed_time(e1) for e0, e1 in t) for name, t in times.items()}
         nbytes = {"pack": 2 * qkv.numel() * 2, "merge": 2 * merged.numel() * 2}
         for name in ("pack", "merge"):
-            ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in times[name])
-            out[f"psa_{name}_{label}_gbs"] = nbytes[name] / (ms * 1e-3) / 1e9
+            out[f"psa_{name}_{label}_gbs"] = nbytes[name] / (ms[name] * 1e-3) / 1e9
             if label != "c2psa":
                 out[f"psa_{name}_{label}_frac_hbm"] = out[f"psa_{name}_{label}_gbs"] / pk["hbm_gbs"]
         del qkv, packed, merged
+    B.fa2_device_status()
     return out
 
 

@@ -121,6 +121,37 @@ def test_extract_v_and_adjoints_bit_exact(dtype, B, nh, kd, H, W):
     assert np.array_equal(_words(d_hi, dtype).reshape(want_hi.shape), want_hi)
 
 
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("B,nh,kd,H,W", [(128, 4, 32, 20, 20), (421, 5, 24, 8, 13)])
+def test_large_rearrangements_bit_exact(dtype, B, nh, kd, H, W):
+    """Batches large enough for the one-thread-per-8x8-block transpose on every one of the
+    four rearrangements (pack, merge and their adjoints); the second shape leaves a partial
+    last block of threads and head sizes that are not powers of two."""
+    G.require_gpu()
+    tag = f"psa_big/{dtype}/{B}/{nh}/{kd}/{H}/{W}"
+    bh, n = B * nh, H * W
+    qkv = _patterns(tag + "/qkv", (B, nh * 4 * kd, H, W), dtype)
+    packed = G.empty((4, bh, n, kd), dtype)
+    binding.psa_pack_qkv(_raw_tensor(qkv, dtype).view(qkv.shape), packed, nh)
+    lo = _patterns(tag + "/lo", (bh, n, kd), dtype)
+    hi = _patterns(tag + "/hi", (bh, n, kd), dtype)
+    merged = G.empty((B, nh * 2 * kd, H, W), dtype)
+    binding.psa_merge_attn_nchw(_raw_tensor(lo, dtype).view(lo.shape), _raw_tensor(hi, dtype).view(hi.shape), merged, nh)
+    d_qkv = G.empty(qkv.shape, dtype)
+    d_packed = _patterns(tag + "/dpacked", (4, bh, n, kd), dtype)
+    binding.psa_pack_qkv_backward(_raw_tensor(d_packed, dtype).view(d_packed.shape), d_qkv, nh)
+    d_merged = _patterns(tag + "/dmerged", (B, nh * 2 * kd, H, W), dtype)
+    d_lo, d_hi = G.empty((bh, n, kd), dtype), G.empty((bh, n, kd), dtype)
+    binding.psa_merge_attn_backward(_raw_tensor(d_merged, dtype).view(d_merged.shape), d_lo, d_hi, nh)
+    binding.fa2_device_status()
+    assert np.array_equal(_words(packed, dtype).reshape(4, bh, n, kd), P.pack_qkv(qkv, nh))
+    assert np.array_equal(_words(merged, dtype).reshape(merged.shape), P.merge_attn_nchw(lo, hi, B, nh, H, W))
+    assert np.array_equal(_words(d_qkv, dtype).reshape(qkv.shape), P.pack_qkv_backward(d_packed, B, nh, H, W))
+    want_lo, want_hi = P.merge_attn_backward(d_merged, nh)
+    assert np.array_equal(_words(d_lo, dtype).reshape(want_lo.shape), want_lo)
+    assert np.array_equal(_words(d_hi, dtype).reshape(want_hi.shape), want_hi)
+
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("B,nh,kd,H,W", [(8, 4, 32, 20, 20), (3, 1, 8, 3, 5)])
 def test_extract_v_backward_accumulates_exactly(dtype, B, nh, kd, H, W):
