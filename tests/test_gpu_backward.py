@@ -7,7 +7,7 @@ import pytest
 from attention_fa2_forward_02_gb300 import binding, synth
 from oracle import attention as A
 from tests import gpu_util as G
-from tests.tolerance import check_16bit
+from tests.tolerance import check_16bit, check_16bit_grad
 
 pytestmark = pytest.mark.gpu
 
@@ -74,6 +74,40 @@ def test_backward_full_size_sampled():
         check_16bit(dk[b], rk, f"dK head {b}")
         check_16bit(dv[b], rv, f"dV head {b}")
 
+
+
+def test_backward_full_size_d64_sampled():
+    """bf16 forward+backward, B=4 H=16 (BH=64), N=4096, d=64 (the one-pass backward with the
+    float32 dQ accumulator): every dQ/dK/dV row of the first and last heads against the oracle."""
+    bh, n, d = 64, 4096, 64
+    q, k, v = G.inputs("config/fwdbwd_d64", bh, n, n, d, "bf16")
+    d_o = synth.tensor("config/fwdbwd_d64/do", (bh, n, d), "bf16")
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, "bf16", scale)
+    w = lambda x: synth.widen(x, "bf16")
+    for b in (0, bh - 1):
+        rq, rk, rv = A.backward_slice(w(q[b:b + 1]), w(k[b:b + 1]), w(v[b:b + 1]), w(d_o[b:b + 1]), scale, 0)
+        check_16bit(dq[b], rq, f"dQ head {b}")
+        check_16bit(dk[b], rk, f"dK head {b}")
+        check_16bit(dv[b], rv, f"dV head {b}")
+
+
+def test_backward_cross_attention_peaked_sampled():
+    """B=1 H=32, N_q=1024 vs N_k=32768, d=128, K scaled by 8 (peaked rows; the one-grid passes
+    kernel puts its dQ CTAs first at this shape): every dQ/dK/dV row of heads 0 and 31."""
+    bh, n_q, n_k, d = 32, 1024, 32768, 128
+    q, k, v = G.inputs("config/cross_k8", bh, n_q, n_k, d, "bf16", k_scale=8.0)
+    d_o = synth.tensor("config/cross_k8/do", (bh, n_q, d), "bf16")
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, "bf16", scale)
+    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+    w = lambda x: synth.widen(x, "bf16")
+    for b in (0, bh - 1):
+        rq, rk, rv = A.backward_slice(w(q[b:b + 1]), w(k[b:b + 1]), w(v[b:b + 1]), w(d_o[b:b + 1]), scale, 0,
+                                      row_chunk=256)
+        check_16bit_grad(dq[b], rq, f"dQ head {b}")
+        check_16bit_grad(dk[b], rk, f"dK head {b}")
+        check_16bit_grad(dv[b], rv, f"dV head {b}")
 
 def _stages(qd, kd, vd, o, dod, lse, scale, ws, dtype):
     """The two-pass backward through its three stage entry points."""

@@ -461,3 +461,19 @@ def test_tolerance_rejects_null_output():
     with pytest.raises(AssertionError):
         check_16bit(ref * 0.9, ref)
     check_16bit(ref + 1e-5, ref)
+
+
+def test_gradient_tolerance_scales_with_magnitude_but_rejects_errors():
+    """Gradients ~30 (peaked rows): their own 16-bit rounding passes; zeroed, 10 %-scaled
+    or biased gradients fail."""
+    from tests.tolerance import check_16bit_grad
+    ref = _rand((256, 64), 91, scale=10.0)
+    rounded = synth.widen(synth.to_storage(ref, "bf16"), "bf16")
+    assert np.max(np.abs(rounded - ref)) > 2e-2  # beyond a fixed absolute 2e-2
+    check_16bit_grad(rounded, ref)
+    for bad in (np.zeros_like(ref), ref * 0.9, ref + 0.05 * np.std(ref)):
+        with pytest.raises(AssertionError):
+            check_16bit_grad(bad, ref)
+    small = _rand((64, 32), 92, scale=1e-2)
+    with pytest.raises(AssertionError):
+        check_16bit_grad(np.zeros_like(small), small)
