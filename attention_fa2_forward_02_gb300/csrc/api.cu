@@ -56,9 +56,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool valid_dtype(fa2_dtype d) { return d == FA2_DTYPE_F32 || d == FA2_DTYPE_F16 || d == FA2_DTYPE_BF16; }
 
-// Any multiple of 8 up to 128: the kernels run at the next of 32, 64, 128 with the
+// 16-bit types: any multiple of 8 up to 128 (rows of whole 16-byte units, as the
+// tensor-memory copies need): the kernels run at the next of 32, 64, 128 with the
 // extra columns read as zeros (TMA fills past the tensor edge) and never stored.
-bool supported_head_dim(int32_t d) { return d >= 8 && d <= 128 && d % 8 == 0; }
+// float32 (plain loads and stores): any head dimension up to 128.
+bool supported_head_dim(int32_t d, fa2_dtype dtype) {
+    if (dtype == FA2_DTYPE_F32) return d >= 1 && d <= 128;
+    return d >= 8 && d <= 128 && d % 8 == 0;
+}
 
 constexpr int64_t kMaxGridY = 65535;
 constexpr int64_t kMaxSeq = (int64_t)1 << 30;
@@ -68,7 +73,7 @@ fa2_status check_attention_sizes(int64_t bh, int64_t n_q, int64_t n_k, int32_t h
     if (bh <= 0 || n_q <= 0 || n_k <= 0 || head_dim <= 0) return FA2_ERR_INVALID_ARG;
     if (!valid_dtype(dtype)) return FA2_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !isfinite(scale)) return FA2_ERR_INVALID_ARG;
-    if (!supported_head_dim(head_dim)) return FA2_ERR_UNSUPPORTED;
+    if (!supported_head_dim(head_dim, dtype)) return FA2_ERR_UNSUPPORTED;
     if (bh > kMaxGridY || n_q > kMaxSeq || n_k > kMaxSeq) return FA2_ERR_UNSUPPORTED;
     return FA2_OK;
 }

@@ -21,11 +21,12 @@
  *  - Layout of attention tensors: [BH, N, HEAD_DIM] with BH = BATCH * N_HEADS
  *    ("vision-rs 0.1.1 flash_attn2.rs", module comment: all tensors stored as
  *    [BATCH * N_HEADS, N_CTX, HEAD_DIM] row-major, contiguous).
- *  - HEAD_DIM: any multiple of 8 from 8 to 128 (rows must be whole 16-byte
- *    units for the tensor-memory copies).  The kernels run at the next of 32,
- *    64, 128; the columns beyond HEAD_DIM are read as zeros and never written.
- *    The pages' builders take any head dimension; one that is not a multiple
- *    of 8 returns FA2_ERR_UNSUPPORTED.
+ *  - HEAD_DIM: for BF16 / F16 any multiple of 8 from 8 to 128 (rows must be
+ *    whole 16-byte units for the tensor-memory copies); for F32 any value from 1
+ *    to 128, as the pages' builders allow (e.g. 7).  The kernels run at the next
+ *    of 32, 64, 128; the columns beyond HEAD_DIM are read as zeros and never
+ *    written.  A 16-bit head dimension that is not a multiple of 8 returns
+ *    FA2_ERR_UNSUPPORTED.
  */
 #ifndef FA2_GB300_H
 #define FA2_GB300_H
@@ -73,7 +74,7 @@ typedef enum {
  *
  * dtype BF16 / F16: head_dim a multiple of 8 in [8, 128]; tensor-core kernel, float32
  * accumulation, the probabilities rounded to dtype before the P.V product.
- * dtype F32: head_dim a multiple of 8 in [8, 128]; a float32 CUDA-core kernel (meant for
+ * dtype F32: any head_dim in [1, 128]; a float32 CUDA-core kernel (meant for
  * small problems; float32 products and sums throughout).
  * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED, FA2_ERR_CUDA.
  */

@@ -63,6 +63,7 @@ def fwd(lib, q=P, k=P, v=P, o=P, l=P, bh=2, nq=64, nk=64, d=64, dt=BF16, scale=0
     ({"q": None}, INVALID), ({"l": None}, INVALID), ({"bh": 0}, INVALID), ({"nq": 0}, INVALID), ({"nk": -1}, INVALID),
     ({"d": 0}, INVALID), ({"dt": 7}, INVALID), ({"scale": 0.0}, INVALID), ({"scale": float("nan")}, INVALID),
     ({"scale": float("inf")}, INVALID), ({"d": 12}, UNSUPPORTED), ({"d": 136}, UNSUPPORTED), ({"d": 7}, UNSUPPORTED),
+    ({"d": 129, "dt": F32}, UNSUPPORTED), ({"d": 12, "dt": F16}, UNSUPPORTED),
     ({"bh": 70000}, UNSUPPORTED), ({"q": PM}, MISALIGNED), ({"o": PM}, MISALIGNED),
 ])
 def test_forward_validation(lib, kw, want):

@@ -81,6 +81,17 @@ def test_forward_page_worked_example(dtype):
     assert abs(lse[0, 0] - g["lse"]) <= 1e-5
 
 
+def test_forward_constant_rows_example_at_its_own_head_dim():
+    """The constant-input example exactly as the page's unit test states it: N = 5,
+    head_dim 7 (float32, the only type whose rows need not be 16-byte multiples)."""
+    g = load("constant_rows.txt")
+    n, d = int(g["n_q"]), int(g["head_dim"])
+    q, k, v = (np.full((1, n, d), g[f"fill_{x}"], dtype=np.float32) for x in ("q", "k", "v"))
+    o, lse = run_forward(q, k, v, "f32", g["scale"])
+    assert np.all(o == g["fill_o"])
+    assert np.max(np.abs(lse - g["lse"])) <= 1e-5
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 def test_forward_constant_rows_example(dtype):
     """The constant-input example (q=1, k=0.5, v=2) at GPU head_dim 32 and several tiles of rows."""

@@ -45,7 +45,7 @@ def test_forward_backward_any_head_dim(d, dtype):
     check_16bit(G.to_f64(dv), rv, "dV")
 
 
-@pytest.mark.parametrize("d", [8, 16, 48, 104])
+@pytest.mark.parametrize("d", [1, 3, 7, 8, 16, 48, 100, 104, 127])
 def test_forward_f32_any_head_dim(d):
     torch = G.require_gpu()
     bh, n_q, n_k = 2, 64, 90
