@@ -485,9 +485,26 @@ def separate_passes(torch, B, b, stream, scale, reps=20):
             "bwd_dq_pass_ms": t[2], "bwd_dkdv_pass_tflops": 0.8 * BWD_FLOPS / t[1] / 1e9}
 
 
+def _batched_ms(torch, fn, reps=20, batch=8):
+    """Device time of one fn() call: `batch` calls back to back between two events (the host
+    queues them ahead of the GPU, so no launch cost falls inside), median over `reps`."""
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(batch):
+            fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) / batch)
+    return statistics.median(ts)
+
+
 def other_configs(torch, B, dev, pk, reps=20):
     """The other attention shapes of the workload list, timed after the main region (seeded
-    N(0,1) inputs; each call timed alone with CUDA events, median of `reps`):
+    N(0,1) inputs; median of `reps` timings of 8 back-to-back calls each):
     forward B=4 H=16 N=4096 d=64, and cross attention B=1 H=32 N_q=1024 N_k=32768 d=128
     with K scaled by 8 (peaked rows), forward and backward."""
     out = {}
@@ -503,17 +520,7 @@ def other_configs(torch, B, dev, pk, reps=20):
         fl = 4.0 * bh * nq * nk * d
 
         def med(fn):
-            for _ in range(3):
-                fn()
-            ts = []
-            for _ in range(reps):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record()
-                fn()
-                b.record()
-                b.synchronize()
-                ts.append(a.elapsed_time(b))
-            return statistics.median(ts)
+            return _batched_ms(torch, fn, reps)
         f_ms = med(lambda: B.fa2_forward(q, k, v, o, lse, scale))
         out[f"{tag}_fwd_ms"] = f_ms
         out[f"{tag}_fwd_tflops"] = fl / f_ms / 1e9
@@ -623,7 +630,7 @@ def psa_bandwidth(torch, B, dev, pk):
     """psa_pack_qkv / psa_merge_attn_nchw GB/s: at the C2PSA shape (3.3 MB per tensor,
     L2-resident; a CUDA graph of 50 back-to-back calls, so that the few-microsecond kernels
     and not the host's launch cost are timed) and at B=1024 (419 MB per tensor, larger than
-    L2: every call reads from and writes to HBM; median of per-call events)."""
+    L2: every call reads from and writes to HBM; median of 50 timings of 4 back-to-back calls)."""
     out = {}
     for label, b in (("c2psa", PSA_B), ("hbm_b1024", 1024)):
         qkv = torch.randn((b, PSA_NH * 4 * PSA_KD, PSA_H, PSA_W), device=dev).to(torch.float16)
@@ -636,19 +643,8 @@ def psa_bandwidth(torch, B, dev, pk):
             for name, fn in calls.items():
                 ms[name] = _graph_ms_per_call(torch, fn)
         else:
-            times = {"pack": [], "merge": []}
-            for _ in range(5):
-                for fn in calls.values():
-                    fn()
-            for _ in range(50):
-                for name, fn in calls.items():
-                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    e0.record()
-                    fn()
-                    e1.record()
-                    times[name].append((e0, e1))
-            torch.cuda.synchronize()
-            ms = {name: statistics.median(e0.elapsed_time(e1) for e0, e1 in t) for name, t in times.items()}
+            for name, fn in calls.items():
+                ms[name] = _batched_ms(torch, fn, reps=50, batch=4)
         nbytes = {"pack": 2 * qkv.numel() * 2, "merge": 2 * merged.numel() * 2}
         for name in ("pack", "merge"):
             out[f"psa_{name}_{label}_gbs"] = nbytes[name] / (ms[name] * 1e-3) / 1e9
