@@ -401,7 +401,7 @@ def run_ours(args):
     # results (O, LSE, dQ, dK, dV, the merged C2PSA output) back.  Two buffer sets
     # and two copy streams let the copies of steps s+2 (in) and s (out) run while
     # step s+1 computes.
-    e2e_steps = max(4, args.steps // 10)
+    e2e_steps = max(4, args.steps // 5)
     sets.append(alloc_set(False))
     out_names = ["o", "lse", "dq", "dk", "dv", "merged"]
     host_out = {n: torch.empty(sets[0][n].shape, dtype=sets[0][n].dtype).pin_memory() for n in out_names}
