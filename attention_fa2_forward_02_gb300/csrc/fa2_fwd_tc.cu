@@ -13,6 +13,19 @@
 //   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
 //   warps 2-5   softmax for Q0 (one thread per query row / TMEM lane)
 //   warps 6-9   softmax for Q1
+//   warp 10     (head size 128) waits for the TMA copies on behalf of the issuer
+// At head size 128 the issuer never waits on an mbarrier: a shared-memory access (an
+// mbarrier test included) by the warp that issues tcgen05.mma costs a few hundred
+// clocks of tensor-pipe time each. Warp 10 and the softmax groups signal it through
+// named barriers instead (barrier.arrive; the issuer's barrier.sync is not a memory
+// access): one barrier per query tile for "P ready", one per ring stage for "V
+// loaded" and "K loaded". A producer cannot arrive twice on one barrier before the
+// issuer has synced on it (its next arrival needs a tile the issuer has not yet
+// released or issued), and every producer arrives exactly once per event whatever
+// happens: a failed bounded wait skips the work, not the arrival, and raises the
+// watchdog status. The issuer itself never gives up; a failure elsewhere only makes
+// it multiply stale tiles until its loop ends. Smaller heads, paced by the softmax,
+// keep lane 0 of the issuer waiting on the mbarriers itself, which wakes it sooner.
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128) S0 = Q0 K^T   [128,256) S1 = Q1 K^T   [256,256+D) O0   [256+D,256+2D) O1
 // The probabilities P (16-bit) are written back over the first 64 columns of
@@ -33,7 +46,22 @@ namespace {
 constexpr int BM = 128;            // query rows per tile = TMEM lanes
 constexpr int BN = 128;            // keys per K/V tile
 constexpr int kQTiles = 2;         // query tiles per CTA
-constexpr int kThreads = 320;      // 10 warps
+constexpr int kRelayWarp = 10;
+// Named barriers (0 is __syncthreads): 1 + t: P of query tile t ready (softmax group
+// t + issuer, 160 threads); then per ring stage s: V loaded, K loaded (relay + issuer,
+// 64 threads).
+constexpr uint32_t kNbP = 1;
+__host__ __device__ constexpr uint32_t nb_v(int s) { return 1 + 2 + (uint32_t)s; }
+__host__ __device__ constexpr uint32_t nb_k(int S, int s) { return 1 + 2 + (uint32_t)(S + s); }
+
+// Named-barrier signal and wait for whole warps (`count` threads in all); neither is a
+// memory access.
+__device__ __forceinline__ void nb_arrive(uint32_t id, uint32_t count) {
+    asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void nb_sync(uint32_t id, uint32_t count) {
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
@@ -43,6 +71,12 @@ constexpr float kLn2 = 0.693147180559945309f;
 template <int D, int kNV>
 struct FwdCfg : Tile16<D> {
     static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
+    // Head size 128 (one value tensor): the issuer is fed through named barriers and
+    // a TMA relay warp (11 warps). Smaller heads, where the softmax rather than the
+    // tensor pipe sets the pace, keep the issuer's own mbarrier waits (10 warps): there
+    // a lane-0 mbarrier wait wakes it sooner.
+    static constexpr bool kNamed = D == 128 && kNV == 1;
+    static constexpr int kThreads = kNamed ? 352 : 320;
     static constexpr int kQTileBytes = BM * D * 2;
     static constexpr int kKVTileBytes = BN * D * 2;
     static constexpr int kVStageBytes = kNV * kKVTileBytes;
@@ -58,7 +92,7 @@ struct FwdCfg : Tile16<D> {
 };
 
 template <int D, bool kBf16, int kNV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
     fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v2,
                       void* __restrict__ o_ptr, void* __restrict__ o2_ptr, float* __restrict__ lse_ptr, int n_q, int n_k,
@@ -162,30 +196,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if constexpr (C::kNamed) {
+            // The whole warp walks the loop and waits for its producers' named-barrier
+            // signals; lane 0 issues.
             const uint32_t idesc_s = idesc_f16_f32acc(BM, BN, kBf16, false, false);
             const uint32_t idesc_o = idesc_f16_f32acc(BM, D, kBf16, false, true);
             auto issue_s = [&](int t, int s) {
                 const uint32_t d_tmem = tmem + (uint32_t)(t * BN);
                 const uint32_t qa = q_smem + t * C::kQTileBytes;
                 const uint32_t kb = k_smem + s * C::kKVTileBytes;
-#pragma unroll
+    #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(d_tmem, C::kmajor(qa, kk, BM), C::kmajor(kb, kk, BN), idesc_s, kk > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int t, int s, bool acc) {
-#pragma unroll
+    #pragma unroll
                 for (int v = 0; v < kNV; ++v) {
                     const uint32_t d_tmem = tmem + 256u + (uint32_t)((t * kNV + v) * D);
                     const uint32_t vb = v_smem + s * C::kVStageBytes + v * C::kKVTileBytes;
-#pragma unroll
+    #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
                         mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
                                (acc || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = mbar_wait(B_Q, 0, wd) && mbar_wait(B_KF(0), 0, wd);
-            if (ok) {
+            static_assert(1 + 2 + 2 * S <= 16, "named barriers");
+            nb_sync(nb_k(S, 0), 64);  // Q and the first K tile
+            if (lane == 0) {
                 tc_fence_after();
                 issue_s(0, 0);
                 mma_commit(B_SF(0));
@@ -193,31 +230,113 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(B_SF(1));
                 mma_commit(B_KE(0));
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
+            __syncwarp();
+            for (int j = 0; j < n_kv; ++j) {
                 const int s = j % S;
                 const int jn = j + 1;
                 const int sn = jn % S;
-                if (!(ok = mbar_wait(B_VF(s), (j / S) & 1, wd))) break;
+                nb_sync(nb_v(s), 64);  // V tile j
                 for (int t = 0; t < kQTiles; ++t) {
-                    if (!(ok = mbar_wait(B_PF(t), j & 1, wd))) break;
-                    tc_fence_after();
-                    issue_pv(t, s, j > 0);
-                    if (t == kQTiles - 1) mma_commit(B_VE(s));
-                    if (jn < n_kv) {
-                        if (t == 0) {
-                            if (!(ok = mbar_wait(B_KF(sn), (jn / S) & 1, wd))) break;
-                            tc_fence_after();
-                        }
-                        issue_s(t, sn);
-                        mma_commit(B_SF(t));
-                        if (t == kQTiles - 1) mma_commit(B_KE(sn));
+                    nb_sync(kNbP + t, BM + 32);  // P of query tile t
+                    if (lane == 0) {
+                        tc_fence_after();
+                        issue_pv(t, s, j > 0);
+                        if (t == kQTiles - 1) mma_commit(B_VE(s));
                     }
+                    if (jn < n_kv) {
+                        if (t == 0) nb_sync(nb_k(S, sn), 64);  // K tile j + 1
+                        if (lane == 0) {
+                            tc_fence_after();
+                            issue_s(t, sn);
+                            mma_commit(B_SF(t));
+                            if (t == kQTiles - 1) mma_commit(B_KE(sn));
+                        }
+                    }
+                    __syncwarp();
                 }
             }
             // Completion of everything issued: the softmax groups read O after it,
             // and tensor memory is released only after it.
-            mma_commit(B_OD);
-            drain_wait(B_OD, 0);
+            if (lane == 0) {
+                mma_commit(B_OD);
+                drain_wait(B_OD, 0);
+            }
+            __syncwarp();
+        } else {
+            // lane 0 waits on the mbarriers itself
+            if (lane == 0) {
+                const uint32_t idesc_s = idesc_f16_f32acc(BM, BN, kBf16, false, false);
+                const uint32_t idesc_o = idesc_f16_f32acc(BM, D, kBf16, false, true);
+                auto issue_s = [&](int t, int s) {
+                    const uint32_t d_tmem = tmem + (uint32_t)(t * BN);
+                    const uint32_t qa = q_smem + t * C::kQTileBytes;
+                    const uint32_t kb = k_smem + s * C::kKVTileBytes;
+    #pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(d_tmem, C::kmajor(qa, kk, BM), C::kmajor(kb, kk, BN), idesc_s, kk > 0 ? 1u : 0u);
+                };
+                auto issue_pv = [&](int t, int s, bool acc) {
+    #pragma unroll
+                    for (int v = 0; v < kNV; ++v) {
+                        const uint32_t d_tmem = tmem + 256u + (uint32_t)((t * kNV + v) * D);
+                        const uint32_t vb = v_smem + s * C::kVStageBytes + v * C::kKVTileBytes;
+    #pragma unroll
+                        for (int kk = 0; kk < BN / 16; ++kk)
+                            mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
+                                   (acc || kk > 0) ? 1u : 0u);
+                    }
+                };
+                bool ok = mbar_wait(B_Q, 0, wd) && mbar_wait(B_KF(0), 0, wd);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0, 0);
+                    mma_commit(B_SF(0));
+                    issue_s(1, 0);
+                    mma_commit(B_SF(1));
+                    mma_commit(B_KE(0));
+                }
+                for (int j = 0; ok && j < n_kv; ++j) {
+                    const int s = j % S;
+                    const int jn = j + 1;
+                    const int sn = jn % S;
+                    if (!(ok = mbar_wait(B_VF(s), (j / S) & 1, wd))) break;
+                    for (int t = 0; t < kQTiles; ++t) {
+                        if (!(ok = mbar_wait(B_PF(t), j & 1, wd))) break;
+                        tc_fence_after();
+                        issue_pv(t, s, j > 0);
+                        if (t == kQTiles - 1) mma_commit(B_VE(s));
+                        if (jn < n_kv) {
+                            if (t == 0) {
+                                if (!(ok = mbar_wait(B_KF(sn), (jn / S) & 1, wd))) break;
+                                tc_fence_after();
+                            }
+                            issue_s(t, sn);
+                            mma_commit(B_SF(t));
+                            if (t == kQTiles - 1) mma_commit(B_KE(sn));
+                        }
+                    }
+                }
+                // Completion of everything issued: the softmax groups read O after it,
+                // and tensor memory is released only after it.
+                mma_commit(B_OD);
+                drain_wait(B_OD, 0);
+            }
+        }
+    } else if (C::kNamed && warp == kRelayWarp) {
+        // ------------------------------------------------------------------ TMA relay
+        // Waits for the copies the issuer needs, in the order it needs them.
+        bool ok = warp_wait(B_Q, 0, wd) && warp_wait(B_KF(0), 0, wd);
+        nb_arrive(nb_k(S, 0), 64);
+        for (int j = 0; j < n_kv; ++j) {
+            const int s = j % S;
+            const int jn = j + 1;
+            const int sn = jn % S;
+            ok = ok && warp_wait(B_VF(s), (j / S) & 1, wd);
+            nb_arrive(nb_v(s), 64);
+            if (jn < n_kv) {
+                ok = ok && warp_wait(B_KF(sn), (jn / S) & 1, wd);
+                nb_arrive(nb_k(S, sn), 64);
+            }
         }
     } else {
         // ------------------------------------------------------------------ softmax groups
@@ -231,92 +350,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         for (int j = 0; j < n_kv; ++j) {
-            if (!(ok = warp_wait(B_SF(t), j & 1, wd))) break;
-            tc_fence_after();
-            // The score row (128 columns) into registers: one read of the S tile per key tile.
-            uint32_t sr[BN / 32][32];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + 32u * c, sr[c]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
-            // Only the last key tile can be partial: its columns past the last key become
-            // -inf, which drops them from the maximum and gives them probability 0.
-            const int valid = n_k - j * BN;
-            if (valid < BN) {
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (32 * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
-            }
-            // The row maximum: 8 independent chains of three-input maxima.
-            float mx;
-            {
-                float m8[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        m8[i & 7] = fmax3(m8[i & 7], __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
-                mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-            }
-            const float m_new = mx * scale_log2;
-            float alpha = 1.f;   // factor for O and l when the reference maximum moves
-            bool rescale = false;
-            if (j == 0) {
-                m2 = m_new;
-            } else {
-                const bool need = m_new > m2 + kRescaleThreshold;
-                rescale = __any_sync(0xffffffffu, need);
-                if (need) {
-                    alpha = ex2_approx(m2 - m_new);
-                    l *= alpha;
+            // a failed wait skips the work of this and later tiles, not the meeting
+            ok = ok && warp_wait(B_SF(t), j & 1, wd);
+            if (ok) {
+                tc_fence_after();
+                // The score row (128 columns) into registers: one read of the S tile per key tile.
+                uint32_t sr[BN / 32][32];
+    #pragma unroll
+                for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + 32u * c, sr[c]);
+                tmem_ld_wait();
+    #pragma unroll
+                for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
+                // Only the last key tile can be partial: its columns past the last key become
+                // -inf, which drops them from the maximum and gives them probability 0.
+                const int valid = n_k - j * BN;
+                if (valid < BN) {
+    #pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (32 * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
+                }
+                // The row maximum: 8 independent chains of three-input maxima.
+                float mx;
+                {
+                    float m8[8];
+    #pragma unroll
+                    for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
+    #pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+    #pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            m8[i & 7] = fmax3(m8[i & 7], __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
+                    mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                }
+                const float m_new = mx * scale_log2;
+                float alpha = 1.f;   // factor for O and l when the reference maximum moves
+                bool rescale = false;
+                if (j == 0) {
                     m2 = m_new;
-                }
-            }
-            // p = 2^(s*scale*log2e - m2) from the registers, row sum in two packed partial
-            // sums, P packed to 16 bits and stored over the score columns (all already read).
-            {
-                const float2 negm2 = make_float2(-m2, -m2);
-                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 x = make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
-                        float2 y = __ffma2_rn(x, scale2, negm2);
-                        y.x = ex2_approx(y.x);
-                        y.y = ex2_approx(y.y);
-                        if (i & 1) acc1 = __fadd2_rn(acc1, y);
-                        else acc0 = __fadd2_rn(acc0, y);
-                        pk[i] = pack2<kBf16>(y.x, y.y);
+                } else {
+                    const bool need = m_new > m2 + kRescaleThreshold;
+                    rescale = __any_sync(0xffffffffu, need);
+                    if (need) {
+                        alpha = ex2_approx(m2 - m_new);
+                        l *= alpha;
+                        m2 = m_new;
                     }
-                    tmem_st16(s_addr + 16u * c, pk);
                 }
-                l += (acc0.x + acc1.x) + (acc0.y + acc1.y);
-            }
-            // The O rescale, when some row's reference maximum moved: before P is released
-            // to the P.V product (which is issued only after the arrival below), and after
-            // the previous P.V product (whose completion preceded this S tile's).
-            if (rescale) {
-#pragma unroll
-                for (int c = 0; c < kNV * D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(o_addr + 32u * c, o);
-                    tmem_ld_wait();
-                    reg_fence(o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    tmem_st32(o_addr + 32u * c, o);
+                // p = 2^(s*scale*log2e - m2) from the registers, row sum in two packed partial
+                // sums, P packed to 16 bits and stored over the score columns (all already read).
+                {
+                    const float2 negm2 = make_float2(-m2, -m2);
+                    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    #pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) {
+                        uint32_t pk[16];
+    #pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 x = make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
+                            float2 y = __ffma2_rn(x, scale2, negm2);
+                            y.x = ex2_approx(y.x);
+                            y.y = ex2_approx(y.y);
+                            if (i & 1) acc1 = __fadd2_rn(acc1, y);
+                            else acc0 = __fadd2_rn(acc0, y);
+                            pk[i] = pack2<kBf16>(y.x, y.y);
+                        }
+                        tmem_st16(s_addr + 16u * c, pk);
+                    }
+                    l += (acc0.x + acc1.x) + (acc0.y + acc1.y);
                 }
+                // The O rescale, when some row's reference maximum moved: before P is released
+                // to the P.V product (which is issued only after the arrival below), and after
+                // the previous P.V product (whose completion preceded this S tile's).
+                if (rescale) {
+    #pragma unroll
+                    for (int c = 0; c < kNV * D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(o_addr + 32u * c, o);
+                        tmem_ld_wait();
+                        reg_fence(o);
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        tmem_st32(o_addr + 32u * c, o);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(B_PF(t));
+            // P of this tile ready for the issuer
+            if constexpr (C::kNamed) nb_arrive(kNbP + t, BM + 32);
+            else mbar_arrive(B_PF(t));
         }
         if (ok) ok = warp_wait(B_OD, 0, wd);
         if (ok) {
@@ -377,7 +501,7 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((p.n_q + BM * kQTiles - 1) / (BM * kQTiles)), (unsigned)p.bh, 1);
     const float scale_log2 = p.scale * 1.4426950408889634f;
-    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k, p.d,
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k, p.d,
                                                     scale_log2, p.status);
     return cudaGetLastError();
 }
