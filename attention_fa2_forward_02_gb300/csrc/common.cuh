@@ -104,6 +104,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, Watchdo
     return __all_sync(0xffffffffu, ok);
 }
 
+// Named-barrier signal and wait for whole warps (`count` threads in all; barrier 0 is
+// __syncthreads). Neither is a memory access: the warp that issues tcgen05.mma waits
+// on these rather than on mbarriers, since any shared-memory access of that warp
+// between MMA groups costs tensor-pipe time.
+__device__ __forceinline__ void nb_arrive(uint32_t id, uint32_t count) {
+    asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void nb_sync(uint32_t id, uint32_t count) {
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Bounded wait that ignores the abort flag: drains work already issued.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();

@@ -106,7 +106,24 @@ struct BwdCfg : Tile16<D> {
     static constexpr int kSmemDq = kDqBar + kNumBars * 8 + 16 + 1024;
     static_assert(kSmemDkv <= 227 * 1024 && kSmemDq <= 227 * 1024, "shared memory budget");
     static_assert(kStageDkv % 1024 == 0, "stage alignment");
+    // Head size 128 (one value tensor): the MMA issuer waits only on named barriers,
+    // fed by the elementwise warps and by a relay warp (warp 10) that waits for the TMA
+    // stages; a shared-memory access (an mbarrier test included) by the issuing warp
+    // between MMA groups costs a few hundred clocks of tensor-pipe time. Otherwise
+    // lane 0 of the issuer waits on the mbarriers itself.
+    static constexpr bool kNamed = D == 128 && kNV == 1;
+    static constexpr int kThreads = kNamed ? kBwdThreads + 32 : kBwdThreads;
 };
+
+// Named barriers of the issuer (head size 128): 1 "P^T ready" (dK/dV) / "S read" (dQ;
+// first "Q, dO in tensor memory"), 2 "dS ready", 3 + s "stage s loaded" (relay). A
+// producer cannot arrive twice on one of them before the issuer has synced on it, and
+// arrives once per event whatever happens (a failed bounded wait skips its work, not
+// its arrival, and raises the watchdog status); the issuer never gives up.
+constexpr int kBwdRelayWarp = 10;
+constexpr uint32_t kNbE1 = 1, kNbE2 = 2;
+constexpr uint32_t kNbElem = kElemThreads + 32;  // elementwise warps + issuer
+__host__ __device__ constexpr uint32_t nb_stage(int s) { return 3 + (uint32_t)s; }
 
 // ------------------------------------------------------------------------------ dK / dV
 //
@@ -193,7 +210,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if constexpr (C::kNamed) {
             const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
             const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
             auto issue_st = [&](int s) {  // S^T = K Q^T
@@ -201,54 +218,130 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(tmem, C::kmajor(k_smem, kk, BT), C::kmajor(stage_q(s), kk, BT), idesc_s, kk > 0);
             };
-            auto issue_dpt = [&](int s) {  // dP^T = sum over pairs of V dO^T
+            auto issue_dpt = [&](int s) {  // dP^T = V dO^T
 #pragma unroll
-                for (int v = 0; v < kNV; ++v)
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(tmem + 128u, C::kmajor(v_smem(v), kk, BT), C::kmajor(stage_do(s, v), kk, BT), idesc_s,
-                               (v > 0 || kk > 0));
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128u, C::kmajor(v_smem(0), kk, BT), C::kmajor(stage_do(s, 0), kk, BT), idesc_s, kk > 0);
             };
-            bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
-            if (ok) {
+            static_assert(nb_stage(S - 1) < 16, "named barriers");
+            nb_sync(nb_stage(0), 64);  // K, V and the first Q / dO stage
+            if (lane == 0) {
                 tc_fence_after();
                 issue_st(0);
                 mma_commit(bars.s_full());
                 issue_dpt(0);
                 mma_commit(bars.dp_full());
             }
-            for (int i = 0; ok && i < n_qt; ++i) {
+            __syncwarp();
+            for (int i = 0; i < n_qt; ++i) {
                 const int s = i % S;
                 const int sn = (i + 1) % S;
                 const bool more = i + 1 < n_qt;
-                if (!(ok = mbar_wait(bars.e1(), i & 1, wd))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int v = 0; v < kNV; ++v)
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO (one accumulator per pair)
-                        mma_ts(tmem + 256u + (uint32_t)(v * D), tmem + kPackedCol + (uint32_t)(kk * 8),
-                               C::mnmajor(stage_do(s, v), kk, BT), idesc_g, (i > 0 || kk > 0));
-                if (more) {
-                    if (!(ok = mbar_wait(bars.full(sn), ((i + 1) / S) & 1, wd))) break;
+                nb_sync(kNbE1, kNbElem);  // P^T(i) in tensor memory
+                if (lane == 0) {
                     tc_fence_after();
-                    issue_st(sn);
-                    mma_commit(bars.s_full());
-                }
-                if (!(ok = mbar_wait(bars.e2(), i & 1, wd))) break;
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
-                    mma_ts(tmem + 256u + (uint32_t)(kNV * D), tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
-                           C::mnmajor(stage_q(s), kk, BT), idesc_g, (i > 0 || kk > 0));
-                mma_commit(bars.empty(s));
+                    for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
+                        mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_do(s, 0), kk, BT),
+                               idesc_g, (i > 0 || kk > 0));
+                }
+                __syncwarp();
                 if (more) {
-                    issue_dpt(sn);
+                    nb_sync(nb_stage(sn), 64);  // Q, dO of tile i + 1
+                    if (lane == 0) {
+                        tc_fence_after();
+                        issue_st(sn);
+                        mma_commit(bars.s_full());
+                    }
+                    __syncwarp();
+                }
+                nb_sync(kNbE2, kNbElem);  // dS^T(i) in tensor memory
+                if (lane == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
+                        mma_ts(tmem + 256u + (uint32_t)D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
+                               C::mnmajor(stage_q(s), kk, BT), idesc_g, (i > 0 || kk > 0));
+                    mma_commit(bars.empty(s));
+                    if (more) {
+                        issue_dpt(sn);
+                        mma_commit(bars.dp_full());
+                    }
+                }
+                __syncwarp();
+            }
+            if (lane == 0) {
+                mma_commit(bars.done());
+                drain_wait(bars.done(), 0);
+            }
+            __syncwarp();
+        } else {
+            if (lane == 0) {
+                const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
+                const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
+                auto issue_st = [&](int s) {  // S^T = K Q^T
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss(tmem, C::kmajor(k_smem, kk, BT), C::kmajor(stage_q(s), kk, BT), idesc_s, kk > 0);
+                };
+                auto issue_dpt = [&](int s) {  // dP^T = sum over pairs of V dO^T
+#pragma unroll
+                    for (int v = 0; v < kNV; ++v)
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss(tmem + 128u, C::kmajor(v_smem(v), kk, BT), C::kmajor(stage_do(s, v), kk, BT), idesc_s,
+                                   (v > 0 || kk > 0));
+                };
+                bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
+                if (ok) {
+                    tc_fence_after();
+                    issue_st(0);
+                    mma_commit(bars.s_full());
+                    issue_dpt(0);
                     mma_commit(bars.dp_full());
                 }
+                for (int i = 0; ok && i < n_qt; ++i) {
+                    const int s = i % S;
+                    const int sn = (i + 1) % S;
+                    const bool more = i + 1 < n_qt;
+                    if (!(ok = mbar_wait(bars.e1(), i & 1, wd))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int v = 0; v < kNV; ++v)
+#pragma unroll
+                        for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO (one accumulator per pair)
+                            mma_ts(tmem + 256u + (uint32_t)(v * D), tmem + kPackedCol + (uint32_t)(kk * 8),
+                                   C::mnmajor(stage_do(s, v), kk, BT), idesc_g, (i > 0 || kk > 0));
+                    if (more) {
+                        if (!(ok = mbar_wait(bars.full(sn), ((i + 1) / S) & 1, wd))) break;
+                        tc_fence_after();
+                        issue_st(sn);
+                        mma_commit(bars.s_full());
+                    }
+                    if (!(ok = mbar_wait(bars.e2(), i & 1, wd))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
+                        mma_ts(tmem + 256u + (uint32_t)(kNV * D), tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
+                               C::mnmajor(stage_q(s), kk, BT), idesc_g, (i > 0 || kk > 0));
+                    mma_commit(bars.empty(s));
+                    if (more) {
+                        issue_dpt(sn);
+                        mma_commit(bars.dp_full());
+                    }
+                }
+                mma_commit(bars.done());
+                drain_wait(bars.done(), 0);
             }
-            mma_commit(bars.done());
-            drain_wait(bars.done(), 0);
+        }
+    } else if (C::kNamed && warp == kBwdRelayWarp) {
+        // TMA relay: signals each Q / dO stage (the first with K and V) to the issuer
+        bool ok = warp_wait(bars.resident(), 0, wd) && warp_wait(bars.full(0), 0, wd);
+        nb_arrive(nb_stage(0), 64);
+        for (int i = 1; i < n_qt; ++i) {
+            const int s = i % S;
+            ok = ok && warp_wait(bars.full(s), (i / S) & 1, wd);
+            nb_arrive(nb_stage(s), 64);
         }
     } else {
         // Two warps per TMEM lane quarter; warp `half` owns query columns [64*half, 64*half + 64).
@@ -258,9 +351,18 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
         const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         bool ok = true;
+        // a failed wait skips the work of this and later tiles, not the signals
+        auto signal = [&](uint32_t nb, uint32_t mbar) {
+            if constexpr (C::kNamed) nb_arrive(nb, kNbElem);
+            else mbar_arrive(mbar);
+        };
         for (int i = 0; i < n_qt; ++i) {
             const int s = i % S;
-            if (!(ok = warp_wait(bars.s_full(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) break;
+            if (!(ok = ok && warp_wait(bars.s_full(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) {
+                signal(kNbE1, bars.e1());
+                signal(kNbE2, bars.e2());
+                continue;
+            }
             tc_fence_after();
             const float* l2 = reinterpret_cast<const float*>(smem + (stage_l2(s) - base));
             const float* dl = reinterpret_cast<const float*>(smem + (stage_dl(s) - base));
@@ -296,9 +398,12 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bars.e1());
+            signal(kNbE1, bars.e1());
             // step 2: dS^T = P^T * (dP^T - D), chunk by chunk in write-safe order
-            if (!(ok = warp_wait(bars.dp_full(), i & 1, wd))) break;
+            if (!(ok = warp_wait(bars.dp_full(), i & 1, wd))) {
+                signal(kNbE2, bars.e2());
+                continue;
+            }
             tc_fence_after();
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -323,7 +428,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bars.e2());
+            signal(kNbE2, bars.e2());
         }
         if (ok) ok = warp_wait(bars.done(), 0, wd);
         if (ok) {
@@ -426,7 +531,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if constexpr (C::kNamed) {
             const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
             const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
             auto issue_s = [&](int s) {  // S = Q K^T, Q from tensor memory
@@ -434,46 +539,115 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ts(tmem, tmem + (uint32_t)(C::kQCol + kk * 8), C::kmajor(stage_k(s), kk, BT), idesc_s, kk > 0);
             };
-            auto issue_dp = [&](int s) {  // dP = sum over pairs of dO V^T, dO from tensor memory
+            auto issue_dp = [&](int s) {  // dP = dO V^T, dO from tensor memory
 #pragma unroll
-                for (int v = 0; v < kNV; ++v)
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ts(tmem + 128u, tmem + (uint32_t)(C::kDoCol + v * D / 2 + kk * 8),
-                               C::kmajor(stage_v(s, v), kk, BT), idesc_s, (v > 0 || kk > 0));
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ts(tmem + 128u, tmem + (uint32_t)(C::kDoCol + kk * 8), C::kmajor(stage_v(s, 0), kk, BT), idesc_s, kk > 0);
             };
-            bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
-            if (ok) {
+            static_assert(nb_stage(S - 1) < 16, "named barriers");
+            nb_sync(kNbE1, kNbElem);   // Q and dO copied into tensor memory
+            nb_sync(nb_stage(0), 64);  // the first K / V stage
+            if (lane == 0) {
                 tc_fence_after();
                 issue_s(0);
                 mma_commit(bars.s_full());
                 issue_dp(0);
                 mma_commit(bars.dp_full());
             }
-            for (int j = 0; ok && j < n_kt; ++j) {
+            __syncwarp();
+            for (int j = 0; j < n_kt; ++j) {
                 const int s = j % S;
                 const int sn = (j + 1) % S;
                 const bool more = j + 1 < n_kt;
+                nb_sync(kNbE1, kNbElem);  // S(j) read: its columns may be overwritten
                 if (more) {
-                    if (!(ok = mbar_wait(bars.e1(), j & 1, wd) && mbar_wait(bars.full(sn), ((j + 1) / S) & 1, wd))) break;
-                    tc_fence_after();
-                    issue_s(sn);
-                    mma_commit(bars.s_full());
+                    nb_sync(nb_stage(sn), 64);  // K, V of tile j + 1
+                    if (lane == 0) {
+                        tc_fence_after();
+                        issue_s(sn);
+                        mma_commit(bars.s_full());
+                    }
+                    __syncwarp();
                 }
-                if (!(ok = mbar_wait(bars.e2(), j & 1, wd))) break;
-                tc_fence_after();
+                nb_sync(kNbE2, kNbElem);  // dS(j) in tensor memory
+                if (lane == 0) {
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
-                    mma_ts(tmem + 256u, tmem + 128u + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_k(s), kk, BT),
-                           idesc_g, (j > 0 || kk > 0));
-                mma_commit(bars.empty(s));
-                if (more) {
-                    issue_dp(sn);
+                    for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
+                        mma_ts(tmem + 256u, tmem + 128u + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_k(s), kk, BT),
+                               idesc_g, (j > 0 || kk > 0));
+                    mma_commit(bars.empty(s));
+                    if (more) {
+                        issue_dp(sn);
+                        mma_commit(bars.dp_full());
+                    }
+                }
+                __syncwarp();
+            }
+            if (lane == 0) {
+                mma_commit(bars.done());
+                drain_wait(bars.done(), 0);
+            }
+            __syncwarp();
+        } else {
+            if (lane == 0) {
+                const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
+                const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
+                auto issue_s = [&](int s) {  // S = Q K^T, Q from tensor memory
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ts(tmem, tmem + (uint32_t)(C::kQCol + kk * 8), C::kmajor(stage_k(s), kk, BT), idesc_s, kk > 0);
+                };
+                auto issue_dp = [&](int s) {  // dP = sum over pairs of dO V^T, dO from tensor memory
+#pragma unroll
+                    for (int v = 0; v < kNV; ++v)
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ts(tmem + 128u, tmem + (uint32_t)(C::kDoCol + v * D / 2 + kk * 8),
+                                   C::kmajor(stage_v(s, v), kk, BT), idesc_s, (v > 0 || kk > 0));
+                };
+                bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(0);
+                    mma_commit(bars.s_full());
+                    issue_dp(0);
                     mma_commit(bars.dp_full());
                 }
+                for (int j = 0; ok && j < n_kt; ++j) {
+                    const int s = j % S;
+                    const int sn = (j + 1) % S;
+                    const bool more = j + 1 < n_kt;
+                    if (more) {
+                        if (!(ok = mbar_wait(bars.e1(), j & 1, wd) && mbar_wait(bars.full(sn), ((j + 1) / S) & 1, wd))) break;
+                        tc_fence_after();
+                        issue_s(sn);
+                        mma_commit(bars.s_full());
+                    }
+                    if (!(ok = mbar_wait(bars.e2(), j & 1, wd))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
+                        mma_ts(tmem + 256u, tmem + 128u + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_k(s), kk, BT),
+                               idesc_g, (j > 0 || kk > 0));
+                    mma_commit(bars.empty(s));
+                    if (more) {
+                        issue_dp(sn);
+                        mma_commit(bars.dp_full());
+                    }
+                }
+                mma_commit(bars.done());
+                drain_wait(bars.done(), 0);
             }
-            mma_commit(bars.done());
-            drain_wait(bars.done(), 0);
+        }
+    } else if (C::kNamed && warp == kBwdRelayWarp) {
+        // TMA relay: signals each K / V stage to the issuer
+        bool ok = warp_wait(bars.full(0), 0, wd);
+        nb_arrive(nb_stage(0), 64);
+        for (int j = 1; j < n_kt; ++j) {
+            const int s = j % S;
+            ok = ok && warp_wait(bars.full(s), (j / S) & 1, wd);
+            nb_arrive(nb_stage(s), 64);
         }
     } else {
         // Two warps per TMEM lane quarter; warp `half` owns key columns [64*half, 64*half + 64).
@@ -522,13 +696,23 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bars.resident());
+            if constexpr (C::kNamed) nb_arrive(kNbE1, kNbElem);
+            else mbar_arrive(bars.resident());
         }
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         const float2 neg_l2 = make_float2(my_nl2, my_nl2), neg_d = make_float2(my_nd, my_nd);
         bool ok = true;
+        // a failed wait skips the work of this and later tiles, not the signals
+        auto signal = [&](uint32_t nb, uint32_t mbar) {
+            if constexpr (C::kNamed) nb_arrive(nb, kNbElem);
+            else mbar_arrive(mbar);
+        };
         for (int j = 0; j < n_kt; ++j) {
-            if (!(ok = warp_wait(bars.s_full(), j & 1, wd))) break;
+            if (!(ok = ok && warp_wait(bars.s_full(), j & 1, wd))) {
+                signal(kNbE1, bars.e1());
+                signal(kNbE2, bars.e2());
+                continue;
+            }
             tc_fence_after();
             const int valid = n_k - j * BT;
             // step 1: P = 2^(S * scale * log2e - LSE2) in registers; then S may be overwritten
@@ -541,7 +725,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
                 reg_fence(ra);
                 reg_fence(rb);
                 tc_fence_before();
-                mbar_arrive(bars.e1());
+                signal(kNbE1, bars.e1());
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const uint32_t* r = cc == 0 ? ra : rb;
@@ -557,7 +741,10 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
             }
             // step 2: dS = P * (dP - D), zero past the last key (where P may even overflow);
             // both owned chunks read before either is overwritten by its 16-bit result
-            if (!(ok = warp_wait(bars.dp_full(), j & 1, wd))) break;
+            if (!(ok = warp_wait(bars.dp_full(), j & 1, wd))) {
+                signal(kNbE2, bars.e2());
+                continue;
+            }
             tc_fence_after();
             uint32_t rp[2][32];
             tmem_ld32(t_dp + 32u * owned_chunk(half, 0), rp[0]);
@@ -587,7 +774,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bars.e2());
+            signal(kNbE2, bars.e2());
         }
         if (ok) ok = warp_wait(bars.done(), 0, wd);
         if (ok) {
@@ -616,7 +803,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
 // ------------------------------------------------------------------------------ kernels
 
 template <int D, bool kBf16, int kNV>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
@@ -628,7 +815,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 template <int D, bool kBf16, int kNV>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_v2, const uint16_t* __restrict__ q_ptr,
                   const uint16_t* __restrict__ do_ptr, const uint16_t* __restrict__ do2_ptr,
@@ -648,7 +835,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //     shapes whose dQ CTAs (n_kt key tiles each) are much longer than the dK/dV
 //     CTAs (n_qt query tiles each): started first, they do not end in a tail.
 template <int D, bool kBf16, int kNV>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_passes_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
@@ -719,7 +906,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         constexpr int smem = C::kSmemDkv > C::kSmemDq ? C::kSmemDkv : C::kSmemDq;
         e = ensure_smem_limit(reinterpret_cast<const void*>(both), smem, 42 + (slot - 16) / 2);  // slots 42..51
         if (e != cudaSuccess) return e;
-        both<<<dim3((unsigned)(n_kt + n_qt), (unsigned)p.bh, 1), kBwdThreads, smem, stream>>>(
+        both<<<dim3((unsigned)(n_kt + n_qt), (unsigned)p.bh, 1), C::kThreads, smem, stream>>>(
             tq, tk, tv, tdo, tv2, tdo2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
             static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, p.dk, p.dv, p.dv2, (int)p.n_q,
             (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, n_kt >= 4 * n_qt ? 1 : 0);
@@ -729,7 +916,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         auto dkdv = bwd_dkdv_kernel<D, kBf16, kNV>;
         e = ensure_smem_limit(reinterpret_cast<const void*>(dkdv), C::kSmemDkv, slot);
         if (e != cudaSuccess) return e;
-        dkdv<<<dim3((unsigned)n_kt, (unsigned)p.bh, 1), kBwdThreads, C::kSmemDkv, stream>>>(
+        dkdv<<<dim3((unsigned)n_kt, (unsigned)p.bh, 1), C::kThreads, C::kSmemDkv, stream>>>(
             tq, tk, tv, tdo, tv2, tdo2, p.lse2, p.delta, p.dk, p.dv, p.dv2, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad,
             p.d, p.scale, scale_log2, p.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -738,7 +925,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     auto dqk = bwd_dq_kernel<D, kBf16, kNV>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
     if (e != cudaSuccess) return e;
-    dqk<<<dim3((unsigned)n_qt, (unsigned)p.bh, 1), kBwdThreads, C::kSmemDq, stream>>>(
+    dqk<<<dim3((unsigned)n_qt, (unsigned)p.bh, 1), C::kThreads, C::kSmemDq, stream>>>(
         tk, tv, tv2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
         static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k,
         (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status);

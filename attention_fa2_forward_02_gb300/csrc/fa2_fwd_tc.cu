@@ -54,14 +54,6 @@ constexpr uint32_t kNbP = 1;
 __host__ __device__ constexpr uint32_t nb_v(int s) { return 1 + 2 + (uint32_t)s; }
 __host__ __device__ constexpr uint32_t nb_k(int S, int s) { return 1 + 2 + (uint32_t)(S + s); }
 
-// Named-barrier signal and wait for whole warps (`count` threads in all); neither is a
-// memory access.
-__device__ __forceinline__ void nb_arrive(uint32_t id, uint32_t count) {
-    asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-__device__ __forceinline__ void nb_sync(uint32_t id, uint32_t count) {
-    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
@@ -205,16 +197,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 const uint32_t d_tmem = tmem + (uint32_t)(t * BN);
                 const uint32_t qa = q_smem + t * C::kQTileBytes;
                 const uint32_t kb = k_smem + s * C::kKVTileBytes;
-    #pragma unroll
+#pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss(d_tmem, C::kmajor(qa, kk, BM), C::kmajor(kb, kk, BN), idesc_s, kk > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int t, int s, bool acc) {
-    #pragma unroll
+#pragma unroll
                 for (int v = 0; v < kNV; ++v) {
                     const uint32_t d_tmem = tmem + 256u + (uint32_t)((t * kNV + v) * D);
                     const uint32_t vb = v_smem + s * C::kVStageBytes + v * C::kKVTileBytes;
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk)
                         mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
                                (acc || kk > 0) ? 1u : 0u);
@@ -271,16 +263,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                     const uint32_t d_tmem = tmem + (uint32_t)(t * BN);
                     const uint32_t qa = q_smem + t * C::kQTileBytes;
                     const uint32_t kb = k_smem + s * C::kKVTileBytes;
-    #pragma unroll
+#pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
                         mma_ss(d_tmem, C::kmajor(qa, kk, BM), C::kmajor(kb, kk, BN), idesc_s, kk > 0 ? 1u : 0u);
                 };
                 auto issue_pv = [&](int t, int s, bool acc) {
-    #pragma unroll
+#pragma unroll
                     for (int v = 0; v < kNV; ++v) {
                         const uint32_t d_tmem = tmem + 256u + (uint32_t)((t * kNV + v) * D);
                         const uint32_t vb = v_smem + s * C::kVStageBytes + v * C::kKVTileBytes;
-    #pragma unroll
+#pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
                             mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
                                    (acc || kk > 0) ? 1u : 0u);
@@ -356,18 +348,18 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 tc_fence_after();
                 // The score row (128 columns) into registers: one read of the S tile per key tile.
                 uint32_t sr[BN / 32][32];
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < BN / 32; ++c) tmem_ld32(s_addr + 32u * c, sr[c]);
                 tmem_ld_wait();
-    #pragma unroll
+#pragma unroll
                 for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
                 // Only the last key tile can be partial: its columns past the last key become
                 // -inf, which drops them from the maximum and gives them probability 0.
                 const int valid = n_k - j * BN;
                 if (valid < BN) {
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < BN / 32; ++c)
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; ++i)
                             if (32 * c + i >= valid) sr[c][i] = __float_as_uint(-INFINITY);
                 }
@@ -375,11 +367,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 float mx;
                 {
                     float m8[8];
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 8; ++i) m8[i] = -INFINITY;
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < BN / 32; ++c)
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 16; ++i)
                             m8[i & 7] = fmax3(m8[i & 7], __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
                     mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
@@ -403,10 +395,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 {
                     const float2 negm2 = make_float2(-m2, -m2);
                     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < BN / 32; ++c) {
                         uint32_t pk[16];
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const float2 x = make_float2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
                             float2 y = __ffma2_rn(x, scale2, negm2);
@@ -424,13 +416,13 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 // to the P.V product (which is issued only after the arrival below), and after
                 // the previous P.V product (whose completion preceded this S tile's).
                 if (rescale) {
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < kNV * D / 32; ++c) {
                         uint32_t o[32];
                         tmem_ld32(o_addr + 32u * c, o);
                         tmem_ld_wait();
                         reg_fence(o);
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                         tmem_st32(o_addr + 32u * c, o);
                     }
