@@ -189,28 +189,32 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
         if constexpr (C::kNamed) {
-            // The whole warp walks the loop and waits for its producers' named-barrier
-            // signals; lane 0 issues.
             const uint32_t idesc_s = idesc_f16_f32acc(BM, BN, kBf16, false, false);
             const uint32_t idesc_o = idesc_f16_f32acc(BM, D, kBf16, false, true);
+            // Descriptors of query tile / ring stage 0 at k-step 0, built once; every other
+            // operand adds a constant to the start-address field (16-byte units; shared
+            // addresses stay below 256 KB, so nothing carries out of the field). The
+            // issuer shares its sub-partition with two busy softmax warps: the fewer
+            // instructions it needs per MMA, the fuller it keeps the tensor pipe.
+            const uint64_t dq0 = C::kmajor(q_smem, 0, BM);
+            const uint64_t dk0 = C::kmajor(k_smem, 0, BN);
+            const uint64_t dv0 = C::mnmajor(v_smem, 0, BN);
             auto issue_s = [&](int t, int s) {
                 const uint32_t d_tmem = tmem + (uint32_t)(t * BN);
-                const uint32_t qa = q_smem + t * C::kQTileBytes;
-                const uint32_t kb = k_smem + s * C::kKVTileBytes;
+                const uint64_t qa = dq0 + (uint64_t)((t * C::kQTileBytes) >> 4);
+                const uint64_t kb = dk0 + (uint64_t)((s * C::kKVTileBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(d_tmem, C::kmajor(qa, kk, BM), C::kmajor(kb, kk, BN), idesc_s, kk > 0 ? 1u : 0u);
+                    mma_ss(d_tmem, qa + (uint64_t)(C::koff(kk, BM) >> 4), kb + (uint64_t)(C::koff(kk, BN) >> 4), idesc_s,
+                           kk > 0 ? 1u : 0u);
             };
             auto issue_pv = [&](int t, int s, bool acc) {
+                const uint32_t d_tmem = tmem + 256u + (uint32_t)(t * D);
+                const uint64_t vb = dv0 + (uint64_t)((s * C::kVStageBytes) >> 4);
 #pragma unroll
-                for (int v = 0; v < kNV; ++v) {
-                    const uint32_t d_tmem = tmem + 256u + (uint32_t)((t * kNV + v) * D);
-                    const uint32_t vb = v_smem + s * C::kVStageBytes + v * C::kKVTileBytes;
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
-                               (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), vb + (uint64_t)(kk * C::kAtomRowBytes), idesc_o,
+                           (acc || kk > 0) ? 1u : 0u);
             };
             static_assert(1 + 2 + 2 * S <= 16, "named barriers");
             nb_sync(nb_k(S, 0), 64);  // Q and the first K tile
