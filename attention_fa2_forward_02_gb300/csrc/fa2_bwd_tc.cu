@@ -213,15 +213,29 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
         if constexpr (C::kNamed) {
             const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
             const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
+            // Descriptors built once (stage 0, k-step 0); every other operand adds a
+            // constant to the start-address field (16-byte units; shared addresses stay
+            // below 256 KB). Fewer instructions per MMA keep the issuer, which shares its
+            // sub-partition with two elementwise warps, ahead of the tensor pipe.
+            const uint64_t dk0 = C::kmajor(k_smem, 0, BT), dv0 = C::kmajor(v_smem(0), 0, BT);
+            const uint64_t dq0 = C::kmajor(stage_q(0), 0, BT), ddo0 = C::kmajor(stage_do(0, 0), 0, BT);
+            const uint64_t mq0 = C::mnmajor(stage_q(0), 0, BT), mdo0 = C::mnmajor(stage_do(0, 0), 0, BT);
+            auto st_off = [&](int s) { return (uint64_t)((s * C::kStageDkv) >> 4); };
             auto issue_st = [&](int s) {  // S^T = K Q^T
+                const uint64_t b = dq0 + st_off(s);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem, C::kmajor(k_smem, kk, BT), C::kmajor(stage_q(s), kk, BT), idesc_s, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t o = (uint64_t)(C::koff(kk, BT) >> 4);
+                    mma_ss(tmem, dk0 + o, b + o, idesc_s, kk > 0);
+                }
             };
             auto issue_dpt = [&](int s) {  // dP^T = V dO^T
+                const uint64_t b = ddo0 + st_off(s);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128u, C::kmajor(v_smem(0), kk, BT), C::kmajor(stage_do(s, 0), kk, BT), idesc_s, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t o = (uint64_t)(C::koff(kk, BT) >> 4);
+                    mma_ss(tmem + 128u, dv0 + o, b + o, idesc_s, kk > 0);
+                }
             };
             static_assert(nb_stage(S - 1) < 16, "named barriers");
             nb_sync(nb_stage(0), 64);  // K, V and the first Q / dO stage
@@ -240,9 +254,10 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                 nb_sync(kNbE1, kNbElem);  // P^T(i) in tensor memory
                 if (lane == 0) {
                     tc_fence_after();
+                    const uint64_t b = mdo0 + st_off(s);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
-                        mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_do(s, 0), kk, BT),
+                        mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), b + (uint64_t)(kk * C::kAtomRowBytes),
                                idesc_g, (i > 0 || kk > 0));
                 }
                 __syncwarp();
@@ -258,10 +273,11 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                 nb_sync(kNbE2, kNbElem);  // dS^T(i) in tensor memory
                 if (lane == 0) {
                     tc_fence_after();
+                    const uint64_t b = mq0 + st_off(s);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
                         mma_ts(tmem + 256u + (uint32_t)D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
-                               C::mnmajor(stage_q(s), kk, BT), idesc_g, (i > 0 || kk > 0));
+                               b + (uint64_t)(kk * C::kAtomRowBytes), idesc_g, (i > 0 || kk > 0));
                     mma_commit(bars.empty(s));
                     if (more) {
                         issue_dpt(sn);
@@ -534,15 +550,22 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
         if constexpr (C::kNamed) {
             const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);
             const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);
+            // descriptors built once (stage 0, k-step 0), as in the dK/dV pass
+            const uint64_t dk0 = C::kmajor(stage_k(0), 0, BT), dv0 = C::kmajor(stage_v(0, 0), 0, BT);
+            const uint64_t mk0 = C::mnmajor(stage_k(0), 0, BT);
+            auto st_off = [&](int s) { return (uint64_t)((s * C::kStageDq) >> 4); };
             auto issue_s = [&](int s) {  // S = Q K^T, Q from tensor memory
+                const uint64_t b = dk0 + st_off(s);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts(tmem, tmem + (uint32_t)(C::kQCol + kk * 8), C::kmajor(stage_k(s), kk, BT), idesc_s, kk > 0);
+                    mma_ts(tmem, tmem + (uint32_t)(C::kQCol + kk * 8), b + (uint64_t)(C::koff(kk, BT) >> 4), idesc_s, kk > 0);
             };
             auto issue_dp = [&](int s) {  // dP = dO V^T, dO from tensor memory
+                const uint64_t b = dv0 + st_off(s);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts(tmem + 128u, tmem + (uint32_t)(C::kDoCol + kk * 8), C::kmajor(stage_v(s, 0), kk, BT), idesc_s, kk > 0);
+                    mma_ts(tmem + 128u, tmem + (uint32_t)(C::kDoCol + kk * 8), b + (uint64_t)(C::koff(kk, BT) >> 4), idesc_s,
+                           kk > 0);
             };
             static_assert(nb_stage(S - 1) < 16, "named barriers");
             nb_sync(kNbE1, kNbElem);   // Q and dO copied into tensor memory
@@ -572,9 +595,10 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
                 nb_sync(kNbE2, kNbElem);  // dS(j) in tensor memory
                 if (lane == 0) {
                     tc_fence_after();
+                    const uint64_t b = mk0 + st_off(s);
 #pragma unroll
                     for (int kk = 0; kk < BT / 16; ++kk)  // dQ += dS K
-                        mma_ts(tmem + 256u, tmem + 128u + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_k(s), kk, BT),
+                        mma_ts(tmem + 256u, tmem + 128u + kPackedCol + (uint32_t)(kk * 8), b + (uint64_t)(kk * C::kAtomRowBytes),
                                idesc_g, (j > 0 || kk > 0));
                     mma_commit(bars.empty(s));
                     if (more) {
