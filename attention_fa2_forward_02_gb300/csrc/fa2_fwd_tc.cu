@@ -263,22 +263,27 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
             if (lane == 0) {
                 const uint32_t idesc_s = idesc_f16_f32acc(BM, BN, kBf16, false, false);
                 const uint32_t idesc_o = idesc_f16_f32acc(BM, D, kBf16, false, true);
+                // descriptors built once, as in the head-size-128 issuer above
+                const uint64_t dq0 = C::kmajor(q_smem, 0, BM);
+                const uint64_t dk0 = C::kmajor(k_smem, 0, BN);
+                const uint64_t dv0 = C::mnmajor(v_smem, 0, BN);
                 auto issue_s = [&](int t, int s) {
                     const uint32_t d_tmem = tmem + (uint32_t)(t * BN);
-                    const uint32_t qa = q_smem + t * C::kQTileBytes;
-                    const uint32_t kb = k_smem + s * C::kKVTileBytes;
+                    const uint64_t qa = dq0 + (uint64_t)((t * C::kQTileBytes) >> 4);
+                    const uint64_t kb = dk0 + (uint64_t)((s * C::kKVTileBytes) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss(d_tmem, C::kmajor(qa, kk, BM), C::kmajor(kb, kk, BN), idesc_s, kk > 0 ? 1u : 0u);
+                        mma_ss(d_tmem, qa + (uint64_t)(C::koff(kk, BM) >> 4), kb + (uint64_t)(C::koff(kk, BN) >> 4), idesc_s,
+                               kk > 0 ? 1u : 0u);
                 };
                 auto issue_pv = [&](int t, int s, bool acc) {
 #pragma unroll
                     for (int v = 0; v < kNV; ++v) {
                         const uint32_t d_tmem = tmem + 256u + (uint32_t)((t * kNV + v) * D);
-                        const uint32_t vb = v_smem + s * C::kVStageBytes + v * C::kKVTileBytes;
+                        const uint64_t vb = dv0 + (uint64_t)((s * C::kVStageBytes + v * C::kKVTileBytes) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), C::mnmajor(vb, kk, BN), idesc_o,
+                            mma_ts(d_tmem, tmem + (uint32_t)(t * BN + kk * 8), vb + (uint64_t)(kk * C::kAtomRowBytes), idesc_o,
                                    (acc || kk > 0) ? 1u : 0u);
                     }
                 };
