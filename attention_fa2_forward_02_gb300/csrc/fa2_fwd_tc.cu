@@ -13,8 +13,8 @@
 //   warp 1      allocates tensor memory; lane 0 issues every tcgen05.mma
 //   warps 2-5   softmax for Q0 (one thread per query row / TMEM lane)
 //   warps 6-9   softmax for Q1
-//   warp 10     (head size 128) waits for the TMA copies on behalf of the issuer
-// At head size 128 the issuer never waits on an mbarrier: a shared-memory access (an
+//   warp 10     (one value tensor) waits for the TMA copies on behalf of the issuer
+// With one value tensor the issuer never waits on an mbarrier: a shared-memory access (an
 // mbarrier test included) by the warp that issues tcgen05.mma costs a few hundred
 // clocks of tensor-pipe time each. Warp 10 and the softmax groups signal it through
 // named barriers instead (barrier.arrive; the issuer's barrier.sync is not a memory
@@ -24,8 +24,8 @@
 // released or issued), and every producer arrives exactly once per event whatever
 // happens: a failed bounded wait skips the work, not the arrival, and raises the
 // watchdog status. The issuer itself never gives up; a failure elsewhere only makes
-// it multiply stale tiles until its loop ends. Smaller heads, paced by the softmax,
-// keep lane 0 of the issuer waiting on the mbarriers itself, which wakes it sooner.
+// it multiply stale tiles until its loop ends. The two-value PSA form keeps lane 0 of
+// the issuer waiting on the mbarriers itself.
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128) S0 = Q0 K^T   [128,256) S1 = Q1 K^T   [256,256+D) O0   [256+D,256+2D) O1
 // The probabilities P (16-bit) are written back over the first 64 columns of
@@ -63,11 +63,9 @@ constexpr float kLn2 = 0.693147180559945309f;
 template <int D, int kNV>
 struct FwdCfg : Tile16<D> {
     static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
-    // Head size 128 (one value tensor): the issuer is fed through named barriers and
-    // a TMA relay warp (11 warps). Smaller heads, where the softmax rather than the
-    // tensor pipe sets the pace, keep the issuer's own mbarrier waits (10 warps): there
-    // a lane-0 mbarrier wait wakes it sooner.
-    static constexpr bool kNamed = D == 128 && kNV == 1;
+    // One value tensor: the issuer is fed through named barriers and a TMA relay warp
+    // (11 warps). The two-value PSA form keeps the issuer's own mbarrier waits.
+    static constexpr bool kNamed = kNV == 1;
     static constexpr int kThreads = kNamed ? 352 : 320;
     static constexpr int kQTileBytes = BM * D * 2;
     static constexpr int kKVTileBytes = BN * D * 2;
@@ -263,7 +261,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
             if (lane == 0) {
                 const uint32_t idesc_s = idesc_f16_f32acc(BM, BN, kBf16, false, false);
                 const uint32_t idesc_o = idesc_f16_f32acc(BM, D, kBf16, false, true);
-                // descriptors built once, as in the head-size-128 issuer above
+                // descriptors built once, as in the named-barrier issuer above
                 const uint64_t dq0 = C::kmajor(q_smem, 0, BM);
                 const uint64_t dk0 = C::kmajor(k_smem, 0, BN);
                 const uint64_t dv0 = C::mnmajor(v_smem, 0, BN);
