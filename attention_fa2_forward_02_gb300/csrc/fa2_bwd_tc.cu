@@ -106,16 +106,16 @@ struct BwdCfg : Tile16<D> {
     static constexpr int kSmemDq = kDqBar + kNumBars * 8 + 16 + 1024;
     static_assert(kSmemDkv <= 227 * 1024 && kSmemDq <= 227 * 1024, "shared memory budget");
     static_assert(kStageDkv % 1024 == 0, "stage alignment");
-    // Head size 128 (one value tensor): the MMA issuer waits only on named barriers,
-    // fed by the elementwise warps and by a relay warp (warp 10) that waits for the TMA
-    // stages; a shared-memory access (an mbarrier test included) by the issuing warp
-    // between MMA groups costs a few hundred clocks of tensor-pipe time. Otherwise
-    // lane 0 of the issuer waits on the mbarriers itself.
-    static constexpr bool kNamed = D == 128 && kNV == 1;
+    // One value tensor: the MMA issuer waits only on named barriers, fed by the
+    // elementwise warps and by a relay warp (warp 10) that waits for the TMA stages; a
+    // shared-memory access (an mbarrier test included) by the issuing warp between MMA
+    // groups costs a few hundred clocks of tensor-pipe time. The two-value PSA form
+    // keeps lane 0 of the issuer waiting on the mbarriers itself.
+    static constexpr bool kNamed = kNV == 1;
     static constexpr int kThreads = kNamed ? kBwdThreads + 32 : kBwdThreads;
 };
 
-// Named barriers of the issuer (head size 128): 1 "P^T ready" (dK/dV) / "S read" (dQ;
+// Named barriers of the issuer (one value tensor): 1 "P^T ready" (dK/dV) / "S read" (dQ;
 // first "Q, dO in tensor memory"), 2 "dS ready", 3 + s "stage s loaded" (relay). A
 // producer cannot arrive twice on one of them before the issuer has synced on it, and
 // arrives once per event whatever happens (a failed bounded wait skips its work, not
