@@ -108,10 +108,10 @@ cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
 
 // fa2_backward runs the one-pass kernel (dQ through float32 reductions) for
 // kernel head sizes up to 64 and the two-pass kernels above.  Measured on GB300
-// at BH = 32, N = 8192: head size 32 / 64: 1.62 / 1.79 ms one-pass against
-// 2.05 / 2.25 ms two-pass; head size 128: 2.99 ms against 2.78 ms, where the
-// reductions (4 bytes per query row, key tile and head column) reach the L2's
-// reduction throughput.
+// at BH = 32, N = 8192 (preprocess included): head size 32 / 64: 1.51 / 1.65 ms
+// one-pass against 1.58 / 1.75 ms for the two passes in one grid; head size 128:
+// 2.99 ms against 2.27 ms, where the reductions (4 bytes per query row, key tile
+// and head column) reach the L2's reduction throughput.
 static bool use_one_pass(int32_t head_dim) { return pad_head_dim(head_dim) <= 64; }
 
 // Workspace of the two-pass backward (the stage entry points, the PSA backward):

@@ -19,6 +19,17 @@ constexpr uint32_t kBwdTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kBwdBars = 8;  // barriers besides the per-stage full / empty pairs
 
+// Named barriers (bar.arrive by the producers, bar.sync by the whole issuing warp) in
+// place of mbarrier waits in the MMA issuer: a shared-memory access by the issuing warp
+// between MMA groups, an mbarrier test included, costs a few hundred clocks of
+// tensor-pipe time. Warp kBwdRelayWarp waits for the TMA stages and relays them. A
+// producer cannot arrive twice on one barrier before the issuer has synced on it, and
+// arrives once per event whatever happens (a failed bounded wait skips its work, not its
+// arrival, and raises the watchdog status); the issuer never gives up.
+constexpr int kBwdRelayWarp = 10;
+constexpr uint32_t kNbE1 = 1, kNbE2 = 2;
+constexpr uint32_t kNbElem = kElemThreads + 32;  // elementwise warps + issuer
+
 // Barriers of the backward kernels:
 //   resident  K, V loaded once per CTA (TMA transaction count); in the dQ pass,
 //             Q and dO copied into tensor memory (256 arrivals)

@@ -27,7 +27,10 @@
 //
 // MMA order per query tile i (one thread issues, the tensor core runs in order):
 //   [e1(i)] dV += P^T(i) dO(i);  [dq_read(i-1)] dP^T(i) -> dp_full;
-//   S^T(i+1) -> s_full;  [e2(i)] dK += dS^T(i) Q(i);  dQ_i = dS(i) K -> dq_full, empty
+//   [stage i+1] S^T(i+1) -> s_full;  [e2(i)] dK += dS^T(i) Q(i);  dQ_i = dS(i) K -> dq_full, empty
+// The bracketed events reach the issuing warp as named barriers: e1, dq_read, e2 from
+// the elementwise warps, "stage loaded" from a relay warp (warp 10) that waits on the
+// TMA barriers.
 // Elementwise warps per query tile i:
 //   [s_full] P^T(i) -> e1;  [dq_full(i-1)] read dQ_(i-1), reduce into the
 //   accumulator -> dq_read;  [dp_full] dS^T(i) into TMEM, dS(i) into shared memory -> e2
@@ -58,10 +61,16 @@ struct FusedCfg : Tile16<D> {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(kStage % 1024 == 0 && kSmemDs % 1024 == 0, "operand alignment");
     static_assert(256 + 2 * D <= (int)kBwdTmemCols, "tensor memory budget");
+    static constexpr int kThreads = kBwdThreads + 32;  // + the TMA relay warp
 };
 
+// Named barriers of this kernel besides kNbE1 / kNbE2: dQ of the previous query tile
+// read out of tensor memory, and stage s loaded.
+constexpr uint32_t kNbDqRead = 3;
+__host__ __device__ constexpr uint32_t nb_fstage(int s) { return 4 + (uint32_t)s; }
+
 template <int D, bool kBf16>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
     bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const float* __restrict__ lse2, const float* __restrict__ delta, float* __restrict__ dq_acc,
@@ -139,59 +148,99 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);  // S^T, dP^T
-            const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);    // dV, dK: A from TMEM
-            const uint32_t idesc_q = idesc_f16_f32acc(BT, D, kBf16, true, true);     // dQ: both MN-major
-            auto issue_st = [&](int s) {  // S^T = K Q^T
+        // The whole warp syncs on the named barriers; lane 0 issues.
+        const uint32_t idesc_s = idesc_f16_f32acc(BT, BT, kBf16, false, false);  // S^T, dP^T
+        const uint32_t idesc_g = idesc_f16_f32acc(BT, D, kBf16, false, true);    // dV, dK: A from TMEM
+        const uint32_t idesc_q = idesc_f16_f32acc(BT, D, kBf16, true, true);     // dQ: both MN-major
+        // Descriptors built once (stage 0, k-step 0); every other operand adds a constant
+        // to the start-address field (16-byte units; shared addresses stay below 256 KB).
+        const uint64_t dk0 = C::kmajor(k_smem, 0, BT), dv0 = C::kmajor(v_smem, 0, BT);
+        const uint64_t dq0 = C::kmajor(stage_q(0), 0, BT), ddo0 = C::kmajor(stage_do(0), 0, BT);
+        const uint64_t mq0 = C::mnmajor(stage_q(0), 0, BT), mdo0 = C::mnmajor(stage_do(0), 0, BT);
+        const uint64_t mk0 = C::mnmajor(k_smem, 0, BT), mds0 = DsTile::mnmajor(ds_smem(0), 0, BT);
+        auto st_off = [&](int s) { return (uint64_t)((s * C::kStage) >> 4); };
+        auto issue_st = [&](int s) {  // S^T = K Q^T
+            const uint64_t b = dq0 + st_off(s);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem, C::kmajor(k_smem, kk, BT), C::kmajor(stage_q(s), kk, BT), idesc_s, kk > 0);
-            };
-            bool ok = mbar_wait(bars.resident(), 0, wd) && mbar_wait(bars.full(0), 0, wd);
-            if (ok) {
-                tc_fence_after();
-                issue_st(0);
-                mma_commit(bars.s_full());
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t o = (uint64_t)(C::koff(kk, BT) >> 4);
+                mma_ss(tmem, dk0 + o, b + o, idesc_s, kk > 0);
             }
-            for (int i = 0; ok && i < n_qt; ++i) {
-                const int s = i % S;
-                const int sn = (i + 1) % S;
-                const bool more = i + 1 < n_qt;
-                if (!(ok = mbar_wait(bars.e1(), i & 1, wd))) break;
+        };
+        static_assert(nb_fstage(S - 1) < 16, "named barriers");
+        nb_sync(nb_fstage(0), 64);  // K, V and the first Q / dO stage
+        if (lane == 0) {
+            tc_fence_after();
+            issue_st(0);
+            mma_commit(bars.s_full());
+        }
+        __syncwarp();
+        for (int i = 0; i < n_qt; ++i) {
+            const int s = i % S;
+            const int sn = (i + 1) % S;
+            const bool more = i + 1 < n_qt;
+            nb_sync(kNbE1, kNbElem);  // P^T(i) in tensor memory
+            if (lane == 0) {
                 tc_fence_after();
+                const uint64_t b = mdo0 + st_off(s);
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
-                    mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), C::mnmajor(stage_do(s), kk, BT), idesc_g,
-                           (i > 0 || kk > 0));
-                if (i > 0) {  // dP^T overwrites the columns of dQ_(i-1)
-                    if (!(ok = mbar_wait(bars.dq_read(), (i - 1) & 1, wd))) break;
-                    tc_fence_after();
-                }
+                    mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), b + (uint64_t)(kk * C::kAtomRowBytes),
+                           idesc_g, (i > 0 || kk > 0));
+            }
+            __syncwarp();
+            if (i > 0) nb_sync(kNbDqRead, kNbElem);  // dP^T overwrites the columns of dQ_(i-1)
+            if (lane == 0) {
+                if (i > 0) tc_fence_after();
+                const uint64_t b = ddo0 + st_off(s);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)  // dP^T = V dO^T
-                    mma_ss(tmem + 128u, C::kmajor(v_smem, kk, BT), C::kmajor(stage_do(s), kk, BT), idesc_s, kk > 0);
+                for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
+                    const uint64_t o = (uint64_t)(C::koff(kk, BT) >> 4);
+                    mma_ss(tmem + 128u, dv0 + o, b + o, idesc_s, kk > 0);
+                }
                 mma_commit(bars.dp_full());
-                if (more) {
-                    if (!(ok = mbar_wait(bars.full(sn), ((i + 1) / S) & 1, wd))) break;
+            }
+            __syncwarp();
+            if (more) {
+                nb_sync(nb_fstage(sn), 64);  // Q, dO of tile i + 1
+                if (lane == 0) {
                     tc_fence_after();
                     issue_st(sn);
                     mma_commit(bars.s_full());
                 }
-                if (!(ok = mbar_wait(bars.e2(), i & 1, wd))) break;
+                __syncwarp();
+            }
+            nb_sync(kNbE2, kNbElem);  // dS^T(i) in tensor memory, dS(i) in shared memory
+            if (lane == 0) {
                 tc_fence_after();
+                const uint64_t b = mq0 + st_off(s);
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
                     mma_ts(tmem + 256u + (uint32_t)D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
-                           C::mnmajor(stage_q(s), kk, BT), idesc_g, (i > 0 || kk > 0));
+                           b + (uint64_t)(kk * C::kAtomRowBytes), idesc_g, (i > 0 || kk > 0));
+                const uint64_t a = mds0 + (C::kDsInDo ? st_off(s) : 0);
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dQ_i = dS K (keys are the reduction dimension)
-                    mma_ss(tmem + 128u, DsTile::mnmajor(ds_smem(s), kk, BT), C::mnmajor(k_smem, kk, BT), idesc_q, kk > 0);
+                    mma_ss(tmem + 128u, a + (uint64_t)(kk * DsTile::kAtomRowBytes),
+                           mk0 + (uint64_t)(kk * C::kAtomRowBytes), idesc_q, kk > 0);
                 mma_commit(bars.dq_full());
                 mma_commit(bars.empty(s));
             }
+            __syncwarp();
+        }
+        if (lane == 0) {
             mma_commit(bars.done());
             drain_wait(bars.done(), 0);
+        }
+        __syncwarp();
+    } else if (warp == kBwdRelayWarp) {
+        // ------------------------------------------------------------------ TMA relay
+        bool ok = warp_wait(bars.resident(), 0, wd) && warp_wait(bars.full(0), 0, wd);
+        nb_arrive(nb_fstage(0), 64);
+        for (int i = 1; i < n_qt; ++i) {
+            const int s = i % S;
+            ok = ok && warp_wait(bars.full(s), (i / S) & 1, wd);
+            nb_arrive(nb_fstage(s), 64);
         }
     } else {
         // ------------------------------------------------------------------ elementwise warps
@@ -207,8 +256,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // Reads dQ of the i-th visited query tile out of TMEM and adds it into the
         // accumulator, laid out per (bh, query tile) as [D/4][128 rows][4] floats so
         // that a warp's 16-byte reductions cover 512 contiguous bytes.
-        auto reduce_dq = [&](int i) -> bool {
-            if (!warp_wait(bars.dq_full(), i & 1, wd)) return false;
+        // A failed wait skips the work of this and later tiles, not the arrivals (the
+        // last tile's dQ read is awaited by no MMA and signals nothing).
+        auto reduce_dq = [&](int i, bool ok) -> bool {
+            if (!(ok && warp_wait(bars.dq_full(), i & 1, wd))) {
+                if (i + 1 < n_qt) nb_arrive(kNbDqRead, kNbElem);
+                return false;
+            }
             tc_fence_after();
             float4* tile = reinterpret_cast<float4*>(dq_acc) + ((size_t)bh * n_qt + qtile(i)) * (size_t)(D / 4) * BT + r;
             if constexpr (D >= 64) {
@@ -238,13 +292,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                           __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
             }
             tc_fence_before();
-            mbar_arrive(bars.dq_read());
+            if (i + 1 < n_qt) nb_arrive(kNbDqRead, kNbElem);
             return true;
         };
         bool ok = true;
         for (int i = 0; i < n_qt; ++i) {
             const int s = i % S;
-            if (!(ok = warp_wait(bars.s_full(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) break;
+            if (!(ok = ok && warp_wait(bars.s_full(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) {
+                nb_arrive(kNbE1, kNbElem);
+                if (i > 0) nb_arrive(kNbDqRead, kNbElem);
+                nb_arrive(kNbE2, kNbElem);
+                continue;
+            }
             tc_fence_after();
             const float* l2 = reinterpret_cast<const float*>(smem + (stage_l2(s) - base));
             const float* dl = reinterpret_cast<const float*>(smem + (stage_dl(s) - base));
@@ -280,13 +339,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(bars.e1());
+            nb_arrive(kNbE1, kNbElem);
             // the previous query tile's dQ, while dV(i) runs
-            if (i > 0 && !(ok = reduce_dq(i - 1))) break;
+            if (i > 0) ok = reduce_dq(i - 1, ok);
             // step 2: dS^T = P^T * (dP^T - D) into TMEM (for dK) and as dS into shared memory
             // (for dQ); both owned chunks read before either is overwritten.  Rows of keys
             // past the last one (zero K rows, where P may even overflow) get dS = 0.
-            if (!(ok = warp_wait(bars.dp_full(), i & 1, wd))) break;
+            if (!(ok = ok && warp_wait(bars.dp_full(), i & 1, wd))) {
+                nb_arrive(kNbE2, kNbElem);
+                continue;
+            }
             tc_fence_after();
             const uint32_t ds_row = ds_smem(s) + (uint32_t)r * 128u;  // row r of the [keys, queries] tile
             const uint32_t swz = (uint32_t)(r & 7);                   // 128-byte swizzle of that row
@@ -322,9 +384,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(bars.e2());
+            nb_arrive(kNbE2, kNbElem);
         }
-        if (ok && n_qt > 0) ok = reduce_dq(n_qt - 1);
+        if (n_qt > 0) ok = reduce_dq(n_qt - 1, ok);
         if (ok) ok = warp_wait(bars.done(), 0, wd);
         if (ok) {
             tc_fence_after();
@@ -393,7 +455,7 @@ cudaError_t fused_impl(const BwdParams& p, cudaStream_t stream, int slot) {
     e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot);
     if (e != cudaSuccess) return e;
     const int n_qt = (int)((p.n_q + BT - 1) / BT);
-    kern<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), kBwdThreads, C::kSmemBytes, stream>>>(
+    kern<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), C::kThreads, C::kSmemBytes, stream>>>(
         tq, tk, tv, tdo, p.lse2, p.delta, p.dq_acc, p.dk, p.dv, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.d, p.scale,
         p.scale * kLog2e, p.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

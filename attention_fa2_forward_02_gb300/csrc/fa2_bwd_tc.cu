@@ -115,14 +115,8 @@ struct BwdCfg : Tile16<D> {
     static constexpr int kThreads = kNamed ? kBwdThreads + 32 : kBwdThreads;
 };
 
-// Named barriers of the issuer (one value tensor): 1 "P^T ready" (dK/dV) / "S read" (dQ;
-// first "Q, dO in tensor memory"), 2 "dS ready", 3 + s "stage s loaded" (relay). A
-// producer cannot arrive twice on one of them before the issuer has synced on it, and
-// arrives once per event whatever happens (a failed bounded wait skips its work, not
-// its arrival, and raises the watchdog status); the issuer never gives up.
-constexpr int kBwdRelayWarp = 10;
-constexpr uint32_t kNbE1 = 1, kNbE2 = 2;
-constexpr uint32_t kNbElem = kElemThreads + 32;  // elementwise warps + issuer
+// Named barriers of the issuer (one value tensor): kNbE1 "P^T ready" (dK/dV) / "S read"
+// (dQ; first "Q, dO in tensor memory"), kNbE2 "dS ready", 3 + s "stage s loaded" (relay).
 __host__ __device__ constexpr uint32_t nb_stage(int s) { return 3 + (uint32_t)s; }
 
 // ------------------------------------------------------------------------------ dK / dV
