@@ -122,6 +122,31 @@ def test_forward_invariants(dtype):
     check_lse(lse, want, "LSE (identical keys)")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_forward_rising_scores_rescale_often(dtype, d):
+    """Keys scaled up along the sequence (by 1 + 3 j / 128 for key j), so that each key tile's
+    row maximum exceeds the previous one by more than the rescale threshold: the O / l
+    rescale of the online softmax runs at nearly every tile, which the N(0, 1) inputs of
+    the other tests rarely reach."""
+    bh, n_q, n_k = 2, 300, 1000
+    q = synth.tensor(f"rise/{d}/q", (bh, n_q, d), dtype)
+    ramp = 1.0 + 3.0 * np.arange(n_k, dtype=np.float64) / 128.0
+    k = synth.to_storage(synth.normal(synth.BASE_SEED, f"rise/{d}/k", bh * n_k * d).reshape(bh, n_k, d)
+                         * ramp[None, :, None], dtype)
+    v = synth.tensor(f"rise/{d}/v", (bh, n_k, d), dtype)
+    scale = 1 / math.sqrt(d)
+    w = lambda x: synth.widen(x, dtype)
+    # the regime: tile maxima (log2 units) rise by more than the threshold of 8 on average
+    s2 = np.einsum("bid,bjd->bij", w(q), w(k)) * scale / math.log(2.0)
+    tile_max = np.stack([s2[:, :, j:j + 128].max(axis=2) for j in range(0, n_k, 128)], axis=2)
+    assert np.mean(np.diff(tile_max, axis=2)) > 8.0
+    o, lse = run_forward(q, k, v, dtype, scale)
+    o_ref, lse_ref = A.forward(w(q), w(k), w(v), scale)
+    check_16bit(o, o_ref, "O (rising scores)")
+    check_lse(lse, lse_ref, "LSE (rising scores)")
+
+
 def test_forward_deterministic_and_in_bounds():
     """Two runs agree bit for bit, and nothing is written outside O and LSE (guard bands)."""
     torch = G.require_gpu()
