@@ -17,7 +17,7 @@ constexpr int kElemThreads = 256;
 constexpr uint32_t kPackedCol = 32;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kBwdBars = 8;  // barriers besides the per-stage full / empty pairs
+constexpr int kBwdBars = 9;  // barriers besides the per-stage full / empty pairs
 
 // Named barriers (bar.arrive by the producers, bar.sync by the whole issuing warp) in
 // place of mbarrier waits in the MMA issuer: a shared-memory access by the issuing warp
@@ -42,7 +42,10 @@ constexpr uint32_t kNbElem = kElemThreads + 32;  // elementwise warps + issuer
 //   e2        elementwise step 2 done: dS^T / dS is in place (256 arrivals)
 //   dq_full   one-pass kernel: the dQ product of a query tile is in TMEM (tcgen05.commit)
 //   dq_read   one-pass kernel: that product has been read out (256 arrivals)
-//   done      every MMA issued has completed         (tcgen05.commit)
+//   done      every MMA issued has completed; the dK/dV pass: every MMA of the
+//             current key tile                       (tcgen05.commit)
+//   kv_free   dK/dV pass over several key tiles: the last products reading the
+//             current tile's K and V have completed  (tcgen05.commit)
 struct Bars {
     uint32_t base;
     int S;
@@ -56,6 +59,7 @@ struct Bars {
     __device__ uint32_t done() const { return base + 8u * (5 + 2 * S); }
     __device__ uint32_t dq_full() const { return base + 8u * (6 + 2 * S); }
     __device__ uint32_t dq_read() const { return base + 8u * (7 + 2 * S); }
+    __device__ uint32_t kv_free() const { return base + 8u * (8 + 2 * S); }
 };
 
 __device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_flag, uint32_t resident_count) {
@@ -72,6 +76,7 @@ __device__ __forceinline__ void init_bars(const Bars& b, volatile int* abort_fla
     mbar_init(b.done(), 1);
     mbar_init(b.dq_full(), 1);
     mbar_init(b.dq_read(), kElemThreads);
+    mbar_init(b.kv_free(), 1);
     fence_barrier_init();
 }
 

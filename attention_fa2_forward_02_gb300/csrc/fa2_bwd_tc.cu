@@ -128,7 +128,13 @@ __host__ __device__ constexpr uint32_t nb_stage(int s) { return 3 + (uint32_t)s;
 // S^T(i+1) overwrites the columns holding P^T(i) only after dV(i), which reads
 // them, was issued; dP^T(i+1) likewise follows dK(i).
 
-// One CTA of the dK/dV pass: key tile kt of head bh.  The tensor maps are the
+// One CTA of the dK/dV pass: key tiles kt, kt + 1, ..., kt + n_items - 1 of head bh,
+// one after another (n_items > 1 with one value tensor only). Steps run over
+// g = u * n_qt + i (key tile u of the CTA, query tile i), so the stage ring and its
+// barriers carry on from one key tile to the next; the next tile's K and V load as soon
+// as the products reading the current ones have completed (kv_free, during the
+// current tile's last query tiles), and its first S^T and dP^T are issued while the
+// elementwise warps write the current tile's dK and dV. The tensor maps are the
 // kernel's own __grid_constant__ parameters (TMA reads them from parameter space).
 template <int D, bool kBf16, int kNV>
 __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
@@ -136,7 +142,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                                          const float* __restrict__ lse2, const float* __restrict__ delta,
                                          void* __restrict__ dk, void* __restrict__ dv, void* __restrict__ dv2, int n_q,
                                          int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
-                                         unsigned int* status, int kt, int bh) {
+                                         unsigned int* status, int kt, int n_items, int bh) {
     using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -144,8 +150,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_addr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int k0 = kt * BT;
     const int n_qt = (n_q + BT - 1) / BT;
+    if constexpr (!C::kNamed) n_items = 1;
 
     const Bars bars{base + C::kDkvBar, S};
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kDkvBar + C::kNumBars * 8);
@@ -174,33 +180,40 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             prefetch_tmap(&tm_do);
-            mbar_arrive_expect_tx(bars.resident(), (1 + kNV) * C::kTile);
-            for (int a = 0; a < C::kAtoms; ++a) {
-                tma_load_3d(k_smem + a * BT * C::kAtomRowBytes, &tm_k, bars.resident(), a * C::kAtomCols, k0, bh);
-                for (int v = 0; v < kNV; ++v)
-                    tma_load_3d(v_smem(v) + a * BT * C::kAtomRowBytes, v ? &tm_v2 : &tm_v, bars.resident(),
-                                a * C::kAtomCols, k0, bh);
-            }
-            int issued = 0;
+            int issued = 0, armed = 0;  // stage fills issued (steps), K / V fills armed (key tiles)
             bool ok = true;
-            for (int i = 0; i < n_qt; ++i) {
-                const int s = i % S;
-                if (i >= S && !(ok = mbar_wait(bars.empty(s), ((i / S) & 1) ^ 1, wd))) break;
-                mbar_arrive_expect_tx(bars.full(s), (1 + kNV) * C::kTile + 2 * BT * 4);
+            for (int u = 0; ok && u < n_items; ++u) {
+                // K and V of key tile u, once the products reading the previous ones have completed
+                if (u > 0 && !(ok = mbar_wait(bars.kv_free(), (u - 1) & 1, wd))) break;
+                const int k0 = (kt + u) * BT;
+                mbar_arrive_expect_tx(bars.resident(), (1 + kNV) * C::kTile);
                 for (int a = 0; a < C::kAtoms; ++a) {
-                    tma_load_3d(stage_q(s) + a * BT * C::kAtomRowBytes, &tm_q, bars.full(s), a * C::kAtomCols, i * BT, bh);
+                    tma_load_3d(k_smem + a * BT * C::kAtomRowBytes, &tm_k, bars.resident(), a * C::kAtomCols, k0, bh);
                     for (int v = 0; v < kNV; ++v)
-                        tma_load_3d(stage_do(s, v) + a * BT * C::kAtomRowBytes, v ? &tm_do2 : &tm_do, bars.full(s),
-                                    a * C::kAtomCols, i * BT, bh);
+                        tma_load_3d(v_smem(v) + a * BT * C::kAtomRowBytes, v ? &tm_v2 : &tm_v, bars.resident(),
+                                    a * C::kAtomCols, k0, bh);
                 }
-                const size_t w = (size_t)bh * n_q_pad + (size_t)i * BT;
-                bulk_load(stage_l2(s), lse2 + w, BT * 4, bars.full(s));
-                bulk_load(stage_dl(s), delta + w, BT * 4, bars.full(s));
-                issued = i + 1;
+                armed = u + 1;
+                for (int i = 0; i < n_qt; ++i) {
+                    const int g = u * n_qt + i, s = g % S;
+                    if (g >= S && !(ok = mbar_wait(bars.empty(s), ((g / S) & 1) ^ 1, wd))) break;
+                    mbar_arrive_expect_tx(bars.full(s), (1 + kNV) * C::kTile + 2 * BT * 4);
+                    for (int a = 0; a < C::kAtoms; ++a) {
+                        tma_load_3d(stage_q(s) + a * BT * C::kAtomRowBytes, &tm_q, bars.full(s), a * C::kAtomCols, i * BT,
+                                    bh);
+                        for (int v = 0; v < kNV; ++v)
+                            tma_load_3d(stage_do(s, v) + a * BT * C::kAtomRowBytes, v ? &tm_do2 : &tm_do, bars.full(s),
+                                        a * C::kAtomCols, i * BT, bh);
+                    }
+                    const size_t w = (size_t)bh * n_q_pad + (size_t)i * BT;
+                    bulk_load(stage_l2(s), lse2 + w, BT * 4, bars.full(s));
+                    bulk_load(stage_dl(s), delta + w, BT * 4, bars.full(s));
+                    issued = g + 1;
+                }
             }
             if (!ok) {
-                drain_wait(bars.resident(), 0);
-                for (int i = (issued > S ? issued - S : 0); i < issued; ++i) drain_wait(bars.full(i % S), (i / S) & 1);
+                if (armed > 0) drain_wait(bars.resident(), (armed - 1) & 1);
+                for (int g = (issued > S ? issued - S : 0); g < issued; ++g) drain_wait(bars.full(g % S), (g / S) & 1);
             }
         }
     } else if (warp == 1) {
@@ -232,58 +245,68 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                 }
             };
             static_assert(nb_stage(S - 1) < 16, "named barriers");
-            nb_sync(nb_stage(0), 64);  // K, V and the first Q / dO stage
-            if (lane == 0) {
-                tc_fence_after();
-                issue_st(0);
-                mma_commit(bars.s_full());
-                issue_dpt(0);
-                mma_commit(bars.dp_full());
-            }
-            __syncwarp();
-            for (int i = 0; i < n_qt; ++i) {
-                const int s = i % S;
-                const int sn = (i + 1) % S;
-                const bool more = i + 1 < n_qt;
-                nb_sync(kNbE1, kNbElem);  // P^T(i) in tensor memory
+            for (int u = 0; u < n_items; ++u) {
+                const int g0 = u * n_qt;
+                const bool next_tile = u + 1 < n_items;
+                // S^T(0) overwrites the columns of the previous tile's last P^T only after its
+                // dV was issued, dP^T(0) those of its last dS^T after its dK (issue order);
+                // dV and dK of this tile restart their accumulators only after the
+                // elementwise warps, which read the previous tile's out first, meet at e1.
+                nb_sync(nb_stage(g0 % S), 64);  // K, V of key tile u and its first Q / dO stage
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint64_t b = mdo0 + st_off(s);
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
-                        mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), b + (uint64_t)(kk * C::kAtomRowBytes),
-                               idesc_g, (i > 0 || kk > 0));
+                    issue_st(g0 % S);
+                    mma_commit(bars.s_full());
+                    issue_dpt(g0 % S);
+                    mma_commit(bars.dp_full());
+                    if (n_qt == 1 && next_tile) mma_commit(bars.kv_free());  // last readers of K, V issued
                 }
                 __syncwarp();
-                if (more) {
-                    nb_sync(nb_stage(sn), 64);  // Q, dO of tile i + 1
+                for (int i = 0; i < n_qt; ++i) {
+                    const int g = g0 + i;
+                    const int s = g % S;
+                    const int sn = (g + 1) % S;
+                    const bool more = i + 1 < n_qt;
+                    nb_sync(kNbE1, kNbElem);  // P^T(i) in tensor memory
                     if (lane == 0) {
                         tc_fence_after();
-                        issue_st(sn);
-                        mma_commit(bars.s_full());
+                        const uint64_t b = mdo0 + st_off(s);
+#pragma unroll
+                        for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
+                            mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), b + (uint64_t)(kk * C::kAtomRowBytes),
+                                   idesc_g, (i > 0 || kk > 0));
+                    }
+                    __syncwarp();
+                    if (more) {
+                        nb_sync(nb_stage(sn), 64);  // Q, dO of tile i + 1
+                        if (lane == 0) {
+                            tc_fence_after();
+                            issue_st(sn);
+                            mma_commit(bars.s_full());
+                        }
+                        __syncwarp();
+                    }
+                    nb_sync(kNbE2, kNbElem);  // dS^T(i) in tensor memory
+                    if (lane == 0) {
+                        tc_fence_after();
+                        const uint64_t b = mq0 + st_off(s);
+#pragma unroll
+                        for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
+                            mma_ts(tmem + 256u + (uint32_t)D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
+                                   b + (uint64_t)(kk * C::kAtomRowBytes), idesc_g, (i > 0 || kk > 0));
+                        mma_commit(bars.empty(s));
+                        if (more) {
+                            issue_dpt(sn);
+                            mma_commit(bars.dp_full());
+                            if (i + 2 == n_qt && next_tile) mma_commit(bars.kv_free());  // last readers of K, V issued
+                        }
                     }
                     __syncwarp();
                 }
-                nb_sync(kNbE2, kNbElem);  // dS^T(i) in tensor memory
-                if (lane == 0) {
-                    tc_fence_after();
-                    const uint64_t b = mq0 + st_off(s);
-#pragma unroll
-                    for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
-                        mma_ts(tmem + 256u + (uint32_t)D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
-                               b + (uint64_t)(kk * C::kAtomRowBytes), idesc_g, (i > 0 || kk > 0));
-                    mma_commit(bars.empty(s));
-                    if (more) {
-                        issue_dpt(sn);
-                        mma_commit(bars.dp_full());
-                    }
-                }
+                if (lane == 0) mma_commit(bars.done());  // dV, dK of key tile u complete
                 __syncwarp();
             }
-            if (lane == 0) {
-                mma_commit(bars.done());
-                drain_wait(bars.done(), 0);
-            }
+            if (lane == 0) drain_wait(bars.done(), (uint32_t)((n_items - 1) & 1));
             __syncwarp();
         } else {
             if (lane == 0) {
@@ -345,14 +368,16 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             }
         }
     } else if (C::kNamed && warp == kBwdRelayWarp) {
-        // TMA relay: signals each Q / dO stage (the first with K and V) to the issuer
-        bool ok = warp_wait(bars.resident(), 0, wd) && warp_wait(bars.full(0), 0, wd);
-        nb_arrive(nb_stage(0), 64);
-        for (int i = 1; i < n_qt; ++i) {
-            const int s = i % S;
-            ok = ok && warp_wait(bars.full(s), (i / S) & 1, wd);
-            nb_arrive(nb_stage(s), 64);
-        }
+        // TMA relay: signals each Q / dO stage (each key tile's first with its K and V) to
+        // the issuer
+        bool ok = true;
+        for (int u = 0; u < n_items; ++u)
+            for (int i = 0; i < n_qt; ++i) {
+                const int g = u * n_qt + i, s = g % S;
+                if (i == 0) ok = ok && warp_wait(bars.resident(), u & 1, wd);
+                ok = ok && warp_wait(bars.full(s), (g / S) & 1, wd);
+                nb_arrive(nb_stage(s), 64);
+            }
     } else {
         // Two warps per TMEM lane quarter; warp `half` owns query columns [64*half, 64*half + 64).
         const int quarter = warp & 3;
@@ -366,9 +391,11 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             if constexpr (C::kNamed) nb_arrive(nb, kNbElem);
             else mbar_arrive(mbar);
         };
+        for (int u = 0; u < n_items; ++u) {
         for (int i = 0; i < n_qt; ++i) {
-            const int s = i % S;
-            if (!(ok = ok && warp_wait(bars.s_full(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) {
+            const int g = u * n_qt + i;
+            const int s = g % S;
+            if (!(ok = ok && warp_wait(bars.s_full(), g & 1, wd) && warp_wait(bars.full(s), (g / S) & 1, wd))) {
                 signal(kNbE1, bars.e1());
                 signal(kNbE2, bars.e2());
                 continue;
@@ -410,7 +437,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             tc_fence_before();
             signal(kNbE1, bars.e1());
             // step 2: dS^T = P^T * (dP^T - D), chunk by chunk in write-safe order
-            if (!(ok = warp_wait(bars.dp_full(), i & 1, wd))) {
+            if (!(ok = warp_wait(bars.dp_full(), g & 1, wd))) {
                 signal(kNbE2, bars.e2());
                 continue;
             }
@@ -440,10 +467,11 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             tc_fence_before();
             signal(kNbE2, bars.e2());
         }
-        if (ok) ok = warp_wait(bars.done(), 0, wd);
+        // dK, dV of key tile u: read out of tensor memory before this warp's next e1 arrival
+        if (ok) ok = warp_wait(bars.done(), (uint32_t)(u & 1), wd);
         if (ok) {
             tc_fence_after();
-            const int key = k0 + quarter * 32 + lane;
+            const int key = (kt + u) * BT + quarter * 32 + lane;
             const size_t row = (size_t)bh * n_k + key;
             // half 0 writes dV (each pair's), half 1 writes dK (scaled)
 #pragma unroll
@@ -461,6 +489,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                 }
             }
         }
+        }  // key tiles
     }
 
     tc_fence_before();
@@ -829,7 +858,7 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
                     void* __restrict__ dv, void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale,
                     float scale_log2, unsigned int* status) {
     dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, lse2, delta, dk, dv, dv2, n_q, n_k, n_q_pad, d_act,
-                            scale, scale_log2, status, blockIdx.x, blockIdx.y);
+                            scale, scale_log2, status, blockIdx.x, 1, blockIdx.y);
 }
 
 template <int D, bool kBf16, int kNV>
@@ -845,13 +874,15 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
 
 // Both passes in one launch.  The passes are independent once D and LSE2 are in
 // the workspace; one grid lets the CTAs of one fill the SMs the other leaves idle
-// in its last wave.  Order of the CTAs (x fastest, then the head y):
-//   dq_first == 0: per head, x < n_kt runs the dK/dV pass for key tile x and the
-//     rest the dQ pass for query tile x - n_kt, so that a head's two sets of CTAs
-//     run together and share its Q, K, V, dO in L2;
+// in its last wave.  A dK/dV CTA takes kt_per_cta consecutive key tiles (the last
+// of a head fewer), n_kc = ceil(n_kt / kt_per_cta) of them per head.  Order of the
+// CTAs (x fastest, then the head y):
+//   dq_first == 0: per head, x < n_kc runs the dK/dV pass for key tiles from
+//     x * kt_per_cta and the rest the dQ pass for query tile x - n_kc, so that a
+//     head's two sets of CTAs run together and share its Q, K, V, dO in L2;
 //   dq_first == 1: the dQ CTAs of all heads first, then all dK/dV CTAs - for
 //     shapes whose dQ CTAs (n_kt key tiles each) are much longer than the dK/dV
-//     CTAs (n_qt query tiles each): started first, they do not end in a tail.
+//     CTAs: started first, they do not end in a tail.
 template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_passes_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -861,32 +892,47 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
                       const uint16_t* __restrict__ do2_ptr, const float* __restrict__ lse2,
                       const float* __restrict__ delta, void* __restrict__ dq, void* __restrict__ dk, void* __restrict__ dv,
                       void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
-                      unsigned int* status, int dq_first) {
+                      unsigned int* status, int dq_first, int kt_per_cta) {
     const int n_kt = (n_k + BT - 1) / BT, n_qt = (n_q + BT - 1) / BT;
-    int dkdv_tile = -1, dq_tile = -1, bh;
+    const int n_kc = (n_kt + kt_per_cta - 1) / kt_per_cta;
+    int dkdv_cta_x = -1, dq_tile = -1, bh;
     if (!dq_first) {
         bh = blockIdx.y;
-        if ((int)blockIdx.x < n_kt) dkdv_tile = blockIdx.x;
-        else dq_tile = blockIdx.x - n_kt;
+        if ((int)blockIdx.x < n_kc) dkdv_cta_x = blockIdx.x;
+        else dq_tile = blockIdx.x - n_kc;
     } else {
         const int lin = blockIdx.y * gridDim.x + blockIdx.x, n_dq = (int)gridDim.y * n_qt;
         if (lin < n_dq) {
             bh = lin / n_qt;
             dq_tile = lin % n_qt;
         } else {
-            bh = (lin - n_dq) / n_kt;
-            dkdv_tile = (lin - n_dq) % n_kt;
+            bh = (lin - n_dq) / n_kc;
+            dkdv_cta_x = (lin - n_dq) % n_kc;
         }
     }
-    if (dkdv_tile >= 0)
+    if (dkdv_cta_x >= 0) {
+        const int kt = dkdv_cta_x * kt_per_cta;
+        const int items = n_kt - kt < kt_per_cta ? n_kt - kt : kt_per_cta;
         dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, lse2, delta, dk, dv, dv2, n_q, n_k, n_q_pad,
-                                d_act, scale, scale_log2, status, dkdv_tile, bh);
+                                d_act, scale, scale_log2, status, kt, items, bh);
+    }
     else
         dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act,
                               scale, scale_log2, status, dq_tile, bh);
 }
 
 // ------------------------------------------------------------------------------ launch
+
+// Key tiles per dK/dV CTA of the one-grid launch: at least 32 query tiles per CTA, so
+// that the fixed cost of a key tile (K and V load, pipeline fill, dK / dV write-out,
+// about 5.6 us on GB300) is partly hidden behind the next tile's work. Measured on
+// GB300 (bf16, head size 128, BH = 32): N_q = 1024, N_k = 32768 1.353 -> 1.270 ms with
+// 4 key tiles per CTA (1.301 with 8); N_q = N_k = 8192 keeps 1 (2 read 2.345 against
+// 2.303 ms).
+static int dkdv_tiles_per_cta(int n_qt) {
+    const int m = (32 + n_qt - 1) / n_qt;
+    return m < 1 ? 1 : (m > 8 ? 8 : m);
+}
 
 template <int D, bool kBf16, int kNV>
 cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int stages) {
@@ -924,10 +970,12 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         constexpr int smem = C::kSmemDkv > C::kSmemDq ? C::kSmemDkv : C::kSmemDq;
         e = ensure_smem_limit(reinterpret_cast<const void*>(both), smem, 42 + (slot - 16) / 2);  // slots 42..51
         if (e != cudaSuccess) return e;
-        both<<<dim3((unsigned)(n_kt + n_qt), (unsigned)p.bh, 1), C::kThreads, smem, stream>>>(
+        const int m = C::kNamed ? dkdv_tiles_per_cta(n_qt) : 1;
+        const int n_kc = (n_kt + m - 1) / m;
+        both<<<dim3((unsigned)(n_kc + n_qt), (unsigned)p.bh, 1), C::kThreads, smem, stream>>>(
             tq, tk, tv, tdo, tv2, tdo2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
             static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, p.dk, p.dv, p.dv2, (int)p.n_q,
-            (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, n_kt >= 4 * n_qt ? 1 : 0);
+            (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, n_kt >= 4 * m * n_qt ? 1 : 0, m);
         return cudaGetLastError();
     }
     if (stages & kBwdDkDv) {
