@@ -198,3 +198,36 @@ def test_backward_far_negative_scores_with_a_partial_key_tile(d):
     check_16bit(dq, rq, "dQ")
     check_16bit(dk, rk, "dK")
     check_16bit(dv, rv, "dV")
+
+
+@pytest.mark.parametrize("n_q,n_k", [
+    (505, 1147),   # 4 query tiles: 8 key tiles per dK/dV CTA, 9 key tiles -> CTAs of 8 and 1
+    (100, 333),    # 1 query tile: 3 key tiles in one CTA (K and V freed right after the first products)
+    (200, 2100),   # 2 query tiles: 17 key tiles -> CTAs of 8, 8 and 1
+    (100, 4096),   # 1 query tile, 32 key tiles: dQ CTAs first, then 4 dK/dV CTAs of 8 key tiles
+])
+def test_backward_passes_over_several_key_tiles_equal_the_stages(n_q, n_k):
+    """The one-grid passes kernel runs a head's dK/dV in CTAs of several consecutive key tiles
+    when the head has few query tiles; its gradients equal, bit for bit, those of the stage
+    entry points (one key tile per dK/dV CTA), and the oracle's."""
+    torch = G.require_gpu()
+    bh, d, dtype = 2, 128, "bf16"
+    q, k, v = G.inputs(f"bwd/multikt/{n_q}/{n_k}", bh, n_q, n_k, d, dtype)
+    d_o = synth.tensor(f"bwd/multikt/{n_q}/{n_k}/do", (bh, n_q, d), dtype)
+    qd, kd, vd, dod = (G.to_device(x, dtype) for x in (q, k, v, d_o))
+    scale = 1 / math.sqrt(d)
+    o = G.empty((bh, n_q, d), dtype)
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_BF16), dtype=torch.uint8,
+                     device="cuda")
+    staged = _stages(qd, kd, vd, o, dod, lse, scale, ws, dtype)
+    one_grid = [G.empty(tuple(x.shape), dtype) for x in (qd, kd, vd)]
+    binding.fa2_backward_passes(qd, kd, vd, dod, ws, *one_grid, scale)
+    binding.fa2_device_status()
+    for name, a, b in zip(("dQ", "dK", "dV"), staged, one_grid):
+        assert torch.equal(a, b), f"fa2_backward_passes {name} differs from _dkdv + _dq"
+    w = lambda x: synth.widen(x, dtype)
+    ref = A.backward(w(q), w(k), w(v), w(d_o), scale)
+    for name, a, r in zip(("dQ", "dK", "dV"), one_grid, ref):
+        check_16bit(G.to_f64(a), r, f"one-grid {name}")
