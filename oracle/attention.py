@@ -99,12 +99,23 @@ def backward(q: np.ndarray, k: np.ndarray, v: np.ndarray, d_o: np.ndarray, scale
     return dq, dk, dv
 
 
-def backward_slice(q, k, v, d_o, scale: float, bh: int, row_chunk: int = 1024):
+def backward_slice(q, k, v, d_o, scale: float, bh: int, row_chunk: int = 1024, o=None, lse=None,
+                   rounding_scales: bool = False):
     """Backward of one (batch, head) slice, with the score matrix built in row chunks.
 
     Same arithmetic as :func:`backward` for ``q[bh]`` etc.; chunking only bounds
     memory for long sequences (each chunk holds ``row_chunk x Nk`` scores).
     Returns (dQ [Nq, d], dK [Nk, d], dV [Nk, d]).
+
+    ``o`` and ``lse`` ([BH, Nq, d] and [BH, Nq]) are the stored forward outputs that
+    the backward kernels of flash_attn2.rs read from memory (``D_q = rowsum(O_q *
+    dO_q)`` from the stored O, ``p = exp(q.k*scale - L)`` from the stored L); when
+    given, D and P are formed from them instead of from this function's own exact O
+    and LSE.  With ``rounding_scales``, three more arrays are returned, one per
+    gradient element: the root-sum-square of the terms of its last product,
+    sqrt(sum_j (dS_ij k_jc)^2) * scale for dQ, sqrt(sum_i (dS_ij q_ic)^2) * scale for
+    dK and sqrt(sum_i (P_ij dO_ic)^2) for dV - the scale on which rounding each term's
+    16-bit operand (dS, P) moves the sum.
     """
     qb = np.asarray(q[bh], dtype=np.float64)
     kb = np.asarray(k[bh], dtype=np.float64)
@@ -114,20 +125,33 @@ def backward_slice(q, k, v, d_o, scale: float, bh: int, row_chunk: int = 1024):
     dq = np.zeros_like(qb)
     dk = np.zeros_like(kb)
     dv = np.zeros_like(vb)
+    if rounding_scales:
+        sq_q, sq_k, sq_v = np.zeros_like(qb), np.zeros_like(kb), np.zeros_like(vb)
     for r0 in range(0, nq, row_chunk):
         r1 = min(nq, r0 + row_chunk)
         s = scale * (qb[r0:r1] @ kb.T)
-        m = s.max(axis=-1, keepdims=True)
-        e = np.exp(s - m)
-        l = e.sum(axis=-1, keepdims=True)
-        o = (e / l) @ vb
-        lse = m + np.log(l)
-        p = np.exp(s - lse)
-        d_row = np.sum(o * dob[r0:r1], axis=-1, keepdims=True)
+        if o is None or lse is None:
+            m = s.max(axis=-1, keepdims=True)
+            e = np.exp(s - m)
+            l = e.sum(axis=-1, keepdims=True)
+            o_rows = (e / l) @ vb
+            lse_rows = m + np.log(l)
+        if o is not None:
+            o_rows = np.asarray(o[bh, r0:r1], dtype=np.float64)
+        if lse is not None:
+            lse_rows = np.asarray(lse[bh, r0:r1], dtype=np.float64)[:, None]
+        p = np.exp(s - lse_rows)
+        d_row = np.sum(o_rows * dob[r0:r1], axis=-1, keepdims=True)
         dv += p.T @ dob[r0:r1]
         ds = p * (dob[r0:r1] @ vb.T - d_row)
         dq[r0:r1] = scale * (ds @ kb)
         dk += scale * (ds.T @ qb[r0:r1])
+        if rounding_scales:
+            sq_q[r0:r1] = (ds * ds) @ (kb * kb)
+            sq_k += (ds * ds).T @ (qb[r0:r1] * qb[r0:r1])
+            sq_v += (p * p).T @ (dob[r0:r1] * dob[r0:r1])
+    if rounding_scales:
+        return dq, dk, dv, scale * np.sqrt(sq_q), scale * np.sqrt(sq_k), np.sqrt(sq_v)
     return dq, dk, dv
 
 

@@ -59,7 +59,7 @@ def test_backward_gradient_identities():
     assert np.max(np.abs(dk.sum(axis=1))) <= 0.02 * np.max(np.abs(dk)) * math.sqrt(n)
 
 
-def test_backward_full_size_sampled():
+def test_backward_full_size_whole_heads():
     """bf16 forward+backward, B=2 H=16 (BH=32), N=8192, d=128: every dQ/dK/dV row of two heads
     against the oracle's chunked per-head backward."""
     bh, n, d = 32, 8192, 128
@@ -76,7 +76,7 @@ def test_backward_full_size_sampled():
 
 
 
-def test_backward_full_size_d64_sampled():
+def test_backward_full_size_d64_whole_heads():
     """bf16 forward+backward, B=4 H=16 (BH=64), N=4096, d=64 (the one-pass backward with the
     float32 dQ accumulator): every dQ/dK/dV row of the first and last heads against the oracle."""
     bh, n, d = 64, 4096, 64
@@ -92,22 +92,56 @@ def test_backward_full_size_d64_sampled():
         check_16bit(dv[b], rv, f"dV head {b}")
 
 
-def test_backward_cross_attention_peaked_sampled():
+def test_backward_cross_attention_peaked_whole_heads():
     """B=1 H=32, N_q=1024 vs N_k=32768, d=128, K scaled by 8 (peaked rows; the one-grid passes
-    kernel puts its dQ CTAs first at this shape): every dQ/dK/dV row of heads 0 and 31."""
+    kernel puts its dQ CTAs first at this shape).  The backward reads a stored O and LSE: for the
+    two checked heads those are the oracle's (O rounded to bfloat16, LSE to float32), the same
+    ones the oracle's backward reads, so that both sides form the same D; the other heads keep
+    the GPU forward's.  Two runs give bit-identical gradients, and every dQ/dK/dV element of
+    heads 0 and 31 is within 2e-2 + u|ref| + 8u R of the oracle (tests/tolerance.py)."""
+    torch = G.require_gpu()
     bh, n_q, n_k, d = 32, 1024, 32768, 128
     q, k, v = G.inputs("config/cross_k8", bh, n_q, n_k, d, "bf16", k_scale=8.0)
     d_o = synth.tensor("config/cross_k8/do", (bh, n_q, d), "bf16")
     scale = 1 / math.sqrt(d)
-    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, "bf16", scale)
-    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
     w = lambda x: synth.widen(x, "bf16")
-    for b in (0, bh - 1):
-        rq, rk, rv = A.backward_slice(w(q[b:b + 1]), w(k[b:b + 1]), w(v[b:b + 1]), w(d_o[b:b + 1]), scale, 0,
-                                      row_chunk=256)
-        check_16bit_grad(dq[b], rq, f"dQ head {b}")
-        check_16bit_grad(dk[b], rk, f"dK head {b}")
-        check_16bit_grad(dv[b], rv, f"dV head {b}")
+    qd, kd, vd, dod = (G.to_device(x, "bf16") for x in (q, k, v, d_o))
+    o = G.empty((bh, n_q, d), "bf16")
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    heads = (0, bh - 1)
+    stored = {}
+    for b in heads:
+        o_ref = np.empty((n_q, d))
+        l_ref = np.empty(n_q)
+        for r0 in range(0, n_q, 128):
+            rows = np.arange(r0, r0 + 128)
+            o_ref[rows], l_ref[rows] = A.forward_rows(w(q[b:b + 1]), w(k[b:b + 1]), w(v[b:b + 1]), scale, 0, rows)
+        o_st = synth.to_storage(o_ref[None], "bf16")
+        l_st = l_ref.astype(np.float32)
+        o[b] = G.to_device(o_st, "bf16")[0]
+        lse[b] = torch.from_numpy(l_st).cuda()
+        stored[b] = (synth.widen(o_st, "bf16"), l_st.astype(np.float64)[None])
+    code = binding.DTYPE_BF16
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, code), dtype=torch.uint8, device="cuda")
+    runs = []
+    for _ in range(2):
+        grads = [G.empty(x.shape, "bf16") for x in (q, k, v)]
+        binding.fa2_backward(qd, kd, vd, o, dod, lse, *grads, ws, scale)
+        binding.fa2_device_status()
+        runs.append([G.to_f64(g) for g in grads])
+    for name, a, b in zip(("dQ", "dK", "dV"), *runs):
+        assert np.array_equal(a, b), f"{name} differs between two runs"
+    dq, dk, dv = runs[0]
+    assert np.all(np.isfinite(dq)) and np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+    for b in heads:
+        o_st, l_st = stored[b]
+        rq, rk, rv, sq, sk, sv = A.backward_slice(w(q[b:b + 1]), w(k[b:b + 1]), w(v[b:b + 1]), w(d_o[b:b + 1]), scale,
+                                                  0, row_chunk=256, o=o_st, lse=l_st, rounding_scales=True)
+        check_16bit_grad(dq[b], rq, sq, "bf16", f"dQ head {b}")
+        check_16bit_grad(dk[b], rk, sk, "bf16", f"dK head {b}")
+        check_16bit_grad(dv[b], rv, sv, "bf16", f"dV head {b}")
+
 
 def _stages(qd, kd, vd, o, dod, lse, scale, ws, dtype):
     """The two-pass backward through its three stage entry points."""
@@ -200,27 +234,36 @@ def test_backward_far_negative_scores_with_a_partial_key_tile(d):
     check_16bit(dv, rv, "dV")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [32, 64, 128])
 @pytest.mark.parametrize("n_q,n_k", [
     (505, 1147),   # 4 query tiles: 8 key tiles per dK/dV CTA, 9 key tiles -> CTAs of 8 and 1
     (100, 333),    # 1 query tile: 3 key tiles in one CTA (K and V freed right after the first products)
     (200, 2100),   # 2 query tiles: 17 key tiles -> CTAs of 8, 8 and 1
     (100, 4096),   # 1 query tile, 32 key tiles: dQ CTAs first, then 4 dK/dV CTAs of 8 key tiles
 ])
-def test_backward_passes_over_several_key_tiles_equal_the_stages(n_q, n_k):
+def test_backward_passes_over_several_key_tiles_equal_the_stages(n_q, n_k, d, dtype):
     """The one-grid passes kernel runs a head's dK/dV in CTAs of several consecutive key tiles
-    when the head has few query tiles; its gradients equal, bit for bit, those of the stage
-    entry points (one key tile per dK/dV CTA), and the oracle's."""
+    when the head has few query tiles (at every head size: fa2_backward_passes, and at head
+    sizes up to 64 the two-pass fallback of fa2_backward_noalloc); its gradients equal, bit for
+    bit, those of the stage entry points (one key tile per dK/dV CTA), and the oracle's.
+    The launch takes fewer key tiles per CTA when that would leave fewer dK/dV CTAs than
+    SMs, so each shape runs with enough heads to keep the counts in the comments."""
     torch = G.require_gpu()
-    bh, d, dtype = 2, 128, "bf16"
-    q, k, v = G.inputs(f"bwd/multikt/{n_q}/{n_k}", bh, n_q, n_k, d, dtype)
-    d_o = synth.tensor(f"bwd/multikt/{n_q}/{n_k}/do", (bh, n_q, d), dtype)
+    n_qt, n_kt = -(-n_q // 128), -(-n_k // 128)
+    m = min(8, -(-32 // n_qt))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    bh = max(2, -(-sms // -(-n_kt // m)))
+    tag = f"bwd/multikt/{n_q}/{n_k}/{d}/{dtype}"
+    q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
+    d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)
     qd, kd, vd, dod = (G.to_device(x, dtype) for x in (q, k, v, d_o))
     scale = 1 / math.sqrt(d)
     o = G.empty((bh, n_q, d), dtype)
     lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
     binding.fa2_forward(qd, kd, vd, o, lse, scale)
-    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_BF16), dtype=torch.uint8,
-                     device="cuda")
+    code = {"bf16": binding.DTYPE_BF16, "f16": binding.DTYPE_F16}[dtype]
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, code), dtype=torch.uint8, device="cuda")
     staged = _stages(qd, kd, vd, o, dod, lse, scale, ws, dtype)
     one_grid = [G.empty(tuple(x.shape), dtype) for x in (qd, kd, vd)]
     binding.fa2_backward_passes(qd, kd, vd, dod, ws, *one_grid, scale)
@@ -228,6 +271,7 @@ def test_backward_passes_over_several_key_tiles_equal_the_stages(n_q, n_k):
     for name, a, b in zip(("dQ", "dK", "dV"), staged, one_grid):
         assert torch.equal(a, b), f"fa2_backward_passes {name} differs from _dkdv + _dq"
     w = lambda x: synth.widen(x, dtype)
-    ref = A.backward(w(q), w(k), w(v), w(d_o), scale)
-    for name, a, r in zip(("dQ", "dK", "dV"), one_grid, ref):
-        check_16bit(G.to_f64(a), r, f"one-grid {name}")
+    for b in (0, bh - 1):
+        ref = A.backward(w(q[b:b + 1]), w(k[b:b + 1]), w(v[b:b + 1]), w(d_o[b:b + 1]), scale)
+        for name, a, r in zip(("dQ", "dK", "dV"), one_grid, ref):
+            check_16bit(G.to_f64(a[b]), r[0], f"one-grid {name} of head {b}")

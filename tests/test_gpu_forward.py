@@ -167,7 +167,9 @@ def test_forward_deterministic_and_in_bounds():
     assert torch.all(l_buf[:guard] == -7.0) and torch.all(l_buf[-guard:] == -7.0)
 
 
-def _sampled_rows(tag, bh, n_q, n_k, d, k_scale, bh_list, rows):
+def _whole_heads(tag, bh, n_q, n_k, d, k_scale, heads, row_chunk=512):
+    """GPU forward of the whole problem; every row of O and LSE of the listed heads against
+    the oracle, element by element (the oracle runs on chunks of query rows to bound its memory)."""
     torch = G.require_gpu()
     q, k, v = G.inputs(tag, bh, n_q, n_k, d, "bf16", k_scale=k_scale)
     scale = 1 / math.sqrt(d)
@@ -176,28 +178,33 @@ def _sampled_rows(tag, bh, n_q, n_k, d, k_scale, bh_list, rows):
     lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
     binding.fa2_forward(qd, kd, vd, o, lse, scale)
     binding.fa2_device_status()
-    for b in bh_list:
-        o_ref, l_ref = A.forward_rows(synth.widen(q[b:b + 1], "bf16"), synth.widen(k[b:b + 1], "bf16"),
-                                      synth.widen(v[b:b + 1], "bf16"), scale, 0, rows)
-        check_16bit(G.to_f64(o[b, rows]), o_ref, f"O rows of head {b}")
-        check_lse(G.to_f64(lse[b, rows]), l_ref, f"LSE rows of head {b}")
-    return o, lse
+    o_all, lse_all = G.to_f64(o), G.to_f64(lse)
+    assert np.all(np.isfinite(o_all)) and np.all(np.isfinite(lse_all))
+    for b in heads:
+        w = lambda x: synth.widen(x[b:b + 1], "bf16")  # noqa: E731
+        qb, kb, vb = w(q), w(k), w(v)
+        o_ref = np.empty((n_q, d))
+        l_ref = np.empty(n_q)
+        for r0 in range(0, n_q, row_chunk):
+            rows = np.arange(r0, min(n_q, r0 + row_chunk))
+            o_ref[rows], l_ref[rows] = A.forward_rows(qb, kb, vb, scale, 0, rows)
+        check_16bit(o_all[b], o_ref, f"O of head {b}")
+        check_lse(lse_all[b], l_ref, f"LSE of head {b}")
 
 
-def test_forward_full_size_d64_sampled():
-    """Non-causal bf16 forward, B=4 H=16 (BH=64), N=4096, d=64: sampled rows against the oracle."""
-    rows = np.array([0, 1, 127, 128, 2047, 2048, 4094, 4095])
-    _sampled_rows("config/fwd_d64", 64, 4096, 4096, 64, 1.0, [0, 31, 63], rows)
+def test_forward_full_size_d64_whole_heads():
+    """Non-causal bf16 forward, B=4 H=16 (BH=64), N=4096, d=64: every row of O and LSE of the
+    first and last heads against the oracle."""
+    _whole_heads("config/fwd_d64", 64, 4096, 4096, 64, 1.0, [0, 63])
 
 
-def test_forward_full_size_d128_sampled():
-    """bf16 forward, B=2 H=16 (BH=32), N=8192, d=128: sampled rows against the oracle."""
-    rows = np.array([0, 255, 256, 4000, 8191])
-    _sampled_rows("config/fwdbwd_d128", 32, 8192, 8192, 128, 1.0, [0, 17, 31], rows)
+def test_forward_full_size_d128_whole_heads():
+    """bf16 forward, B=2 H=16 (BH=32), N=8192, d=128: every row of O and LSE of the first and
+    last heads against the oracle."""
+    _whole_heads("config/fwdbwd_d128", 32, 8192, 8192, 128, 1.0, [0, 31])
 
 
-def test_forward_cross_attention_peaked_sampled():
-    """B=1 H=32, N_q=1024 vs N_k=32768, d=128, K scaled by 8 (peaked rows): sampled rows."""
-    rows = np.array([0, 100, 511, 512, 1023])
-    o, lse = _sampled_rows("config/cross_k8", 32, 1024, 32768, 128, 8.0, [0, 31], rows)
-    assert np.all(np.isfinite(G.to_f64(o))) and np.all(np.isfinite(G.to_f64(lse)))
+def test_forward_cross_attention_peaked_whole_heads():
+    """B=1 H=32, N_q=1024 vs N_k=32768, d=128, K scaled by 8 (peaked rows): every row of O and
+    LSE of the first and last heads against the oracle."""
+    _whole_heads("config/cross_k8", 32, 1024, 32768, 128, 8.0, [0, 31], row_chunk=128)

@@ -223,6 +223,56 @@ def test_backward_slice_pinned():
     assert pin_gradient_closed_forms(sliced)
 
 
+def test_backward_slice_from_stored_outputs():
+    """backward_slice with the stored O and LSE (what the page's backward kernels read):
+    given the exact ones it reproduces the default; a stored LSE larger by c scales every
+    gradient by exp(-c) (P = exp(s - LSE)); a stored O whose row sum D is larger by t moves
+    dS by -t P, so dQ by -t scale P K and dK by -t scale P^T Q, and leaves dV."""
+    q, k, v, d_o = _rand((2, 7, 5), 110), _rand((2, 9, 5), 111), _rand((2, 9, 5), 112), _rand((2, 7, 5), 113)
+    scale = 0.41
+    o, lse = A.forward(q, k, v, scale)
+    for b in range(2):
+        base = A.backward_slice(q, k, v, d_o, scale, b, row_chunk=3)
+        same = A.backward_slice(q, k, v, d_o, scale, b, row_chunk=3, o=o, lse=lse)
+        for x, y in zip(base, same):
+            assert np.allclose(x, y, atol=1e-13)
+        c = 0.7
+        shifted = A.backward_slice(q, k, v, d_o, scale, b, row_chunk=4, o=o, lse=lse + c)
+        for x, y in zip(base, shifted):
+            assert np.allclose(y, x * math.exp(-c), atol=1e-13)
+        t = 0.3
+        o2 = o + t * d_o / np.sum(d_o * d_o, axis=-1, keepdims=True)  # D_i + t for every row
+        moved = A.backward_slice(q, k, v, d_o, scale, b, row_chunk=2, o=o2, lse=lse)
+        p = A.probabilities(q[b:b + 1], k[b:b + 1], scale)[0]
+        assert np.allclose(moved[0], base[0] - t * scale * p @ k[b], atol=1e-12)
+        assert np.allclose(moved[1], base[1] - t * scale * p.T @ q[b], atol=1e-12)
+        assert np.allclose(moved[2], base[2], atol=1e-13)
+
+
+def test_backward_slice_rounding_scales_brute():
+    """The root-sum-square scales of the last products, against explicit loops with fsum."""
+    q, k, v, d_o = _rand((1, 4, 3), 114), _rand((1, 5, 3), 115), _rand((1, 5, 3), 116), _rand((1, 4, 3), 117)
+    scale = 0.6
+    o, lse = A.forward(q, k, v, scale)
+    out = A.backward_slice(q, k, v, d_o, scale, 0, row_chunk=3, rounding_scales=True)
+    assert len(out) == 6
+    p = A.probabilities(q, k, scale)[0]
+    dmat = A.bwd_preprocess(o, d_o)[0]
+    ds = [[p[i, j] * (math.fsum(d_o[0, i, t] * v[0, j, t] for t in range(3)) - dmat[i]) for j in range(5)] for i in range(4)]
+    for i in range(4):
+        for c in range(3):
+            want = scale * math.sqrt(math.fsum((ds[i][j] * k[0, j, c]) ** 2 for j in range(5)))
+            assert abs(out[3][i, c] - want) <= 1e-12
+    for j in range(5):
+        for c in range(3):
+            want_k = scale * math.sqrt(math.fsum((ds[i][j] * q[0, i, c]) ** 2 for i in range(4)))
+            want_v = math.sqrt(math.fsum((p[i, j] * d_o[0, i, c]) ** 2 for i in range(4)))
+            assert abs(out[4][j, c] - want_k) <= 1e-12 and abs(out[5][j, c] - want_v) <= 1e-12
+    # the gradients themselves are the default ones
+    for x, y in zip(out[:3], A.backward_slice(q, k, v, d_o, scale, 0)):
+        assert np.allclose(x, y, atol=1e-14)
+
+
 def test_psa_backward_finite_differences():
     """Gradient of L = sum(O_lo * dO_lo) + sum(O_hi * dO_hi) w.r.t. every element of the packed buffer."""
     packed = _rand((4, 1, 4, 3), 95)
@@ -246,6 +296,24 @@ def test_psa_backward_finite_differences():
         packed[idx] = old
         num[idx] = (fp - fm) / (2 * h)
     assert np.allclose(g, num, rtol=1e-6, atol=1e-8)
+
+
+def test_psa_backward_null_control():
+    """With dO_hi = 0 the V_hi call contributes nothing: sections 0-2 are the plain backward of
+    (Q, K, V_lo) and section 3 is zero; symmetrically with dO_lo = 0.  A version that let the
+    hi call's gradient leak into section 2, or dropped the lo call's dQ / dK from the sums,
+    fails one of the two."""
+    packed = _rand((4, 2, 5, 3), 98)
+    d_lo, d_hi = _rand((2, 5, 3), 99), _rand((2, 5, 3), 100)
+    scale = 0.55
+    g = A.psa_backward(packed, d_lo, np.zeros_like(d_hi), scale)
+    dq, dk, dv = A.backward(packed[0], packed[1], packed[2], d_lo, scale)
+    assert np.allclose(g[0], dq, atol=1e-14) and np.allclose(g[1], dk, atol=1e-14)
+    assert np.allclose(g[2], dv, atol=1e-14) and np.all(g[3] == 0)
+    g = A.psa_backward(packed, np.zeros_like(d_lo), d_hi, scale)
+    dq, dk, dv = A.backward(packed[0], packed[1], packed[3], d_hi, scale)
+    assert np.allclose(g[0], dq, atol=1e-14) and np.allclose(g[1], dk, atol=1e-14)
+    assert np.all(g[2] == 0) and np.allclose(g[3], dv, atol=1e-14)
 
 
 def test_preprocess_loop():
@@ -463,17 +531,58 @@ def test_tolerance_rejects_null_output():
     check_16bit(ref + 1e-5, ref)
 
 
-def test_gradient_tolerance_scales_with_magnitude_but_rejects_errors():
-    """Gradients ~30 (peaked rows): their own 16-bit rounding passes; zeroed, 10 %-scaled
-    or biased gradients fail."""
+def _peaked_backward_case(seed):
+    """A small peaked problem (keys scaled by 8), its stored O / LSE, the oracle's gradients and
+    rounding scales, and an emulation of the 16-bit backward on the same stored O / LSE: dS and
+    P rounded to bfloat16 before their products, float64 sums, outputs rounded to bfloat16."""
+    bh, nq, nk, d = 1, 96, 600, 32
+    q = synth.to_storage(_rand((bh, nq, d), seed), "bf16")
+    k = synth.to_storage(8.0 * _rand((bh, nk, d), seed + 1), "bf16")
+    v = synth.to_storage(_rand((bh, nk, d), seed + 2), "bf16")
+    d_o = synth.to_storage(_rand((bh, nq, d), seed + 3), "bf16")
+    w = lambda x: synth.widen(x, "bf16")  # noqa: E731
+    bfr = lambda x: synth.widen(synth.to_storage(x, "bf16"), "bf16")  # noqa: E731
+    scale = 1 / math.sqrt(d)
+    o, lse = A.forward(w(q), w(k), w(v), scale)
+    o = bfr(o)
+    lse = lse.astype(np.float32).astype(np.float64)
+    ref = A.backward_slice(w(q), w(k), w(v), w(d_o), scale, 0, o=o, lse=lse, rounding_scales=True)
+    qb, kb, vb, dob = w(q)[0], w(k)[0], w(v)[0], w(d_o)[0]
+    p = np.exp(scale * qb @ kb.T - lse[0][:, None])
+    ds = bfr(p * (dob @ vb.T - np.sum(o[0] * dob, axis=-1, keepdims=True)))
+    emu = (bfr(scale * ds @ kb), bfr(scale * ds.T @ qb), bfr(bfr(p).T @ dob))
+    return ref, emu
+
+
+def test_gradient_tolerance_accepts_the_16bit_arithmetic():
+    """The bound accepts what rounding dS / P and the outputs to bfloat16 does to the gradients
+    of peaked rows, including dQ, whose terms cancel; a bound of 2e-2 + 2^-7 |ref| would not."""
     from tests.tolerance import check_16bit_grad
-    ref = _rand((256, 64), 91, scale=10.0)
-    rounded = synth.widen(synth.to_storage(ref, "bf16"), "bf16")
-    assert np.max(np.abs(rounded - ref)) > 2e-2  # beyond a fixed absolute 2e-2
-    check_16bit_grad(rounded, ref)
-    for bad in (np.zeros_like(ref), ref * 0.9, ref + 0.05 * np.std(ref)):
+    ref, emu = _peaked_backward_case(120)
+    for g, r, rss in zip(emu, ref[:3], ref[3:]):
+        check_16bit_grad(g, r, rss)
+    assert np.max(np.abs(ref[0])) > 1.0  # peaked: gradients well above the fixed bar
+    assert np.any(np.abs(emu[0] - ref[0]) > 2e-2 + 2.0 ** -7 * np.abs(ref[0]))
+
+
+def test_gradient_tolerance_rejects_errors():
+    """Zeroed, 10 %-scaled or biased gradients fail (the RMS guard), and so do a few single
+    elements off by 0.1 or by 5 %, although the rest of the array is exact."""
+    from tests.tolerance import check_16bit_grad
+    ref, emu = _peaked_backward_case(121)
+    dq, rss = ref[0], ref[3]
+    for bad in (np.zeros_like(dq), dq * 0.9, dq + 0.05 * np.std(dq)):
         with pytest.raises(AssertionError):
-            check_16bit_grad(bad, ref)
-    small = _rand((64, 32), 92, scale=1e-2)
+            check_16bit_grad(bad, dq, rss)
+    allowed = 2e-2 + 2.0 ** -8 * np.abs(dq) + 8 * 2.0 ** -8 * rss
+    small = np.argsort(allowed, axis=None)[:3]            # the three tightest elements
+    bad = emu[0].copy()
+    bad.flat[small] += 0.1
     with pytest.raises(AssertionError):
-        check_16bit_grad(np.zeros_like(small), small)
+        check_16bit_grad(bad, dq, rss)
+    big = np.unravel_index(int(np.argmax(np.abs(dq) / allowed)), dq.shape)
+    bad = emu[0].copy()
+    bad[big] = dq[big] * 1.05
+    assert abs(bad[big] - dq[big]) > allowed[big]           # a 5 % error there is beyond its allowance
+    with pytest.raises(AssertionError):
+        check_16bit_grad(bad, dq, rss)

@@ -5,8 +5,10 @@ service with a memory budget fixed at start-up) cannot hand fa2_backward a
 workspace; this entry point takes it from the library's fixed device scratch
 instead.  The test calls it through the C ABI twice in a row, on two different
 problems, and checks each result against fa2_backward with a caller-owned
-workspace, within the parity bar the other GPU tests use.  It also checks that
-a problem needing more than the fixed scratch is refused without a launch.
+workspace: bit for bit where that computation is deterministic (every gradient at
+head size 128, dK and dV at 64), within the parity bar the other GPU tests use for
+the one-pass dQ, whose float32 sums land in any order.  It also checks that a
+problem needing more than the fixed scratch is refused without a launch.
 
 The file name makes pytest collect it last.
 """
@@ -48,20 +50,28 @@ def _with_workspace(qd, kd, vd, o, dod, lse, scale):
 
 
 def test_noalloc_matches_backward_on_two_calls_in_a_row():
+    """Head size 128 runs the deterministic two passes, so the result must equal
+    fa2_backward's bit for bit; head size 64 runs the one-pass kernel, whose dQ sums land
+    in any order, so dQ is compared within the parity bar (dK and dV bit for bit).
+    The outputs sit between guard bands that must stay untouched."""
     torch = G.require_gpu()
     problems = [("noalloc/a", 3, 700, 520, 128, "bf16"), ("noalloc/b", 2, 129, 300, 64, "f16")]
     results = []
     for tag, bh, n_q, n_k, d, dtype in problems:
         args = _problem(tag, bh, n_q, n_k, d, dtype)
-        got = [torch.empty_like(args[0]), torch.empty_like(args[1]), torch.empty_like(args[2])]
-        binding.fa2_backward_noalloc(*args[:6], *got, args[6])
-        results.append((args, got))
+        got = [G.Guarded(tuple(x.shape), x.dtype) for x in args[:3]]
+        binding.fa2_backward_noalloc(*args[:6], *(g.t for g in got), args[6])
+        results.append((d, args, got))
     binding.fa2_device_status()
-    for args, got in results:
+    for d, args, got in results:
         want = _with_workspace(*args)
         torch.cuda.synchronize()
         for name, a, b in zip(("dQ", "dK", "dV"), got, want):
-            check_16bit(G.to_f64(a), G.to_f64(b), f"fa2_backward_noalloc {name}")
+            a.assert_intact(f"fa2_backward_noalloc {name}")
+            if d > 64 or name != "dQ":
+                assert torch.equal(a.t, b), f"fa2_backward_noalloc {name} differs from fa2_backward (head size {d})"
+            else:
+                check_16bit(G.to_f64(a.t), G.to_f64(b), f"fa2_backward_noalloc {name}")
 
 
 def test_noalloc_two_pass_when_the_accumulator_does_not_fit():
