@@ -133,6 +133,20 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _same_dtype(where, ref, **others):
+    """Every tensor of `others` has `ref`'s dtype (the library reads them all as one type)."""
+    for name, t in others.items():
+        if t.dtype != ref.dtype:
+            raise TypeError(f"{where}: {name} is {t.dtype}, expected {ref.dtype} like the other tensors")
+
+
+def _require_f32(where, **tensors):
+    import torch
+    for name, t in tensors.items():
+        if t.dtype != torch.float32:
+            raise TypeError(f"{where}: {name} must be float32, got {t.dtype}")
+
+
 def _dev(t, name, ndim=None):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
@@ -163,14 +177,13 @@ def fa2_backward_workspace_size(bh: int, n_q: int, n_k: int, head_dim: int, dtyp
 
 def fa2_backward(q, k, v, o, d_o, lse, dq, dk, dv, workspace, softmax_scale: float, stream=None) -> None:
     """dQ, dK, dV of attention; workspace is a CUDA uint8 tensor of fa2_backward_workspace_size bytes."""
-    import torch
     bh, n_q, d = q.shape
     n_k = k.shape[1]
     if (k.shape != (bh, n_k, d) or v.shape != k.shape or o.shape != q.shape or d_o.shape != q.shape
             or lse.shape != (bh, n_q) or dq.shape != q.shape or dk.shape != k.shape or dv.shape != k.shape):
         raise ValueError("inconsistent shapes")
-    if lse.dtype != torch.float32:
-        raise TypeError("lse is float32")
+    _same_dtype("fa2_backward", q, k=k, v=v, o=o, d_o=d_o, dq=dq, dk=dk, dv=dv)
+    _require_f32("fa2_backward", lse=lse)
     st = library().fa2_backward(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(o, "o", 3), _dev(d_o, "d_o", 3),
                                 _dev(lse, "lse", 2), _dev(dq, "dq", 3), _dev(dk, "dk", 3), _dev(dv, "dv", 3),
                                 _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
@@ -186,6 +199,8 @@ def fa2_backward_noalloc(q, k, v, o, d_o, lse, dq, dk, dv, softmax_scale: float,
     if (k.shape != (bh, n_k, d) or v.shape != k.shape or o.shape != q.shape or d_o.shape != q.shape
             or lse.shape != (bh, n_q) or dq.shape != q.shape or dk.shape != k.shape or dv.shape != k.shape):
         raise ValueError("inconsistent shapes")
+    _same_dtype("fa2_backward_noalloc", q, k=k, v=v, o=o, d_o=d_o, dq=dq, dk=dk, dv=dv)
+    _require_f32("fa2_backward_noalloc", lse=lse)
     st = library().fa2_backward_noalloc(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(o, "o", 3),
                                         _dev(d_o, "d_o", 3), _dev(lse, "lse", 2), _dev(dq, "dq", 3),
                                         _dev(dk, "dk", 3), _dev(dv, "dv", 3), bh, n_q, n_k, d, _dtype_code(q),
@@ -193,14 +208,25 @@ def fa2_backward_noalloc(q, k, v, o, d_o, lse, dq, dk, dv, softmax_scale: float,
     _check(st, "fa2_backward_noalloc")
 
 
-def _bwd_sizes(q, k, workspace):
+def _bwd_sizes(where, q, k, v, d_o, workspace, **outputs):
+    """Sizes of a backward stage call, after checking shapes and dtypes."""
     bh, n_q, d = q.shape
-    return bh, n_q, k.shape[1], d, workspace.numel() * workspace.element_size()
+    n_k = k.shape[1]
+    want = {"dq": q.shape, "dk": k.shape, "dv": k.shape}
+    if k.shape != (bh, n_k, d) or v.shape != k.shape or d_o.shape != q.shape or \
+            any(t.shape != want[name] for name, t in outputs.items()):
+        raise ValueError(f"{where}: inconsistent shapes")
+    _same_dtype(where, q, k=k, v=v, d_o=d_o, **outputs)
+    return bh, n_q, n_k, d, workspace.numel() * workspace.element_size()
 
 
 def fa2_backward_preprocess(o, d_o, lse, workspace, n_k: int, stream=None) -> None:
     """Stage 1 of the two-pass backward: fills the workspace (row sums D and the base-2 LSE)."""
     bh, n_q, d = o.shape
+    if d_o.shape != o.shape or lse.shape != (bh, n_q):
+        raise ValueError("inconsistent shapes")
+    _same_dtype("fa2_backward_preprocess", o, d_o=d_o)
+    _require_f32("fa2_backward_preprocess", lse=lse)
     st = library().fa2_backward_preprocess(_dev(o, "o", 3), _dev(d_o, "d_o", 3), _dev(lse, "lse", 2),
                                            _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
                                            bh, n_q, n_k, d, _dtype_code(o), _stream(stream))
@@ -209,7 +235,7 @@ def fa2_backward_preprocess(o, d_o, lse, workspace, n_k: int, stream=None) -> No
 
 def fa2_backward_dkdv(q, k, v, d_o, workspace, dk, dv, softmax_scale: float, stream=None) -> None:
     """Stage 2 of the two-pass backward: dK and dV (the pass over key tiles)."""
-    bh, n_q, n_k, d, wsb = _bwd_sizes(q, k, workspace)
+    bh, n_q, n_k, d, wsb = _bwd_sizes("fa2_backward_dkdv", q, k, v, d_o, workspace, dk=dk, dv=dv)
     st = library().fa2_backward_dkdv(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(d_o, "d_o", 3),
                                      _dev(workspace, "workspace"), wsb, _dev(dk, "dk", 3), _dev(dv, "dv", 3),
                                      bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
@@ -218,7 +244,7 @@ def fa2_backward_dkdv(q, k, v, d_o, workspace, dk, dv, softmax_scale: float, str
 
 def fa2_backward_dq(q, k, v, d_o, workspace, dq, softmax_scale: float, stream=None) -> None:
     """Stage 3 of the two-pass backward: dQ (the pass over query tiles)."""
-    bh, n_q, n_k, d, wsb = _bwd_sizes(q, k, workspace)
+    bh, n_q, n_k, d, wsb = _bwd_sizes("fa2_backward_dq", q, k, v, d_o, workspace, dq=dq)
     st = library().fa2_backward_dq(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(d_o, "d_o", 3),
                                    _dev(workspace, "workspace"), wsb, _dev(dq, "dq", 3),
                                    bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale), _stream(stream))
@@ -227,7 +253,7 @@ def fa2_backward_dq(q, k, v, d_o, workspace, dq, softmax_scale: float, stream=No
 
 def fa2_backward_passes(q, k, v, d_o, workspace, dq, dk, dv, softmax_scale: float, stream=None) -> None:
     """Stages 2 and 3 of the two-pass backward in one launch: dQ, dK and dV from a filled workspace."""
-    bh, n_q, n_k, d, wsb = _bwd_sizes(q, k, workspace)
+    bh, n_q, n_k, d, wsb = _bwd_sizes("fa2_backward_passes", q, k, v, d_o, workspace, dq=dq, dk=dk, dv=dv)
     st = library().fa2_backward_passes(_dev(q, "q", 3), _dev(k, "k", 3), _dev(v, "v", 3), _dev(d_o, "d_o", 3),
                                        _dev(workspace, "workspace"), wsb, _dev(dq, "dq", 3), _dev(dk, "dk", 3),
                                        _dev(dv, "dv", 3), bh, n_q, n_k, d, _dtype_code(q), float(softmax_scale),
@@ -261,6 +287,7 @@ def psa_fa2_forward(packed, o_lo, o_hi, lse, softmax_scale: float, stream=None) 
     _, bh, n, kd = packed.shape
     if o_lo.shape != (bh, n, kd) or o_hi.shape != o_lo.shape or lse.shape != (bh, n) or lse.dtype != torch.float32:
         raise ValueError("o_lo / o_hi are [BH, N, KD]; lse is float32 [BH, N]")
+    _same_dtype("psa_fa2_forward", packed, o_lo=o_lo, o_hi=o_hi)
     st = library().psa_fa2_forward(_dev(packed, "packed", 4), _dev(o_lo, "o_lo", 3), _dev(o_hi, "o_hi", 3),
                                    _dev(lse, "lse", 2), bh, n, kd, _dtype_code(packed), float(softmax_scale),
                                    _stream(stream))
@@ -277,6 +304,8 @@ def psa_fa2_backward(packed, o_lo, o_hi, d_o_lo, d_o_hi, lse, d_packed, workspac
             raise ValueError(f"{name} must be [BH, N, KD]")
     if d_packed.shape != packed.shape or lse.shape != (bh, n):
         raise ValueError("d_packed like packed; lse [BH, N]")
+    _same_dtype("psa_fa2_backward", packed, o_lo=o_lo, o_hi=o_hi, d_o_lo=d_o_lo, d_o_hi=d_o_hi, d_packed=d_packed)
+    _require_f32("psa_fa2_backward", lse=lse)
     st = library().psa_fa2_backward(_dev(packed, "packed", 4), _dev(o_lo, "o_lo", 3), _dev(o_hi, "o_hi", 3),
                                     _dev(d_o_lo, "d_o_lo", 3), _dev(d_o_hi, "d_o_hi", 3), _dev(lse, "lse", 2),
                                     _dev(d_packed, "d_packed", 4), _dev(workspace, "workspace"),
@@ -310,6 +339,7 @@ def psa_merge_attn_backward(d_merged, d_lo, d_hi, num_heads: int, stream=None) -
     b, c, h, w = d_merged.shape
     if d_lo.shape != d_hi.shape or d_lo.numel() * 2 != d_merged.numel():
         raise ValueError("d_lo and d_hi must together hold d_merged's elements")
+    _same_dtype("psa_merge_attn_backward", d_merged, d_lo=d_lo, d_hi=d_hi)
     st = library().psa_merge_attn_backward(_dev(d_merged, "d_merged", 4), _dev(d_lo, "d_lo"), _dev(d_hi, "d_hi"), c, h,
                                            w, b, num_heads, _dtype_code(d_merged), _stream(stream))
     _check(st, "psa_merge_attn_backward")

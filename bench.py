@@ -97,6 +97,29 @@ def env_rank():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the CPU baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                name = line.split(":", 1)[1].strip()
+                if name and not name.isdigit():
+                    vendor = next((ln.split(":", 1)[1].strip() for ln in out.splitlines()
+                                   if ln.split(":")[0].strip() == "Vendor ID"), "")
+                    return f"{vendor} {name}".strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -214,8 +237,8 @@ def cpu_oracle_sample(q, k, v, d_o, budget_s: float, block_rows: int = 1024):
             break
     dt = time.perf_counter() - t0
     flops = 3.5 * 4.0 * blocks * block_rows * N * D
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
-            "sample": f"{blocks} block(s) of {block_rows} query rows x {N} keys (HEAD_DIM {D}, {head + 1} head(s)): "
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": host_cores(), "cpu_model": cpu_model(),
+            "kind": "oracle", "sample": f"{blocks} block(s) of {block_rows} query rows x {N} keys (HEAD_DIM {D}, {head + 1} head(s)): "
                       f"forward+backward in float64 numpy ({dt:.1f} s); FLOPs counted as for the GPU step"}
 
 
@@ -248,7 +271,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample": sample},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -268,6 +292,25 @@ def reduce_max(x: float, dist=None, device=None) -> float:
 def job_throughput(world: int, step_flops: float, ms_step: float) -> float:
     """Whole-job TFLOP/s: every rank runs its own batch (weak scaling) in the max-over-ranks step time."""
     return world * step_flops / (ms_step * 1e-3) / 1e12
+
+
+def roofline_peak(elapsed_ms: float, clocks: dict):
+    """Which measured peak the roofline fraction divides by, and the rule that chose it.
+
+    The burst figure (a cuBLAS GEMM timed alone, at full clock) fits a timed region shorter
+    than a second or one whose SM clock stayed at its maximum; the sustained figure (the same
+    GEMM looped for seconds under the power cap, at a lower clock) fits a long region that
+    ran below the maximum clock."""
+    sm, smax = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    at_max = sm is not None and smax is not None and sm >= 0.99 * smax
+    if elapsed_ms < 1000.0:
+        return "burst", f"timed region {elapsed_ms:.0f} ms < 1 s: burst peak"
+    if at_max:
+        return "burst", f"median SM clock {sm:.0f} MHz = maximum {smax:.0f} MHz: burst peak"
+    if sm is None:
+        return "sustained", f"timed region {elapsed_ms:.0f} ms >= 1 s, no clock samples: sustained peak"
+    return "sustained", (f"timed region {elapsed_ms:.0f} ms >= 1 s at median SM clock {sm:.0f} MHz "
+                         f"< maximum {smax:.0f} MHz: sustained peak")
 
 
 def run_ours(args):
@@ -399,9 +442,12 @@ def run_ours(args):
     dominant = max(KERNEL_FLOPS, key=lambda n: per[n])
     achieved = KERNEL_FLOPS[dominant] / (per[dominant] * 1e-3) / 1e12
     traffic = load_traffic(dominant)
-    roofline = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_sustained"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sustained"], "traffic": traffic,
-                "peak_kind": f"bf16 dense, sustained ({pk['source']})",
+    peak_kind, peak_rule = roofline_peak(elapsed_ms, clocks)
+    peak = pk["bf16"] if peak_kind == "burst" else pk["bf16_sustained"]
+    roofline = {"kernel": dominant, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_kind": f"bf16 dense, {peak_kind} ({pk['source']})", "peak_rule": peak_rule,
+                "frac_burst": achieved / pk["bf16"], "frac_sustained": achieved / pk["bf16_sustained"],
                 "flops_per_launch": KERNEL_FLOPS[dominant]}
     bwd_ms = per["fa2_bwd_preprocess"] + per["fa2_bwd_passes"]
     components = {
@@ -425,7 +471,7 @@ def run_ours(args):
     # results (O, LSE, dQ, dK, dV, the merged C2PSA output) back.  Two buffer sets
     # and two copy streams let the copies of steps s+2 (in) and s (out) run while
     # step s+1 computes.
-    e2e_steps = max(4, args.steps // 5)
+    e2e_steps = max(50, args.steps // 5)
     sets.append(alloc_set(False))
     c2psa_graph(sets[1])
     out_names = ["o", "lse", "dq", "dk", "dv", "merged"]

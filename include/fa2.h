@@ -6,7 +6,9 @@
  * entry point allocates device memory, synchronises, or throws; each returns an
  * fa2_status.  Arguments are validated on the host before anything is launched:
  * a call that returns anything but FA2_OK has launched nothing, except
- * FA2_ERR_CUDA, which reports a failed launch.
+ * FA2_ERR_CUDA, which reports a failed launch.  FA2_OK means "enqueued": a kernel
+ * that later gives up a bounded wait on the device is reported only by
+ * fa2_device_status (see there), and leaves that call's outputs partly written.
  *
  * Common conventions
  *  - All tensor pointers are caller-owned DEVICE memory, contiguous, row-major,
@@ -348,11 +350,28 @@ fa2_status psa_extract_v_backward(const void* d_v, void* d_qkv, int32_t qkv_h, i
 /*
  * fa2_device_status - the watchdog word of the library's kernels.
  *
- * Every wait inside the library's kernels is bounded in time.  A kernel that
- * gives up a wait records it in a device-side word, drains the copies it has
- * in flight, frees its tensor memory and returns.  This call synchronises
- * `stream`, reads that word on the current device, clears it and returns
- * FA2_OK or FA2_ERR_DEVICE_TIMEOUT (FA2_ERR_CUDA if the synchronisation failed).
+ * Every wait of a kernel's threads on an mbarrier (a TMA copy landing, a tensor-core
+ * product completing, another warp's signal) is bounded in time: about one second of
+ * %globaltimer without progress.  A thread that gives up records it in a device-side
+ * word, raises its CTA's abort flag, drains the copies it has in flight and returns;
+ * the CTA frees its tensor memory and exits.  This call synchronises `stream`, reads
+ * that word on the current device, clears it and returns FA2_OK or
+ * FA2_ERR_DEVICE_TIMEOUT (FA2_ERR_CUDA if the synchronisation failed).
+ *
+ * What this does NOT cover, stated plainly:
+ *  - A launch call (fa2_forward, fa2_backward, ...) returns FA2_OK once its kernels
+ *    are enqueued.  If a wait later gives up on the device, the outputs of that call
+ *    are left partly written (the CTAs that gave up skip their remaining work) while
+ *    the launch status stayed FA2_OK: only fa2_device_status reports it.  Callers that
+ *    need to know must call it (it synchronises) before trusting the outputs.
+ *  - The warp that issues the tensor-core products waits on named barriers
+ *    (barrier.sync), which have no time limit.  They complete because every producer
+ *    arrives exactly once per event even after a failed wait of its own (the failure
+ *    skips work, not arrivals); the bound on the whole kernel therefore rests on the
+ *    producers' bounded waits, not on a limit of the issuer's own.
+ *  - The limit counts wall-clock time, including time the context spends descheduled
+ *    on a shared or time-sliced GPU; a long preemption can trip it with no fault in
+ *    the kernel.
  */
 fa2_status fa2_device_status(void* stream);
 

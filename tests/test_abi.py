@@ -108,3 +108,39 @@ def test_binding_fails_loudly_without_library(tmp_path):
             binding.library(str(tmp_path / "missing.so"))
         finally:
             binding._lib = saved
+
+
+def test_binding_rejects_mixed_dtypes(lib):
+    """Every wrapper that hands the library one dtype code for several tensors checks that
+    they share that dtype (the library would otherwise read one type as another)."""
+    torch = pytest.importorskip("torch")
+    bh, n, d = 1, 16, 32
+    bf = lambda *s: torch.zeros(s, dtype=torch.bfloat16)  # noqa: E731
+    hf = lambda *s: torch.zeros(s, dtype=torch.float16)  # noqa: E731
+    f32 = lambda *s: torch.zeros(s, dtype=torch.float32)  # noqa: E731
+    q, k, v, o, do = (bf(bh, n, d) for _ in range(5))
+    lse, ws = f32(bh, n), torch.zeros(4096, dtype=torch.uint8)
+    odd = hf(bh, n, d)
+    with pytest.raises(TypeError):
+        binding.fa2_backward(q, k, v, o, do, lse, odd, bf(bh, n, d), bf(bh, n, d), ws, 0.17)
+    with pytest.raises(TypeError):
+        binding.fa2_backward(q, k, odd, o, do, lse, bf(bh, n, d), bf(bh, n, d), bf(bh, n, d), ws, 0.17)
+    with pytest.raises(TypeError):
+        binding.fa2_backward(q, k, v, o, do, f32(bh, n).half(), bf(bh, n, d), bf(bh, n, d), bf(bh, n, d), ws, 0.17)
+    with pytest.raises(TypeError):
+        binding.fa2_backward_noalloc(q, k, v, odd, do, lse, bf(bh, n, d), bf(bh, n, d), bf(bh, n, d), 0.17)
+    with pytest.raises(TypeError):
+        binding.fa2_backward_preprocess(o, odd, lse, ws, n)
+    with pytest.raises(TypeError):
+        binding.fa2_backward_dkdv(q, k, v, do, ws, odd, bf(bh, n, d), 0.17)
+    with pytest.raises(TypeError):
+        binding.fa2_backward_dq(q, k, v, odd, ws, bf(bh, n, d), 0.17)
+    with pytest.raises(TypeError):
+        binding.fa2_backward_passes(q, k, v, do, ws, bf(bh, n, d), bf(bh, n, d), odd, 0.17)
+    packed = bf(4, bh, n, d)
+    with pytest.raises(TypeError):
+        binding.psa_fa2_forward(packed, bf(bh, n, d), odd, lse, 0.17)
+    with pytest.raises(TypeError):
+        binding.psa_fa2_backward(packed, o, o, do, odd, lse, bf(4, bh, n, d), ws, 0.17)
+    with pytest.raises(TypeError):
+        binding.psa_merge_attn_backward(bf(1, 2 * d, 4, 4), hf(1, 16, d), bf(1, 16, d), 1)

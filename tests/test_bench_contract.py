@@ -41,3 +41,14 @@ def test_our_arm_fails_loudly_without_a_gpu():
     r = _run("--steps", "1", "--warmup", "3", timeout=120)
     assert r.returncode != 0
     assert not [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+
+
+def test_roofline_peak_rule():
+    """The roofline fraction divides by the burst peak for a short timed region or one held at
+    the maximum SM clock, by the sustained peak for a long region below it."""
+    import bench
+    assert bench.roofline_peak(57.0, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})[0] == "burst"
+    assert bench.roofline_peak(57.0, {"unavailable": "no samples"})[0] == "burst"
+    assert bench.roofline_peak(1500.0, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})[0] == "burst"
+    assert bench.roofline_peak(1500.0, {"sm_mhz": 1942.0, "sm_max_mhz": 2070.0})[0] == "sustained"
+    assert bench.roofline_peak(1500.0, {"unavailable": "no samples"})[0] == "sustained"
