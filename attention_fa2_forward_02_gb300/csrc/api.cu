@@ -94,6 +94,18 @@ bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, co
 
 bool watchdog_word(unsigned int** out) { return status_word(out); }
 
+int sm_count() {
+    static std::atomic<int> counts[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int n = counts[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+        counts[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

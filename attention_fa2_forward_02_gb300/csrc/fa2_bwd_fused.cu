@@ -1,5 +1,5 @@
 // fa2_bwd_fused.cu - attention backward in one pass over key tiles, on the
-// sm_103a tensor cores (tcgen05 + TMEM + TMA).
+// sm_103a tensor cores (tcgen05 + TMEM + TMA), for kernel head sizes 32 and 64.
 //
 // What it computes: the gradients of "vision-rs 0.1.1 flash_attn2.rs", kernels
 // flash_attention2_backward_dq and flash_attention2_backward_dkv:
@@ -7,37 +7,49 @@
 //   dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
 // That page computes dQ in a pass of its own over query rows, which forms S and
 // dP a second time.  Here the pass over key tiles also forms the product
-// dS_(i,j) K_j of the query tile i it is visiting and adds it, with float32
-// vector reductions, into a dQ accumulator in the workspace; a last small
-// kernel scales the sums and rounds them into dq.  Each dQ element is then a
-// float32 sum of per-key-tile float32 partial sums, added in whatever order the
-// CTAs reach it (not bit-reproducible from run to run).
+// dS_(i,j) K_j of the query tile i it is visiting and adds it into a float32 dQ
+// accumulator in the workspace; a last small kernel scales the sums and rounds
+// them into dq.  Each dQ element is then a float32 sum of per-key-tile float32
+// partial sums, added in whatever order the CTAs reach it (not bit-reproducible
+// from run to run).
 //
 // Per CTA: one 128-key tile (K, V resident in shared memory), looping over the
 // query tiles of its head starting at tile (key tile index mod n_qt), so that the
 // CTAs of a head add into different query tiles at any one time.
 // Tensor memory (512 columns x 128 lanes):
 //   [0, 128)      S^T = K Q^T; then P^T, 16-bit, in columns [32, 96)
-//   [128, 256)    dP^T = V dO^T; then dS^T, 16-bit, in [160, 224); then dQ_i (D columns)
-//   [256, 256+D)  dV      [256+D, 256+2D)  dK
+//   [128, 256)    dP^T = V dO^T; then dS^T, 16-bit, in [160, 224)
+//   [256, 256+D) dV    [256+D, 256+2D) dK    [256+2D+b*D, 256+3D+b*D) dQ of query
+//   tiles with i % 2 == b: two buffers, so that the next dP^T need not wait for the
+//   current dQ to be read out.
 // dS itself (queries x keys, the A operand of the dQ product) is written by the
-// elementwise warps into shared memory: over the dO tile of the stage (D = 128:
-// dV and dP^T, the only readers of dO, have completed by then) or into a
-// buffer of its own (D < 128, where a dO tile is too small).
+// elementwise warps into a shared-memory buffer of its own.
+//
+// The dQ additions leave the elementwise warps' path: each warp copies its 32 rows x
+// D/2 columns of a finished dQ tile out of tensor memory into a 4 KB (D = 64) block of
+// shared memory and one of its lanes hands that block to the TMA engine as one bulk
+// float32 reduction into the accumulator (cp.reduce.async.bulk ... add.f32); the engine
+// performs the additions in L2 while the warps go on.  Before the warp rewrites its
+// block for the next tile, that lane waits until the engine has read the previous one.
+// The accumulator is laid out per (head, query tile) as [4 quarters][2 halves][D/8]
+// [32 rows][4 floats] (quarter = row / 32, half = column / (D/2)), so that each warp's
+// block is one contiguous run and the rounding kernel still reads 512 contiguous bytes
+// per warp.
 //
 // MMA order per query tile i (one thread issues, the tensor core runs in order):
-//   [e1(i)] dV += P^T(i) dO(i);  [dq_read(i-1)] dP^T(i) -> dp_full;
+//   [e1(i)] dV += P^T(i) dO(i);  dP^T(i) -> dp_full;
 //   [stage i+1] S^T(i+1) -> s_full;  [e2(i)] dK += dS^T(i) Q(i);  dQ_i = dS(i) K -> dq_full, empty
-// The bracketed events reach the issuing warp as named barriers: e1, dq_read, e2 from
-// the elementwise warps, "stage loaded" from a relay warp (warp 10) that waits on the
-// TMA barriers.
+// The bracketed events reach the issuing warp as named barriers: e1, e2 from the
+// elementwise warps, "stage loaded" from a relay warp (warp 10) that waits on the
+// TMA barriers.  dQ_i goes to buffer i % 2, last written by dQ_(i-2), which the warps
+// read out before their e2(i-1) arrival: no barrier of its own.
 // Elementwise warps per query tile i:
-//   [s_full] P^T(i) -> e1;  [dq_full(i-1)] read dQ_(i-1), reduce into the
-//   accumulator -> dq_read;  [dp_full] dS^T(i) into TMEM, dS(i) into shared memory -> e2
-// so the warps compute P under dK / dQ, reduce dQ under dV and compute dS under
+//   [s_full] P^T(i) -> e1;  [dq_full(i-1)] dQ_(i-1) to shared memory, bulk reduction;
+//   [dp_full] dS^T(i) into TMEM, dS(i) into shared memory -> e2
+// so the warps compute P under dK / dQ, stage dQ under dV and dP^T and compute dS under
 // S^T, while the tensor core runs dV, dP^T, S^T, dK, dQ back to back.
 // In-order execution of the tensor core is what makes the column reuse safe: an
-// MMA that overwrites columns another reads (S^T(i+1) over P^T(i), dQ_i over
+// MMA that overwrites columns another reads (S^T(i+1) over P^T(i), dP^T(i+1) over
 // dS^T(i)) is always issued after the MMA that reads them.
 #include "bwd_common.cuh"
 #include "internal.h"
@@ -47,27 +59,29 @@ namespace {
 
 template <int D>
 struct FusedCfg : Tile16<D> {
-    static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);
+    static_assert(D == 32 || D == 64, "the one-pass kernel serves head sizes up to 64");
+    static constexpr int kStages = D == 64 ? 3 : 4;
     static constexpr int kTile = BT * D * 2;
     static constexpr int kDsBytes = BT * BT * 2;
-    static constexpr bool kDsInDo = kTile == kDsBytes;  // D = 128: dS over the stage's dO tile
-    // K, V resident; per stage Q_i, dO_i, lse2_i, delta_i; then (D < 128) the dS buffer; barriers
+    // per elementwise warp: 32 rows x D/2 float32 of a dQ tile, staged for the bulk reduction
+    static constexpr int kDqBlockBytes = 32 * (D / 2) * 4;
+    // K, V resident; per stage Q_i, dO_i, lse2_i, delta_i; the dS buffer; the dQ blocks; barriers
     static constexpr int kStage = 2 * kTile + 2 * BT * 4;
     static constexpr int kSmemStages = 2 * kTile;
     static constexpr int kSmemDs = kSmemStages + kStages * kStage;
-    static constexpr int kSmemBar = kSmemDs + (kDsInDo ? 0 : kDsBytes);
+    static constexpr int kSmemDq = kSmemDs + kDsBytes;
+    static constexpr int kSmemBar = kSmemDq + 8 * kDqBlockBytes;
     static constexpr int kNumBars = 2 * kStages + kBwdBars;
     static constexpr int kSmemBytes = kSmemBar + kNumBars * 8 + 16 + 1024;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(kStage % 1024 == 0 && kSmemDs % 1024 == 0, "operand alignment");
-    static_assert(256 + 2 * D <= (int)kBwdTmemCols, "tensor memory budget");
+    static constexpr uint32_t kDqCol = 256 + 2 * D;  // the two dQ buffers
+    static_assert(kDqCol + 2 * D <= kBwdTmemCols, "tensor memory budget");
     static constexpr int kThreads = kBwdThreads + 32;  // + the TMA relay warp
 };
 
-// Named barriers of this kernel besides kNbE1 / kNbE2: dQ of the previous query tile
-// read out of tensor memory, and stage s loaded.
-constexpr uint32_t kNbDqRead = 3;
-__host__ __device__ constexpr uint32_t nb_fstage(int s) { return 4 + (uint32_t)s; }
+// Named barriers of this kernel besides kNbE1 / kNbE2: stage s loaded.
+__host__ __device__ constexpr uint32_t nb_fstage(int s) { return 3 + (uint32_t)s; }
 
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
@@ -100,7 +114,7 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
     auto stage_do = [&](int s) { return stage_q(s) + C::kTile; };
     auto stage_l2 = [&](int s) { return stage_q(s) + 2 * C::kTile; };
     auto stage_dl = [&](int s) { return stage_l2(s) + BT * 4; };
-    auto ds_smem = [&](int s) { return C::kDsInDo ? stage_do(s) : base + C::kSmemDs; };
+    const uint32_t ds_smem = base + C::kSmemDs;
 
     if (threadIdx.x == 0) init_bars(bars, abort_flag, 1);
     if (warp == 1) {
@@ -157,7 +171,7 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
         const uint64_t dk0 = C::kmajor(k_smem, 0, BT), dv0 = C::kmajor(v_smem, 0, BT);
         const uint64_t dq0 = C::kmajor(stage_q(0), 0, BT), ddo0 = C::kmajor(stage_do(0), 0, BT);
         const uint64_t mq0 = C::mnmajor(stage_q(0), 0, BT), mdo0 = C::mnmajor(stage_do(0), 0, BT);
-        const uint64_t mk0 = C::mnmajor(k_smem, 0, BT), mds0 = DsTile::mnmajor(ds_smem(0), 0, BT);
+        const uint64_t mk0 = C::mnmajor(k_smem, 0, BT), mds0 = DsTile::mnmajor(ds_smem, 0, BT);
         auto st_off = [&](int s) { return (uint64_t)((s * C::kStage) >> 4); };
         auto issue_st = [&](int s) {  // S^T = K Q^T
             const uint64_t b = dq0 + st_off(s);
@@ -187,16 +201,11 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
                 for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
                     mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), b + (uint64_t)(kk * C::kAtomRowBytes),
                            idesc_g, (i > 0 || kk > 0));
-            }
-            __syncwarp();
-            if (i > 0) nb_sync(kNbDqRead, kNbElem);  // dP^T overwrites the columns of dQ_(i-1)
-            if (lane == 0) {
-                if (i > 0) tc_fence_after();
-                const uint64_t b = ddo0 + st_off(s);
+                const uint64_t bd = ddo0 + st_off(s);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
                     const uint64_t o = (uint64_t)(C::koff(kk, BT) >> 4);
-                    mma_ss(tmem + 128u, dv0 + o, b + o, idesc_s, kk > 0);
+                    mma_ss(tmem + 128u, dv0 + o, bd + o, idesc_s, kk > 0);
                 }
                 mma_commit(bars.dp_full());
             }
@@ -218,10 +227,9 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
                 for (int kk = 0; kk < BT / 16; ++kk)  // dK += dS^T Q
                     mma_ts(tmem + 256u + (uint32_t)D, tmem + 128u + kPackedCol + (uint32_t)(kk * 8),
                            b + (uint64_t)(kk * C::kAtomRowBytes), idesc_g, (i > 0 || kk > 0));
-                const uint64_t a = mds0 + (C::kDsInDo ? st_off(s) : 0);
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk)  // dQ_i = dS K (keys are the reduction dimension)
-                    mma_ss(tmem + 128u, a + (uint64_t)(kk * DsTile::kAtomRowBytes),
+                    mma_ss(tmem + C::kDqCol + (uint32_t)((i & 1) * D), mds0 + (uint64_t)(kk * DsTile::kAtomRowBytes),
                            mk0 + (uint64_t)(kk * C::kAtomRowBytes), idesc_q, kk > 0);
                 mma_commit(bars.dq_full());
                 mma_commit(bars.empty(s));
@@ -251,48 +259,35 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
         const int r = quarter * 32 + lane;  // key row (score tiles) and query row (dQ tile) of this thread
+        const uint32_t t_dq0 = tmem + lane_off + C::kDqCol + (uint32_t)(half * (D / 2));
         const bool key_valid = k0 + r < n_k;
         const float2 scale2 = make_float2(scale_log2, scale_log2);
-        // Reads dQ of the i-th visited query tile out of TMEM and adds it into the
-        // accumulator, laid out per (bh, query tile) as [D/4][128 rows][4] floats so
-        // that a warp's 16-byte reductions cover 512 contiguous bytes.
-        // A failed wait skips the work of this and later tiles, not the arrivals (the
-        // last tile's dQ read is awaited by no MMA and signals nothing).
+        // dQ of the i-th visited query tile: this warp's 32 rows x D/2 columns out of TMEM
+        // into its block of shared memory, then one bulk float32 reduction of the block into
+        // the accumulator by lane 0 (see the layout above). A failed wait skips the work.
+        const uint32_t dq_block = base + C::kSmemDq + (uint32_t)((warp - 2) * C::kDqBlockBytes);
         auto reduce_dq = [&](int i, bool ok) -> bool {
-            if (!(ok && warp_wait(bars.dq_full(), i & 1, wd))) {
-                if (i + 1 < n_qt) nb_arrive(kNbDqRead, kNbElem);
-                return false;
-            }
+            if (!(ok && warp_wait(bars.dq_full(), i & 1, wd))) return false;
             tc_fence_after();
-            float4* tile = reinterpret_cast<float4*>(dq_acc) + ((size_t)bh * n_qt + qtile(i)) * (size_t)(D / 4) * BT + r;
-            if constexpr (D >= 64) {
+            uint32_t v[D / 2];
+            if constexpr (D == 64) tmem_ld32(t_dq0 + (uint32_t)((i & 1) * D), v);
+            else tmem_ld16(t_dq0 + (uint32_t)((i & 1) * D), v);
+            if (lane == 0) bulk_wait_group_read0();  // the engine has read this block's previous contents
+            tmem_ld_wait();
+            reg_fence(v);
+            __syncwarp();
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    const int col0 = half * (D / 2) + 32 * c;
-                    uint32_t v[32];
-                    tmem_ld32(t_dp + (uint32_t)col0, v);
-                    tmem_ld_wait();
-                    reg_fence(v);
-#pragma unroll
-                    for (int g = 0; g < 8; ++g)
-                        atomicAdd(tile + (size_t)(col0 / 4 + g) * BT,
-                                  make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                                              __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
-                }
-            } else {
-                const int col0 = half * (D / 2);
-                uint32_t v[16];
-                tmem_ld16(t_dp + (uint32_t)col0, v);
-                tmem_ld_wait();
-                reg_fence(v);
-#pragma unroll
-                for (int g = 0; g < 4; ++g)
-                    atomicAdd(tile + (size_t)(col0 / 4 + g) * BT,
-                              make_float4(__uint_as_float(v[4 * g]), __uint_as_float(v[4 * g + 1]),
-                                          __uint_as_float(v[4 * g + 2]), __uint_as_float(v[4 * g + 3])));
-            }
+            for (int g = 0; g < D / 8; ++g)  // [D/8][32 rows][4 floats]
+                st_shared_v4(dq_block + (uint32_t)((g * 32 + lane) * 16), v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
+            fence_proxy_async_smem();
             tc_fence_before();
-            if (i + 1 < n_qt) nb_arrive(kNbDqRead, kNbElem);
+            __syncwarp();
+            if (lane == 0) {
+                float* tile = dq_acc + ((size_t)bh * n_qt + qtile(i)) * (size_t)(BT * D) +
+                              (size_t)(quarter * 2 + half) * (C::kDqBlockBytes / 4);
+                bulk_reduce_add_f32(tile, dq_block, C::kDqBlockBytes);
+                bulk_commit_group();
+            }
             return true;
         };
         bool ok = true;
@@ -300,7 +295,6 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
             const int s = i % S;
             if (!(ok = ok && warp_wait(bars.s_full(), i & 1, wd) && warp_wait(bars.full(s), (i / S) & 1, wd))) {
                 nb_arrive(kNbE1, kNbElem);
-                if (i > 0) nb_arrive(kNbDqRead, kNbElem);
                 nb_arrive(kNbE2, kNbElem);
                 continue;
             }
@@ -340,7 +334,7 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             nb_arrive(kNbE1, kNbElem);
-            // the previous query tile's dQ, while dV(i) runs
+            // the previous query tile's dQ, while dV(i) and dP^T(i) run
             if (i > 0) ok = reduce_dq(i - 1, ok);
             // step 2: dS^T = P^T * (dP^T - D) into TMEM (for dK) and as dS into shared memory
             // (for dQ); both owned chunks read before either is overwritten.  Rows of keys
@@ -350,7 +344,7 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
                 continue;
             }
             tc_fence_after();
-            const uint32_t ds_row = ds_smem(s) + (uint32_t)r * 128u;  // row r of the [keys, queries] tile
+            const uint32_t ds_row = ds_smem + (uint32_t)r * 128u;  // row r of the [keys, queries] tile
             const uint32_t swz = (uint32_t)(r & 7);                   // 128-byte swizzle of that row
             uint32_t rp[2][32];
             tmem_ld32(t_dp + 32u * owned_chunk(half, 0), rp[0]);
@@ -387,6 +381,8 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
             nb_arrive(kNbE2, kNbElem);
         }
         if (n_qt > 0) ok = reduce_dq(n_qt - 1, ok);
+        if (lane == 0) bulk_wait_group0();  // this warp's reductions complete before the CTA exits
+        __syncwarp();
         if (ok) ok = warp_wait(bars.done(), 0, wd);
         if (ok) {
             tc_fence_after();
@@ -416,7 +412,8 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
 }
 
 // dq[bh, row, :d_act] = scale * the accumulated sums, rounded to the 16-bit dtype.
-// One thread per query row; a warp's loads cover 512 contiguous bytes.
+// One thread per query row; for each 4-column group a warp's loads cover 512
+// contiguous bytes of the [quarter][half][D/8][32 rows][4] tile layout.
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(BT)
     bwd_dq_round_kernel(const float4* __restrict__ dq_acc, void* __restrict__ dq, int n_q, int d_act, float scale) {
@@ -424,12 +421,20 @@ __global__ void __launch_bounds__(BT)
     const int row = qt * BT + r;
     if (row >= n_q) return;
     const int n_qt = gridDim.x;
-    const float4* tile = dq_acc + ((size_t)bh * n_qt + qt) * (size_t)(D / 4) * BT + r;
+    const float4* tile = dq_acc + ((size_t)bh * n_qt + qt) * (size_t)(D / 4) * BT;
     uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(dq) + ((size_t)bh * n_q + row) * d_act);
+    const int quarter = r >> 5, lane = r & 31;
 #pragma unroll
-    for (int g = 0; g < D / 8; ++g) {
+    for (int g = 0; g < D / 8; ++g) {  // output columns [8g, 8g + 8): float4 groups 2g and 2g + 1
         if (8 * g >= d_act) break;
-        const float4 a = tile[(size_t)(2 * g) * BT], b = tile[(size_t)(2 * g + 1) * BT];
+        float4 ab[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int c4 = 2 * g + u;                          // 4-column group of the row
+            const int half = c4 / (D / 8), gi = c4 % (D / 8);  // its half and group within the half
+            ab[u] = tile[(size_t)((quarter * 2 + half) * (D / 8) + gi) * 32 + lane];
+        }
+        const float4 a = ab[0], b = ab[1];
         out[g] = make_uint4(pack2<kBf16>(a.x * scale, a.y * scale), pack2<kBf16>(a.z * scale, a.w * scale),
                             pack2<kBf16>(b.x * scale, b.y * scale), pack2<kBf16>(b.z * scale, b.w * scale));
     }
@@ -471,8 +476,7 @@ cudaError_t launch_bwd_fused(const BwdParams& p, cudaStream_t stream) {
     switch (pad_head_dim(p.d)) {
         case 32: return bf ? fused_impl<32, true>(p, stream, 36) : fused_impl<32, false>(p, stream, 37);
         case 64: return bf ? fused_impl<64, true>(p, stream, 38) : fused_impl<64, false>(p, stream, 39);
-        case 128: return bf ? fused_impl<128, true>(p, stream, 40) : fused_impl<128, false>(p, stream, 41);
-        default: return cudaErrorInvalidValue;
+        default: return cudaErrorInvalidValue;  // head sizes above 64 run the two-pass kernels
     }
 }
 

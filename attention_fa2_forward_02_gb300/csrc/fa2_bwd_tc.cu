@@ -928,10 +928,13 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
 // about 5.6 us on GB300) is partly hidden behind the next tile's work. Measured on
 // GB300 (bf16, head size 128, BH = 32): N_q = 1024, N_k = 32768 1.353 -> 1.270 ms with
 // 4 key tiles per CTA (1.301 with 8); N_q = N_k = 8192 keeps 1 (2 read 2.345 against
-// 2.303 ms).
-static int dkdv_tiles_per_cta(int n_qt) {
-    const int m = (32 + n_qt - 1) / n_qt;
-    return m < 1 ? 1 : (m > 8 ? 8 : m);
+// 2.303 ms). Fewer key tiles per CTA where that would leave fewer dK/dV CTAs than SMs
+// (few heads): there the grid's parallelism matters more than the hidden fixed cost.
+static int dkdv_tiles_per_cta(int n_qt, int n_kt, int64_t bh, int sms) {
+    int m = (32 + n_qt - 1) / n_qt;
+    m = m < 1 ? 1 : (m > 8 ? 8 : m);
+    while (m > 1 && bh * (int64_t)((n_kt + m - 1) / m) < sms) --m;
+    return m;
 }
 
 template <int D, bool kBf16, int kNV>
@@ -970,7 +973,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         constexpr int smem = C::kSmemDkv > C::kSmemDq ? C::kSmemDkv : C::kSmemDq;
         e = ensure_smem_limit(reinterpret_cast<const void*>(both), smem, 42 + (slot - 16) / 2);  // slots 42..51
         if (e != cudaSuccess) return e;
-        const int m = C::kNamed ? dkdv_tiles_per_cta(n_qt) : 1;
+        const int m = C::kNamed ? dkdv_tiles_per_cta(n_qt, n_kt, p.bh, sm_count()) : 1;
         const int n_kc = (n_kt + m - 1) / m;
         both<<<dim3((unsigned)(n_kc + n_qt), (unsigned)p.bh, 1), C::kThreads, smem, stream>>>(
             tq, tk, tv, tdo, tv2, tdo2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),

@@ -108,6 +108,9 @@ bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, co
 // Device address of the watchdog word on the current device (looked up once per device).
 bool watchdog_word(unsigned int** out);
 
+// Number of SMs of the current device (looked up once per device; 148 if the query fails).
+int sm_count();
+
 // Raises the dynamic shared-memory limit of `func` on the current device once.
 cudaError_t ensure_smem_limit(const void* func, int bytes, int slot);
 
