@@ -96,6 +96,34 @@ __device__ __forceinline__ void store_row_chunk(void* base, size_t row, int d_ac
     }
 }
 
+// Gradient tiles written by TMA stores. Each elementwise warp owns 32 rows (its TMEM lane
+// quarter) of a 128-row tile; per 32-column chunk it packs its rows into its own 2 KB slab
+// of shared memory (32 rows x 64 bytes, the box of the output's tensor map) and one lane
+// stores the box. Plain per-thread stores would write a 16-byte piece of a different row
+// (a different cache line) per lane and instruction; the TMA writes whole rows. The map's
+// bounds clip the rows past the last one and the columns past the head size.
+constexpr int kOutSlabBytes = 32 * 32 * 2;
+constexpr int kOutStageBytes = 8 * kOutSlabBytes;  // one slab per elementwise warp
+
+template <bool kBf16>
+__device__ __forceinline__ void store_chunk_tma(const CUtensorMap* map, uint32_t slab, int col0, int row0, int n_rows,
+                                                int d_act, int bh, const uint32_t (&r)[32], float mul) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack2<kBf16>(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    if (lane_id() == 0) bulk_wait_group_read0();  // the previous store has read the slab
+    __syncwarp();
+    const uint32_t row = slab + lane_id() * 64u;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) st_shared_v4(row + 16u * w, pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane_id() == 0 && row0 < n_rows && col0 < d_act) {
+        tma_store_3d(map, slab, col0, row0, bh);
+        bulk_commit_group();
+    }
+}
+
 // The two 32-column chunks an elementwise warp owns, in the order that lets it
 // write 16-bit results at kPackedCol without overwriting a column it has not read.
 __device__ __forceinline__ int owned_chunk(int half, int cc) { return 2 * half + (half == 0 ? 1 - cc : cc); }

@@ -87,6 +87,7 @@ template <int D, bool kBf16>
 __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
     bwd_fused_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                      const float* __restrict__ lse2, const float* __restrict__ delta, float* __restrict__ dq_acc,
                      void* __restrict__ dk, void* __restrict__ dv, int n_q, int n_k, int n_q_pad, int d_act, float scale,
                      float scale_log2, unsigned int* status) {
@@ -386,11 +387,9 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
         if (ok) ok = warp_wait(bars.done(), 0, wd);
         if (ok) {
             tc_fence_after();
-            const int key = k0 + r;
-            const size_t row = (size_t)bh * n_k + key;
-            // half 0 writes dV, half 1 writes dK (scaled)
+            // half 0 writes dV, half 1 writes dK (scaled); the warp's dQ block (its bulk
+            // reductions complete) serves as the slab of the TMA stores
             const uint32_t src = tmem + lane_off + 256u + (uint32_t)(half * D);
-            void* dst = half ? dk : dv;
             const float mul = half ? scale : 1.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -398,8 +397,10 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
                 tmem_ld32(src + 32u * c, v);
                 tmem_ld_wait();
                 reg_fence(v);
-                store_row_chunk<kBf16>(dst, row, d_act, c, v, mul, key < n_k);
+                store_chunk_tma<kBf16>(half ? &tm_dk : &tm_dv, dq_block, 32 * c, k0 + quarter * 32, n_k, d_act, bh, v, mul);
             }
+            if (lane == 0) bulk_wait_group0();  // the stores complete before the CTA exits
+            __syncwarp();
         }
     }
 
@@ -448,20 +449,22 @@ cudaError_t fused_impl(const BwdParams& p, cudaStream_t stream, int slot) {
     if (e != cudaSuccess) return e;
     const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdk, tdv;
     // maps over the true head dimension p.d <= D: TMA fills the box columns past it with zeros
     const uint64_t d = (uint64_t)p.d;
     if (!encode_tmap_3d(&tq, dt, 2, p.q, d, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
         !encode_tmap_3d(&tdo, dt, 2, p.d_o, d, (uint64_t)p.n_q, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
         !encode_tmap_3d(&tk, dt, 2, p.k, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
-        !encode_tmap_3d(&tv, dt, 2, p.v, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
+        !encode_tmap_3d(&tv, dt, 2, p.v, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
+        !encode_tmap_3d(&tdk, dt, 2, p.dk, d, (uint64_t)p.n_k, (uint64_t)p.bh, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_3d(&tdv, dt, 2, p.dv, d, (uint64_t)p.n_k, (uint64_t)p.bh, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     auto kern = bwd_fused_kernel<D, kBf16>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot);
     if (e != cudaSuccess) return e;
     const int n_qt = (int)((p.n_q + BT - 1) / BT);
     kern<<<dim3((unsigned)((p.n_k + BT - 1) / BT), (unsigned)p.bh, 1), C::kThreads, C::kSmemBytes, stream>>>(
-        tq, tk, tv, tdo, p.lse2, p.delta, p.dq_acc, p.dk, p.dv, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.d, p.scale,
+        tq, tk, tv, tdo, tdk, tdv, p.lse2, p.delta, p.dq_acc, p.dk, p.dv, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad, p.d, p.scale,
         p.scale * kLog2e, p.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_dq_round_kernel<D, kBf16><<<dim3((unsigned)n_qt, (unsigned)p.bh, 1), BT, 0, stream>>>(

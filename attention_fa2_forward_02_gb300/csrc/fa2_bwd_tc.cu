@@ -92,12 +92,14 @@ struct BwdCfg : Tile16<D> {
     static_assert(256 + (kNV + 1) * D <= (int)kBwdTmemCols, "tensor memory budget");
     // dK/dV kernel: K, V (and V2) resident; per stage Q_i, dO_i (and dO2_i), lse2_i, delta_i
     static constexpr int kStageDkv = (1 + kNV) * kTile + 2 * BT * 4;
-    static constexpr int kDkvBar = (1 + kNV) * kTile + kStages * kStageDkv;
+    static constexpr int kDkvOut = (1 + kNV) * kTile + kStages * kStageDkv;  // the warps' output slabs
+    static constexpr int kDkvBar = kDkvOut + kOutStageBytes;
     // dQ kernel: Q, dO (and dO2) live in tensor memory (copied once per CTA); per
     // stage K_j, V_j (and V2_j) in shared memory
     static constexpr int kStagesDq = D == 128 ? 3 : 4;
     static constexpr int kStageDq = (1 + kNV) * kTile;
-    static constexpr int kDqBar = kStagesDq * kStageDq;
+    static constexpr int kDqOut = kStagesDq * kStageDq;  // the warps' output slabs
+    static constexpr int kDqBar = kDqOut + kOutStageBytes;
     static constexpr int kQCol = 256 + D;                              // Q as 16-bit pairs: D/2 columns
     static constexpr int kDoCol = 256 + D + D / 2;                     // dO (then dO2): D/2 columns each
     static_assert(kDoCol + kNV * D / 2 <= (int)kBwdTmemCols, "tensor memory budget of the dQ pass");
@@ -105,7 +107,7 @@ struct BwdCfg : Tile16<D> {
     static constexpr int kSmemDkv = kDkvBar + kNumBars * 8 + 16 + 1024;
     static constexpr int kSmemDq = kDqBar + kNumBars * 8 + 16 + 1024;
     static_assert(kSmemDkv <= 227 * 1024 && kSmemDq <= 227 * 1024, "shared memory budget");
-    static_assert(kStageDkv % 1024 == 0, "stage alignment");
+    static_assert(kStageDkv % 1024 == 0 && kDkvOut % 1024 == 0 && kDqOut % 1024 == 0, "stage alignment");
     // One value tensor: the MMA issuer waits only on named barriers, fed by the
     // elementwise warps and by a relay warp (warp 10) that waits for the TMA stages; a
     // shared-memory access (an mbarrier test included) by the issuing warp between MMA
@@ -139,7 +141,7 @@ __host__ __device__ constexpr uint32_t nb_stage(int s) { return 3 + (uint32_t)s;
 template <int D, bool kBf16, int kNV>
 __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                          const CUtensorMap& tm_do, const CUtensorMap& tm_v2, const CUtensorMap& tm_do2,
-                                         const float* __restrict__ lse2, const float* __restrict__ delta,
+                                         const CUtensorMap& tm_dk, const CUtensorMap& tm_dv, const float* __restrict__ lse2, const float* __restrict__ delta,
                                          void* __restrict__ dk, void* __restrict__ dv, void* __restrict__ dv2, int n_q,
                                          int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
                                          unsigned int* status, int kt, int n_items, int bh) {
@@ -384,6 +386,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
         const int half = (warp - 2) >> 2;
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128u;
+        const uint32_t out_slab = base + C::kDkvOut + (uint32_t)((warp - 2) * kOutSlabBytes);
         const float2 scale2 = make_float2(scale_log2, scale_log2);
         bool ok = true;
         // a failed wait skips the work of this and later tiles, not the signals
@@ -471,7 +474,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
         if (ok) ok = warp_wait(bars.done(), (uint32_t)(u & 1), wd);
         if (ok) {
             tc_fence_after();
-            const int key = (kt + u) * BT + quarter * 32 + lane;
+            const int key0 = (kt + u) * BT + quarter * 32;  // first key row of this warp
+            const int key = key0 + lane;
             const size_t row = (size_t)bh * n_k + key;
             // half 0 writes dV (each pair's), half 1 writes dK (scaled)
 #pragma unroll
@@ -485,11 +489,16 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                     tmem_ld32(src + 32u * c, r);
                     tmem_ld_wait();
                     reg_fence(r);
-                    store_row_chunk<kBf16>(dst, row, d_act, c, r, mul, key < n_k);
+                    if constexpr (C::kNamed)
+                        store_chunk_tma<kBf16>(half ? &tm_dk : &tm_dv, out_slab, 32 * c, key0, n_k, d_act, bh, r, mul);
+                    else
+                        store_row_chunk<kBf16>(dst, row, d_act, c, r, mul, key < n_k);
                 }
             }
         }
         }  // key tiles
+        if (lane == 0) bulk_wait_group0();  // this warp's stores complete before the CTA exits
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -514,7 +523,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
 // One CTA of the dQ pass: query tile qt of head bh.
 template <int D, bool kBf16, int kNV>
 __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_v2,
-                                       const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
+                                       const CUtensorMap& tm_dq, const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
                                        const uint16_t* __restrict__ do2_ptr, const float* __restrict__ lse2,
                                        const float* __restrict__ delta, void* __restrict__ dq, int n_q, int n_k,
                                        int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status,
@@ -826,6 +835,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
         if (ok) ok = warp_wait(bars.done(), 0, wd);
         if (ok) {
             tc_fence_after();
+            const uint32_t out_slab = base + C::kDqOut + (uint32_t)((warp - 2) * kOutSlabBytes);
             // the two warps of a quarter split the dQ columns: 32-column chunks alternate
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -834,8 +844,13 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
                 tmem_ld32(tmem + lane_off + 256u + 32u * c, r);
                 tmem_ld_wait();
                 reg_fence(r);
-                store_row_chunk<kBf16>(dq, (size_t)bh * n_q + row, d_act, c, r, scale, row < n_q);
+                if constexpr (C::kNamed)
+                    store_chunk_tma<kBf16>(&tm_dq, out_slab, 32 * c, q0 + quarter * 32, n_q, d_act, bh, r, scale);
+                else
+                    store_row_chunk<kBf16>(dq, (size_t)bh * n_q + row, d_act, c, r, scale, row < n_q);
             }
+            if (lane == 0) bulk_wait_group0();  // this warp's stores complete before the CTA exits
+            __syncwarp();
         }
     }
 
@@ -854,22 +869,24 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dk,
                     void* __restrict__ dv, void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale,
                     float scale_log2, unsigned int* status) {
-    dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, lse2, delta, dk, dv, dv2, n_q, n_k, n_q_pad, d_act,
-                            scale, scale_log2, status, blockIdx.x, 1, blockIdx.y);
+    dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, tm_dk, tm_dv, lse2, delta, dk, dv, dv2, n_q, n_k,
+                            n_q_pad, d_act, scale, scale_log2, status, blockIdx.x, 1, blockIdx.y);
 }
 
 template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const __grid_constant__ CUtensorMap tm_v2, const uint16_t* __restrict__ q_ptr,
+                  const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_dq,
+                  const uint16_t* __restrict__ q_ptr,
                   const uint16_t* __restrict__ do_ptr, const uint16_t* __restrict__ do2_ptr,
                   const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dq, int n_q,
                   int n_k, int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status) {
-    dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act, scale,
-                          scale_log2, status, blockIdx.x, blockIdx.y);
+    dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, tm_dq, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act,
+                          scale, scale_log2, status, blockIdx.x, blockIdx.y);
 }
 
 // Both passes in one launch.  The passes are independent once D and LSE2 are in
@@ -888,7 +905,8 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_passes_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
-                      const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
+                      const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                      const __grid_constant__ CUtensorMap tm_dv, const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
                       const uint16_t* __restrict__ do2_ptr, const float* __restrict__ lse2,
                       const float* __restrict__ delta, void* __restrict__ dq, void* __restrict__ dk, void* __restrict__ dv,
                       void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
@@ -913,11 +931,11 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     if (dkdv_cta_x >= 0) {
         const int kt = dkdv_cta_x * kt_per_cta;
         const int items = n_kt - kt < kt_per_cta ? n_kt - kt : kt_per_cta;
-        dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, lse2, delta, dk, dv, dv2, n_q, n_k, n_q_pad,
-                                d_act, scale, scale_log2, status, kt, items, bh);
+        dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, tm_dk, tm_dv, lse2, delta, dk, dv, dv2, n_q, n_k,
+                                n_q_pad, d_act, scale, scale_log2, status, kt, items, bh);
     }
     else
-        dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act,
+        dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, tm_dq, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act,
                               scale, scale_log2, status, dq_tile, bh);
 }
 
@@ -953,7 +971,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     if (!(stages & (kBwdDkDv | kBwdDq))) return cudaSuccess;
     const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUtensorMap tq, tk, tv, tdo, tv2, tdo2;
+    CUtensorMap tq, tk, tv, tdo, tv2, tdo2, tdq, tdk, tdv;
     const void* v2 = kNV == 2 ? p.v2 : p.v;
     const void* do2 = kNV == 2 ? p.d_o2 : p.d_o;
     // maps over the true head dimension p.d <= D: TMA fills the box columns past it with zeros
@@ -964,6 +982,16 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         !encode_tmap_3d(&tk, dt, 2, p.k, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
         !encode_tmap_3d(&tv, dt, 2, p.v, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw) ||
         !encode_tmap_3d(&tv2, dt, 2, v2, d, (uint64_t)p.n_k, (uint64_t)p.bh, C::kAtomCols, BT, sw))
+        return cudaErrorInvalidValue;
+    // the gradients, stored by TMA in boxes of 32 columns x 32 rows (one warp's slab); the
+    // two-value PSA form writes its gradients with plain stores and passes these unused
+    const bool named = C::kNamed;
+    const void* out_dq = named && p.dq ? p.dq : p.q;
+    const void* out_dk = named && p.dk ? p.dk : p.k;
+    const void* out_dv = named && p.dv ? p.dv : p.v;
+    if (!encode_tmap_3d(&tdq, dt, 2, out_dq, d, (uint64_t)p.n_q, (uint64_t)p.bh, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_3d(&tdk, dt, 2, out_dk, d, (uint64_t)p.n_k, (uint64_t)p.bh, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tmap_3d(&tdv, dt, 2, out_dv, d, (uint64_t)p.n_k, (uint64_t)p.bh, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     const float scale_log2 = p.scale * kLog2e;
     cudaError_t e = cudaSuccess;
@@ -976,7 +1004,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         const int m = C::kNamed ? dkdv_tiles_per_cta(n_qt, n_kt, p.bh, sm_count()) : 1;
         const int n_kc = (n_kt + m - 1) / m;
         both<<<dim3((unsigned)(n_kc + n_qt), (unsigned)p.bh, 1), C::kThreads, smem, stream>>>(
-            tq, tk, tv, tdo, tv2, tdo2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
+            tq, tk, tv, tdo, tv2, tdo2, tdq, tdk, tdv, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
             static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, p.dk, p.dv, p.dv2, (int)p.n_q,
             (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, n_kt >= 4 * m * n_qt ? 1 : 0, m);
         return cudaGetLastError();
@@ -986,7 +1014,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         e = ensure_smem_limit(reinterpret_cast<const void*>(dkdv), C::kSmemDkv, slot);
         if (e != cudaSuccess) return e;
         dkdv<<<dim3((unsigned)n_kt, (unsigned)p.bh, 1), C::kThreads, C::kSmemDkv, stream>>>(
-            tq, tk, tv, tdo, tv2, tdo2, p.lse2, p.delta, p.dk, p.dv, p.dv2, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad,
+            tq, tk, tv, tdo, tv2, tdo2, tdk, tdv, p.lse2, p.delta, p.dk, p.dv, p.dv2, (int)p.n_q, (int)p.n_k, (int)p.n_q_pad,
             p.d, p.scale, scale_log2, p.status);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -995,7 +1023,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
     if (e != cudaSuccess) return e;
     dqk<<<dim3((unsigned)n_qt, (unsigned)p.bh, 1), C::kThreads, C::kSmemDq, stream>>>(
-        tk, tv, tv2, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
+        tk, tv, tv2, tdq, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
         static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k,
         (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status);
     return cudaGetLastError();
