@@ -165,6 +165,12 @@ fa2_status backward_common(const void* q, const void* k, const void* v, const vo
     p.delta = static_cast<float*>(workspace);
     p.lse2 = p.delta + bh * p.n_q_pad;
     if (one_pass) p.dq_acc = p.lse2 + bh * p.n_q_pad;  // 16-byte aligned: n_q_pad is a multiple of 128
+    // the split dQ pass of the two-pass kernels, when the workspace also holds its partial sums
+    const size_t part = (!one_pass && (stages & kBwdDq)) ? dq_partial_bytes(bh, n_q, n_k, head_dim) : 0;
+    if (part && workspace_bytes >= two_pass_workspace_size(bh, n_q, n_k, head_dim, dtype) + part) {
+        p.dq_part = p.lse2 + bh * p.n_q_pad;
+        p.dq_splits = dq_key_splits(bh, n_q, n_k);
+    }
     p.bh = bh; p.n_q = n_q; p.n_k = n_k; p.d = head_dim; p.dtype = (int)dtype; p.scale = softmax_scale;
     if (!status_word(&p.status)) return FA2_ERR_CUDA;
     const cudaError_t e = one_pass ? launch_bwd_fused(p, static_cast<cudaStream_t>(stream))
@@ -222,7 +228,8 @@ fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* ls
 // The one-pass backward adds the float32 dQ accumulator, [bh, n_q_pad, pad_head_dim(head_dim)].
 size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype) {
     const size_t two_pass = two_pass_workspace_size(bh, n_q, n_k, head_dim, dtype);
-    if (two_pass == 0 || !use_one_pass(head_dim)) return two_pass;
+    if (two_pass == 0) return 0;
+    if (!use_one_pass(head_dim)) return two_pass + dq_partial_bytes(bh, n_q, n_k, head_dim);
     const int64_t n_q_pad = (n_q + 127) / 128 * 128;
     return two_pass + (size_t)(bh * n_q_pad) * (size_t)pad_head_dim(head_dim) * sizeof(float);
 }

@@ -124,6 +124,24 @@ __device__ __forceinline__ void store_chunk_tma(const CUtensorMap* map, uint32_t
     }
 }
 
+// The float32 form: 16 of the 32 columns in r (from `first`) as one box of 32 rows x 64
+// bytes, stored unscaled into plane `plane` (the boxes always lie inside that tensor).
+__device__ __forceinline__ void store_chunk_tma_f32(const CUtensorMap* map, uint32_t slab, int col0, int row0, int plane,
+                                                    const uint32_t (&r)[32], int first) {
+    if (lane_id() == 0) bulk_wait_group_read0();  // the previous store has read the slab
+    __syncwarp();
+    const uint32_t row = slab + lane_id() * 64u;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+        st_shared_v4(row + 16u * w, r[first + 4 * w], r[first + 4 * w + 1], r[first + 4 * w + 2], r[first + 4 * w + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane_id() == 0) {
+        tma_store_3d(map, slab, col0, row0, plane);
+        bulk_commit_group();
+    }
+}
+
 // The two 32-column chunks an elementwise warp owns, in the order that lets it
 // write 16-bit results at kPackedCol without overwriting a column it has not read.
 __device__ __forceinline__ int owned_chunk(int half, int cc) { return 2 * half + (half == 0 ? 1 - cc : cc); }

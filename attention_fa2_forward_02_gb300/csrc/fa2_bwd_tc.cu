@@ -520,14 +520,16 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
 // into tensor memory (16-bit pairs, the layout an MMA reads its A operand in), so
 // S and dP read only K and V from shared memory.
 
-// One CTA of the dQ pass: query tile qt of head bh.
+// One CTA of the dQ pass: query tile qt of head bh, over key tiles [j0, j1). With plane < 0
+// the CTA covers all key tiles and writes dq; otherwise it writes its float32 partial sum
+// (unscaled) to plane `plane` of the split dQ pass's partial sums, through tm_dqp.
 template <int D, bool kBf16, int kNV>
 __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_v2,
                                        const CUtensorMap& tm_dq, const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
                                        const uint16_t* __restrict__ do2_ptr, const float* __restrict__ lse2,
                                        const float* __restrict__ delta, void* __restrict__ dq, int n_q, int n_k,
                                        int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status,
-                                       int qt, int bh) {
+                                       int qt, int bh, const CUtensorMap& tm_dqp, int j0, int j1, int plane) {
     using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStagesDq;
     extern __shared__ uint8_t smem_raw[];
@@ -536,7 +538,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
     uint8_t* smem = smem_raw + (base - raw_addr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = qt * BT;
-    const int n_kt = (n_k + BT - 1) / BT;
+    const int nj = j1 - j0;  // key tiles of this CTA
 
     const Bars bars{base + C::kDqBar, S};
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kDqBar + C::kNumBars * 8);
@@ -562,15 +564,15 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
             if (kNV == 2) prefetch_tmap(&tm_v2);
             int issued = 0;
             bool ok = true;
-            for (int j = 0; j < n_kt; ++j) {
+            for (int j = 0; j < nj; ++j) {
                 const int s = j % S;
                 if (j >= S && !(ok = mbar_wait(bars.empty(s), ((j / S) & 1) ^ 1, wd))) break;
                 mbar_arrive_expect_tx(bars.full(s), (1 + kNV) * C::kTile);
                 for (int a = 0; a < C::kAtoms; ++a) {
-                    tma_load_3d(stage_k(s) + a * BT * C::kAtomRowBytes, &tm_k, bars.full(s), a * C::kAtomCols, j * BT, bh);
+                    tma_load_3d(stage_k(s) + a * BT * C::kAtomRowBytes, &tm_k, bars.full(s), a * C::kAtomCols, (j0 + j) * BT, bh);
                     for (int v = 0; v < kNV; ++v)
                         tma_load_3d(stage_v(s, v) + a * BT * C::kAtomRowBytes, v ? &tm_v2 : &tm_v, bars.full(s),
-                                    a * C::kAtomCols, j * BT, bh);
+                                    a * C::kAtomCols, (j0 + j) * BT, bh);
                 }
                 issued = j + 1;
             }
@@ -610,10 +612,10 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
                 mma_commit(bars.dp_full());
             }
             __syncwarp();
-            for (int j = 0; j < n_kt; ++j) {
+            for (int j = 0; j < nj; ++j) {
                 const int s = j % S;
                 const int sn = (j + 1) % S;
-                const bool more = j + 1 < n_kt;
+                const bool more = j + 1 < nj;
                 nb_sync(kNbE1, kNbElem);  // S(j) read: its columns may be overwritten
                 if (more) {
                     nb_sync(nb_stage(sn), 64);  // K, V of tile j + 1
@@ -670,10 +672,10 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
                     issue_dp(0);
                     mma_commit(bars.dp_full());
                 }
-                for (int j = 0; ok && j < n_kt; ++j) {
+                for (int j = 0; ok && j < nj; ++j) {
                     const int s = j % S;
                     const int sn = (j + 1) % S;
-                    const bool more = j + 1 < n_kt;
+                    const bool more = j + 1 < nj;
                     if (more) {
                         if (!(ok = mbar_wait(bars.e1(), j & 1, wd) && mbar_wait(bars.full(sn), ((j + 1) / S) & 1, wd))) break;
                         tc_fence_after();
@@ -700,7 +702,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
         // TMA relay: signals each K / V stage to the issuer
         bool ok = warp_wait(bars.full(0), 0, wd);
         nb_arrive(nb_stage(0), 64);
-        for (int j = 1; j < n_kt; ++j) {
+        for (int j = 1; j < nj; ++j) {
             const int s = j % S;
             ok = ok && warp_wait(bars.full(s), (j / S) & 1, wd);
             nb_arrive(nb_stage(s), 64);
@@ -763,14 +765,14 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
             if constexpr (C::kNamed) nb_arrive(nb, kNbElem);
             else mbar_arrive(mbar);
         };
-        for (int j = 0; j < n_kt; ++j) {
+        for (int j = 0; j < nj; ++j) {
             if (!(ok = ok && warp_wait(bars.s_full(), j & 1, wd))) {
                 signal(kNbE1, bars.e1());
                 signal(kNbE2, bars.e2());
                 continue;
             }
             tc_fence_after();
-            const int valid = n_k - j * BT;
+            const int valid = n_k - (j0 + j) * BT;
             // step 1: P = 2^(S * scale * log2e - LSE2) in registers; then S may be overwritten
             float2 p[2][16];
             {
@@ -844,10 +846,16 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
                 tmem_ld32(tmem + lane_off + 256u + 32u * c, r);
                 tmem_ld_wait();
                 reg_fence(r);
-                if constexpr (C::kNamed)
-                    store_chunk_tma<kBf16>(&tm_dq, out_slab, 32 * c, q0 + quarter * 32, n_q, d_act, bh, r, scale);
-                else
+                if constexpr (C::kNamed) {
+                    if (plane < 0) {
+                        store_chunk_tma<kBf16>(&tm_dq, out_slab, 32 * c, q0 + quarter * 32, n_q, d_act, bh, r, scale);
+                    } else {  // two 16-column float32 boxes of the partial sum
+                        store_chunk_tma_f32(&tm_dqp, out_slab, 32 * c, q0 + quarter * 32, plane, r, 0);
+                        store_chunk_tma_f32(&tm_dqp, out_slab, 32 * c + 16, q0 + quarter * 32, plane, r, 16);
+                    }
+                } else {
                     store_row_chunk<kBf16>(dq, (size_t)bh * n_q + row, d_act, c, r, scale, row < n_q);
+                }
             }
             if (lane == 0) bulk_wait_group0();  // this warp's stores complete before the CTA exits
             __syncwarp();
@@ -863,6 +871,46 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tm_k, const CUtensorMa
 }
 
 // ------------------------------------------------------------------------------ kernels
+
+// The work of the x-th dQ CTA of head bh when the pass divides each query tile's keys into
+// `splits` ranges: range r = x / n_qt, query tile x mod n_qt (the query tiles of one key
+// range next to each other, so that they share its K and V tiles in L2), key tiles
+// [r L, min(n_kt, r L + L)) with L = ceil(n_kt / splits), partial-sum plane r * heads + bh.
+struct DqWork {
+    int qt, j0, j1, plane;
+};
+__device__ __forceinline__ DqWork dq_work(int x, int bh, int n_qt, int n_kt, int splits, int heads) {
+    if (splits <= 1) return DqWork{x, 0, n_kt, -1};
+    const int r = x / n_qt, len = (n_kt + splits - 1) / splits;
+    const int j0 = r * len, j1 = j0 + len < n_kt ? j0 + len : n_kt;
+    return DqWork{x % n_qt, j0, j1, r * heads + bh};
+}
+
+// dq = scale * (the split dQ pass's float32 partial sums added in key-range order), rounded to
+// the 16-bit type: one thread per 4 columns of a row, a warp's loads 512 contiguous bytes.
+template <bool kBf16>
+__global__ void __launch_bounds__(256)
+    bwd_dq_combine_kernel(const float4* __restrict__ part, void* __restrict__ dq, int heads, int n_q, int n_q_pad,
+                          int hd, int d_act, int splits, float scale) {
+    const int groups = d_act / 4;
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (i >= (int64_t)heads * n_q * groups) return;
+    const int g = (int)(i % groups);
+    const int64_t rowi = i / groups;  // head * n_q + row
+    const int row = (int)(rowi % n_q), b = (int)(rowi / n_q);
+    const int64_t plane = (int64_t)heads * n_q_pad * (hd / 4);
+    const float4* src = part + ((int64_t)b * n_q_pad + row) * (hd / 4) + g;
+    float4 acc = src[0];
+    for (int r = 1; r < splits; ++r) {
+        const float4 x = src[r * plane];
+        acc.x += x.x;
+        acc.y += x.y;
+        acc.z += x.z;
+        acc.w += x.w;
+    }
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(dq) + rowi * d_act + 4 * g) =
+        make_uint2(pack2<kBf16>(acc.x * scale, acc.y * scale), pack2<kBf16>(acc.z * scale, acc.w * scale));
+}
 
 template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
@@ -881,19 +929,21 @@ template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_dq,
-                  const uint16_t* __restrict__ q_ptr,
+                  const __grid_constant__ CUtensorMap tm_dqp, const uint16_t* __restrict__ q_ptr,
                   const uint16_t* __restrict__ do_ptr, const uint16_t* __restrict__ do2_ptr,
                   const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dq, int n_q,
-                  int n_k, int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status) {
+                  int n_k, int n_q_pad, int d_act, float scale, float scale_log2, unsigned int* status, int splits) {
+    const int n_qt = (n_q + BT - 1) / BT;
+    const DqWork w = dq_work((int)blockIdx.x, (int)blockIdx.y, n_qt, (n_k + BT - 1) / BT, splits, (int)gridDim.y);
     dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, tm_dq, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act,
-                          scale, scale_log2, status, blockIdx.x, blockIdx.y);
+                          scale, scale_log2, status, w.qt, (int)blockIdx.y, tm_dqp, w.j0, w.j1, w.plane);
 }
 
 // Both passes in one launch.  The passes are independent once D and LSE2 are in
 // the workspace; one grid lets the CTAs of one fill the SMs the other leaves idle
 // in its last wave.  A dK/dV CTA takes kt_per_cta consecutive key tiles (the last
 // of a head fewer), n_kc = ceil(n_kt / kt_per_cta) of them per head.  Order of the
-// CTAs (x fastest, then the head y):
+// CTAs (x fastest, then the head y), the dQ CTAs of a head numbered as dq_work takes them:
 //   dq_first == 0: per head, x < n_kc runs the dK/dV pass for key tiles from
 //     x * kt_per_cta and the rest the dQ pass for query tile x - n_kc, so that a
 //     head's two sets of CTAs run together and share its Q, K, V, dO in L2;
@@ -906,23 +956,25 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_v2, const __grid_constant__ CUtensorMap tm_do2,
                       const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
-                      const __grid_constant__ CUtensorMap tm_dv, const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
+                      const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dqp,
+                      const uint16_t* __restrict__ q_ptr, const uint16_t* __restrict__ do_ptr,
                       const uint16_t* __restrict__ do2_ptr, const float* __restrict__ lse2,
                       const float* __restrict__ delta, void* __restrict__ dq, void* __restrict__ dk, void* __restrict__ dv,
                       void* __restrict__ dv2, int n_q, int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
-                      unsigned int* status, int dq_first, int kt_per_cta) {
+                      unsigned int* status, int dq_first, int kt_per_cta, int splits) {
     const int n_kt = (n_k + BT - 1) / BT, n_qt = (n_q + BT - 1) / BT;
     const int n_kc = (n_kt + kt_per_cta - 1) / kt_per_cta;
-    int dkdv_cta_x = -1, dq_tile = -1, bh;
+    const int n_dqc = n_qt * (splits > 1 ? splits : 1);  // dQ CTAs per head
+    int dkdv_cta_x = -1, dq_x = -1, bh;
     if (!dq_first) {
         bh = blockIdx.y;
         if ((int)blockIdx.x < n_kc) dkdv_cta_x = blockIdx.x;
-        else dq_tile = blockIdx.x - n_kc;
+        else dq_x = blockIdx.x - n_kc;
     } else {
-        const int lin = blockIdx.y * gridDim.x + blockIdx.x, n_dq = (int)gridDim.y * n_qt;
+        const int lin = blockIdx.y * gridDim.x + blockIdx.x, n_dq = (int)gridDim.y * n_dqc;
         if (lin < n_dq) {
-            bh = lin / n_qt;
-            dq_tile = lin % n_qt;
+            bh = lin / n_dqc;
+            dq_x = lin % n_dqc;
         } else {
             bh = (lin - n_dq) / n_kc;
             dkdv_cta_x = (lin - n_dq) % n_kc;
@@ -934,9 +986,11 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
         dkdv_cta<D, kBf16, kNV>(tm_q, tm_k, tm_v, tm_do, tm_v2, tm_do2, tm_dk, tm_dv, lse2, delta, dk, dv, dv2, n_q, n_k,
                                 n_q_pad, d_act, scale, scale_log2, status, kt, items, bh);
     }
-    else
+    else {
+        const DqWork w = dq_work(dq_x, bh, n_qt, n_kt, splits, (int)gridDim.y);
         dq_cta<D, kBf16, kNV>(tm_k, tm_v, tm_v2, tm_dq, q_ptr, do_ptr, do2_ptr, lse2, delta, dq, n_q, n_k, n_q_pad, d_act,
-                              scale, scale_log2, status, dq_tile, bh);
+                              scale, scale_log2, status, w.qt, bh, tm_dqp, w.j0, w.j1, w.plane);
+    }
 }
 
 // ------------------------------------------------------------------------------ launch
@@ -971,7 +1025,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     if (!(stages & (kBwdDkDv | kBwdDq))) return cudaSuccess;
     const CUtensorMapDataType dt = kBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const CUtensorMapSwizzle sw = D >= 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    CUtensorMap tq, tk, tv, tdo, tv2, tdo2, tdq, tdk, tdv;
+    CUtensorMap tq, tk, tv, tdo, tv2, tdo2, tdq, tdk, tdv, tdqp;
     const void* v2 = kNV == 2 ? p.v2 : p.v;
     const void* do2 = kNV == 2 ? p.d_o2 : p.d_o;
     // maps over the true head dimension p.d <= D: TMA fills the box columns past it with zeros
@@ -993,7 +1047,25 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         !encode_tmap_3d(&tdk, dt, 2, out_dk, d, (uint64_t)p.n_k, (uint64_t)p.bh, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_tmap_3d(&tdv, dt, 2, out_dv, d, (uint64_t)p.n_k, (uint64_t)p.bh, 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
+    // the split dQ pass's float32 partial sums: [splits * bh, n_q_pad, D], boxes of 16 x 32
+    // (without a split the map is encoded over q and never used)
+    const int splits = C::kNamed && p.dq_part ? p.dq_splits : 1;
+    const bool split = splits > 1;
+    if (!encode_tmap_3d(&tdqp, split ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, split ? 4 : 2,
+                        split ? static_cast<const void*>(p.dq_part) : p.q, split ? (uint64_t)D : d,
+                        split ? (uint64_t)p.n_q_pad : (uint64_t)p.n_q, (uint64_t)(split ? splits * p.bh : p.bh),
+                        split ? 16 : 32, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
     const float scale_log2 = p.scale * kLog2e;
+    // the combine of a split dQ pass, after the kernel that wrote the partial sums
+    auto combine = [&]() -> cudaError_t {
+        if (!split) return cudaSuccess;
+        const int64_t threads = p.bh * p.n_q * (p.d / 4);
+        bwd_dq_combine_kernel<kBf16><<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
+            reinterpret_cast<const float4*>(p.dq_part), p.dq, (int)p.bh, (int)p.n_q, (int)p.n_q_pad, D, p.d, splits,
+            p.scale);
+        return cudaGetLastError();
+    };
     cudaError_t e = cudaSuccess;
     const int n_kt = (int)((p.n_k + BT - 1) / BT), n_qt = (int)((p.n_q + BT - 1) / BT);
     if ((stages & (kBwdDkDv | kBwdDq)) == (kBwdDkDv | kBwdDq)) {
@@ -1003,11 +1075,13 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         if (e != cudaSuccess) return e;
         const int m = C::kNamed ? dkdv_tiles_per_cta(n_qt, n_kt, p.bh, sm_count()) : 1;
         const int n_kc = (n_kt + m - 1) / m;
-        both<<<dim3((unsigned)(n_kc + n_qt), (unsigned)p.bh, 1), C::kThreads, smem, stream>>>(
-            tq, tk, tv, tdo, tv2, tdo2, tdq, tdk, tdv, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
+        const int dq_len = (n_kt + splits - 1) / splits;  // key tiles per dQ CTA
+        both<<<dim3((unsigned)(n_kc + n_qt * splits), (unsigned)p.bh, 1), C::kThreads, smem, stream>>>(
+            tq, tk, tv, tdo, tv2, tdo2, tdq, tdk, tdv, tdqp, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
             static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, p.dk, p.dv, p.dv2, (int)p.n_q,
-            (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, n_kt >= 4 * m * n_qt ? 1 : 0, m);
-        return cudaGetLastError();
+            (int)p.n_k, (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, dq_len >= 4 * m * n_qt ? 1 : 0, m, splits);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return combine();
     }
     if (stages & kBwdDkDv) {
         auto dkdv = bwd_dkdv_kernel<D, kBf16, kNV>;
@@ -1022,11 +1096,12 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     auto dqk = bwd_dq_kernel<D, kBf16, kNV>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(dqk), C::kSmemDq, slot + 1);
     if (e != cudaSuccess) return e;
-    dqk<<<dim3((unsigned)n_qt, (unsigned)p.bh, 1), C::kThreads, C::kSmemDq, stream>>>(
-        tk, tv, tv2, tdq, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
+    dqk<<<dim3((unsigned)(n_qt * splits), (unsigned)p.bh, 1), C::kThreads, C::kSmemDq, stream>>>(
+        tk, tv, tv2, tdq, tdqp, static_cast<const uint16_t*>(p.q), static_cast<const uint16_t*>(p.d_o),
         static_cast<const uint16_t*>(kNV == 2 ? p.d_o2 : p.d_o), p.lse2, p.delta, p.dq, (int)p.n_q, (int)p.n_k,
-        (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status);
-    return cudaGetLastError();
+        (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, splits);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return combine();
 }
 
 }  // namespace

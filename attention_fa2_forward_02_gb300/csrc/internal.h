@@ -16,6 +16,31 @@ enum Dtype : int { kF32 = 0, kF16 = 1, kBf16 = 2 };
 // The kernel size a head dimension runs at (head_dim is a multiple of 8, <= 128).
 inline int pad_head_dim(int d) { return d <= 32 ? 32 : (d <= 64 ? 64 : 128); }
 
+// Key ranges the dQ pass of the two-pass backward divides each query tile's keys into when
+// the unsplit dQ CTAs (one per query tile, each looping over all key tiles of its head)
+// would not fill one wave of a 148-SM part: enough ranges for about one dQ CTA per SM, at
+// least 8 key tiles per range, at most 8 ranges. Each range's CTA writes a float32 partial
+// sum and a last kernel adds them in range order (bit-reproducible). With a wave of dQ
+// CTAs or more the split only adds the partial sums' traffic (measured on GB300 at
+// B=1 H=32 N_q=1024 N_k=32768: 1.249 ms unsplit, 1.259 ms in two ranges). A function of the
+// sizes alone, so that the results do not depend on the device.
+inline int dq_key_splits(int64_t bh, int64_t n_q, int64_t n_k) {
+    const int64_t n_qt = (n_q + 127) / 128, n_kt = (n_k + 127) / 128;
+    const int64_t dq_ctas = bh * n_qt;
+    int64_t s = (148 + dq_ctas - 1) / dq_ctas;
+    if (s > n_kt / 8) s = n_kt / 8;
+    if (s > 8) s = 8;
+    return s < 2 ? 1 : (int)s;
+}
+
+// Bytes of the float32 dQ partial sums of a split dQ pass ([splits, bh, n_q_pad, kernel
+// head size]); 0 when the pass is not split.
+inline size_t dq_partial_bytes(int64_t bh, int64_t n_q, int64_t n_k, int d) {
+    const int s = dq_key_splits(bh, n_q, n_k);
+    if (s < 2) return 0;
+    return (size_t)s * (size_t)bh * (size_t)((n_q + 127) / 128 * 128) * (size_t)pad_head_dim(d) * sizeof(float);
+}
+
 struct FwdParams {
     const void* q;
     const void* k;
@@ -57,6 +82,10 @@ struct BwdParams {
     // float32 dQ accumulator of the one-pass backward, [bh, n_q_pad, pad_head_dim(d)],
     // inside the workspace; zeroed by the preprocess stage when set
     float* dq_acc = nullptr;
+    // float32 dQ partial sums of a split dQ pass, [dq_splits, bh, n_q_pad,
+    // pad_head_dim(d)], inside the workspace (null: the dQ pass is not split)
+    float* dq_part = nullptr;
+    int dq_splits = 1;
 };
 
 // The PSA rearrangements.  Pack / merge and their adjoints are batched 2-D

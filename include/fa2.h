@@ -90,10 +90,20 @@ fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, flo
  * and hd = head_dim rounded up to 32, 64 or 128, the workspace holds
  *   the row sums D = rowsum(O * dO), float32 [bh, n_q_pad]      (4 * bh * n_q_pad bytes),
  *   a base-2 copy of the LSE, float32 [bh, n_q_pad]             (4 * bh * n_q_pad bytes),
- *   for head_dim <= 64 only (the one-pass backward), the float32 dQ accumulator
- *   [bh, n_q_pad, hd]                                           (4 * bh * n_q_pad * hd bytes).
+ *   for head_dim <= 64 (the one-pass backward), the float32 dQ accumulator
+ *   [bh, n_q_pad, hd]                                           (4 * bh * n_q_pad * hd bytes),
+ *   for head_dim > 64 when the dQ pass is split, its float32 partial sums
+ *   [splits, bh, n_q_pad, hd]                          (4 * splits * bh * n_q_pad * hd bytes).
+ * The dQ pass (one CTA per 128-row query tile, looping over all key tiles) is split when
+ * its CTAs, ceil(n_q / 128) * bh of them, would be fewer than about 148 (one wave): each
+ * query tile's keys are divided into splits = min(ceil(148 / (bh * ceil(n_q / 128))),
+ * floor(ceil(n_k / 128) / 8), 8) ranges (no split if that is below 2), each range's CTA
+ * writes a float32 partial sum and a last kernel adds them in range order, so dq stays
+ * bit-reproducible (it can differ in the last bits from the unsplit pass's sum).
  * The three stage entry points below need only the first two parts
- * (8 * bh * n_q_pad bytes); a buffer of this size serves them as well.
+ * (8 * bh * n_q_pad bytes); a buffer of this size serves them as well (the dQ pass then
+ * runs unsplit); given the partial sums' room too, they split the dQ pass as fa2_backward
+ * does, and their results equal fa2_backward's bit for bit for head_dim > 64.
  */
 size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype);
 

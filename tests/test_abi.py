@@ -144,3 +144,22 @@ def test_binding_rejects_mixed_dtypes(lib):
         binding.psa_fa2_backward(packed, o, o, do, odd, lse, bf(4, bh, n, d), ws, 0.17)
     with pytest.raises(TypeError):
         binding.psa_merge_attn_backward(bf(1, 2 * d, 4, 4), hf(1, 16, d), bf(1, 16, d), 1)
+
+
+def test_workspace_holds_the_split_dq_partial_sums(lib):
+    """Head size > 64: the workspace adds room for the split dQ pass's float32 partial sums
+    exactly when the unsplit dQ CTAs would be fewer than about 148 (fa2.h)."""
+    ws = lambda bh, nq, nk, d: lib.fa2_backward_workspace_size(bh, nq, nk, d, BF16)  # noqa: E731
+    pad = lambda n: -(-n // 128) * 128  # noqa: E731
+    # 2 heads x 1 query tile, 256 key tiles: 8 ranges
+    assert ws(2, 128, 32768, 128) == 8 * 2 * 128 + 8 * 2 * 128 * 128 * 4
+    # 1 head x 3 query tiles, 64 key tiles: 8 ranges; head size 120 runs at 128
+    assert ws(1, 300, 8192, 120) == 8 * pad(300) + 8 * 1 * pad(300) * 128 * 4
+    # 3 heads x 2 query tiles, 20 key tiles: min(ceil(148 / 6), 20 // 8) = 2 ranges
+    assert ws(3, 200, 2500, 128) == 8 * 3 * pad(200) + 2 * 3 * pad(200) * 128 * 4
+    # a wave of dQ CTAs or more (B=1 H=32 N_q=1024: 256), or fewer than 16 key tiles: no split
+    assert ws(32, 1024, 32768, 128) == 8 * 32 * 1024
+    assert ws(32, 8192, 8192, 128) == 8 * 32 * 8192
+    assert ws(2, 128, 1900, 128) == 8 * 2 * 128
+    # head size <= 64: the one-pass workspace (D, LSE2 and the dQ accumulator)
+    assert ws(2, 128, 32768, 64) == 8 * 2 * 128 + 2 * 128 * 64 * 4

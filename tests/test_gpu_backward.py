@@ -275,3 +275,67 @@ def test_backward_passes_over_several_key_tiles_equal_the_stages(n_q, n_k, d, dt
         ref = A.backward(w(q[b:b + 1]), w(k[b:b + 1]), w(v[b:b + 1]), w(d_o[b:b + 1]), scale)
         for name, a, r in zip(("dQ", "dK", "dV"), one_grid, ref):
             check_16bit(G.to_f64(a[b]), r[0], f"one-grid {name} of head {b}")
+
+
+def _dq_splits(bh, n_q, n_k):
+    """The number of key ranges the library's dQ pass takes for these sizes (include/fa2.h,
+    fa2_backward_workspace_size): about 148 dQ CTAs, at least 8 key tiles per range, at most 8."""
+    n_qt, n_kt = -(-n_q // 128), -(-n_k // 128)
+    s = min(-(-148 // (bh * n_qt)), n_kt // 8, 8)
+    return s if s >= 2 else 1
+
+
+@pytest.mark.parametrize("bh,n_q,n_k,d,dtype", [
+    (2, 128, 4096, 128, "bf16"),   # 2 dQ CTAs of 32 key tiles unsplit: 4 ranges of 8
+    (3, 200, 2500, 128, "f16"),    # ragged keys (20 key tiles, the last partial): 2 ranges of 10
+    (1, 300, 8192, 128, "bf16"),   # 3 query tiles x 8 ranges of 8 key tiles
+    (2, 100, 3000, 64, "bf16"),    # head size 64 through the stage entry points: 3 ranges of 8 key tiles
+])
+def test_backward_split_dq_pass(bh, n_q, n_k, d, dtype):
+    """Few query tiles per head and many keys: the dQ pass divides each query tile's keys into
+    ranges whose CTAs write float32 partial sums, added in range order by a last kernel, when
+    the workspace holds them (fa2_backward_workspace_size bytes).  The gradients are
+    bit-reproducible, equal bit for bit between fa2_backward_passes and the stages given the
+    same workspace, within the parity bar of the unsplit pass (a workspace without room for
+    the partial sums) and of the oracle; nothing is written outside dq, dk, dv or the
+    workspace."""
+    torch = G.require_gpu()
+    splits = _dq_splits(bh, n_q, n_k)
+    assert splits >= 2
+    tag = f"bwd/split/{bh}/{n_q}/{n_k}/{d}/{dtype}"
+    q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
+    d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)
+    qd, kd, vd, dod = (G.to_device(x, dtype) for x in (q, k, v, d_o))
+    scale = 1 / math.sqrt(d)
+    o = G.empty((bh, n_q, d), dtype)
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    n_q_pad = -(-n_q // 128) * 128
+    hd = 32 if d <= 32 else (64 if d <= 64 else 128)
+    ws_bytes = 8 * bh * n_q_pad + splits * bh * n_q_pad * hd * 4
+    if d > 64:
+        code = {"bf16": binding.DTYPE_BF16, "f16": binding.DTYPE_F16}[dtype]
+        assert binding.fa2_backward_workspace_size(bh, n_q, n_k, d, code) == ws_bytes
+    ws = G.Guarded((ws_bytes,), torch.uint8)
+    runs = []
+    for _ in range(2):
+        grads = [G.guarded(tuple(x.shape), dtype) for x in (qd, kd, vd)]
+        binding.fa2_backward_preprocess(o, dod, lse, ws.t, n_k)
+        binding.fa2_backward_passes(qd, kd, vd, dod, ws.t, *(g.t for g in grads), scale)
+        runs.append(grads)
+    staged = _stages(qd, kd, vd, o, dod, lse, scale, ws.t, dtype)
+    small = torch.empty(8 * bh * n_q_pad, dtype=torch.uint8, device="cuda")  # no room for partial sums
+    unsplit = _stages(qd, kd, vd, o, dod, lse, scale, small, dtype)
+    binding.fa2_device_status()
+    ws.assert_intact("workspace")
+    for name, a, b, c in zip(("dQ", "dK", "dV"), runs[0], runs[1], staged):
+        a.assert_intact(name)
+        assert torch.equal(a.t, b.t), f"{name} differs between two runs"
+        assert torch.equal(a.t, c), f"fa2_backward_passes {name} differs from the stages"
+    check_16bit(G.to_f64(runs[0][0].t), G.to_f64(unsplit[0]), "split dQ against the unsplit pass")
+    for name, a, u in zip(("dK", "dV"), runs[0][1:], unsplit[1:]):
+        assert torch.equal(a.t, u), f"{name} depends on the dQ split"
+    w = lambda x: synth.widen(x, dtype)  # noqa: E731
+    ref = A.backward(w(q), w(k), w(v), w(d_o), scale)
+    for name, a, r in zip(("dQ", "dK", "dV"), runs[0], ref):
+        check_16bit(G.to_f64(a.t), r, f"{name} (dQ pass in {splits} key ranges)")
