@@ -528,6 +528,10 @@ def run_ours(args):
         "fa2_bwd_ms": bwd_ms, "fa2_bwd_tflops": BWD_FLOPS / bwd_ms / 1e9,
         "fa2_bwd_frac_burst_peak": BWD_FLOPS / bwd_ms / 1e9 / pk["bf16"],
         "fa2_bwd_preprocess_ms": per["fa2_bwd_preprocess"], "fa2_bwd_passes_ms": per["fa2_bwd_passes"],
+        # the preprocess reads O, dO (16-bit) and LSE and writes D and LSE2 (float32): HBM-bound
+        "fa2_bwd_preprocess_gbs": (2 * BH * N * D * 2 + BH * N * 4 + 2 * BH * N * 4) / (per["fa2_bwd_preprocess"] * 1e-3) / 1e9,
+        "fa2_bwd_preprocess_frac_hbm": (2 * BH * N * D * 2 + BH * N * 4 + 2 * BH * N * 4) / (per["fa2_bwd_preprocess"] * 1e-3)
+        / 1e9 / pk["hbm_gbs"],
         "c2psa_block_us": per["c2psa_block"] * 1e3,
         "peak_bf16_burst_tflops": pk["bf16"], "peak_source": pk["source"],
     }
