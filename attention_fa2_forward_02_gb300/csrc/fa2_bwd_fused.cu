@@ -34,7 +34,8 @@
 // The accumulator is laid out per (head, query tile) as [4 quarters][2 halves][D/8]
 // [32 rows][4 floats] (quarter = row / 32, half = column / (D/2)), so that each warp's
 // block is one contiguous run and the rounding kernel still reads 512 contiguous bytes
-// per warp.
+// per warp.  At the end the CTA's dK and dV leave by TMA stores, each warp staging its
+// 32-row chunks in the same block.
 //
 // MMA order per query tile i (one thread issues, the tensor core runs in order):
 //   [e1(i)] dV += P^T(i) dO(i);  dP^T(i) -> dp_full;
