@@ -8,7 +8,9 @@ problems, and checks each result against fa2_backward with a caller-owned
 workspace: bit for bit where that computation is deterministic (every gradient at
 head size 128, dK and dV at 64), within the parity bar the other GPU tests use for
 the one-pass dQ, whose float32 sums land in any order.  It also checks that a
-problem needing more than the fixed scratch is refused without a launch.
+problem needing more than the fixed scratch is refused without a launch, and that
+a problem whose dQ pass is split over key ranges (partial sums in the scratch)
+matches fa2_backward bit for bit.
 
 The file name makes pytest collect it last.
 """
@@ -100,3 +102,22 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
                                                 64, 32768, 128, 128, binding.DTYPE_BF16, 0.088, None)
     assert st == SCRATCH_LIMIT
     binding.fa2_device_status()
+
+
+def test_noalloc_with_the_split_dq_pass():
+    """Two heads of one query tile and 4096 keys at head size 128: fa2_backward splits the dQ
+    pass into key ranges whose float32 partial sums live in the workspace; from the fixed
+    scratch, fa2_backward_noalloc does the same and must equal fa2_backward bit for bit."""
+    torch = G.require_gpu()
+    bh, n_q, n_k, d = 2, 128, 4096, 128
+    ws_bytes = binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_BF16)
+    assert ws_bytes > 8 * bh * 128  # the partial sums are part of it
+    args = _problem("noalloc/split", bh, n_q, n_k, d, "bf16")
+    got = [G.Guarded(tuple(x.shape), x.dtype) for x in args[:3]]
+    binding.fa2_backward_noalloc(*args[:6], *(g.t for g in got), args[6])
+    binding.fa2_device_status()
+    want = _with_workspace(*args)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("dQ", "dK", "dV"), got, want):
+        a.assert_intact(f"fa2_backward_noalloc {name}")
+        assert torch.equal(a.t, b), f"fa2_backward_noalloc {name} differs from fa2_backward"
