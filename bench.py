@@ -129,19 +129,32 @@ def host_cores():
 
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 20 ms; only those stamped inside the timed region count.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    `begin()` and `end()` bracket the timed region on the host clock (the GPU work of the
+    region runs between them: its launches follow begin() and end() follows the final
+    synchronize). nvidia-smi stamps each sample with its local wall-clock time; the offset
+    of that clock from the host's epoch time (its time zone, a whole number of quarter
+    hours) is taken from when the samples arrive. A region shorter than the sampling
+    interval may hold no sample: the record then says so and gives no clock. power.draw
+    is an average over a window longer than a short region, so its maximum there
+    understates the draw."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMED = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    INTERVAL_MS = 20
 
-    def __init__(self, device_id: str):
-        self.lines = []
+    def __init__(self, device_id: str, start: bool = True):
+        self.lines = []  # (host time received, line)
         self.proc = None
+        self.t_begin = self.t_end = None
+        if not start:
+            return
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", device_id, f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -150,35 +163,60 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
 
     def stop(self):
-        if self.proc is None:
+        if self.proc is None and not self.lines:
             return {"unavailable": "nvidia-smi not found"}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.thread.join(timeout=5)
-        sm, smax, power, reasons = [], [], [], set()
-        for line in self.lines:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+        return self.summary()
+
+    @staticmethod
+    def _stamp(text):
+        import datetime
+        return datetime.datetime.strptime(text, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+
+    def summary(self):
+        rows = []  # (received, stamped, sm, sm max, power, reasons)
+        for received, line in self.lines:
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-                power.append(float(f[3]))
+                rows.append((received, self._stamp(f[0]), float(f[2]), float(f[3]), float(f[4]),
+                             [n for n, v in zip(self.NAMED, f[6:10]) if v.lower() == "active"]))
             except ValueError:
                 continue
-            for name, val in zip(self.NAMED, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        if not rows:
             return {"unavailable": "no samples"}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power)}
+        offsets = sorted(r[0] - r[1] for r in rows)
+        zone = round(offsets[len(offsets) // 2] / 900.0) * 900.0  # the stamps' time-zone offset
+        t0 = self.t_begin if self.t_begin is not None else -math.inf
+        t1 = self.t_end if self.t_end is not None else math.inf
+        inside = [r for r in rows if t0 <= r[1] + zone <= t1]
+        out = {"sm_max_mhz": max(r[3] for r in rows), "samples": len(inside), "samples_total": len(rows),
+               "interval_ms": self.INTERVAL_MS, "region_s": (round(t1 - t0, 4) if self.t_begin is not None
+                                                            and self.t_end is not None else None)}
+        if not inside:
+            out.update({"sm_mhz": None, "reasons": [], "power_w_max": None,
+                        "note": "no sample fell inside the timed region (shorter than the sampling interval)"})
+            return out
+        out.update({"sm_mhz": statistics.median(r[2] for r in inside), "sm_min_mhz": min(r[2] for r in inside),
+                    "reasons": sorted({n for r in inside for n in r[5]}),
+                    "power_w_max": max(r[4] for r in inside)})
+        return out
 
 
 # ---------------------------------------------------------------------------- ncu traffic
@@ -423,11 +461,13 @@ def run_ours(args):
         dev_id = str(local)
     sampler = ClockSampler(dev_id)
     time.sleep(0.3)
+    sampler.begin()
     e_begin.record(stream)
     for s in range(args.steps):
         step(ev=evs[s])
     e_end.record(stream)
     torch.cuda.synchronize()
+    sampler.end()
     clocks = sampler.stop()
     elapsed_ms = max_over_ranks(e_begin.elapsed_time(e_end))
     B.fa2_device_status()
@@ -463,6 +503,7 @@ def run_ours(args):
     e2e_sampler = ClockSampler(dev_id)
     time.sleep(0.3)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_sampler.begin()
     a.record(stream)
     for hs in h2d_streams:
         hs.wait_event(a)
@@ -498,6 +539,7 @@ def run_ours(args):
         stream.wait_stream(ds)
     b.record(stream)
     torch.cuda.synchronize()
+    e2e_sampler.end()
     e2e_clocks = e2e_sampler.stop()
     e2e_ms = max_over_ranks(a.elapsed_time(b)) / e2e_steps
     e2e = {"value": job_throughput(world, STEP_FLOPS, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

@@ -52,3 +52,35 @@ def test_roofline_peak_rule():
     assert bench.roofline_peak(1500.0, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})[0] == "burst"
     assert bench.roofline_peak(1500.0, {"sm_mhz": 1942.0, "sm_max_mhz": 2070.0})[0] == "sustained"
     assert bench.roofline_peak(1500.0, {"unavailable": "no samples"})[0] == "sustained"
+
+
+def test_clock_samples_are_taken_from_inside_the_timed_region():
+    """Only the nvidia-smi samples stamped inside the timed region describe it: a sample
+    before or after (an idle GPU at full clock) is left out, the stamps' time zone is
+    recovered from when the samples arrived, and a region shorter than the sampling
+    interval reports no clock rather than the idle one."""
+    import datetime
+    import bench
+
+    zone = 3600.0  # the stamps are an hour ahead of the host's epoch time
+    t_begin, t_end = 1_000_000.0, 1_000_000.1
+
+    def line(t, sm, power, cap="Not Active"):
+        stamp = datetime.datetime.fromtimestamp(t + zone).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return (t + 0.002, f"{stamp}, 0, {sm}, 2070, {power}, 0x0, Not Active, Not Active, Not Active, {cap}")
+
+    s = bench.ClockSampler("0", start=False)
+    s.lines = [line(t_begin - 0.05, 2070, 150.0), line(t_begin + 0.01, 1900, 900.0, "Active"),
+               line(t_begin + 0.05, 1800, 1300.0, "Active"), line(t_begin + 0.09, 1850, 1200.0),
+               line(t_end + 0.03, 2070, 1000.0), (t_end, "not, a, sample")]
+    s.t_begin, s.t_end = t_begin, t_end
+    r = s.summary()
+    assert r["samples"] == 3 and r["samples_total"] == 5
+    assert r["sm_mhz"] == 1850 and r["sm_min_mhz"] == 1800 and r["sm_max_mhz"] == 2070
+    assert r["power_w_max"] == 1300.0 and r["reasons"] == ["sw_power_cap"]
+    assert bench.roofline_peak(1500.0, r)[0] == "sustained"
+
+    s.t_begin, s.t_end = t_begin + 0.06, t_begin + 0.08  # between two samples
+    r = s.summary()
+    assert r["samples"] == 0 and r["sm_mhz"] is None and "note" in r
+    assert bench.roofline_peak(20.0, r)[0] == "burst"
