@@ -249,6 +249,28 @@ def test_backward_slice_from_stored_outputs():
         assert np.allclose(moved[2], base[2], atol=1e-13)
 
 
+def test_repeated_keys_reduce_to_the_distinct_ones():
+    """Keys repeated c times (key j a copy of key j mod P): the oracle on all c*P keys gives
+    the P-key O and dQ, the P-key LSE + ln c, and the P-key dK, dV over c for every copy,
+    including the rounding scales (dQ's over sqrt(c)). The large-size GPU test checks the
+    kernels through this reduction."""
+    n_p, c = 7, 5
+    q, d_o = _rand((1, 6, 4), 118), _rand((1, 6, 4), 119)
+    kp, vp = _rand((1, n_p, 4), 120), _rand((1, n_p, 4), 121)
+    k, v = np.tile(kp, (1, c, 1)), np.tile(vp, (1, c, 1))
+    scale = 0.53
+    o_p, l_p = A.forward(q, kp, vp, scale)
+    o, lse = A.forward(q, k, v, scale)
+    assert np.allclose(o, o_p, atol=1e-13) and np.allclose(lse, l_p + math.log(c), atol=1e-13)
+    full = A.backward_slice(q, k, v, d_o, scale, 0, row_chunk=4, rounding_scales=True)
+    red = A.backward_slice(q, kp, vp, d_o, scale, 0, row_chunk=4, rounding_scales=True)
+    assert np.allclose(full[0], red[0], atol=1e-13)
+    assert np.allclose(full[3], red[3] / math.sqrt(c), atol=1e-13)
+    for j in range(n_p * c):
+        for x, y in ((full[1], red[1]), (full[2], red[2]), (full[4], red[4]), (full[5], red[5])):
+            assert np.allclose(c * x[j], y[j % n_p], atol=1e-13)
+
+
 def test_backward_slice_rounding_scales_brute():
     """The root-sum-square scales of the last products, against explicit loops with fsum."""
     q, k, v, d_o = _rand((1, 4, 3), 114), _rand((1, 5, 3), 115), _rand((1, 5, 3), 116), _rand((1, 4, 3), 117)
@@ -586,3 +608,34 @@ def test_gradient_tolerance_rejects_errors():
     assert abs(bad[big] - dq[big]) > allowed[big]           # a 5 % error there is beyond its allowance
     with pytest.raises(AssertionError):
         check_16bit_grad(bad, dq, rss)
+
+
+def test_long_accumulation_bound():
+    """Recursive float32 summation that truncates each partial sum toward zero (as the
+    O accumulator's additions behave over very many key tiles) drifts linearly with the
+    number of additions: over 20,000 additions its error stays under n 2^-24 sum|x| and is
+    far above the random-walk size sqrt(n) 2^-24 sum|x|. check_16bit_long accepts an error
+    within 2e-2 max|ref| + n 2^-24 sum|x| per element and rejects one past it."""
+    from tests.tolerance import check_16bit_long
+    rng = np.random.default_rng(122)
+    x = (rng.standard_normal(20000) * 0.01 + 0.004).astype(np.float32)
+    acc = np.float32(0.0)
+    for xi in x:
+        exact = float(acc) + float(xi)
+        r = np.float32(exact)
+        if abs(float(r)) > abs(exact):
+            r = np.nextafter(r, np.float32(0.0))
+        acc = r
+    err = abs(float(acc) - math.fsum(float(t) for t in x))
+    total = math.fsum(abs(float(t)) for t in x)
+    n = len(x)
+    assert err <= n * 2.0 ** -24 * total
+    assert err > 20 * math.sqrt(n) * 2.0 ** -24 * total
+    ref = np.linspace(-0.3, 0.3, 64).reshape(4, 16)
+    weighted = np.full_like(ref, 0.8)
+    slack = 131079 * 2.0 ** -24 * 0.8
+    check_16bit_long(ref + 0.9 * (2e-2 * 0.3 + slack), ref, weighted, 131079, "within")
+    with pytest.raises(AssertionError):
+        check_16bit_long(ref + 1.1 * (2e-2 * 0.3 + slack), ref, weighted, 131079, "past")
+    with pytest.raises(AssertionError):
+        check_16bit_long(ref + 1.1 * 2e-2 * 0.3, ref, weighted, 0, "no additions")

@@ -26,6 +26,15 @@ of |ref|.  The test feeds both sides the same stored O and LSE, so that D (from 
 16-bit O pins D closer than about 2^-8 * sum_d |O_d dO_d|.  An RMS guard (RMS error
 <= 2^-6 * RMS of the oracle) on top makes a scaled, biased or zeroed gradient fail
 even where each element would pass.
+
+Outputs summed over very many key tiles in one float32 accumulator (`check_16bit_long`):
+the forward adds one key tile's P V at a time into O (and its row sums into l), so
+recursive summation over n tiles can move O_id by up to n * 2^-24 * sum_j P_ij |v_jd|
+(the standard bound, (n - 1) u times the sum of the absolute terms, for float32 u), and
+the additions that follow the tensor core's accumulation do approach it. That term
+is about 1.5e-5 at 256 key tiles; over 131,079 of them (16.8M keys) it reaches about
+0.8 % of the absolute weighted sum. The relative bound then becomes
+2e-2 * max|ref| + n * 2^-24 * sum_j P_ij |v_jd|, elementwise; the 2e-2 absolute bar stays.
 """
 import numpy as np
 
@@ -54,6 +63,21 @@ def check_16bit(got, ref, what="output"):
     bound = REL_16 * scale if scale > 0 else ZERO_REF_ABS
     ok = np.all(np.isfinite(got)) and err <= ABS_16 and err <= bound
     assert ok, f"{what}: max|err| = {err:.3e}, max|ref| = {scale:.3e} (bounds {ABS_16} and {REL_16}*max|ref|)"
+
+
+def check_16bit_long(got, ref, abs_weighted, n_adds, what="output"):
+    """The 16-bit bar for an output accumulated over n_adds key tiles in float32:
+    max|err| <= 2e-2, and elementwise |err| <= 2e-2 * max|ref| + n_adds * 2^-24 * abs_weighted,
+    abs_weighted = sum_j P_ij |v_jd| from the oracle."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err, scale = attention_error(got, ref)
+    allowed = REL_16 * scale + n_adds * 2.0 ** -24 * np.asarray(abs_weighted, dtype=np.float64)
+    excess = np.abs(got - ref) - allowed
+    ok = np.all(np.isfinite(got)) and err <= ABS_16 and np.all(excess <= 0)
+    worst = int(np.argmax(excess)) if excess.size else 0
+    assert ok, (f"{what}: max|err| = {err:.3e} (bar {ABS_16}); worst element exceeds its bound "
+                f"{allowed.flat[worst]:.3e} by {excess.flat[worst]:.3e}")
 
 
 def check_f32(got, ref, what="output"):
