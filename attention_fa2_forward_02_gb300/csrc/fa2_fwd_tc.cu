@@ -37,6 +37,15 @@
 // new tile maximum exceeds the reference maximum by at most 8 (base-2 units);
 // the reference then lags the true maximum by at most 8, so every exponent is
 // <= 2^8 and the final O = acc / l is the same quotient up to rounding.
+//
+// Few CTAs, many keys (fewer query-tile pairs than SMs): a thread-block cluster of
+// `splits` CTAs (2, 4 or 8) shares a query-tile pair, CTA r taking key tiles
+// [r L, min(n_kv, r L + L)), L = ceil(n_kv / splits). Each ends with its own (O_r, m_r,
+// l_r) per row; the cluster then combines them through distributed shared memory in the
+// Q/K/V buffers its loops no longer use: every CTA sends each row's (m_r, l_r) to all,
+// scales its O_r by 2^(m_r - M) / L (M the largest m_r, L the sum of l_r 2^(m_r - M)) and
+// sends each CTA the columns that CTA stores; each adds the parts in rank order (so the
+// result does not depend on timing) and writes its columns of O, rank 0 the LSE, M + log2 L.
 #include "common.cuh"
 #include "internal.h"
 
@@ -79,6 +88,10 @@ struct FwdCfg : Tile16<D> {
     static constexpr int kSmemBytes = kSmemMisc + 16 + 1024;  // + slack to align the base to 1024
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
     static_assert(256 + 2 * kNV * D <= (int)kTmemCols, "tensor memory budget");
+    // cluster combine: (m, l) of every CTA's 256 rows, then every CTA's share of each row
+    static constexpr int kExchMl = 0;
+    static constexpr int kExchRecv = 8 * 256 * 8;
+    static_assert(kExchRecv + 256 * D * 4 <= kSmemBar, "cluster combine buffers");
 };
 
 template <int D, bool kBf16, int kNV>
@@ -86,7 +99,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
     fa2_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v2,
                       void* __restrict__ o_ptr, void* __restrict__ o2_ptr, float* __restrict__ lse_ptr, int n_q, int n_k,
-                      int d_act, float scale_log2, unsigned int* status) {
+                      int d_act, float scale_log2, unsigned int* status, int splits) {
     using C = FwdCfg<D, kNV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -97,8 +110,16 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int bh = blockIdx.y;
-    const int q0 = blockIdx.x * (BM * kQTiles);
-    const int n_kv = (n_k + BN - 1) / BN;
+    // splits > 1: the CTAs of a cluster (consecutive blockIdx.x; the cluster is splits x 1 x 1,
+    // so blockIdx.x mod splits is the CTA's rank in it) share a query-tile pair
+    const int rank = (int)(blockIdx.x % (unsigned)splits);
+    const int q0 = (blockIdx.x / splits) * (BM * kQTiles);
+    const int n_kv_all = (n_k + BN - 1) / BN;
+    const int kv_len = (n_kv_all + splits - 1) / splits;
+    const int j0 = rank * kv_len;                          // this CTA's key tiles: [j0, j0 + n_kv)
+    const int n_kv = min(n_kv_all, j0 + kv_len) - j0;
+    float ep_m2 = 0.f, ep_l = 0.f;  // a softmax thread's row state, kept for the cluster combine
+    bool ep_ok = false;
 
     const uint32_t bars = base + C::kSmemBar;
     const uint32_t B_Q = bars;
@@ -163,7 +184,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 mbar_arrive_expect_tx(B_KF(s), C::kKVTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_3d(k_smem + s * C::kKVTileBytes + a * BN * C::kAtomRowBytes, &tm_k, B_KF(s),
-                                a * C::kAtomCols, j * BN, bh);
+                                a * C::kAtomCols, (j0 + j) * BN, bh);
                 if (j >= S && !(ok = mbar_wait(B_VE(s), release_parity, wd))) {
                     issued = 2 * j + 1;
                     break;
@@ -172,7 +193,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 for (int v = 0; v < kNV; ++v)
                     for (int a = 0; a < C::kAtoms; ++a)
                         tma_load_3d(v_smem + s * C::kVStageBytes + v * C::kKVTileBytes + a * BN * C::kAtomRowBytes,
-                                    v ? &tm_v2 : &tm_v, B_VF(s), a * C::kAtomCols, j * BN, bh);
+                                    v ? &tm_v2 : &tm_v, B_VF(s), a * C::kAtomCols, (j0 + j) * BN, bh);
                 issued = 2 * j + 2;
             }
             if (!ok) {
@@ -362,7 +383,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 for (int c = 0; c < BN / 32; ++c) reg_fence(sr[c]);
                 // Only the last key tile can be partial: its columns past the last key become
                 // -inf, which drops them from the maximum and gives them probability 0.
-                const int valid = n_k - j * BN;
+                const int valid = n_k - (j0 + j) * BN;
                 if (valid < BN) {
 #pragma unroll
                     for (int c = 0; c < BN / 32; ++c)
@@ -442,7 +463,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
             else mbar_arrive(B_PF(t));
         }
         if (ok) ok = warp_wait(B_OD, 0, wd);
-        if (ok) {
+        if (splits > 1) {
+            ep_m2 = m2;
+            ep_l = l;
+            ep_ok = ok;
+        } else if (ok) {
             tc_fence_after();
             const int row = q0 + t * BM + quarter * 32 + lane;
             const float inv_l = 1.f / l;
@@ -476,6 +501,61 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (splits > 1) {
+        // Every thread of every CTA of the cluster meets at each of the three barriers.
+        const bool row_thread = warp >= 2 && warp < 10;  // the softmax threads: one query row each
+        const int t = (warp - 2) >> 2, quarter = warp & 3;
+        const int row_l = t * BM + quarter * 32 + lane;  // row within the pair, 0..255
+        const int w = D / splits;                         // columns this CTA stores: [rank w, rank w + w)
+        const uint32_t ml = base + C::kExchMl, recv = base + C::kExchRecv;
+        cluster_sync_all();  // every CTA has left its key loop: its Q/K/V buffers are free
+        if (row_thread)
+            for (int r = 0; r < splits; ++r)
+                st_cluster_v2(cluster_map(ml + (uint32_t)((rank * 256 + row_l) * 8), (uint32_t)r), ep_m2, ep_l);
+        cluster_sync_all();
+        float big_m = -INFINITY, big_l = 0.f;
+        if (row_thread) {
+            const float2* mlp = reinterpret_cast<const float2*>(smem + C::kExchMl);
+            for (int r = 0; r < splits; ++r) big_m = fmaxf(big_m, mlp[r * 256 + row_l].x);
+            for (int r = 0; r < splits; ++r) big_l += mlp[r * 256 + row_l].y * ex2_approx(mlp[r * 256 + row_l].x - big_m);
+            const float f = ep_ok ? ex2_approx(ep_m2 - big_m) / big_l : 0.f;
+            tc_fence_after();
+            const uint32_t o_addr = tmem + ((uint32_t)(quarter * 32) << 16) + 256u + (uint32_t)(t * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(o_addr + 32u * c, r);
+                tmem_ld_wait();
+                reg_fence(r);
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const int col = 32 * c + 4 * g, owner = col / w;
+                    const uint32_t dst = recv + (uint32_t)(((rank * 256 + row_l) * w + col - owner * w) * 4);
+                    st_cluster_v4(cluster_map(dst, (uint32_t)owner), __uint_as_float(r[4 * g]) * f,
+                                  __uint_as_float(r[4 * g + 1]) * f, __uint_as_float(r[4 * g + 2]) * f,
+                                  __uint_as_float(r[4 * g + 3]) * f);
+                }
+            }
+        }
+        cluster_sync_all();
+        if (row_thread) {
+            const float* part = reinterpret_cast<const float*>(smem + C::kExchRecv);
+            const int row = q0 + row_l;
+            uint16_t* orow = reinterpret_cast<uint16_t*>(o_ptr) + ((size_t)bh * n_q + row) * d_act;
+            for (int g = 0; g < w; g += 4) {
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int r = 0; r < splits; ++r)  // in rank order
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) a[i] += part[(r * 256 + row_l) * w + g + i];
+                const int col = rank * w + g;  // d_act is a multiple of 8: a 4-column group is all in or all out
+                if (row < n_q && col < d_act)
+                    *reinterpret_cast<uint2*>(orow + col) = make_uint2(pack2<kBf16>(a[0], a[1]), pack2<kBf16>(a[2], a[3]));
+            }
+            if (rank == 0 && row < n_q) lse_ptr[(size_t)bh * n_q + row] = (big_m + lg2_approx(big_l)) * kLn2;
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -498,11 +578,29 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
     auto kern = fa2_fwd_tc_kernel<D, kBf16, kNV>;
     cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemBytes, slot);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((p.n_q + BM * kQTiles - 1) / (BM * kQTiles)), (unsigned)p.bh, 1);
+    const int64_t pairs = (p.n_q + BM * kQTiles - 1) / (BM * kQTiles);
     const float scale_log2 = p.scale * 1.4426950408889634f;
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k, p.d,
-                                                    scale_log2, p.status);
-    return cudaGetLastError();
+    const int splits = kNV == 1 ? fwd_key_splits(pairs * p.bh, (p.n_k + BN - 1) / BN) : 1;
+    if (splits == 1) {
+        const dim3 grid((unsigned)pairs, (unsigned)p.bh, 1);
+        kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k,
+                                                        p.d, scale_log2, p.status, 1);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(pairs * splits), (unsigned)p.bh, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)splits;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k, p.d, scale_log2,
+                              p.status, splits);
 }
 
 }  // namespace

@@ -33,6 +33,21 @@ inline int dq_key_splits(int64_t bh, int64_t n_q, int64_t n_k) {
     return s < 2 ? 1 : (int)s;
 }
 
+// Key ranges of the forward's cluster split (one CTA per range, the ranges of a query-tile
+// pair in one thread-block cluster): when the forward's CTAs (query-tile pairs x heads) would
+// fill at most half of a 148-SM part, the largest power of two up to 8 that keeps at most
+// 148 CTAs and at least 8 key tiles per range; else 1. A function of the sizes alone, so
+// that the results do not depend on the device.
+inline int fwd_key_splits(int64_t ctas, int64_t n_kt) {
+    if (ctas < 1 || 2 * ctas > 148) return 1;
+    int64_t cap = 148 / ctas;
+    if (cap > n_kt / 8) cap = n_kt / 8;
+    if (cap > 8) cap = 8;
+    int s = 1;
+    while (2 * s <= cap) s *= 2;
+    return s;
+}
+
 // Bytes of the float32 dQ partial sums of a split dQ pass ([splits, bh, n_q_pad, kernel
 // head size]); 0 when the pass is not split.
 inline size_t dq_partial_bytes(int64_t bh, int64_t n_q, int64_t n_k, int d) {

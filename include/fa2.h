@@ -78,9 +78,14 @@ typedef enum {
  * accumulation, the probabilities rounded to dtype before the P.V product.
  * dtype F32: any head_dim in [1, 128]; a float32 CUDA-core kernel (meant for
  * small problems; float32 products and sums throughout).
+ * Few query tiles, many keys (bh * ceil(n_q / 256) CTAs filling at most half of 148 SMs,
+ * at least 16 key tiles): the keys of each 256-row query block are split over a
+ * thread-block cluster of 2, 4 or 8 CTAs whose (O, max, sum) are combined in distributed
+ * shared memory, in a fixed order (the result depends on the sizes only).
  * Precision over long key ranges: each row's O and l are summed one 128-key tile at a
- * time in float32, so the error can grow like ceil(n_k / 128) * 2^-24 times
- * sum_j P_ij |v_j| (about 1.5e-5 at 32768 keys, 0.8 % at 16.8M keys).
+ * time in float32 over a CTA's key range, so the error can grow like (key tiles per
+ * CTA) * 2^-24 times sum_j P_ij |v_j| (about 1.5e-5 at 256 key tiles; 0.8 % at 131,079,
+ * which one head of 16.8M keys would give a single CTA, 0.1 % as the cluster's 8 ranges).
  * n_q and n_k are limited to 2^30 and bh to 65535 (FA2_ERR_UNSUPPORTED past them).
  * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED, FA2_ERR_CUDA.
  */

@@ -208,3 +208,62 @@ def test_forward_cross_attention_peaked_whole_heads():
     """B=1 H=32, N_q=1024 vs N_k=32768, d=128, K scaled by 8 (peaked rows): every row of O and
     LSE of the first and last heads against the oracle."""
     _whole_heads("config/cross_k8", 32, 1024, 32768, 128, 8.0, [0, 31], row_chunk=128)
+
+
+def _fwd_key_splits(ctas, n_kt):
+    """Mirror of the library's choice of key ranges per query-tile pair (a cluster of that many
+    CTAs): a power of two up to 8, at most 148 CTAs in all, at least 8 key tiles per range,
+    and only while the CTAs would fill at most half of 148 SMs."""
+    if 2 * ctas > 148:
+        return 1
+    cap = min(148 // ctas, n_kt // 8, 8)
+    s = 1
+    while 2 * s <= cap:
+        s *= 2
+    return s
+
+
+# (bh, n_q, n_k, splits the library takes): a query row alone, ragged query and key tails
+SPLIT_SHAPES = [(2, 128, 32768, 8), (1, 300, 5000, 4), (3, 200, 2100, 2), (2, 1, 4096, 4)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [32, 40, 64, 72, 128])
+@pytest.mark.parametrize("bh,n_q,n_k,splits", SPLIT_SHAPES)
+def test_forward_key_ranges_in_a_cluster(dtype, d, bh, n_q, n_k, splits):
+    """Few query tiles, many keys: the CTAs of a cluster each take a key range of a query-tile
+    pair and combine (O, m, l) through distributed shared memory. Every element of O and LSE
+    against the oracle; two runs bit-identical; nothing written outside O and LSE."""
+    torch = G.require_gpu()
+    assert _fwd_key_splits(bh * ((n_q + 255) // 256), (n_k + 127) // 128) == splits
+    q, k, v = G.inputs(f"fwdsplit/{dtype}/{d}/{bh}/{n_q}/{n_k}", bh, n_q, n_k, d, dtype)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd = (G.to_device(x, dtype) for x in (q, k, v))
+    runs = []
+    for _ in range(2):
+        o = G.guarded((bh, n_q, d), dtype)
+        lse = G.guarded((bh, n_q), "f32")
+        binding.fa2_forward(qd, kd, vd, o.t, lse.t, scale)
+        binding.fa2_device_status()
+        o.assert_intact("O")
+        lse.assert_intact("LSE")
+        runs.append((o.t.clone(), lse.t.clone()))
+    assert torch.equal(runs[0][0], runs[1][0]) and torch.equal(runs[0][1], runs[1][1])
+    o_ref, lse_ref = A.forward(synth.widen(q, dtype), synth.widen(k, dtype), synth.widen(v, dtype), scale)
+    check_16bit(G.to_f64(runs[0][0]), o_ref, "O")
+    check_lse(G.to_f64(runs[0][1]), lse_ref)
+
+
+def test_forward_key_ranges_peaked_rows():
+    """Keys scaled by 8 (peaked rows): the key ranges of a pair end with maxima far apart, so
+    the combine's rescaling by 2^(m_r - M) carries the result. B·H = 2, N_q = 200, N_k = 20000,
+    d = 128, eight ranges."""
+    G.require_gpu()
+    bh, n_q, n_k, d = 2, 200, 20000, 128
+    assert _fwd_key_splits(bh, (n_k + 127) // 128) == 8
+    q, k, v = G.inputs("fwdsplit/peaked", bh, n_q, n_k, d, "bf16", k_scale=8.0)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_forward(q, k, v, "bf16", scale)
+    o_ref, lse_ref = A.forward(synth.widen(q, "bf16"), synth.widen(k, "bf16"), synth.widen(v, "bf16"), scale)
+    check_16bit(o, o_ref, "O")
+    check_lse(lse, lse_ref)
