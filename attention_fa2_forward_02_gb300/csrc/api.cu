@@ -124,7 +124,11 @@ cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
 // one-pass against 1.58 / 1.75 ms for the two passes in one grid; head size 128:
 // 2.99 ms against 2.27 ms, where the reductions (4 bytes per query row, key tile
 // and head column) reach the L2's reduction throughput.
-static bool use_one_pass(int32_t head_dim) { return pad_head_dim(head_dim) <= 64; }
+// Shapes with many more queries than keys in few heads take the two passes at every head
+// size: their dK/dV pass splits each key tile's queries over a cluster (dkv_query_splits).
+static bool use_one_pass(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim) {
+    return pad_head_dim(head_dim) <= 64 && dkv_query_splits(bh, n_q, n_k) == 1;
+}
 
 // Workspace of the two-pass backward (the stage entry points, the PSA backward):
 // D and LSE2, float32, padded to a multiple of 128 rows per head.
@@ -154,7 +158,7 @@ fa2_status backward_common(const void* q, const void* k, const void* v, const vo
     const void* ptrs[] = {q, k, v, o, d_o, lse, dq, dk, dv};
     for (const void* ptr : ptrs)
         if (ptr && !aligned16(ptr)) return FA2_ERR_MISALIGNED;
-    one_pass = one_pass && stages == kBwdAll && use_one_pass(head_dim);
+    one_pass = one_pass && stages == kBwdAll && use_one_pass(bh, n_q, n_k, head_dim);
     const size_t need = one_pass ? fa2_backward_workspace_size(bh, n_q, n_k, head_dim, dtype)
                                  : two_pass_workspace_size(bh, n_q, n_k, head_dim, dtype);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return FA2_ERR_WORKSPACE;
@@ -229,7 +233,7 @@ fa2_status psa_fa2_forward(const void* packed, void* o_lo, void* o_hi, float* ls
 size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim, fa2_dtype dtype) {
     const size_t two_pass = two_pass_workspace_size(bh, n_q, n_k, head_dim, dtype);
     if (two_pass == 0) return 0;
-    if (!use_one_pass(head_dim)) return two_pass + dq_partial_bytes(bh, n_q, n_k, head_dim);
+    if (!use_one_pass(bh, n_q, n_k, head_dim)) return two_pass + dq_partial_bytes(bh, n_q, n_k, head_dim);
     const int64_t n_q_pad = (n_q + 127) / 128 * 128;
     return two_pass + (size_t)(bh * n_q_pad) * (size_t)pad_head_dim(head_dim) * sizeof(float);
 }

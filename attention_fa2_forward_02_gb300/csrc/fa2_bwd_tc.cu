@@ -138,13 +138,21 @@ __host__ __device__ constexpr uint32_t nb_stage(int s) { return 3 + (uint32_t)s;
 // current tile's last query tiles), and its first S^T and dP^T are issued while the
 // elementwise warps write the current tile's dK and dV. The tensor maps are the
 // kernel's own __grid_constant__ parameters (TMA reads them from parameter space).
-template <int D, bool kBf16, int kNV>
+//
+// kSplitQ: one key tile (n_items = 1) over one of `splits` query ranges, the CTAs of the
+// ranges in one thread-block cluster (consecutive blockIdx.x, blockIdx.x mod splits the
+// rank; range r = query tiles [r L, min(n_qt, r L + L)), L = ceil(n_qt / splits)). Each
+// ends with its range's share of dK and dV in tensor memory; every CTA then sends each
+// CTA the columns that CTA writes, through distributed shared memory in the buffers its
+// loops no longer use, and each adds the shares of its columns in rank order and stores
+// them.
+template <int D, bool kBf16, int kNV, bool kSplitQ = false>
 __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                          const CUtensorMap& tm_do, const CUtensorMap& tm_v2, const CUtensorMap& tm_do2,
                                          const CUtensorMap& tm_dk, const CUtensorMap& tm_dv, const float* __restrict__ lse2, const float* __restrict__ delta,
                                          void* __restrict__ dk, void* __restrict__ dv, void* __restrict__ dv2, int n_q,
                                          int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
-                                         unsigned int* status, int kt, int n_items, int bh) {
+                                         unsigned int* status, int kt, int n_items, int bh, int splits = 1) {
     using C = BwdCfg<D, kNV>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -152,8 +160,17 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* smem = smem_raw + (base - raw_addr);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_qt = (n_q + BT - 1) / BT;
+    int n_qt = (n_q + BT - 1) / BT, q_lo = 0, rank = 0;  // query tiles [q_lo, q_lo + n_qt)
+    if constexpr (kSplitQ) {
+        static_assert(kNV == 1, "split query ranges with one value tensor");
+        rank = (int)(blockIdx.x % (unsigned)splits);
+        const int len = (n_qt + splits - 1) / splits;
+        q_lo = rank * len;
+        n_qt = min(n_qt, q_lo + len) - q_lo;
+        n_items = 1;
+    }
     if constexpr (!C::kNamed) n_items = 1;
+    bool elem_ok = false;  // an elementwise thread's state at the end, for the split's combine
 
     const Bars bars{base + C::kDkvBar, S};
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kDkvBar + C::kNumBars * 8);
@@ -201,13 +218,13 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                     if (g >= S && !(ok = mbar_wait(bars.empty(s), ((g / S) & 1) ^ 1, wd))) break;
                     mbar_arrive_expect_tx(bars.full(s), (1 + kNV) * C::kTile + 2 * BT * 4);
                     for (int a = 0; a < C::kAtoms; ++a) {
-                        tma_load_3d(stage_q(s) + a * BT * C::kAtomRowBytes, &tm_q, bars.full(s), a * C::kAtomCols, i * BT,
-                                    bh);
+                        tma_load_3d(stage_q(s) + a * BT * C::kAtomRowBytes, &tm_q, bars.full(s), a * C::kAtomCols,
+                                    (q_lo + i) * BT, bh);
                         for (int v = 0; v < kNV; ++v)
                             tma_load_3d(stage_do(s, v) + a * BT * C::kAtomRowBytes, v ? &tm_do2 : &tm_do, bars.full(s),
-                                        a * C::kAtomCols, i * BT, bh);
+                                        a * C::kAtomCols, (q_lo + i) * BT, bh);
                     }
-                    const size_t w = (size_t)bh * n_q_pad + (size_t)i * BT;
+                    const size_t w = (size_t)bh * n_q_pad + (size_t)(q_lo + i) * BT;
                     bulk_load(stage_l2(s), lse2 + w, BT * 4, bars.full(s));
                     bulk_load(stage_dl(s), delta + w, BT * 4, bars.full(s));
                     issued = g + 1;
@@ -472,7 +489,8 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
         }
         // dK, dV of key tile u: read out of tensor memory before this warp's next e1 arrival
         if (ok) ok = warp_wait(bars.done(), (uint32_t)(u & 1), wd);
-        if (ok) {
+        if constexpr (kSplitQ) elem_ok = ok;  // the cluster adds the ranges' shares below
+        else if (ok) {
             tc_fence_after();
             const int key0 = (kt + u) * BT + quarter * 32;  // first key row of this warp
             const int key = key0 + lane;
@@ -503,6 +521,56 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (kSplitQ) {
+        // Every thread of every CTA of the cluster meets at each of the two barriers. The
+        // shares land in [splits][128 rows][dV, dK][w columns] float32 from shared address 0
+        // (the K, V and stage buffers, idle once every CTA's loops are over).
+        static_assert(128 * 2 * D * 4 <= C::kDkvBar, "split combine buffer");
+        const bool elem = warp >= 2 && warp < 10;
+        const int quarter = warp & 3, half = (warp - 2) >> 2;  // half 0: dV, half 1: dK
+        const int row = quarter * 32 + lane;                   // key row within the tile
+        const int w = D / splits;                               // columns this CTA writes: [rank w, rank w + w)
+        cluster_sync_all();
+        if (elem) {
+            tc_fence_after();
+            const uint32_t src = tmem + ((uint32_t)(quarter * 32) << 16) + 256u + (uint32_t)(half * D);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(src + 32u * c, r);
+                tmem_ld_wait();
+                reg_fence(r);
+                const float keep = elem_ok ? 1.f : 0.f;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    const int col = 32 * c + 4 * g, owner = col / w;
+                    const uint32_t dst = base + (uint32_t)((((rank * 128 + row) * 2 + half) * w + col - owner * w) * 4);
+                    st_cluster_v4(cluster_map(dst, (uint32_t)owner), __uint_as_float(r[4 * g]) * keep,
+                                  __uint_as_float(r[4 * g + 1]) * keep, __uint_as_float(r[4 * g + 2]) * keep,
+                                  __uint_as_float(r[4 * g + 3]) * keep);
+                }
+            }
+        }
+        cluster_sync_all();
+        if (elem) {
+            const float* part = reinterpret_cast<const float*>(smem);
+            const int key = kt * BT + row;
+            const float mul = half ? scale : 1.f;
+            uint16_t* grow = static_cast<uint16_t*>(half ? dk : dv) + ((size_t)bh * n_k + key) * d_act;
+            for (int g = 0; g < w; g += 4) {
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int r = 0; r < splits; ++r)  // in rank order
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) a[i] += part[((r * 128 + row) * 2 + half) * w + g + i];
+                const int col = rank * w + g;  // d_act is a multiple of 8: a 4-column group is all in or all out
+                if (key < n_k && col < d_act)
+                    *reinterpret_cast<uint2*>(grow + col) =
+                        make_uint2(pack2<kBf16>(a[0] * mul, a[1] * mul), pack2<kBf16>(a[2] * mul, a[3] * mul));
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kBwdTmemCols);
@@ -925,6 +993,21 @@ __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
                             n_q_pad, d_act, scale, scale_log2, status, blockIdx.x, 1, blockIdx.y);
 }
 
+// The dK/dV pass with each key tile's queries split over a cluster of `splits` CTAs
+// (grid x = key tiles x splits, cluster splits x 1 x 1).
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(BwdCfg<D, 1>::kThreads, 1)
+    bwd_dkdv_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                          const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                          const float* __restrict__ lse2, const float* __restrict__ delta, void* __restrict__ dk,
+                          void* __restrict__ dv, int n_q, int n_k, int n_q_pad, int d_act, float scale, float scale_log2,
+                          unsigned int* status, int splits) {
+    dkdv_cta<D, kBf16, 1, true>(tm_q, tm_k, tm_v, tm_do, tm_v, tm_do, tm_dk, tm_dv, lse2, delta, dk, dv, nullptr, n_q,
+                                n_k, n_q_pad, d_act, scale, scale_log2, status, (int)(blockIdx.x / (unsigned)splits), 1,
+                                blockIdx.y, splits);
+}
+
 template <int D, bool kBf16, int kNV>
 __global__ void __launch_bounds__(BwdCfg<D, kNV>::kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -1068,6 +1151,29 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     };
     cudaError_t e = cudaSuccess;
     const int n_kt = (int)((p.n_k + BT - 1) / BT), n_qt = (int)((p.n_q + BT - 1) / BT);
+    // many queries, few key tiles: the dK/dV pass over query ranges in clusters, then the dQ pass
+    const int qsplits = C::kNamed ? dkv_query_splits(p.bh, p.n_q, p.n_k) : 1;
+    if (qsplits > 1 && (stages & kBwdDkDv)) {
+        auto kern = bwd_dkdv_split_kernel<D, kBf16>;
+        e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemDkv, 52 + (slot - 16) / 2);  // slots 52..61
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(n_kt * qsplits), (unsigned)p.bh, 1);
+        cfg.blockDim = dim3(C::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::kSmemDkv;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)qsplits;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tdk, tdv, p.lse2, p.delta, p.dk, p.dv, (int)p.n_q, (int)p.n_k,
+                               (int)p.n_q_pad, p.d, p.scale, scale_log2, p.status, qsplits);
+        if (e != cudaSuccess) return e;
+        stages &= ~kBwdDkDv;  // the dQ pass follows on its own
+    }
     if ((stages & (kBwdDkDv | kBwdDq)) == (kBwdDkDv | kBwdDq)) {
         auto both = bwd_passes_kernel<D, kBf16, kNV>;
         constexpr int smem = C::kSmemDkv > C::kSmemDq ? C::kSmemDkv : C::kSmemDq;

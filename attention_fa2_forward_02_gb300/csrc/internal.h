@@ -48,6 +48,23 @@ inline int fwd_key_splits(int64_t ctas, int64_t n_kt) {
     return s;
 }
 
+// Query ranges the dK/dV pass divides each key tile's queries into (one CTA per range, the
+// ranges of a key tile in one thread-block cluster that adds their dK and dV in distributed
+// shared memory): when the dK/dV CTAs (key tiles x heads) would fill at most half of a
+// 148-SM part, the largest power of two up to 8 that keeps at most 148 CTAs and at least
+// 8 query tiles per range; else 1. Used for queries far outnumbering the keys of few heads,
+// where unsplit dK/dV CTAs would each walk every query tile. A function of the sizes alone.
+inline int dkv_query_splits(int64_t bh, int64_t n_q, int64_t n_k) {
+    const int64_t ctas = bh * ((n_k + 127) / 128), n_qt = (n_q + 127) / 128;
+    if (ctas < 1 || 2 * ctas > 148) return 1;
+    int64_t cap = 148 / ctas;
+    if (cap > n_qt / 8) cap = n_qt / 8;
+    if (cap > 8) cap = 8;
+    int s = 1;
+    while (2 * s <= cap) s *= 2;
+    return s;
+}
+
 // Bytes of the float32 dQ partial sums of a split dQ pass ([splits, bh, n_q_pad, kernel
 // head size]); 0 when the pass is not split.
 inline size_t dq_partial_bytes(int64_t bh, int64_t n_q, int64_t n_k, int d) {

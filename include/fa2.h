@@ -103,6 +103,9 @@ fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, flo
  *   [bh, n_q_pad, hd]                                           (4 * bh * n_q_pad * hd bytes),
  *   for head_dim > 64 when the dQ pass is split, its float32 partial sums
  *   [splits, bh, n_q_pad, hd]                          (4 * splits * bh * n_q_pad * hd bytes).
+ * Shapes whose dK/dV pass splits its queries over clusters (see fa2_backward) take the
+ * two passes at every head_dim and need no dQ accumulator; their dK/dV shares are added in
+ * shared memory and take no workspace.
  * The dQ pass (one CTA per 128-row query tile, looping over all key tiles) is split when
  * its CTAs, ceil(n_q / 128) * bh of them, would be fewer than about 148 (one wave): each
  * query tile's keys are divided into splits = min(ceil(148 / (bh * ceil(n_q / 128))),
@@ -133,6 +136,13 @@ size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t
  *    The page's dQ pass recomputes S and dP; at these head sizes that costs more
  *    than the reductions.  The reductions land in any order, so dq is not
  *    bit-reproducible from run to run here (dk and dv are).
+ *  - many more queries than keys in few heads (bh * ceil(n_k / 128) key tiles filling
+ *    at most half of 148 SMs, at least 16 query tiles): the two launches at every
+ *    head_dim, the dK/dV pass splitting each key tile's queries over a thread-block
+ *    cluster of 2, 4 or 8 CTAs that add their shares in distributed shared memory,
+ *    in a fixed order (bit-reproducible).
+ *  - few query tiles, many keys: the dQ pass splits each query tile's keys into
+ *    ranges whose float32 partial sums the workspace holds, added in a fixed order.
  *
  *   q, o, d_o   [bh, n_q, head_dim]  dtype, device, read (o and lse as written by fa2_forward)
  *   k, v        [bh, n_k, head_dim]  dtype, device, read

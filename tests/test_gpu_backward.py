@@ -339,3 +339,68 @@ def test_backward_split_dq_pass(bh, n_q, n_k, d, dtype):
     ref = A.backward(w(q), w(k), w(v), w(d_o), scale)
     for name, a, r in zip(("dQ", "dK", "dV"), runs[0], ref):
         check_16bit(G.to_f64(a.t), r, f"{name} (dQ pass in {splits} key ranges)")
+
+
+def _dkv_query_splits(bh, n_q, n_k):
+    """Mirror of the library's choice of query ranges per key tile for the dK/dV pass (a
+    cluster of that many CTAs): a power of two up to 8, at most 148 CTAs, at least 8 query
+    tiles per range, and only while the dK/dV CTAs would fill at most half of 148 SMs."""
+    ctas, n_qt = bh * -(-n_k // 128), -(-n_q // 128)
+    if 2 * ctas > 148:
+        return 1
+    cap = min(148 // ctas, n_qt // 8, 8)
+    s = 1
+    while 2 * s <= cap:
+        s *= 2
+    return s
+
+
+# (bh, n_q, n_k, query ranges the dK/dV pass takes): many queries, few key tiles
+DKV_SPLIT_SHAPES = [(2, 32768, 128, 8), (4, 16384, 256, 8), (3, 3000, 300, 2), (1, 2000, 1000, 2)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [32, 40, 64, 72, 128])
+@pytest.mark.parametrize("bh,n_q,n_k,splits", DKV_SPLIT_SHAPES)
+def test_backward_dkdv_query_ranges_in_a_cluster(dtype, d, bh, n_q, n_k, splits):
+    """Queries far outnumbering the keys of few heads: the dK/dV pass splits each key tile's
+    queries over a cluster of CTAs that add their dK and dV in distributed shared memory
+    (every head size then takes the two passes). dQ, dK, dV against the oracle; two runs
+    bit-identical; nothing written outside the gradients."""
+    torch = G.require_gpu()
+    assert _dkv_query_splits(bh, n_q, n_k) == splits
+    tag = f"bwdsplitq/{dtype}/{d}/{bh}/{n_q}/{n_k}"
+    q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
+    d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)
+    scale = 1 / math.sqrt(d)
+    qd, kd, vd, dod = (G.to_device(x, dtype) for x in (q, k, v, d_o))
+    o = G.empty((bh, n_q, d), dtype)
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    code = {"bf16": binding.DTYPE_BF16, "f16": binding.DTYPE_F16}[dtype]
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, code), dtype=torch.uint8, device="cuda")
+    runs = []
+    for _ in range(2):
+        grads = [G.guarded(tuple(x.shape), dtype) for x in (q, k, v)]
+        binding.fa2_backward(qd, kd, vd, o, dod, lse, *(g.t for g in grads), ws, scale)
+        binding.fa2_device_status()
+        for name, g in zip(("dQ", "dK", "dV"), grads):
+            g.assert_intact(name)
+        runs.append([g.t.clone() for g in grads])
+    for name, a, b in zip(("dQ", "dK", "dV"), *runs):
+        assert torch.equal(a, b), f"{name} differs between two runs"
+    # dK and dV sum over up to 32768 queries (|dK| ~ 10, where a bfloat16 step is 0.04): the
+    # elementwise gradient bound, from the stored O and LSE the kernels read
+    w = lambda x: synth.widen(x, dtype)  # noqa: E731
+    o_st, l_st = G.to_f64(o), G.to_f64(lse)
+    got = [G.to_f64(g) for g in runs[0]]
+    for b in range(bh):
+        rq, rk, rv, sq, sk, sv = A.backward_slice(w(q), w(k), w(v), w(d_o), scale, b, row_chunk=4096, o=o_st,
+                                                  lse=l_st, rounding_scales=True)
+        check_16bit_grad(got[0][b], rq, sq, dtype, f"dQ head {b}")
+        check_16bit_grad(got[1][b], rk, sk, dtype, f"dK head {b}")
+        check_16bit_grad(got[2][b], rv, sv, dtype, f"dV head {b}")
+    if d == 128 and dtype == "bf16":  # the stage entry points take the same split, bit for bit
+        staged = _stages(qd, kd, vd, o, dod, lse, scale, ws, dtype)
+        for name, a, b in zip(("dQ", "dK", "dV"), runs[0], staged):
+            assert torch.equal(a, b), f"{name}: stages differ from fa2_backward"

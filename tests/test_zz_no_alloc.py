@@ -77,10 +77,12 @@ def test_noalloc_matches_backward_on_two_calls_in_a_row():
 
 
 def test_noalloc_two_pass_when_the_accumulator_does_not_fit():
-    """8 heads x 4096 query rows, head_dim 64: the one-pass workspace (8.65 MB with its dQ
-    accumulator) exceeds the fixed 8 MiB scratch, the two-pass one (256 KiB) fits."""
+    """8 heads x 4096 query rows x 1280 keys, head_dim 64: the one-pass workspace (8.65 MB
+    with its dQ accumulator) exceeds the fixed 8 MiB scratch, the two-pass one (256 KiB)
+    fits. (With fewer keys the shape would leave the one-pass kernel anyway: its dK/dV pass
+    would split the queries over clusters, which the two passes do.)"""
     torch = G.require_gpu()
-    bh, n_q, n_k, d = 8, 4096, 512, 64
+    bh, n_q, n_k, d = 8, 4096, 1280, 64
     assert binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_BF16) > 8 << 20
     args = _problem("noalloc/c", bh, n_q, n_k, d, "bf16")
     got = [torch.empty_like(args[0]), torch.empty_like(args[1]), torch.empty_like(args[2])]
