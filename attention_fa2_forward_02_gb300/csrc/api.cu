@@ -124,10 +124,15 @@ cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
 // one-pass against 1.58 / 1.75 ms for the two passes in one grid; head size 128:
 // 2.99 ms against 2.27 ms, where the reductions (4 bytes per query row, key tile
 // and head column) reach the L2's reduction throughput.
-// Shapes with many more queries than keys in few heads take the two passes at every head
-// size: their dK/dV pass splits each key tile's queries over a cluster (dkv_query_splits).
+// The one-pass kernel runs one CTA per key tile of each head; with fewer than half of a
+// 148-SM part's worth of them (bh * ceil(n_k / 128) <= 74) the two passes in one grid,
+// whose dQ CTAs and key-range and query-range splits add parallelism, are faster (GB300,
+// bf16, d = 64: B*H = 2, N = 4096: 0.068 -> 0.050 ms; B*H = 1, N = 8192: 0.117 -> 0.086 ms;
+// at 128 and 256 key-tile CTAs the one-pass kernel stays ahead: 0.070 / 0.076 against
+// 0.089 / 0.086 ms). Those shapes take the two passes at every head size.
 static bool use_one_pass(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim) {
-    return pad_head_dim(head_dim) <= 64 && dkv_query_splits(bh, n_q, n_k) == 1;
+    (void)n_q;
+    return pad_head_dim(head_dim) <= 64 && 2 * bh * ((n_k + 127) / 128) > 148;
 }
 
 // Workspace of the two-pass backward (the stage entry points, the PSA backward):

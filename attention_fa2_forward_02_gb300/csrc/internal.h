@@ -50,13 +50,16 @@ inline int fwd_key_splits(int64_t ctas, int64_t n_kt) {
 
 // Query ranges the dK/dV pass divides each key tile's queries into (one CTA per range, the
 // ranges of a key tile in one thread-block cluster that adds their dK and dV in distributed
-// shared memory): when the dK/dV CTAs (key tiles x heads) would fill at most half of a
-// 148-SM part, the largest power of two up to 8 that keeps at most 148 CTAs and at least
-// 8 query tiles per range; else 1. Used for queries far outnumbering the keys of few heads,
-// where unsplit dK/dV CTAs would each walk every query tile. A function of the sizes alone.
+// shared memory): for queries far outnumbering the keys (at least 16 query tiles per key
+// tile) of few heads (the dK/dV CTAs, key tiles x heads, filling at most half of a 148-SM
+// part), the largest power of two up to 8 that keeps at most 148 CTAs and at least 8 query
+// tiles per range; else 1. The split pass runs apart from the dQ pass, so it pays only
+// where unsplit dK/dV CTAs would each walk far more query tiles than the dQ CTAs walk key
+// tiles (measured on GB300, d = 128: 16 query tiles per key tile 1.2x faster, 8 and fewer
+// slower than the one-grid passes). A function of the sizes alone.
 inline int dkv_query_splits(int64_t bh, int64_t n_q, int64_t n_k) {
-    const int64_t ctas = bh * ((n_k + 127) / 128), n_qt = (n_q + 127) / 128;
-    if (ctas < 1 || 2 * ctas > 148) return 1;
+    const int64_t n_kt = (n_k + 127) / 128, ctas = bh * n_kt, n_qt = (n_q + 127) / 128;
+    if (ctas < 1 || 2 * ctas > 148 || n_qt < 16 * n_kt) return 1;
     int64_t cap = 148 / ctas;
     if (cap > n_qt / 8) cap = n_qt / 8;
     if (cap > 8) cap = 8;

@@ -99,13 +99,12 @@ fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, flo
  * and hd = head_dim rounded up to 32, 64 or 128, the workspace holds
  *   the row sums D = rowsum(O * dO), float32 [bh, n_q_pad]      (4 * bh * n_q_pad bytes),
  *   a base-2 copy of the LSE, float32 [bh, n_q_pad]             (4 * bh * n_q_pad bytes),
- *   for head_dim <= 64 (the one-pass backward), the float32 dQ accumulator
+ *   for the one-pass backward (head_dim <= 64, bh * ceil(n_k / 128) > 74), the float32 dQ accumulator
  *   [bh, n_q_pad, hd]                                           (4 * bh * n_q_pad * hd bytes),
  *   for head_dim > 64 when the dQ pass is split, its float32 partial sums
  *   [splits, bh, n_q_pad, hd]                          (4 * splits * bh * n_q_pad * hd bytes).
- * Shapes whose dK/dV pass splits its queries over clusters (see fa2_backward) take the
- * two passes at every head_dim and need no dQ accumulator; their dK/dV shares are added in
- * shared memory and take no workspace.
+ * A dK/dV pass split over query ranges (see fa2_backward) adds its shares in shared
+ * memory and takes no workspace.
  * The dQ pass (one CTA per 128-row query tile, looping over all key tiles) is split when
  * its CTAs, ceil(n_q / 128) * bh of them, would be fewer than about 148 (one wave): each
  * query tile's keys are divided into splits = min(ceil(148 / (bh * ceil(n_q / 128))),
@@ -130,17 +129,19 @@ size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t
  *  - head_dim > 64: the page's structure, a pass over key tiles (dK, dV) and a
  *    pass over query tiles (dQ), after the row sums D: two launches (the stage
  *    entry points fa2_backward_preprocess and fa2_backward_passes below);
- *  - head_dim <= 64: the row sums D (and a reset of the dQ accumulator), one
- *    pass over key tiles that also adds each tile's share of dQ into a float32
- *    accumulator in the workspace with reductions, and a rounding pass for dq.
+ *  - head_dim <= 64 with more than 74 key tiles in all (bh * ceil(n_k / 128) > 74;
+ *    fewer run the two launches above): the row sums D (and a reset of the dQ
+ *    accumulator), one pass over key tiles that also adds each tile's share of dQ
+ *    into a float32 accumulator in the workspace with reductions, and a rounding
+ *    pass for dq.
  *    The page's dQ pass recomputes S and dP; at these head sizes that costs more
  *    than the reductions.  The reductions land in any order, so dq is not
  *    bit-reproducible from run to run here (dk and dv are).
  *  - many more queries than keys in few heads (bh * ceil(n_k / 128) key tiles filling
- *    at most half of 148 SMs, at least 16 query tiles): the two launches at every
- *    head_dim, the dK/dV pass splitting each key tile's queries over a thread-block
- *    cluster of 2, 4 or 8 CTAs that add their shares in distributed shared memory,
- *    in a fixed order (bit-reproducible).
+ *    at most half of 148 SMs, at least 16 query tiles per key tile): the dK/dV pass
+ *    splits each key tile's queries over a thread-block cluster of 2, 4 or 8 CTAs
+ *    that add their shares in distributed shared memory, in a fixed order
+ *    (bit-reproducible), and the dQ pass follows as its own launch.
  *  - few query tiles, many keys: the dQ pass splits each query tile's keys into
  *    ranges whose float32 partial sums the workspace holds, added in a fixed order.
  *

@@ -48,6 +48,34 @@ def test_backward_vs_oracle(dtype, d, bh, n_q, n_k):
     check_16bit(dv, rv, "dV")
 
 
+def _one_pass(bh, n_k, d):
+    """Whether fa2_backward takes the one-pass kernel: head size up to 64 and more than 74
+    key tiles in all (fewer take the two passes)."""
+    return d <= 64 and 2 * bh * -(-n_k // 128) > 148
+
+
+# many heads, so that head sizes up to 64 take the one-pass kernel; ragged query and key tails
+ONE_PASS_SHAPES = [(80, 300, 150), (160, 129, 77), (75, 64, 1000), (96, 1, 129)]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("d", [32, 40, 64])
+@pytest.mark.parametrize("bh,n_q,n_k", ONE_PASS_SHAPES)
+def test_backward_one_pass_vs_oracle(dtype, d, bh, n_q, n_k):
+    """The one-pass kernel (head size <= 64, more than 74 key tiles in all) on ragged shapes."""
+    assert _one_pass(bh, n_k, d)
+    tag = f"bwd1p/{dtype}/{d}/{bh}/{n_q}/{n_k}"
+    q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
+    d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)
+    scale = 1 / math.sqrt(d)
+    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, dtype, scale)
+    w = lambda x: synth.widen(x, dtype)  # noqa: E731
+    rq, rk, rv = A.backward(w(q), w(k), w(v), w(d_o), scale)
+    check_16bit(dq, rq, "dQ")
+    check_16bit(dk, rk, "dK")
+    check_16bit(dv, rv, "dV")
+
+
 def test_backward_gradient_identities():
     """sum_j dV_j = sum_i dO_i and sum_j dK_j = 0 (the rows of P sum to one) on the GPU result."""
     bh, n, d = 2, 384, 64
@@ -156,10 +184,11 @@ def _stages(qd, kd, vd, o, dod, lse, scale, ws, dtype):
 def test_backward_stages_vs_oracle_and_whole(d, dtype):
     """fa2_backward_preprocess + _dkdv + _dq (the pages' two-pass structure, from the smaller
     two-pass workspace) against the oracle and bit-reproducible from run to run; equal to
-    fa2_backward bit for bit where that is the same two passes (head_dim > 64), within the
-    parity bar of its one-pass result otherwise."""
+    fa2_backward bit for bit where that takes the same two passes (head_dim > 64, or too few
+    key tiles for the one-pass kernel), within the parity bar of its one-pass result
+    otherwise (40 heads here at head size 64)."""
     torch = G.require_gpu()
-    bh, n_q, n_k = 2, 333, 250
+    bh, n_q, n_k = (40 if d <= 64 else 2), 333, 250
     q, k, v = G.inputs(f"bwd/stages/{d}", bh, n_q, n_k, d, dtype)
     d_o = synth.tensor(f"bwd/stages/{d}/do", (bh, n_q, d), dtype)
     qd, kd, vd, dod = (G.to_device(x, dtype) for x in (q, k, v, d_o))
@@ -172,6 +201,7 @@ def test_backward_stages_vs_oracle_and_whole(d, dtype):
     whole = [G.empty(x.shape, dtype) for x in (q, k, v)]
     binding.fa2_backward(qd, kd, vd, o, dod, lse, *whole, ws, scale)
     small = torch.empty(8 * bh * 384, dtype=torch.uint8, device="cuda")  # D and LSE2 only
+    assert _one_pass(bh, n_k, d) == (d <= 64)
     staged = _stages(qd, kd, vd, o, dod, lse, scale, small, dtype)
     again = _stages(qd, kd, vd, o, dod, lse, scale, small, dtype)
     one_grid = [G.empty(tuple(x.shape), dtype) for x in (qd, kd, vd)]
@@ -185,7 +215,7 @@ def test_backward_stages_vs_oracle_and_whole(d, dtype):
     for name, a, b, c, r in zip(("dQ", "dK", "dV"), staged, whole, again, ref):
         check_16bit(G.to_f64(a), r, f"two-pass {name}")
         assert torch.equal(a, c), f"two-pass {name} not reproducible"
-        if d > 64:
+        if not _one_pass(bh, n_k, d):
             assert torch.equal(a, b), f"fa2_backward {name} differs from its stages"
         else:
             check_16bit(G.to_f64(a), G.to_f64(b), f"two-pass vs one-pass {name}")
@@ -196,8 +226,9 @@ def test_backward_reproducibility(d):
     """head_dim > 64 (two passes): every gradient is bit-reproducible.  head_dim <= 64 (one
     pass): dK and dV are; dQ is a float32 sum of per-key-tile partial sums added in arrival
     order, so two runs may differ by rounding, at most one unit in the last place of the
-    16-bit result."""
-    bh, n = 2, 300
+    16-bit result (80 heads at head size 64, for the one-pass kernel)."""
+    bh, n = (80 if d <= 64 else 2), 300
+    assert _one_pass(bh, n, d) == (d <= 64)
     q, k, v = G.inputs(f"bwd/det/{d}", bh, n, n, d, "bf16")
     d_o = synth.tensor(f"bwd/det/{d}/do", (bh, n, d), "bf16")
     a = run_fwd_bwd(q, k, v, d_o, "bf16", 1 / math.sqrt(d))
@@ -213,8 +244,13 @@ def test_backward_reproducibility(d):
 def test_backward_far_negative_scores_with_a_partial_key_tile(d):
     """Every score near -110 (LSE near -105): a padded key of the last, partial key tile has
     score 0 and probability exp(0 - LSE), beyond float32; the kernels must keep it out of
-    dQ (one-pass head size 64, two-pass 128) and stay finite."""
-    bh, n_q, n_k = 1, 150, 200
+    dQ (one-pass head size 64 with its 80 heads, two-pass 128) and stay finite. The keys sit
+    near -6.9 in every column and sum_j dS_ij = 0, so dQ is a small difference of large
+    terms: the elementwise bound with the rounding scale of its last product, from the
+    stored O and LSE the kernels read (tests/tolerance.py)."""
+    torch = G.require_gpu()
+    bh, n_q, n_k = (80 if d <= 64 else 1), 150, 200
+    assert _one_pass(bh, n_k, d) == (d <= 64)
     scale = 1 / math.sqrt(d)
     q = synth.to_storage(np.full((bh, n_q, d), 2.0), "bf16")
     k_base = -110.0 / (2.0 * d * scale)
@@ -222,16 +258,28 @@ def test_backward_far_negative_scores_with_a_partial_key_tile(d):
                          "bf16")
     v = synth.tensor(f"bwd/farneg/{d}/v", (bh, n_k, d), "bf16")
     d_o = synth.tensor(f"bwd/farneg/{d}/do", (bh, n_q, d), "bf16")
-    dq, dk, dv = run_fwd_bwd(q, k, v, d_o, "bf16", scale)
+    qd, kd, vd, dod = (G.to_device(x, "bf16") for x in (q, k, v, d_o))
+    o = G.empty((bh, n_q, d), "bf16")
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    grads = [G.empty(x.shape, "bf16") for x in (q, k, v)]
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_BF16), dtype=torch.uint8,
+                     device="cuda")
+    binding.fa2_backward(qd, kd, vd, o, dod, lse, *grads, ws, scale)
+    binding.fa2_device_status()
+    dq, dk, dv = (G.to_f64(g) for g in grads)
     for x in (dq, dk, dv):
         assert np.all(np.isfinite(x))
-    w = lambda x: synth.widen(x, "bf16")
-    rq, rk, rv = A.backward(w(q), w(k), w(v), w(d_o), scale)
-    _, lse = A.forward(w(q), w(k), w(v), scale)
-    assert np.max(lse) < -89  # exp(-LSE) overflows float32: the regime this test is about
-    check_16bit(dq, rq, "dQ")
-    check_16bit(dk, rk, "dK")
-    check_16bit(dv, rv, "dV")
+    w = lambda x: synth.widen(x, "bf16")  # noqa: E731
+    _, lse_exact = A.forward(w(q[:1]), w(k[:1]), w(v[:1]), scale)
+    assert np.max(lse_exact) < -89  # exp(-LSE) overflows float32: the regime this test is about
+    o_st, l_st = G.to_f64(o), G.to_f64(lse)
+    for b in range(bh):
+        rq, rk, rv, sq, sk, sv = A.backward_slice(w(q), w(k), w(v), w(d_o), scale, b, o=o_st, lse=l_st,
+                                                  rounding_scales=True)
+        check_16bit_grad(dq[b], rq, sq, "bf16", f"dQ head {b}")
+        check_16bit_grad(dk[b], rk, sk, "bf16", f"dK head {b}")
+        check_16bit_grad(dv[b], rv, sv, "bf16", f"dV head {b}")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
@@ -344,9 +392,11 @@ def test_backward_split_dq_pass(bh, n_q, n_k, d, dtype):
 def _dkv_query_splits(bh, n_q, n_k):
     """Mirror of the library's choice of query ranges per key tile for the dK/dV pass (a
     cluster of that many CTAs): a power of two up to 8, at most 148 CTAs, at least 8 query
-    tiles per range, and only while the dK/dV CTAs would fill at most half of 148 SMs."""
-    ctas, n_qt = bh * -(-n_k // 128), -(-n_q // 128)
-    if 2 * ctas > 148:
+    tiles per range, and only with at least 16 query tiles per key tile while the dK/dV
+    CTAs would fill at most half of 148 SMs."""
+    n_kt = -(-n_k // 128)
+    ctas, n_qt = bh * n_kt, -(-n_q // 128)
+    if 2 * ctas > 148 or n_qt < 16 * n_kt:
         return 1
     cap = min(148 // ctas, n_qt // 8, 8)
     s = 1
@@ -356,7 +406,7 @@ def _dkv_query_splits(bh, n_q, n_k):
 
 
 # (bh, n_q, n_k, query ranges the dK/dV pass takes): many queries, few key tiles
-DKV_SPLIT_SHAPES = [(2, 32768, 128, 8), (4, 16384, 256, 8), (3, 3000, 300, 2), (1, 2000, 1000, 2)]
+DKV_SPLIT_SHAPES = [(2, 32768, 128, 8), (4, 16384, 256, 8), (5, 10200, 600, 4), (40, 2100, 100, 2)]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])

@@ -56,17 +56,17 @@ def test_forward_outputs_fenced(d, dtype):
         check_lse(G.to_f64(lse.t), l_ref)
 
 
-def _backward_inputs(tag, d, dtype):
-    (q, k, v), (qd, kd, vd), o, lse, scale = _forward(tag, d, dtype)
-    d_o = synth.tensor(tag + "/do", (BH, N_Q, d), dtype)
+def _backward_inputs(tag, d, dtype, bh=BH):
+    (q, k, v), (qd, kd, vd), o, lse, scale = _forward(tag, d, dtype, bh)
+    d_o = synth.tensor(tag + "/do", (bh, N_Q, d), dtype)
     dod = G.to_device(d_o, dtype)
     w = lambda x: synth.widen(x, dtype)  # noqa: E731
     ref = A.backward(w(q), w(k), w(v), w(d_o), scale)
     return (qd, kd, vd, o.t, dod, lse.t), ref, scale
 
 
-def _grads(d, dtype):
-    return G.guarded((BH, N_Q, d), dtype), G.guarded((BH, N_K, d), dtype), G.guarded((BH, N_K, d), dtype)
+def _grads(d, dtype, bh=BH):
+    return G.guarded((bh, N_Q, d), dtype), G.guarded((bh, N_K, d), dtype), G.guarded((bh, N_K, d), dtype)
 
 
 def _check_grads(grads, ref, what):
@@ -75,15 +75,17 @@ def _check_grads(grads, ref, what):
         check_16bit(G.to_f64(g.t), r, f"{what} {name}")
 
 
-@pytest.mark.parametrize("d,dtype", [(40, "bf16"), (64, "bf16"), (64, "f16"), (128, "bf16"), (128, "f16")])
-def test_backward_outputs_and_workspace_fenced(d, dtype):
-    """fa2_backward: the one-pass kernel with its float32 dQ accumulator (head size <= 64)
-    and the two passes in one grid (> 64); the workspace is fenced at exactly
-    fa2_backward_workspace_size bytes."""
+@pytest.mark.parametrize("d,dtype,bh", [(40, "bf16", 80), (64, "bf16", 80), (64, "f16", BH), (128, "bf16", BH),
+                                         (128, "f16", BH)])
+def test_backward_outputs_and_workspace_fenced(d, dtype, bh):
+    """fa2_backward: the one-pass kernel with its float32 dQ accumulator (head size <= 64 with
+    80 heads, more than 74 key tiles in all) and the two passes in one grid (head size > 64,
+    or too few key tiles); the workspace is fenced at exactly fa2_backward_workspace_size
+    bytes."""
     torch = G.require_gpu()
-    (qd, kd, vd, o, dod, lse), ref, scale = _backward_inputs(f"guard/bwd/{d}/{dtype}", d, dtype)
-    grads = _grads(d, dtype)
-    ws = G.Guarded((binding.fa2_backward_workspace_size(BH, N_Q, N_K, d, CODES[dtype]),), torch.uint8)
+    (qd, kd, vd, o, dod, lse), ref, scale = _backward_inputs(f"guard/bwd/{d}/{dtype}/{bh}", d, dtype, bh)
+    grads = _grads(d, dtype, bh)
+    ws = G.Guarded((binding.fa2_backward_workspace_size(bh, N_Q, N_K, d, CODES[dtype]),), torch.uint8)
     binding.fa2_backward(qd, kd, vd, o, dod, lse, *(g.t for g in grads), ws.t, scale)
     binding.fa2_device_status()
     ws.assert_intact("workspace")

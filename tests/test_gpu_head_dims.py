@@ -19,10 +19,13 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("d", [8, 16, 24, 40, 48, 56, 72, 96, 120])
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
-def test_forward_backward_any_head_dim(d, dtype):
+@pytest.mark.parametrize("bh", [2, 50])
+def test_forward_backward_any_head_dim(d, dtype, bh):
+    """Two heads (the backward's two passes at every head size) and 50 heads of 3 key tiles
+    (150 in all: the one-pass backward up to head size 64)."""
     torch = G.require_gpu()
-    bh, n_q, n_k = 2, 200, 333
-    tag = f"hd/{dtype}/{d}"
+    n_q, n_k = 200, 333
+    tag = f"hd/{dtype}/{d}/{bh}"
     q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
     d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)
     scale = 1 / math.sqrt(d)

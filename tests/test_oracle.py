@@ -587,6 +587,36 @@ def test_gradient_tolerance_accepts_the_16bit_arithmetic():
     assert np.any(np.abs(emu[0] - ref[0]) > 2e-2 + 2.0 ** -7 * np.abs(ref[0]))
 
 
+def test_gradient_tolerance_accepts_cancelling_terms():
+    """Keys near -6.9 in every column (all scores far below zero): sum_j dS_ij = 0, so dQ is a
+    small difference of terms about 7 times larger. The 16-bit emulation (dS, P and the outputs
+    rounded to bfloat16) passes the bound, whose RMS guard includes u RMS(R); its RMS error is
+    above 2^-6 RMS(ref) alone."""
+    from tests.tolerance import check_16bit_grad
+    bh, nq, nk, d = 1, 96, 300, 64
+    scale = 1 / math.sqrt(d)
+    rng = np.random.default_rng(123)
+    q = synth.to_storage(np.full((bh, nq, d), 2.0) + 0.1 * rng.standard_normal((bh, nq, d)), "bf16")
+    k = synth.to_storage(-110.0 / (2.0 * d * scale) + 0.5 * rng.standard_normal((bh, nk, d)), "bf16")
+    v = synth.to_storage(rng.standard_normal((bh, nk, d)), "bf16")
+    d_o = synth.to_storage(rng.standard_normal((bh, nq, d)), "bf16")
+    w = lambda x: synth.widen(x, "bf16")  # noqa: E731
+    bfr = lambda x: synth.widen(synth.to_storage(x, "bf16"), "bf16")  # noqa: E731
+    o, lse = A.forward(w(q), w(k), w(v), scale)
+    o = bfr(o)
+    lse = lse.astype(np.float32).astype(np.float64)
+    rq, rk, rv, sq, sk, sv = A.backward_slice(w(q), w(k), w(v), w(d_o), scale, 0, o=o, lse=lse, rounding_scales=True)
+    qb, kb, vb, dob = w(q)[0], w(k)[0], w(v)[0], w(d_o)[0]
+    p = np.exp(scale * qb @ kb.T - lse[0][:, None])
+    ds = bfr(p * (dob @ vb.T - np.sum(o[0] * dob, axis=-1, keepdims=True)))
+    emu_dq = bfr(scale * ds @ kb)
+    check_16bit_grad(emu_dq, rq, sq, "bf16", "emulated dQ")
+    check_16bit_grad(bfr(scale * ds.T @ qb), rk, sk, "bf16", "emulated dK")
+    check_16bit_grad(bfr(bfr(p).T @ dob), rv, sv, "bf16", "emulated dV")
+    rms = lambda x: math.sqrt(float(np.mean(x ** 2)))  # noqa: E731
+    assert rms(emu_dq - rq) > 2.0 ** -6 * rms(rq)
+
+
 def test_gradient_tolerance_rejects_errors():
     """Zeroed, 10 %-scaled or biased gradients fail (the RMS guard), and so do a few single
     elements off by 0.1 or by 5 %, although the rest of the array is exact."""
