@@ -617,6 +617,20 @@ def test_gradient_tolerance_accepts_cancelling_terms():
     assert rms(emu_dq - rq) > 2.0 ** -6 * rms(rq)
 
 
+def test_gradient_tolerance_on_an_identically_zero_result():
+    """One key: dS = P (dP - D) = 0 up to rounding, so dQ and dK vanish and so do their
+    rounding scales; the RMS guard still allows 1e-5 (the kernels' D and dP, summed in
+    different orders, leave noise near 1e-6) and rejects 1e-4."""
+    from tests.tolerance import check_16bit_grad
+    q, k, v, d_o = _rand((1, 5, 8), 124), _rand((1, 1, 8), 125), _rand((1, 1, 8), 126), _rand((1, 5, 8), 127)
+    rq, rk, rv, sq, sk, sv = A.backward_slice(q, k, v, d_o, 0.3, 0, rounding_scales=True)
+    assert max(np.max(np.abs(rq)), np.max(np.abs(rk)), np.max(sq), np.max(sk)) < 1e-12
+    check_16bit_grad(rq + 2e-6, rq, sq, "bf16", "dQ with noise")
+    with pytest.raises(AssertionError):
+        check_16bit_grad(rq + 1e-4, rq, sq, "bf16", "dQ off by 1e-4")
+    check_16bit_grad(rv, rv, sv, "bf16", "dV")  # not zero: the usual bound
+
+
 def test_gradient_tolerance_rejects_errors():
     """Zeroed, 10 %-scaled or biased gradients fail (the RMS guard), and so do a few single
     elements off by 0.1 or by 5 %, although the rest of the array is exact."""
