@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
             else mbar_arrive(B_PF(t));
         }
         if (ok) ok = warp_wait(B_OD, 0, wd);
-        if (splits > 1) {
+        if (C::kNamed && splits > 1) {
             ep_m2 = m2;
             ep_l = l;
             ep_ok = ok;
@@ -501,7 +501,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (splits > 1) {
+    if (C::kNamed && splits > 1) {  // (the two-value form never splits)
         // Every thread of every CTA of the cluster meets at each of the three barriers.
         const bool row_thread = warp >= 2 && warp < 10;  // the softmax threads: one query row each
         const int t = (warp - 2) >> 2, quarter = warp & 3;

@@ -644,10 +644,15 @@ def other_configs(torch, B, dev, pk, reps=20):
     """The other attention shapes of the workload list, timed after the main region (seeded
     N(0,1) inputs; median of `reps` timings of 8 back-to-back calls each):
     forward B=4 H=16 N=4096 d=64, and cross attention B=1 H=32 N_q=1024 N_k=32768 d=128
-    with K scaled by 8 (peaked rows), forward and backward."""
+    with K scaled by 8 (peaked rows), forward and backward; then two head counts too small
+    to fill the SMs, cross attention either way at d=128: B*H=2, N_q=128, N_k=32768 (the
+    forward's and the dQ pass's key ranges) and B*H=2, N_q=32768, N_k=128 (the dK/dV
+    pass's query ranges)."""
     out = {}
     for tag, bh, nq, nk, d, kscale, with_bwd in (("fwd_b4h16_n4096_d64", 64, 4096, 4096, 64, 1.0, True),
-                                                 ("cross_b1h32_nq1024_nk32768_d128", 32, 1024, 32768, 128, 8.0, True)):
+                                                 ("cross_b1h32_nq1024_nk32768_d128", 32, 1024, 32768, 128, 8.0, True),
+                                                 ("few_heads_bh2_nq128_nk32768_d128", 2, 128, 32768, 128, 1.0, True),
+                                                 ("few_heads_bh2_nq32768_nk128_d128", 2, 32768, 128, 128, 1.0, True)):
         g = torch.Generator(device=dev).manual_seed(synth.BASE_SEED)
         q = torch.randn((bh, nq, d), device=dev, generator=g).to(torch.bfloat16)
         k = (kscale * torch.randn((bh, nk, d), device=dev, generator=g)).to(torch.bfloat16)
