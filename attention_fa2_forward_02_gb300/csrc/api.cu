@@ -118,6 +118,40 @@ cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
     return e;
 }
 
+// Whether a thread-block cluster of `size` (2, 4 or 8) CTAs of `func` (`threads` threads,
+// `smem` dynamic shared-memory bytes, its limit already raised) can be resident at once on
+// the current device; asked of the runtime once per (slot, size, device).
+std::atomic<uint64_t> g_cluster_asked[kMaxSlots][3], g_cluster_fits[kMaxSlots][3];
+
+bool cluster_fits(const void* func, int threads, int smem, int size, int slot) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const int li = size == 2 ? 0 : (size == 4 ? 1 : 2);
+    const bool cached = dev >= 0 && dev < 64 && slot >= 0 && slot < kMaxSlots;
+    const uint64_t bit = cached ? 1ull << dev : 0;
+    if (cached && (g_cluster_asked[slot][li].load(std::memory_order_acquire) & bit))
+        return g_cluster_fits[slot][li].load(std::memory_order_acquire) & bit;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)size, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    const bool fits = cudaOccupancyMaxActiveClusters(&n, func, &cfg) == cudaSuccess && n > 0;
+    if (!fits) (void)cudaGetLastError();  // a refused query leaves no error behind
+    if (cached) {
+        if (fits) g_cluster_fits[slot][li].fetch_or(bit, std::memory_order_acq_rel);
+        g_cluster_asked[slot][li].fetch_or(bit, std::memory_order_acq_rel);
+    }
+    return fits;
+}
+
 // fa2_backward runs the one-pass kernel (dQ through float32 reductions) for
 // kernel head sizes up to 64 and the two-pass kernels above.  Measured on GB300
 // at BH = 32, N = 8192 (preprocess included): head size 32 / 64: 1.51 / 1.65 ms

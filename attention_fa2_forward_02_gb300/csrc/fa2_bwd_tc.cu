@@ -1152,11 +1152,19 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     cudaError_t e = cudaSuccess;
     const int n_kt = (int)((p.n_k + BT - 1) / BT), n_qt = (int)((p.n_q + BT - 1) / BT);
     // many queries, few key tiles: the dK/dV pass over query ranges in clusters, then the dQ pass
-    const int qsplits = C::kNamed ? dkv_query_splits(p.bh, p.n_q, p.n_k) : 1;
+    int qsplits = C::kNamed ? dkv_query_splits(p.bh, p.n_q, p.n_k) : 1;
+    auto split_kern = bwd_dkdv_split_kernel<D, kBf16>;
     if (qsplits > 1 && (stages & kBwdDkDv)) {
-        auto kern = bwd_dkdv_split_kernel<D, kBf16>;
-        e = ensure_smem_limit(reinterpret_cast<const void*>(kern), C::kSmemDkv, 52 + (slot - 16) / 2);  // slots 52..61
+        const int split_slot = 52 + (slot - 16) / 2;  // slots 52..61
+        e = ensure_smem_limit(reinterpret_cast<const void*>(split_kern), C::kSmemDkv, split_slot);
         if (e != cudaSuccess) return e;
+        // a device that cannot hold the whole cluster at once takes fewer ranges
+        while (qsplits > 1 &&
+               !cluster_fits(reinterpret_cast<const void*>(split_kern), C::kThreads, C::kSmemDkv, qsplits, split_slot))
+            qsplits /= 2;
+    }
+    if (qsplits > 1 && (stages & kBwdDkDv)) {
+        auto kern = split_kern;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(n_kt * qsplits), (unsigned)p.bh, 1);
         cfg.blockDim = dim3(C::kThreads, 1, 1);

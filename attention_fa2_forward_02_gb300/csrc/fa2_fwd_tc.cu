@@ -580,7 +580,10 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
     if (e != cudaSuccess) return e;
     const int64_t pairs = (p.n_q + BM * kQTiles - 1) / (BM * kQTiles);
     const float scale_log2 = p.scale * 1.4426950408889634f;
-    const int splits = kNV == 1 ? fwd_key_splits(pairs * p.bh, (p.n_k + BN - 1) / BN) : 1;
+    int splits = kNV == 1 ? fwd_key_splits(pairs * p.bh, (p.n_k + BN - 1) / BN) : 1;
+    // a device that cannot hold the whole cluster at once takes fewer ranges
+    while (splits > 1 && !cluster_fits(reinterpret_cast<const void*>(kern), C::kThreads, C::kSmemBytes, splits, slot))
+        splits /= 2;
     if (splits == 1) {
         const dim3 grid((unsigned)pairs, (unsigned)p.bh, 1);
         kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k,

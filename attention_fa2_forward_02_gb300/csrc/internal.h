@@ -174,6 +174,9 @@ bool watchdog_word(unsigned int** out);
 
 // Number of SMs of the current device (looked up once per device; 148 if the query fails).
 int sm_count();
+// Whether a cluster of `size` CTAs of `func` can be resident at once on the current device
+// (its dynamic shared-memory limit already raised to `smem`); cached per slot and size.
+bool cluster_fits(const void* func, int threads, int smem, int size, int slot);
 
 // Raises the dynamic shared-memory limit of `func` on the current device once.
 cudaError_t ensure_smem_limit(const void* func, int bytes, int slot);

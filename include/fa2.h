@@ -81,7 +81,8 @@ typedef enum {
  * Few query tiles, many keys (bh * ceil(n_q / 256) CTAs filling at most half of 148 SMs,
  * at least 16 key tiles): the keys of each 256-row query block are split over a
  * thread-block cluster of 2, 4 or 8 CTAs whose (O, max, sum) are combined in distributed
- * shared memory, in a fixed order (the result depends on the sizes only).
+ * shared memory, in a fixed order (the result depends on the sizes only, on any device
+ * that can hold such a cluster at once; one that cannot takes fewer ranges).
  * Precision over long key ranges: each row's O and l are summed one 128-key tile at a
  * time in float32 over a CTA's key range, so the error can grow like (key tiles per
  * CTA) * 2^-24 times sum_j P_ij |v_j| (about 1.5e-5 at 256 key tiles; 0.8 % at 131,079,
@@ -141,7 +142,8 @@ size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t
  *    at most half of 148 SMs, at least 16 query tiles per key tile): the dK/dV pass
  *    splits each key tile's queries over a thread-block cluster of 2, 4 or 8 CTAs
  *    that add their shares in distributed shared memory, in a fixed order
- *    (bit-reproducible), and the dQ pass follows as its own launch.
+ *    (bit-reproducible; a device that cannot hold such a cluster at once takes fewer
+ *    ranges), and the dQ pass follows as its own launch.
  *  - few query tiles, many keys: the dQ pass splits each query tile's keys into
  *    ranges whose float32 partial sums the workspace holds, added in a fixed order.
  *
