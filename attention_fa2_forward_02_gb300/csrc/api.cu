@@ -152,8 +152,8 @@ bool cluster_fits(const void* func, int threads, int smem, int size, int slot) {
     return fits;
 }
 
-// fa2_backward runs the one-pass kernel (dQ through float32 reductions) for
-// kernel head sizes up to 64 and the two-pass kernels above.  Measured on GB300
+// fa2_backward runs the one-pass kernel (dQ through float32 reductions) for kernel head
+// sizes up to 64 with enough key tiles (below) and the two-pass kernels otherwise.  Measured on GB300
 // at BH = 32, N = 8192 (preprocess included): head size 32 / 64: 1.51 / 1.65 ms
 // one-pass against 1.58 / 1.75 ms for the two passes in one grid; head size 128:
 // 2.99 ms against 2.27 ms, where the reductions (4 bytes per query row, key tile
