@@ -118,15 +118,16 @@ cudaError_t ensure_smem_limit(const void* func, int bytes, int slot) {
     return e;
 }
 
-// Whether a thread-block cluster of `size` (2, 4 or 8) CTAs of `func` (`threads` threads,
+// Whether a thread-block cluster of `size` (2, 4, 8 or 16) CTAs of `func` (`threads` threads,
 // `smem` dynamic shared-memory bytes, its limit already raised) can be resident at once on
-// the current device; asked of the runtime once per (slot, size, device).
-std::atomic<uint64_t> g_cluster_asked[kMaxSlots][3], g_cluster_fits[kMaxSlots][3];
+// the current device; asked of the runtime once per (slot, size, device). A cluster of 16
+// needs the kernel's non-portable-cluster-size attribute, set here first.
+std::atomic<uint64_t> g_cluster_asked[kMaxSlots][4], g_cluster_fits[kMaxSlots][4];
 
 bool cluster_fits(const void* func, int threads, int smem, int size, int slot) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    const int li = size == 2 ? 0 : (size == 4 ? 1 : 2);
+    const int li = size == 2 ? 0 : (size == 4 ? 1 : (size == 8 ? 2 : 3));
     const bool cached = dev >= 0 && dev < 64 && slot >= 0 && slot < kMaxSlots;
     const uint64_t bit = cached ? 1ull << dev : 0;
     if (cached && (g_cluster_asked[slot][li].load(std::memory_order_acquire) & bit))
@@ -143,7 +144,9 @@ bool cluster_fits(const void* func, int threads, int smem, int size, int slot) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    const bool fits = cudaOccupancyMaxActiveClusters(&n, func, &cfg) == cudaSuccess && n > 0;
+    const bool allowed =
+        size <= 8 || cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+    const bool fits = allowed && cudaOccupancyMaxActiveClusters(&n, func, &cfg) == cudaSuccess && n > 0;
     if (!fits) (void)cudaGetLastError();  // a refused query leaves no error behind
     if (cached) {
         if (fits) g_cluster_fits[slot][li].fetch_or(bit, std::memory_order_acq_rel);

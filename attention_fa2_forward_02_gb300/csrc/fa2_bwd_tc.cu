@@ -141,7 +141,8 @@ __host__ __device__ constexpr uint32_t nb_stage(int s) { return 3 + (uint32_t)s;
 //
 // kSplitQ: one key tile (n_items = 1) over one of `splits` query ranges, the CTAs of the
 // ranges in one thread-block cluster (consecutive blockIdx.x, blockIdx.x mod splits the
-// rank; range r = query tiles [r L, min(n_qt, r L + L)), L = ceil(n_qt / splits)). Each
+// rank; range r = query tiles [floor(r n_qt / splits), floor((r + 1) n_qt / splits)), never
+// empty while n_qt >= splits, which the launch ensures with at least 8 per range). Each
 // ends with its range's share of dK and dV in tensor memory; every CTA then sends each
 // CTA the columns that CTA writes, through distributed shared memory in the buffers its
 // loops no longer use, and each adds the shares of its columns in rank order and stores
@@ -164,10 +165,10 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
     if constexpr (kSplitQ) {
         static_assert(kNV == 1, "split query ranges with one value tensor");
         rank = (int)(blockIdx.x % (unsigned)splits);
-        const int len = (n_qt + splits - 1) / splits;
-        q_lo = rank * len;
-        n_qt = min(n_qt, q_lo + len) - q_lo;
-        n_items = 1;
+        const int all = n_qt;  // balanced ranges: none empty while all >= splits (the launch takes >= 8 per range)
+        q_lo = (int)((int64_t)rank * all / splits);
+        n_qt = (int)((int64_t)(rank + 1) * all / splits) - q_lo;
+        n_items = n_qt > 0 ? 1 : 0;  // an empty range would only meet the cluster's barriers
     }
     if constexpr (!C::kNamed) n_items = 1;
     bool elem_ok = false;  // an elementwise thread's state at the end, for the split's combine
@@ -325,7 +326,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                 if (lane == 0) mma_commit(bars.done());  // dV, dK of key tile u complete
                 __syncwarp();
             }
-            if (lane == 0) drain_wait(bars.done(), (uint32_t)((n_items - 1) & 1));
+            if (lane == 0 && n_items > 0) drain_wait(bars.done(), (uint32_t)((n_items - 1) & 1));
             __syncwarp();
         } else {
             if (lane == 0) {
@@ -540,14 +541,14 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                 tmem_ld32(src + 32u * c, r);
                 tmem_ld_wait();
                 reg_fence(r);
-                const float keep = elem_ok ? 1.f : 0.f;
 #pragma unroll
                 for (int g = 0; g < 8; ++g) {
                     const int col = 32 * c + 4 * g, owner = col / w;
                     const uint32_t dst = base + (uint32_t)((((rank * 128 + row) * 2 + half) * w + col - owner * w) * 4);
-                    st_cluster_v4(cluster_map(dst, (uint32_t)owner), __uint_as_float(r[4 * g]) * keep,
-                                  __uint_as_float(r[4 * g + 1]) * keep, __uint_as_float(r[4 * g + 2]) * keep,
-                                  __uint_as_float(r[4 * g + 3]) * keep);
+                    // a CTA whose waits failed sends exact zeros (its tensor memory may hold anything)
+                    st_cluster_v4(cluster_map(dst, (uint32_t)owner), elem_ok ? __uint_as_float(r[4 * g]) : 0.f,
+                                  elem_ok ? __uint_as_float(r[4 * g + 1]) : 0.f, elem_ok ? __uint_as_float(r[4 * g + 2]) : 0.f,
+                                  elem_ok ? __uint_as_float(r[4 * g + 3]) : 0.f);
                 }
             }
         }
@@ -1152,7 +1153,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     cudaError_t e = cudaSuccess;
     const int n_kt = (int)((p.n_k + BT - 1) / BT), n_qt = (int)((p.n_q + BT - 1) / BT);
     // many queries, few key tiles: the dK/dV pass over query ranges in clusters, then the dQ pass
-    int qsplits = C::kNamed ? dkv_query_splits(p.bh, p.n_q, p.n_k) : 1;
+    int qsplits = C::kNamed ? dkv_query_splits(p.bh, p.n_q, p.n_k, D) : 1;
     auto split_kern = bwd_dkdv_split_kernel<D, kBf16>;
     if (qsplits > 1 && (stages & kBwdDkDv)) {
         const int split_slot = 52 + (slot - 16) / 2;  // slots 52..61

@@ -39,8 +39,8 @@
 // <= 2^8 and the final O = acc / l is the same quotient up to rounding.
 //
 // Few CTAs, many keys (fewer query-tile pairs than SMs): a thread-block cluster of
-// `splits` CTAs (2, 4 or 8) shares a query-tile pair, CTA r taking key tiles
-// [r L, min(n_kv, r L + L)), L = ceil(n_kv / splits). Each ends with its own (O_r, m_r,
+// `splits` CTAs (2, 4, 8, or 16 at head sizes 64 and 128) shares a query-tile pair, CTA r taking key tiles
+// [floor(r n_kv / splits), floor((r + 1) n_kv / splits)), never empty (n_kv >= 8 splits). Each ends with its own (O_r, m_r,
 // l_r) per row; the cluster then combines them through distributed shared memory in the
 // Q/K/V buffers its loops no longer use: every CTA sends each row's (m_r, l_r) to all,
 // scales its O_r by 2^(m_r - M) / L (M the largest m_r, L the sum of l_r 2^(m_r - M)) and
@@ -90,7 +90,7 @@ struct FwdCfg : Tile16<D> {
     static_assert(256 + 2 * kNV * D <= (int)kTmemCols, "tensor memory budget");
     // cluster combine: (m, l) of every CTA's 256 rows, then every CTA's share of each row
     static constexpr int kExchMl = 0;
-    static constexpr int kExchRecv = 8 * 256 * 8;
+    static constexpr int kExchRecv = 16 * 256 * 8;  // up to 16 CTAs' (m, l) of 256 rows
     static_assert(kExchRecv + 256 * D * 4 <= kSmemBar, "cluster combine buffers");
 };
 
@@ -115,9 +115,10 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
     const int rank = (int)(blockIdx.x % (unsigned)splits);
     const int q0 = (blockIdx.x / splits) * (BM * kQTiles);
     const int n_kv_all = (n_k + BN - 1) / BN;
-    const int kv_len = (n_kv_all + splits - 1) / splits;
-    const int j0 = rank * kv_len;                          // this CTA's key tiles: [j0, j0 + n_kv)
-    const int n_kv = min(n_kv_all, j0 + kv_len) - j0;
+    // this CTA's key tiles: [j0, j0 + n_kv), the rank-th of `splits` balanced ranges (none
+    // empty: the launch takes at least 8 key tiles per range)
+    const int j0 = (int)((int64_t)rank * n_kv_all / splits);
+    const int n_kv = (int)((int64_t)(rank + 1) * n_kv_all / splits) - j0;
     float ep_m2 = 0.f, ep_l = 0.f;  // a softmax thread's row state, kept for the cluster combine
     bool ep_ok = false;
 
@@ -531,9 +532,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kNV>::kThreads, 1)
                 for (int g = 0; g < 8; ++g) {
                     const int col = 32 * c + 4 * g, owner = col / w;
                     const uint32_t dst = recv + (uint32_t)(((rank * 256 + row_l) * w + col - owner * w) * 4);
-                    st_cluster_v4(cluster_map(dst, (uint32_t)owner), __uint_as_float(r[4 * g]) * f,
-                                  __uint_as_float(r[4 * g + 1]) * f, __uint_as_float(r[4 * g + 2]) * f,
-                                  __uint_as_float(r[4 * g + 3]) * f);
+                    // a row whose waits failed sends exact zeros (its tensor memory may hold anything)
+                    st_cluster_v4(cluster_map(dst, (uint32_t)owner), ep_ok ? __uint_as_float(r[4 * g]) * f : 0.f,
+                                  ep_ok ? __uint_as_float(r[4 * g + 1]) * f : 0.f,
+                                  ep_ok ? __uint_as_float(r[4 * g + 2]) * f : 0.f,
+                                  ep_ok ? __uint_as_float(r[4 * g + 3]) * f : 0.f);
                 }
             }
         }
@@ -580,7 +583,7 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
     if (e != cudaSuccess) return e;
     const int64_t pairs = (p.n_q + BM * kQTiles - 1) / (BM * kQTiles);
     const float scale_log2 = p.scale * 1.4426950408889634f;
-    int splits = kNV == 1 ? fwd_key_splits(pairs * p.bh, (p.n_k + BN - 1) / BN) : 1;
+    int splits = kNV == 1 ? fwd_key_splits(pairs * p.bh, (p.n_k + BN - 1) / BN, D) : 1;
     // a device that cannot hold the whole cluster at once takes fewer ranges
     while (splits > 1 && !cluster_fits(reinterpret_cast<const void*>(kern), C::kThreads, C::kSmemBytes, splits, slot))
         splits /= 2;

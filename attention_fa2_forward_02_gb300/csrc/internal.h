@@ -33,16 +33,29 @@ inline int dq_key_splits(int64_t bh, int64_t n_q, int64_t n_k) {
     return s < 2 ? 1 : (int)s;
 }
 
+// Largest cluster of the key- and query-range splits over n_tiles tiles: 16 CTAs (a
+// non-portable cluster size) where each CTA's share of a row, kernel head size / 16 columns,
+// is still a whole 16-byte group of float32 (64 and 128) and each range keeps at least 16
+// tiles, else 8. With fewer tiles per range the 16-way exchange of the combine costs more
+// than the shorter loops save (GB300, d = 128: B*H = 4, N_q = 16384, N_k = 256, dK/dV query
+// ranges 8 -> 16: 0.099 -> 0.123 ms; with 16 tiles per range, B*H = 2, N_q = 32768,
+// N_k = 128: 0.117 -> 0.094 ms, and the forward at B*H = 2, N_q = 128, N_k = 32768: 0.074 ->
+// 0.054 ms).
+inline int max_range_splits(int kernel_head_dim, int64_t n_tiles) {
+    return kernel_head_dim >= 64 && n_tiles >= 16 * 16 ? 16 : 8;
+}
+
 // Key ranges of the forward's cluster split (one CTA per range, the ranges of a query-tile
 // pair in one thread-block cluster): when the forward's CTAs (query-tile pairs x heads) would
-// fill at most half of a 148-SM part, the largest power of two up to 8 that keeps at most
-// 148 CTAs and at least 8 key tiles per range; else 1. A function of the sizes alone, so
+// fill at most half of a 148-SM part, the largest power of two up to max_range_splits that
+// keeps at most 148 CTAs and at least 8 key tiles per range; else 1. A function of the sizes alone, so
 // that the results do not depend on the device.
-inline int fwd_key_splits(int64_t ctas, int64_t n_kt) {
+inline int fwd_key_splits(int64_t ctas, int64_t n_kt, int kernel_head_dim) {
+    const int max_splits = max_range_splits(kernel_head_dim, n_kt);
     if (ctas < 1 || 2 * ctas > 148) return 1;
     int64_t cap = 148 / ctas;
     if (cap > n_kt / 8) cap = n_kt / 8;
-    if (cap > 8) cap = 8;
+    if (cap > max_splits) cap = max_splits;
     int s = 1;
     while (2 * s <= cap) s *= 2;
     return s;
@@ -52,17 +65,18 @@ inline int fwd_key_splits(int64_t ctas, int64_t n_kt) {
 // ranges of a key tile in one thread-block cluster that adds their dK and dV in distributed
 // shared memory): for queries far outnumbering the keys (at least 16 query tiles per key
 // tile) of few heads (the dK/dV CTAs, key tiles x heads, filling at most half of a 148-SM
-// part), the largest power of two up to 8 that keeps at most 148 CTAs and at least 8 query
-// tiles per range; else 1. The split pass runs apart from the dQ pass, so it pays only
+// part), the largest power of two up to max_range_splits that keeps at most 148 CTAs and at
+// least 8 query tiles per range; else 1. The split pass runs apart from the dQ pass, so it pays only
 // where unsplit dK/dV CTAs would each walk far more query tiles than the dQ CTAs walk key
 // tiles (measured on GB300, d = 128: 16 query tiles per key tile 1.2x faster, 8 and fewer
 // slower than the one-grid passes). A function of the sizes alone.
-inline int dkv_query_splits(int64_t bh, int64_t n_q, int64_t n_k) {
+inline int dkv_query_splits(int64_t bh, int64_t n_q, int64_t n_k, int kernel_head_dim) {
     const int64_t n_kt = (n_k + 127) / 128, ctas = bh * n_kt, n_qt = (n_q + 127) / 128;
+    const int max_splits = max_range_splits(kernel_head_dim, n_qt);
     if (ctas < 1 || 2 * ctas > 148 || n_qt < 16 * n_kt) return 1;
     int64_t cap = 148 / ctas;
     if (cap > n_qt / 8) cap = n_qt / 8;
-    if (cap > 8) cap = 8;
+    if (cap > max_splits) cap = max_splits;
     int s = 1;
     while (2 * s <= cap) s *= 2;
     return s;
@@ -174,8 +188,9 @@ bool watchdog_word(unsigned int** out);
 
 // Number of SMs of the current device (looked up once per device; 148 if the query fails).
 int sm_count();
-// Whether a cluster of `size` CTAs of `func` can be resident at once on the current device
-// (its dynamic shared-memory limit already raised to `smem`); cached per slot and size.
+// Whether a cluster of `size` (2, 4, 8 or 16) CTAs of `func` can be resident at once on the
+// current device (its dynamic shared-memory limit already raised to `smem`; for 16, the
+// non-portable cluster size is allowed for it first); cached per slot and size.
 bool cluster_fits(const void* func, int threads, int smem, int size, int slot);
 
 // Raises the dynamic shared-memory limit of `func` on the current device once.

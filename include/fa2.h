@@ -80,13 +80,14 @@ typedef enum {
  * small problems; float32 products and sums throughout).
  * Few query tiles, many keys (bh * ceil(n_q / 256) CTAs filling at most half of 148 SMs,
  * at least 16 key tiles): the keys of each 256-row query block are split over a
- * thread-block cluster of 2, 4 or 8 CTAs whose (O, max, sum) are combined in distributed
- * shared memory, in a fixed order (the result depends on the sizes only, on any device
- * that can hold such a cluster at once; one that cannot takes fewer ranges).
+ * thread-block cluster of 2, 4, 8 or 16 CTAs (16 only for head_dim > 32 and at least 256
+ * key tiles; at least 8 key tiles per CTA) whose (O, max, sum) are combined in
+ * distributed shared memory, in a fixed order (the result depends on the sizes only, on
+ * any device that can hold such a cluster at once; one that cannot takes fewer ranges).
  * Precision over long key ranges: each row's O and l are summed one 128-key tile at a
  * time in float32 over a CTA's key range, so the error can grow like (key tiles per
  * CTA) * 2^-24 times sum_j P_ij |v_j| (about 1.5e-5 at 256 key tiles; 0.8 % at 131,079,
- * which one head of 16.8M keys would give a single CTA, 0.1 % as the cluster's 8 ranges).
+ * which one head of 16.8M keys would give a single CTA, 0.05 % as the cluster's 16 ranges).
  * n_q and n_k are limited to 2^30 and bh to 65535 (FA2_ERR_UNSUPPORTED past them).
  * Errors: FA2_ERR_INVALID_ARG, FA2_ERR_UNSUPPORTED, FA2_ERR_MISALIGNED, FA2_ERR_CUDA.
  */
@@ -140,8 +141,9 @@ size_t fa2_backward_workspace_size(int64_t bh, int64_t n_q, int64_t n_k, int32_t
  *    bit-reproducible from run to run here (dk and dv are).
  *  - many more queries than keys in few heads (bh * ceil(n_k / 128) key tiles filling
  *    at most half of 148 SMs, at least 16 query tiles per key tile): the dK/dV pass
- *    splits each key tile's queries over a thread-block cluster of 2, 4 or 8 CTAs
- *    that add their shares in distributed shared memory, in a fixed order
+ *    splits each key tile's queries over a thread-block cluster of 2, 4, 8 or 16 CTAs
+ *    (16 only for head_dim > 32 and at least 256 query tiles; at least 8 query tiles
+ *    per CTA) that add their shares in distributed shared memory, in a fixed order
  *    (bit-reproducible; a device that cannot hold such a cluster at once takes fewer
  *    ranges), and the dQ pass follows as its own launch.
  *  - few query tiles, many keys: the dQ pass splits each query tile's keys into

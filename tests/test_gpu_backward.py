@@ -7,6 +7,7 @@ import pytest
 from attention_fa2_forward_02_gb300 import binding, synth
 from oracle import attention as A
 from tests import gpu_util as G
+from tests.split_rules import dkv_query_splits, dq_key_splits, one_pass
 from tests.tolerance import check_16bit, check_16bit_grad
 
 pytestmark = pytest.mark.gpu
@@ -48,12 +49,6 @@ def test_backward_vs_oracle(dtype, d, bh, n_q, n_k):
     check_16bit(dv, rv, "dV")
 
 
-def _one_pass(bh, n_k, d):
-    """Whether fa2_backward takes the one-pass kernel: head size up to 64 and more than 74
-    key tiles in all (fewer take the two passes)."""
-    return d <= 64 and 2 * bh * -(-n_k // 128) > 148
-
-
 # many heads, so that head sizes up to 64 take the one-pass kernel; ragged query and key tails
 ONE_PASS_SHAPES = [(80, 300, 150), (160, 129, 77), (75, 64, 1000), (96, 1, 129)]
 
@@ -63,7 +58,7 @@ ONE_PASS_SHAPES = [(80, 300, 150), (160, 129, 77), (75, 64, 1000), (96, 1, 129)]
 @pytest.mark.parametrize("bh,n_q,n_k", ONE_PASS_SHAPES)
 def test_backward_one_pass_vs_oracle(dtype, d, bh, n_q, n_k):
     """The one-pass kernel (head size <= 64, more than 74 key tiles in all) on ragged shapes."""
-    assert _one_pass(bh, n_k, d)
+    assert one_pass(bh, n_k, d)
     tag = f"bwd1p/{dtype}/{d}/{bh}/{n_q}/{n_k}"
     q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
     d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)
@@ -201,7 +196,7 @@ def test_backward_stages_vs_oracle_and_whole(d, dtype):
     whole = [G.empty(x.shape, dtype) for x in (q, k, v)]
     binding.fa2_backward(qd, kd, vd, o, dod, lse, *whole, ws, scale)
     small = torch.empty(8 * bh * 384, dtype=torch.uint8, device="cuda")  # D and LSE2 only
-    assert _one_pass(bh, n_k, d) == (d <= 64)
+    assert one_pass(bh, n_k, d) == (d <= 64)
     staged = _stages(qd, kd, vd, o, dod, lse, scale, small, dtype)
     again = _stages(qd, kd, vd, o, dod, lse, scale, small, dtype)
     one_grid = [G.empty(tuple(x.shape), dtype) for x in (qd, kd, vd)]
@@ -215,7 +210,7 @@ def test_backward_stages_vs_oracle_and_whole(d, dtype):
     for name, a, b, c, r in zip(("dQ", "dK", "dV"), staged, whole, again, ref):
         check_16bit(G.to_f64(a), r, f"two-pass {name}")
         assert torch.equal(a, c), f"two-pass {name} not reproducible"
-        if not _one_pass(bh, n_k, d):
+        if not one_pass(bh, n_k, d):
             assert torch.equal(a, b), f"fa2_backward {name} differs from its stages"
         else:
             check_16bit(G.to_f64(a), G.to_f64(b), f"two-pass vs one-pass {name}")
@@ -228,7 +223,7 @@ def test_backward_reproducibility(d):
     order, so two runs may differ by rounding, at most one unit in the last place of the
     16-bit result (80 heads at head size 64, for the one-pass kernel)."""
     bh, n = (80 if d <= 64 else 2), 300
-    assert _one_pass(bh, n, d) == (d <= 64)
+    assert one_pass(bh, n, d) == (d <= 64)
     q, k, v = G.inputs(f"bwd/det/{d}", bh, n, n, d, "bf16")
     d_o = synth.tensor(f"bwd/det/{d}/do", (bh, n, d), "bf16")
     a = run_fwd_bwd(q, k, v, d_o, "bf16", 1 / math.sqrt(d))
@@ -250,7 +245,7 @@ def test_backward_far_negative_scores_with_a_partial_key_tile(d):
     stored O and LSE the kernels read (tests/tolerance.py)."""
     torch = G.require_gpu()
     bh, n_q, n_k = (80 if d <= 64 else 1), 150, 200
-    assert _one_pass(bh, n_k, d) == (d <= 64)
+    assert one_pass(bh, n_k, d) == (d <= 64)
     scale = 1 / math.sqrt(d)
     q = synth.to_storage(np.full((bh, n_q, d), 2.0), "bf16")
     k_base = -110.0 / (2.0 * d * scale)
@@ -325,14 +320,6 @@ def test_backward_passes_over_several_key_tiles_equal_the_stages(n_q, n_k, d, dt
             check_16bit(G.to_f64(a[b]), r[0], f"one-grid {name} of head {b}")
 
 
-def _dq_splits(bh, n_q, n_k):
-    """The number of key ranges the library's dQ pass takes for these sizes (include/fa2.h,
-    fa2_backward_workspace_size): about 148 dQ CTAs, at least 8 key tiles per range, at most 8."""
-    n_qt, n_kt = -(-n_q // 128), -(-n_k // 128)
-    s = min(-(-148 // (bh * n_qt)), n_kt // 8, 8)
-    return s if s >= 2 else 1
-
-
 @pytest.mark.parametrize("bh,n_q,n_k,d,dtype", [
     (2, 128, 4096, 128, "bf16"),   # 2 dQ CTAs of 32 key tiles unsplit: 4 ranges of 8
     (3, 200, 2500, 128, "f16"),    # ragged keys (20 key tiles, the last partial): 2 ranges of 10
@@ -348,7 +335,7 @@ def test_backward_split_dq_pass(bh, n_q, n_k, d, dtype):
     the partial sums) and of the oracle; nothing is written outside dq, dk, dv or the
     workspace."""
     torch = G.require_gpu()
-    splits = _dq_splits(bh, n_q, n_k)
+    splits = dq_key_splits(bh, n_q, n_k)
     assert splits >= 2
     tag = f"bwd/split/{bh}/{n_q}/{n_k}/{d}/{dtype}"
     q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
@@ -389,36 +376,25 @@ def test_backward_split_dq_pass(bh, n_q, n_k, d, dtype):
         check_16bit(G.to_f64(a.t), r, f"{name} (dQ pass in {splits} key ranges)")
 
 
-def _dkv_query_splits(bh, n_q, n_k):
-    """Mirror of the library's choice of query ranges per key tile for the dK/dV pass (a
-    cluster of that many CTAs): a power of two up to 8, at most 148 CTAs, at least 8 query
-    tiles per range, and only with at least 16 query tiles per key tile while the dK/dV
-    CTAs would fill at most half of 148 SMs."""
-    n_kt = -(-n_k // 128)
-    ctas, n_qt = bh * n_kt, -(-n_q // 128)
-    if 2 * ctas > 148 or n_qt < 16 * n_kt:
-        return 1
-    cap = min(148 // ctas, n_qt // 8, 8)
-    s = 1
-    while 2 * s <= cap:
-        s *= 2
-    return s
+# (bh, n_q, n_k): many queries, few key tiles; 16 / 8 / 4 / 2 query ranges (8 for the first at
+# head size 32; the second has 8 query tiles per range at most, below the 16 a cluster of 16 needs)
+DKV_SPLIT_SHAPES = [(2, 32768, 128), (4, 16384, 256), (5, 10200, 600), (40, 2100, 100)]
 
 
-# (bh, n_q, n_k, query ranges the dK/dV pass takes): many queries, few key tiles
-DKV_SPLIT_SHAPES = [(2, 32768, 128, 8), (4, 16384, 256, 8), (5, 10200, 600, 4), (40, 2100, 100, 2)]
+def test_backward_split_shapes_take_every_cluster_size():
+    assert {dkv_query_splits(*s, d) for s in DKV_SPLIT_SHAPES for d in (32, 128)} == {2, 4, 8, 16}
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("d", [32, 40, 64, 72, 128])
-@pytest.mark.parametrize("bh,n_q,n_k,splits", DKV_SPLIT_SHAPES)
-def test_backward_dkdv_query_ranges_in_a_cluster(dtype, d, bh, n_q, n_k, splits):
+@pytest.mark.parametrize("bh,n_q,n_k", DKV_SPLIT_SHAPES)
+def test_backward_dkdv_query_ranges_in_a_cluster(dtype, d, bh, n_q, n_k):
     """Queries far outnumbering the keys of few heads: the dK/dV pass splits each key tile's
     queries over a cluster of CTAs that add their dK and dV in distributed shared memory
     (every head size then takes the two passes). dQ, dK, dV against the oracle; two runs
     bit-identical; nothing written outside the gradients."""
     torch = G.require_gpu()
-    assert _dkv_query_splits(bh, n_q, n_k) == splits
+    assert dkv_query_splits(bh, n_q, n_k, d) > 1
     tag = f"bwdsplitq/{dtype}/{d}/{bh}/{n_q}/{n_k}"
     q, k, v = G.inputs(tag, bh, n_q, n_k, d, dtype)
     d_o = synth.tensor(tag + "/do", (bh, n_q, d), dtype)

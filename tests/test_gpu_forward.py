@@ -8,6 +8,7 @@ from attention_fa2_forward_02_gb300 import binding, synth
 from oracle import attention as A
 from tests import gpu_util as G
 from tests.golden.load import load
+from tests.split_rules import fwd_key_splits
 from tests.tolerance import check_16bit, check_f32, check_lse
 
 pytestmark = pytest.mark.gpu
@@ -210,32 +211,25 @@ def test_forward_cross_attention_peaked_whole_heads():
     _whole_heads("config/cross_k8", 32, 1024, 32768, 128, 8.0, [0, 31], row_chunk=128)
 
 
-def _fwd_key_splits(ctas, n_kt):
-    """Mirror of the library's choice of key ranges per query-tile pair (a cluster of that many
-    CTAs): a power of two up to 8, at most 148 CTAs in all, at least 8 key tiles per range,
-    and only while the CTAs would fill at most half of 148 SMs."""
-    if 2 * ctas > 148:
-        return 1
-    cap = min(148 // ctas, n_kt // 8, 8)
-    s = 1
-    while 2 * s <= cap:
-        s *= 2
-    return s
+# (bh, n_q, n_k): a query row alone, ragged query and key tails; 16 / 4 / 2 / 4 ranges (8 for
+# the first at head size 32: a CTA's 2-column share would not make a 16-byte group)
+SPLIT_SHAPES = [(2, 128, 32768), (1, 300, 5000), (3, 200, 2100), (2, 1, 4096)]
 
 
-# (bh, n_q, n_k, splits the library takes): a query row alone, ragged query and key tails
-SPLIT_SHAPES = [(2, 128, 32768, 8), (1, 300, 5000, 4), (3, 200, 2100, 2), (2, 1, 4096, 4)]
+def test_forward_split_shapes_take_every_cluster_size():
+    sizes = {fwd_key_splits(bh, n_q, n_k, d) for bh, n_q, n_k in SPLIT_SHAPES for d in (32, 128)}
+    assert sizes == {2, 4, 8, 16}
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("d", [32, 40, 64, 72, 128])
-@pytest.mark.parametrize("bh,n_q,n_k,splits", SPLIT_SHAPES)
-def test_forward_key_ranges_in_a_cluster(dtype, d, bh, n_q, n_k, splits):
+@pytest.mark.parametrize("bh,n_q,n_k", SPLIT_SHAPES)
+def test_forward_key_ranges_in_a_cluster(dtype, d, bh, n_q, n_k):
     """Few query tiles, many keys: the CTAs of a cluster each take a key range of a query-tile
     pair and combine (O, m, l) through distributed shared memory. Every element of O and LSE
     against the oracle; two runs bit-identical; nothing written outside O and LSE."""
     torch = G.require_gpu()
-    assert _fwd_key_splits(bh * ((n_q + 255) // 256), (n_k + 127) // 128) == splits
+    assert fwd_key_splits(bh, n_q, n_k, d) > 1
     q, k, v = G.inputs(f"fwdsplit/{dtype}/{d}/{bh}/{n_q}/{n_k}", bh, n_q, n_k, d, dtype)
     scale = 1.0 / math.sqrt(d)
     qd, kd, vd = (G.to_device(x, dtype) for x in (q, k, v))
@@ -256,11 +250,11 @@ def test_forward_key_ranges_in_a_cluster(dtype, d, bh, n_q, n_k, splits):
 
 def test_forward_key_ranges_peaked_rows():
     """Keys scaled by 8 (peaked rows): the key ranges of a pair end with maxima far apart, so
-    the combine's rescaling by 2^(m_r - M) carries the result. B·H = 2, N_q = 200, N_k = 20000,
-    d = 128, eight ranges."""
+    the combine's rescaling by 2^(m_r - M) carries the result. B·H = 2, N_q = 200, N_k = 33000,
+    d = 128, sixteen ranges."""
     G.require_gpu()
-    bh, n_q, n_k, d = 2, 200, 20000, 128
-    assert _fwd_key_splits(bh, (n_k + 127) // 128) == 8
+    bh, n_q, n_k, d = 2, 200, 33000, 128
+    assert fwd_key_splits(bh, n_q, n_k, d) == 16
     q, k, v = G.inputs("fwdsplit/peaked", bh, n_q, n_k, d, "bf16", k_scale=8.0)
     scale = 1.0 / math.sqrt(d)
     o, lse = run_forward(q, k, v, "bf16", scale)

@@ -17,6 +17,7 @@ import pytest
 from attention_fa2_forward_02_gb300 import binding, synth
 from oracle import attention as A
 from tests import gpu_util as G
+from tests.split_rules import balanced_ranges, fwd_key_splits
 from tests.tolerance import check_16bit, check_16bit_grad, check_16bit_long, check_lse
 
 pytestmark = pytest.mark.gpu
@@ -89,8 +90,8 @@ def test_heads_past_2_31_elements():
 
 def test_one_head_of_16m_keys():
     """One head of 16,778,000 keys (2.15e9 elements in K, V, dK, dV; a partial last key tile,
-    N_k mod 128 = 16). The forward's query-tile pair is shared by a cluster of 8 CTAs, each
-    adding 16,385 of the 131,079 key tiles into its float32 O and row sums, so O is held to
+    N_k mod 128 = 16). The forward's query-tile pair is shared by a cluster of 16 CTAs, each
+    adding 8,192 or 8,193 of the 131,079 key tiles into its float32 O and row sums, so O is held to
     the bar for float32 accumulation over that many additions (check_16bit_long: the 2e-2
     absolute bar, and 2e-2 max|ref| + n 2^-24 sum_j P_ij |v_j| per element); LSE, and the
     gradients (dQ summed in the split dQ pass's key ranges, dK and dV over the 200 queries)
@@ -100,8 +101,10 @@ def test_one_head_of_16m_keys():
     assert n_k * D > 2 ** 31 and n_k % 128 == 16
     inputs, outputs, scale = _run("large/long", 1, copies)
     (o, lse, dq, dk_c, dv_c), (o_ref, l_ref), g, weighted = _reference(inputs, outputs, scale, 0, copies)
-    n_kt, ranges = (n_k + 127) // 128, 8
-    check_16bit_long(o, o_ref, weighted, (n_kt + ranges - 1) // ranges, "O")
+    n_kt, ranges = (n_k + 127) // 128, fwd_key_splits(1, N_Q, n_k, D)
+    assert ranges == 16
+    longest = max(hi - lo for lo, hi in balanced_ranges(n_kt, ranges))
+    check_16bit_long(o, o_ref, weighted, longest, "O")
     check_lse(lse, l_ref, "LSE")
     check_16bit_grad(dq, g[0], g[3] / math.sqrt(copies), "bf16", "dQ")
     check_16bit_grad(dk_c, g[1], g[4], "bf16", "dK x c")

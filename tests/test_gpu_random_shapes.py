@@ -18,39 +18,10 @@ import pytest
 from attention_fa2_forward_02_gb300 import binding, synth
 from oracle import attention as A
 from tests import gpu_util as G
+from tests.split_rules import dkv_query_splits, dq_key_splits, fwd_key_splits, one_pass
 from tests.tolerance import check_16bit, check_16bit_grad, check_lse
 
 pytestmark = pytest.mark.gpu
-
-
-def _fwd_splits(bh, n_q, n_k):
-    ctas, n_kt = bh * -(-n_q // 256), -(-n_k // 128)
-    if 2 * ctas > 148:
-        return 1
-    cap, s = min(148 // ctas, n_kt // 8, 8), 1
-    while 2 * s <= cap:
-        s *= 2
-    return s
-
-
-def _one_pass(bh, n_k, d):
-    return d <= 64 and 2 * bh * -(-n_k // 128) > 148
-
-
-def _dkv_splits(bh, n_q, n_k):
-    n_kt, n_qt = -(-n_k // 128), -(-n_q // 128)
-    if 2 * bh * n_kt > 148 or n_qt < 16 * n_kt:
-        return 1
-    cap, s = min(148 // (bh * n_kt), n_qt // 8, 8), 1
-    while 2 * s <= cap:
-        s *= 2
-    return s
-
-
-def _dq_splits(bh, n_q, n_k):
-    n_qt, n_kt = -(-n_q // 128), -(-n_k // 128)
-    s = min(-(-148 // (bh * n_qt)), n_kt // 8, 8)
-    return 1 if s < 2 else s
 
 
 def _draw(count=24, seed=2026):
@@ -71,11 +42,11 @@ SHAPES = _draw()
 
 
 def test_the_draw_reaches_every_kernel_choice():
-    two = [s for s in SHAPES if not _one_pass(s[0], s[2], s[3])]
-    assert any(_fwd_splits(*s[:3]) > 1 for s in SHAPES)
-    assert any(_one_pass(s[0], s[2], s[3]) for s in SHAPES) and two
-    assert {2, 4, 8} <= {_dkv_splits(*s[:3]) for s in two}
-    assert any(_dq_splits(*s[:3]) > 1 and _dkv_splits(*s[:3]) == 1 for s in two)
+    two = [s for s in SHAPES if not one_pass(s[0], s[2], s[3])]
+    assert any(fwd_key_splits(*s[:4]) > 1 for s in SHAPES)
+    assert any(one_pass(s[0], s[2], s[3]) for s in SHAPES) and two
+    assert {2, 4, 8} <= {dkv_query_splits(*s[:4]) for s in two}
+    assert any(dq_key_splits(*s[:3]) > 1 and dkv_query_splits(*s[:4]) == 1 for s in two)
     assert any(s[1] == 1 for s in SHAPES) and any(s[2] <= 2 for s in SHAPES)
 
 
