@@ -40,7 +40,9 @@ constexpr uint32_t kNbElem = kElemThreads + 32;  // elementwise warps + issuer
 //   e1        elementwise step 1 done: P^T is in TMEM (dK/dV passes); S has
 //             been read (dQ pass)                    (256 arrivals)
 //   e2        elementwise step 2 done: dS^T / dS is in place (256 arrivals)
-//   dq_full   one-pass kernel: the dQ product of a query tile is in TMEM (tcgen05.commit)
+//   dq_full   one-pass kernel: the dQ product of a query tile is in TMEM (tcgen05.commit);
+//             as dv_done in the dK/dV pass: every dV product of the current key tile has
+//             completed                              (tcgen05.commit)
 //   dq_read   one-pass kernel: that product has been read out (256 arrivals)
 //   done      every MMA issued has completed; the dK/dV pass: every MMA of the
 //             current key tile                       (tcgen05.commit)
@@ -58,6 +60,7 @@ struct Bars {
     __device__ uint32_t e2() const { return base + 8u * (4 + 2 * S); }
     __device__ uint32_t done() const { return base + 8u * (5 + 2 * S); }
     __device__ uint32_t dq_full() const { return base + 8u * (6 + 2 * S); }
+    __device__ uint32_t dv_done() const { return dq_full(); }
     __device__ uint32_t dq_read() const { return base + 8u * (7 + 2 * S); }
     __device__ uint32_t kv_free() const { return base + 8u * (8 + 2 * S); }
 };

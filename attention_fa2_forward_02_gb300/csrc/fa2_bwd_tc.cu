@@ -295,6 +295,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                         for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
                             mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), b + (uint64_t)(kk * C::kAtomRowBytes),
                                    idesc_g, (i > 0 || kk > 0));
+                        if (!kSplitQ && !more) mma_commit(bars.dv_done());  // dV of key tile u complete
                     }
                     __syncwarp();
                     if (more) {
@@ -412,6 +413,27 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             if constexpr (C::kNamed) nb_arrive(nb, kNbElem);
             else mbar_arrive(mbar);
         };
+        // One value tensor, no query split: each accumulator leaves as soon as the products
+        // that write it have completed, and before the products that restart it are issued.
+        // dV of key tile u (dv_done) right after the tile's last e2, while its last dK
+        // product and the next tile's first S^T and dP^T run; dK of key tile u (done) with
+        // the next tile's first dS^T, while its first dV and second S^T run. Every warp writes
+        // its 32 key rows of the 32-column chunks half, half + 2, ... of each, by TMA stores.
+        constexpr bool kOutInLoop = C::kNamed && !kSplitQ;
+        auto write_acc = [&](int acc, int tile) {  // acc 0: dV, 1: dK (times scale)
+            if (!(ok = ok && warp_wait(acc ? bars.done() : bars.dv_done(), (uint32_t)(tile & 1), wd))) return;
+            tc_fence_after();
+            const uint32_t src = tmem + lane_off + 256u + (uint32_t)(acc * D);
+#pragma unroll
+            for (int c = half; c < D / 32; c += 2) {
+                uint32_t r[32];
+                tmem_ld32(src + 32u * (uint32_t)c, r);
+                tmem_ld_wait();
+                reg_fence(r);
+                store_chunk_tma<kBf16>(acc ? &tm_dk : &tm_dv, out_slab, 32 * c, (kt + tile) * BT + quarter * 32, n_k, d_act,
+                                       bh, r, acc ? scale : 1.f);
+            }
+        };
         for (int u = 0; u < n_items; ++u) {
         for (int i = 0; i < n_qt; ++i) {
             const int g = u * n_qt + i;
@@ -458,7 +480,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
             tc_fence_before();
             signal(kNbE1, bars.e1());
             // step 2: dS^T = P^T * (dP^T - D), chunk by chunk in write-safe order
-            if (!(ok = warp_wait(bars.dp_full(), g & 1, wd))) {
+            if (!(ok = ok && warp_wait(bars.dp_full(), g & 1, wd))) {
                 signal(kNbE2, bars.e2());
                 continue;
             }
@@ -485,37 +507,42 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tm_q, const CUtensor
                 tmem_st16(t_dp + kPackedCol + 16u * c, pk);
             }
             tmem_st_wait();
+            if constexpr (kOutInLoop)
+                if (i == 0 && u > 0) write_acc(1, u - 1);  // read before e2 lets dK(u, 0) restart it
             tc_fence_before();
             signal(kNbE2, bars.e2());
         }
-        // dK, dV of key tile u: read out of tensor memory before this warp's next e1 arrival
-        if (ok) ok = warp_wait(bars.done(), (uint32_t)(u & 1), wd);
-        if constexpr (kSplitQ) elem_ok = ok;  // the cluster adds the ranges' shares below
-        else if (ok) {
-            tc_fence_after();
-            const int key0 = (kt + u) * BT + quarter * 32;  // first key row of this warp
-            const int key = key0 + lane;
-            const size_t row = (size_t)bh * n_k + key;
-            // half 0 writes dV (each pair's), half 1 writes dK (scaled)
+        if constexpr (kOutInLoop) {
+            write_acc(0, u);
+        } else {
+            // the split's share stays in tensor memory for the cluster's combine below; the
+            // two-value form stores dK, dV row by row once all its products have completed
+            if (ok) ok = warp_wait(bars.done(), (uint32_t)(u & 1), wd);
+            if constexpr (kSplitQ) elem_ok = ok;
+            else if (ok) {
+                tc_fence_after();
+                const int key = (kt + u) * BT + quarter * 32 + lane;
+                const size_t row = (size_t)bh * n_k + key;
+                // half 0 writes dV (each pair's), half 1 writes dK (scaled)
 #pragma unroll
-            for (int v = 0; v < (half ? 1 : kNV); ++v) {
-                const uint32_t src = tmem + lane_off + 256u + (uint32_t)((half ? kNV : v) * D);
-                void* dst = half ? dk : (v ? dv2 : dv);
-                const float mul = half ? scale : 1.f;
+                for (int v = 0; v < (half ? 1 : kNV); ++v) {
+                    const uint32_t src = tmem + lane_off + 256u + (uint32_t)((half ? kNV : v) * D);
+                    void* dst = half ? dk : (v ? dv2 : dv);
+                    const float mul = half ? scale : 1.f;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(src + 32u * c, r);
-                    tmem_ld_wait();
-                    reg_fence(r);
-                    if constexpr (C::kNamed)
-                        store_chunk_tma<kBf16>(half ? &tm_dk : &tm_dv, out_slab, 32 * c, key0, n_k, d_act, bh, r, mul);
-                    else
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(src + 32u * c, r);
+                        tmem_ld_wait();
+                        reg_fence(r);
                         store_row_chunk<kBf16>(dst, row, d_act, c, r, mul, key < n_k);
+                    }
                 }
             }
         }
         }  // key tiles
+        if constexpr (kOutInLoop)
+            if (n_items > 0) write_acc(1, n_items - 1);
         if (lane == 0) bulk_wait_group0();  // this warp's stores complete before the CTA exits
         __syncwarp();
     }
