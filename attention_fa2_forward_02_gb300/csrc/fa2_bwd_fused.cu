@@ -37,9 +37,10 @@
 // per warp.  At the end the CTA's dK and dV leave by TMA stores, each warp staging its
 // 32-row chunks in the same block.
 //
-// MMA order per query tile i (one thread issues, the tensor core runs in order):
-//   [e1(i)] dV += P^T(i) dO(i);  dP^T(i) -> dp_full;
-//   [stage i+1] S^T(i+1) -> s_full;  [e2(i)] dK += dS^T(i) Q(i);  dQ_i = dS(i) K -> dq_full, empty
+// MMA order per query tile i (one thread issues, the tensor core runs in order; S^T(0)
+// and dP^T(0) first):
+//   [e1(i)] dV += P^T(i) dO(i);  [stage i+1] S^T(i+1) -> s_full;
+//   [e2(i)] dK += dS^T(i) Q(i);  dQ_i = dS(i) K -> dq_full, empty;  dP^T(i+1) -> dp_full
 // The bracketed events reach the issuing warp as named barriers: e1, e2 from the
 // elementwise warps, "stage loaded" from a relay warp (warp 10) that waits on the
 // TMA barriers.  dQ_i goes to buffer i % 2, last written by dQ_(i-2), which the warps
@@ -47,8 +48,9 @@
 // Elementwise warps per query tile i:
 //   [s_full] P^T(i) -> e1;  [dq_full(i-1)] dQ_(i-1) to shared memory, bulk reduction;
 //   [dp_full] dS^T(i) into TMEM, dS(i) into shared memory -> e2
-// so the warps compute P under dK / dQ, stage dQ under dV and dP^T and compute dS under
-// S^T, while the tensor core runs dV, dP^T, S^T, dK, dQ back to back.
+// so the warps compute P under dK, dQ and dP^T, stage dQ under dV and compute dS under
+// S^T, while the tensor core runs dV, S^T, dK, dQ, dP^T back to back; dP^T(i) is
+// complete by the time the warps turn to dS(i).
 // In-order execution of the tensor core is what makes the column reuse safe: an
 // MMA that overwrites columns another reads (S^T(i+1) over P^T(i), dP^T(i+1) over
 // dS^T(i)) is always issued after the MMA that reads them.
@@ -184,11 +186,21 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
             }
         };
         static_assert(nb_fstage(S - 1) < 16, "named barriers");
+        auto issue_dpt = [&](int s) {  // dP^T = V dO^T
+            const uint64_t bd = ddo0 + st_off(s);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t o = (uint64_t)(C::koff(kk, BT) >> 4);
+                mma_ss(tmem + 128u, dv0 + o, bd + o, idesc_s, kk > 0);
+            }
+            mma_commit(bars.dp_full());
+        };
         nb_sync(nb_fstage(0), 64);  // K, V and the first Q / dO stage
         if (lane == 0) {
             tc_fence_after();
             issue_st(0);
             mma_commit(bars.s_full());
+            issue_dpt(0);
         }
         __syncwarp();
         for (int i = 0; i < n_qt; ++i) {
@@ -203,13 +215,6 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
                 for (int kk = 0; kk < BT / 16; ++kk)  // dV += P^T dO
                     mma_ts(tmem + 256u, tmem + kPackedCol + (uint32_t)(kk * 8), b + (uint64_t)(kk * C::kAtomRowBytes),
                            idesc_g, (i > 0 || kk > 0));
-                const uint64_t bd = ddo0 + st_off(s);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V dO^T
-                    const uint64_t o = (uint64_t)(C::koff(kk, BT) >> 4);
-                    mma_ss(tmem + 128u, dv0 + o, bd + o, idesc_s, kk > 0);
-                }
-                mma_commit(bars.dp_full());
             }
             __syncwarp();
             if (more) {
@@ -235,6 +240,7 @@ __global__ void __launch_bounds__(FusedCfg<D>::kThreads, 1)
                            mk0 + (uint64_t)(kk * C::kAtomRowBytes), idesc_q, kk > 0);
                 mma_commit(bars.dq_full());
                 mma_commit(bars.empty(s));
+                if (more) issue_dpt(sn);  // over dS^T(i), which dK(i) has been issued to read
             }
             __syncwarp();
         }
