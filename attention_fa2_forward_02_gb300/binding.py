@@ -40,6 +40,7 @@ EXPORTS = (
     "fa2_device_status",
     "fa2_watchdog_selftest",
     "fa2_status_string",
+    "fa2_last_launch_info",
 )
 
 
@@ -57,6 +58,13 @@ _c_ptr = ctypes.c_void_p
 _i64 = ctypes.c_int64
 _i32 = ctypes.c_int32
 _f32 = ctypes.c_float
+
+
+class LaunchInfo(ctypes.Structure):
+    """fa2_launch_info of include/fa2.h."""
+    _fields_ = [("fwd_key_ranges", ctypes.c_int32), ("bwd_one_pass", ctypes.c_int32),
+                ("bwd_dkv_query_ranges", ctypes.c_int32), ("bwd_dq_key_ranges", ctypes.c_int32),
+                ("bwd_key_tiles_per_cta", ctypes.c_int32)]
 
 
 def _declare(lib):
@@ -83,6 +91,7 @@ def _declare(lib):
         "fa2_device_status": (ctypes.c_int, [_c_ptr]),
         "fa2_watchdog_selftest": (ctypes.c_int, [_c_ptr]),
         "fa2_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "fa2_last_launch_info": (ctypes.c_int, [ctypes.POINTER(LaunchInfo)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -358,6 +367,13 @@ def psa_extract_v_backward(d_v, d_qkv, num_heads: int, stream=None) -> None:
 def fa2_device_status(stream=None) -> None:
     """Synchronise the stream and raise if a kernel gave up a bounded wait."""
     _check(library().fa2_device_status(_stream(stream)), "fa2_device_status")
+
+
+def fa2_last_launch_info() -> dict:
+    """What this host thread's most recent forward / backward calls launched (fa2.h)."""
+    info = LaunchInfo()
+    _check(library().fa2_last_launch_info(ctypes.byref(info)), "fa2_last_launch_info")
+    return {name: int(getattr(info, name)) for name, _ in LaunchInfo._fields_}
 
 
 def fa2_watchdog_selftest(stream=None) -> None:

@@ -167,6 +167,11 @@ bool cluster_fits(const void* func, int threads, int smem, int size, int slot) {
 // bf16, d = 64: B*H = 2, N = 4096: 0.068 -> 0.050 ms; B*H = 1, N = 8192: 0.117 -> 0.086 ms;
 // at 128 and 256 key-tile CTAs the one-pass kernel stays ahead: 0.070 / 0.076 against
 // 0.089 / 0.086 ms). Those shapes take the two passes at every head size.
+fa2_launch_info& launch_record() {
+    thread_local fa2_launch_info record{};
+    return record;
+}
+
 static bool use_one_pass(int64_t bh, int64_t n_q, int64_t n_k, int32_t head_dim) {
     (void)n_q;
     return pad_head_dim(head_dim) <= 64 && 2 * bh * ((n_k + 127) / 128) > 148;
@@ -219,6 +224,11 @@ fa2_status backward_common(const void* q, const void* k, const void* v, const vo
     }
     p.bh = bh; p.n_q = n_q; p.n_k = n_k; p.d = head_dim; p.dtype = (int)dtype; p.scale = softmax_scale;
     if (!status_word(&p.status)) return FA2_ERR_CUDA;
+    fa2_launch_info& rec = launch_record();  // the launch code fills in the splits it takes
+    rec.bwd_one_pass = one_pass ? 1 : 0;
+    rec.bwd_dkv_query_ranges = 1;
+    rec.bwd_dq_key_ranges = 1;
+    rec.bwd_key_tiles_per_cta = 0;
     const cudaError_t e = one_pass ? launch_bwd_fused(p, static_cast<cudaStream_t>(stream))
                                    : launch_bwd_tc(p, static_cast<cudaStream_t>(stream), stages);
     return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
@@ -249,6 +259,7 @@ fa2_status fa2_forward(const void* q, const void* k, const void* v, void* o, flo
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return FA2_ERR_MISALIGNED;
     FwdParams p{q, k, v, o, lse, bh, n_q, n_k, head_dim, (int)dtype, softmax_scale, nullptr};
     if (!status_word(&p.status)) return FA2_ERR_CUDA;
+    launch_record().fwd_key_ranges = 1;  // the tensor-core launch records its split
     const cudaError_t e = dtype == FA2_DTYPE_F32 ? launch_fwd_f32(p, static_cast<cudaStream_t>(stream))
                                                  : launch_fwd_tc(p, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
@@ -450,6 +461,12 @@ fa2_status fa2_device_status(void* stream) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(g_watchdog_word, &zero, sizeof(zero)) != cudaSuccess) return FA2_ERR_CUDA;
     return FA2_ERR_DEVICE_TIMEOUT;
+}
+
+fa2_status fa2_last_launch_info(fa2_launch_info* info) {
+    if (!info) return FA2_ERR_INVALID_ARG;
+    *info = launch_record();
+    return FA2_OK;
 }
 
 const char* fa2_status_string(fa2_status s) {

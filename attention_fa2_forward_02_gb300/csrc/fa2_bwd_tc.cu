@@ -1162,6 +1162,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
     // (without a split the map is encoded over q and never used)
     const int splits = C::kNamed && p.dq_part ? p.dq_splits : 1;
     const bool split = splits > 1;
+    if (C::kNamed && (stages & kBwdDq)) launch_record().bwd_dq_key_ranges = splits;  // plain attention only
     if (!encode_tmap_3d(&tdqp, split ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt, split ? 4 : 2,
                         split ? static_cast<const void*>(p.dq_part) : p.q, split ? (uint64_t)D : d,
                         split ? (uint64_t)p.n_q_pad : (uint64_t)p.n_q, (uint64_t)(split ? splits * p.bh : p.bh),
@@ -1192,6 +1193,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
             qsplits /= 2;
     }
     if (qsplits > 1 && (stages & kBwdDkDv)) {
+        launch_record().bwd_dkv_query_ranges = qsplits;
         auto kern = split_kern;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(n_kt * qsplits), (unsigned)p.bh, 1);
@@ -1216,6 +1218,7 @@ cudaError_t launch_impl(const BwdParams& p, cudaStream_t stream, int slot, int s
         e = ensure_smem_limit(reinterpret_cast<const void*>(both), smem, 42 + (slot - 16) / 2);  // slots 42..51
         if (e != cudaSuccess) return e;
         const int m = C::kNamed ? dkdv_tiles_per_cta(n_qt, n_kt, p.bh, sm_count()) : 1;
+        if (C::kNamed) launch_record().bwd_key_tiles_per_cta = m;
         const int n_kc = (n_kt + m - 1) / m;
         const int dq_len = (n_kt + splits - 1) / splits;  // key tiles per dQ CTA
         both<<<dim3((unsigned)(n_kc + n_qt * splits), (unsigned)p.bh, 1), C::kThreads, smem, stream>>>(

@@ -587,6 +587,7 @@ cudaError_t launch_impl(const FwdParams& p, cudaStream_t stream, int slot) {
     // a device that cannot hold the whole cluster at once takes fewer ranges
     while (splits > 1 && !cluster_fits(reinterpret_cast<const void*>(kern), C::kThreads, C::kSmemBytes, splits, slot))
         splits /= 2;
+    launch_record().fwd_key_ranges = splits;
     if (splits == 1) {
         const dim3 grid((unsigned)pairs, (unsigned)p.bh, 1);
         kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, tv2, p.o, p.o2, p.lse, (int)p.n_q, (int)p.n_k,

@@ -193,6 +193,10 @@ int sm_count();
 // non-portable cluster size is allowed for it first); cached per slot and size.
 bool cluster_fits(const void* func, int threads, int smem, int size, int slot);
 
+// The calling host thread's record of what its most recent calls launched (returned by
+// fa2_last_launch_info); the launch code writes the choices it made.
+fa2_launch_info& launch_record();
+
 // Raises the dynamic shared-memory limit of `func` on the current device once.
 cudaError_t ensure_smem_limit(const void* func, int bytes, int slot);
 

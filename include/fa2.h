@@ -423,6 +423,33 @@ fa2_status fa2_device_status(void* stream);
  */
 fa2_status fa2_watchdog_selftest(void* stream);
 
+/*
+ * fa2_last_launch_info - which kernels the calling host thread's most recent calls
+ * launched, as the sizes and this device decided (cluster sizes after the residency
+ * check included).  Each field is written by the calls named beside it, when their
+ * arguments were valid, and keeps its value otherwise; all are 0 before any such call.
+ *   fwd_key_ranges         fa2_forward, psa_fa2_forward: CTAs of a thread-block cluster
+ *                          splitting each 256-row query block's keys (1: no split)
+ *   bwd_one_pass           fa2_backward (and _noalloc, and the stage entry points, which
+ *                          set 0): 1 if the one-pass kernel ran
+ *   bwd_dkv_query_ranges   the same calls: CTAs of a cluster splitting each key tile's
+ *                          queries in the dK/dV pass (1: no split, or no dK/dV stage)
+ *   bwd_dq_key_ranges      the same calls: key ranges of the dQ pass's float32 partial
+ *                          sums (1: no split, or no dQ stage)
+ *   bwd_key_tiles_per_cta  the same calls: key tiles per dK/dV CTA of the kernel running
+ *                          both passes in one grid (0: that kernel did not run)
+ * The record is per host thread and describes enqueued work, not completed work.
+ * Errors: FA2_ERR_INVALID_ARG (info is NULL).
+ */
+typedef struct fa2_launch_info {
+    int32_t fwd_key_ranges;
+    int32_t bwd_one_pass;
+    int32_t bwd_dkv_query_ranges;
+    int32_t bwd_dq_key_ranges;
+    int32_t bwd_key_tiles_per_cta;
+} fa2_launch_info;
+fa2_status fa2_last_launch_info(fa2_launch_info* info);
+
 /* fa2_status_string - a static, human-readable message for a status code. */
 const char* fa2_status_string(fa2_status s);
 

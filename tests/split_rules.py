@@ -59,6 +59,17 @@ def dq_key_splits(bh, n_q, n_k):
     return 1 if s < 2 else s
 
 
+def dkdv_tiles_per_cta(bh, n_q, n_k, sms):
+    """Key tiles per dK/dV CTA of the kernel that runs both passes in one grid: enough for
+    32 query tiles per CTA, at most 8, and fewer while the head's dK/dV CTAs would number
+    fewer than the SMs."""
+    n_qt, n_kt = -(-n_q // 128), -(-n_k // 128)
+    m = min(8, max(1, -(-32 // n_qt)))
+    while m > 1 and bh * -(-n_kt // m) < sms:
+        m -= 1
+    return m
+
+
 def balanced_ranges(n, splits):
     """The tiles [lo, hi) of each of `splits` ranges over n tiles, as the cluster splits take
     them: range r = [floor(r n / splits), floor((r + 1) n / splits))."""

@@ -3,6 +3,7 @@ and rejects invalid arguments on the host before any CUDA call (no GPU needed)."
 import ctypes
 import os
 import re
+import threading
 
 import pytest
 
@@ -36,6 +37,27 @@ def test_header_declares_the_calls():
               "fa2_status_string", "fa2_device_status"):
         assert n in names
     assert set(binding.EXPORTS) <= set(names)
+
+
+def test_launch_record_of_a_thread_that_launched_nothing(lib):
+    """fa2_last_launch_info: all zero on a host thread that has launched nothing; a call that
+    fails validation leaves the record alone; NULL is an invalid argument. No GPU needed."""
+    out = {}
+
+    def run():
+        info = binding.LaunchInfo()
+        # a forward with null pointers: rejected before any launch or record
+        out["fwd"] = lib.fa2_forward(None, None, None, None, None, 1, 1, 1, 64, BF16, 0.125, None)
+        out["st"] = lib.fa2_last_launch_info(ctypes.byref(info))
+        out["info"] = [getattr(info, f) for f, _ in binding.LaunchInfo._fields_]
+        out["null"] = lib.fa2_last_launch_info(None)
+
+    t = threading.Thread(target=run)
+    t.start()
+    t.join()
+    assert out["fwd"] == 1  # FA2_ERR_INVALID_ARG
+    assert out["st"] == 0 and out["info"] == [0, 0, 0, 0, 0]
+    assert out["null"] == 1
 
 
 def test_library_exports_every_declared_symbol(lib):

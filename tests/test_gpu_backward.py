@@ -409,6 +409,9 @@ def test_backward_dkdv_query_ranges_in_a_cluster(dtype, d, bh, n_q, n_k):
     for _ in range(2):
         grads = [G.guarded(tuple(x.shape), dtype) for x in (q, k, v)]
         binding.fa2_backward(qd, kd, vd, o, dod, lse, *(g.t for g in grads), ws, scale)
+        info = binding.fa2_last_launch_info()
+        assert (info["bwd_one_pass"], info["bwd_dkv_query_ranges"], info["bwd_dq_key_ranges"],
+                info["bwd_key_tiles_per_cta"]) == (0, dkv_query_splits(bh, n_q, n_k, d), dq_key_splits(bh, n_q, n_k), 0)
         binding.fa2_device_status()
         for name, g in zip(("dQ", "dK", "dV"), grads):
             g.assert_intact(name)

@@ -238,6 +238,8 @@ def test_forward_key_ranges_in_a_cluster(dtype, d, bh, n_q, n_k):
         o = G.guarded((bh, n_q, d), dtype)
         lse = G.guarded((bh, n_q), "f32")
         binding.fa2_forward(qd, kd, vd, o.t, lse.t, scale)
+        # the library launched the cluster the size rule gives (a GB300 holds every size)
+        assert binding.fa2_last_launch_info()["fwd_key_ranges"] == fwd_key_splits(bh, n_q, n_k, d)
         binding.fa2_device_status()
         o.assert_intact("O")
         lse.assert_intact("LSE")

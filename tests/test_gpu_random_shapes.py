@@ -18,7 +18,7 @@ import pytest
 from attention_fa2_forward_02_gb300 import binding, synth
 from oracle import attention as A
 from tests import gpu_util as G
-from tests.split_rules import dkv_query_splits, dq_key_splits, fwd_key_splits, one_pass
+from tests.split_rules import dkdv_tiles_per_cta, dkv_query_splits, dq_key_splits, fwd_key_splits, one_pass
 from tests.tolerance import check_16bit, check_16bit_grad, check_lse
 
 pytestmark = pytest.mark.gpu
@@ -61,10 +61,21 @@ def test_random_shape_vs_oracle(bh, n_q, n_k, d, dtype):
     o = G.empty((bh, n_q, d), dtype)
     lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
     binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    assert binding.fa2_last_launch_info()["fwd_key_ranges"] == fwd_key_splits(bh, n_q, n_k, d)
     grads = [G.empty(x.shape, dtype) for x in (q, k, v)]
     code = {"bf16": binding.DTYPE_BF16, "f16": binding.DTYPE_F16}[dtype]
     ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, code), dtype=torch.uint8, device="cuda")
     binding.fa2_backward(qd, kd, vd, o, dod, lse, *grads, ws, scale)
+    # the kernels the library chose are the ones the size rules give
+    info = binding.fa2_last_launch_info()
+    if one_pass(bh, n_k, d):
+        expect = (1, 1, 1, 0)
+    else:
+        qs = dkv_query_splits(bh, n_q, n_k, d)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        expect = (0, qs, dq_key_splits(bh, n_q, n_k), 0 if qs > 1 else dkdv_tiles_per_cta(bh, n_q, n_k, sms))
+    assert (info["bwd_one_pass"], info["bwd_dkv_query_ranges"], info["bwd_dq_key_ranges"],
+            info["bwd_key_tiles_per_cta"]) == expect
     binding.fa2_device_status()
     o_st, l_st = G.to_f64(o), G.to_f64(lse)
     dq, dk, dv = (G.to_f64(g) for g in grads)
