@@ -88,8 +88,20 @@ bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, co
     const cuuint64_t strides[2] = {d0 * (uint64_t)elem_bytes, d0 * d1 * (uint64_t)elem_bytes};
     const cuuint32_t box[3] = {box0, box1, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    auto encode = [&] {
+        return fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    };
+    CUresult r = encode();
+    if (r == CUDA_ERROR_INVALID_CONTEXT) {
+        // A host thread with no current context yet (the runtime makes one current only at
+        // its first launch or allocation there): the driver call needs one, so make the
+        // primary context of the thread's device current, as the launch would, and retry.
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return false;
+        r = encode();
+    }
+    return r == CUDA_SUCCESS;
 }
 
 bool watchdog_word(unsigned int** out) { return status_word(out); }

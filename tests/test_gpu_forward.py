@@ -250,6 +250,66 @@ def test_forward_key_ranges_in_a_cluster(dtype, d, bh, n_q, n_k):
     check_lse(G.to_f64(runs[0][1]), lse_ref)
 
 
+def test_calls_from_other_host_threads():
+    """The library works from host threads other than the one that first used CUDA (a thread
+    with no current context makes the primary one current before encoding its tensor maps),
+    and fa2_last_launch_info describes the calling thread's own calls: two threads, one
+    launching a 4-CTA cluster split and one no split, each run a forward and a backward and
+    read back their own choices; the outputs match those of the same calls on this thread."""
+    import threading
+
+    torch = G.require_gpu()
+    shapes = {"split": (1, 300, 5000, 64), "plain": (4, 512, 512, 64)}
+    assert fwd_key_splits(*shapes["split"]) == 4 and fwd_key_splits(*shapes["plain"]) == 1
+    work = {}
+    for name, (bh, n_q, n_k, d) in shapes.items():
+        q, k, v = G.inputs(f"fwdthread/{name}", bh, n_q, n_k, d, "bf16")
+        d_o = synth.tensor(f"fwdthread/{name}/do", (bh, n_q, d), "bf16")
+        ins = [G.to_device(x, "bf16") for x in (q, k, v, d_o)]
+        ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_BF16), dtype=torch.uint8,
+                         device="cuda")
+        work[name] = (ins, ws, (bh, n_q, n_k, d))
+
+    def outputs(name):
+        (qd, kd, vd, dod), ws, (bh, n_q, n_k, d) = work[name]
+        o, lse = G.empty((bh, n_q, d), "bf16"), torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+        binding.fa2_forward(qd, kd, vd, o, lse, 0.125)
+        fwd = binding.fa2_last_launch_info()["fwd_key_ranges"]
+        grads = [G.empty(tuple(x.shape), "bf16") for x in (qd, kd, vd)]
+        binding.fa2_backward(qd, kd, vd, o, dod, lse, *grads, ws, 0.125)
+        return fwd, binding.fa2_last_launch_info()["bwd_one_pass"], [o, lse, *grads]
+
+    seen, errors, barrier = {}, [], threading.Barrier(2, timeout=60)
+
+    def run(name):
+        try:
+            result = outputs(name)
+            torch.cuda.synchronize()
+        except Exception as e:  # reported below; the other thread must not wait for ever
+            errors.append(f"{name}: {e}")
+            result = None
+        try:
+            barrier.wait()  # both threads have launched before either compares
+        except threading.BrokenBarrierError:
+            pass
+        seen[name] = result
+
+    threads = [threading.Thread(target=run, args=(name,)) for name in shapes]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    binding.fa2_device_status()
+    for name, want_fwd in (("split", 4), ("plain", 1)):
+        fwd, bwd_one_pass, got = seen[name]
+        assert fwd == want_fwd and bwd_one_pass == 0  # 1 or 4 heads of few key tiles: two passes
+        _, _, here = outputs(name)
+        binding.fa2_device_status()
+        for a, b in zip(got, here):
+            assert torch.equal(a, b), f"{name}: a worker thread's result differs from this thread's"
+
+
 def test_forward_key_ranges_peaked_rows():
     """Keys scaled by 8 (peaked rows): the key ranges of a pair end with maxima far apart, so
     the combine's rescaling by 2^(m_r - M) carries the result. B·H = 2, N_q = 200, N_k = 33000,
