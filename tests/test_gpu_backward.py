@@ -8,7 +8,7 @@ from attention_fa2_forward_02_gb300 import binding, synth
 from oracle import attention as A
 from tests import gpu_util as G
 from tests.split_rules import dkv_query_splits, dq_key_splits, one_pass
-from tests.tolerance import check_16bit, check_16bit_grad
+from tests.tolerance import check_reordered_sum, check_16bit, check_16bit_grad
 
 pytestmark = pytest.mark.gpu
 
@@ -220,8 +220,9 @@ def test_backward_stages_vs_oracle_and_whole(d, dtype):
 def test_backward_reproducibility(d):
     """head_dim > 64 (two passes): every gradient is bit-reproducible.  head_dim <= 64 (one
     pass): dK and dV are; dQ is a float32 sum of per-key-tile partial sums added in arrival
-    order, so two runs may differ by rounding, at most one unit in the last place of the
-    16-bit result (80 heads at head size 64, for the one-pass kernel)."""
+    order, so two runs may differ by the reordering of that sum (`check_reordered_sum`: one
+    unit in the last place of the 16-bit result, plus 2^-16 of the largest |dQ| where the
+    partials cancel) (80 heads at head size 64, for the one-pass kernel)."""
     bh, n = (80 if d <= 64 else 2), 300
     assert one_pass(bh, n, d) == (d <= 64)
     q, k, v = G.inputs(f"bwd/det/{d}", bh, n, n, d, "bf16")
@@ -231,8 +232,7 @@ def test_backward_reproducibility(d):
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
     if d > 64:
         assert np.array_equal(a[0], b[0])
-    ulp = np.maximum(np.abs(a[0]), np.abs(b[0])) * 2.0 ** -7
-    assert np.all(np.abs(a[0] - b[0]) <= ulp + 1e-30)
+    check_reordered_sum(a[0], b[0])
 
 
 @pytest.mark.parametrize("d", [64, 128])

@@ -118,3 +118,20 @@ def check_16bit_grad(got, ref, rss, dtype="bf16", what="gradient"):
                   if worst else "")
         raise AssertionError(f"{what}: {int(np.sum(over))} element(s) beyond 2e-2 + u|ref| + 8u*rss; {detail}"
                              f"RMS err = {rms_err:.3e} (bound {rms_bound:.3e}), finite = {finite}")
+
+
+# Run-to-run agreement of the one-pass backward's dQ (not parity with the oracle): each
+# element is a float32 sum of per-key-tile partial sums added in whatever order the CTAs
+# reach the accumulator, then rounded to the 16-bit type. Two orders can differ by the
+# reordering error of the float32 sum, about (key tiles) 2^-24 times the partials' size, and
+# that can move the rounded result by one unit of its last place, or by more where the
+# partials cancel to a small result. The bound: one unit of the 16-bit type at the larger of
+# the two (2^-7 relative for bfloat16) plus 2^-16 of the tensor's largest magnitude.
+def check_reordered_sum(a, b, what="dQ"):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    bound = np.maximum(np.abs(a), np.abs(b)) * 2.0 ** -7 + 2.0 ** -16 * max(float(np.max(np.abs(a))), 1e-30)
+    excess = np.abs(a - b) - bound
+    if not np.all(excess <= 0):
+        i = np.unravel_index(int(np.argmax(excess)), excess.shape)
+        raise AssertionError(f"{what}: runs differ by {abs(a[i] - b[i]):.3e} at {i} (bound {bound[i]:.3e})")
