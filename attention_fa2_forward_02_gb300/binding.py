@@ -159,6 +159,11 @@ def _require_f32(where, **tensors):
 def _dev(t, name, ndim=None):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    import torch
+    current = torch.cuda.current_device()
+    if t.device.index != current:
+        # the library launches on the current device; another device's memory is not its to read
+        raise ValueError(f"{name} is on {t.device}, but the current device is cuda:{current}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if ndim is not None and t.dim() != ndim:

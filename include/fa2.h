@@ -9,6 +9,8 @@
  * FA2_ERR_CUDA, which reports a failed launch.  FA2_OK means "enqueued": a kernel
  * that later gives up a bounded wait on the device is reported only by
  * fa2_device_status (see there), and leaves that call's outputs partly written.
+ * Device pointers must be memory of the calling thread's current device, where the
+ * kernels run (memory of another device is not checked for and is not valid).
  * Any host thread may call the library.  A thread with no current CUDA context gets the
  * primary context of its current device made current (as a kernel launch would) before
  * the library's first driver call there.

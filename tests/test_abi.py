@@ -39,6 +39,32 @@ def test_header_declares_the_calls():
     assert set(binding.EXPORTS) <= set(names)
 
 
+def test_binding_rejects_a_tensor_of_another_device(monkeypatch):
+    """The binding refuses, before any library call, a tensor that is not on the current
+    device (the kernels would run on the current one). A stand-in tensor and a patched
+    current device: no GPU needed."""
+    torch = pytest.importorskip("torch")
+
+    class FakeCudaTensor:
+        is_cuda = True
+        device = torch.device("cuda", 1)
+
+        def is_contiguous(self):
+            return True
+
+        def dim(self):
+            return 3
+
+        def data_ptr(self):
+            return 0
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    with pytest.raises(ValueError, match="current device"):
+        binding._dev(FakeCudaTensor(), "q", 3)
+    FakeCudaTensor.device = torch.device("cuda", 0)
+    assert binding._dev(FakeCudaTensor(), "q", 3).value is None  # accepted: a null pointer's c_void_p
+
+
 def test_launch_record_of_a_thread_that_launched_nothing(lib):
     """fa2_last_launch_info: all zero on a host thread that has launched nothing; a call that
     fails validation leaves the record alone; NULL is an invalid argument. No GPU needed."""
