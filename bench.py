@@ -604,7 +604,7 @@ def run_ours(args):
     return 0
 
 
-def separate_passes(torch, B, b, stream, scale, reps=20):
+def separate_passes(torch, B, b, stream, scale, reps=50):
     """The backward's stages launched one by one (fa2_backward_preprocess, _dkdv, _dq), outside
     the timed region: how the one-grid fa2_backward_passes splits between the passes."""
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
@@ -623,10 +623,11 @@ def separate_passes(torch, B, b, stream, scale, reps=20):
             "bwd_dq_pass_ms": t[2], "bwd_dkdv_pass_tflops": 0.8 * BWD_FLOPS / t[1] / 1e9}
 
 
-def _batched_ms(torch, fn, reps=20, batch=8):
+def _batched_ms(torch, fn, reps=50, batch=8):
     """Device time of one fn() call: `batch` calls back to back between two events (the host
-    queues them ahead of the GPU, so no launch cost falls inside), median over `reps`."""
-    for _ in range(3):
+    queues them ahead of the GPU, so no launch cost falls inside), median over `reps` after
+    10 warm-up calls."""
+    for _ in range(10):
         fn()
     ts = []
     for _ in range(reps):
@@ -640,7 +641,7 @@ def _batched_ms(torch, fn, reps=20, batch=8):
     return statistics.median(ts)
 
 
-def other_configs(torch, B, dev, pk, reps=20):
+def other_configs(torch, B, dev, pk, reps=50):
     """The other attention shapes of the workload list, timed after the main region (seeded
     N(0,1) inputs; median of `reps` timings of 8 back-to-back calls each):
     forward B=4 H=16 N=4096 d=64, and cross attention B=1 H=32 N_q=1024 N_k=32768 d=128
