@@ -8,7 +8,7 @@ from attention_fa2_forward_02_gb300 import binding, synth
 from oracle import attention as A
 from tests import gpu_util as G
 from tests.split_rules import dkv_query_splits, dq_key_splits, one_pass
-from tests.tolerance import check_reordered_sum, check_16bit, check_16bit_grad
+from tests.tolerance import check_reordered_sum, check_16bit, check_16bit_grad, check_lse
 
 pytestmark = pytest.mark.gpu
 
@@ -433,3 +433,40 @@ def test_backward_dkdv_query_ranges_in_a_cluster(dtype, d, bh, n_q, n_k):
         staged = _stages(qd, kd, vd, o, dod, lse, scale, ws, dtype)
         for name, a, b in zip(("dQ", "dK", "dV"), runs[0], staged):
             assert torch.equal(a, b), f"{name}: stages differ from fa2_backward"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_the_most_heads_a_call_takes(d):
+    """B·H = 65535, the largest the entry points accept (the kernels take the head from the
+    grid's y index, whose limit that is), of 3 queries and 5 keys: forward and backward (at
+    head size 64 the one-pass kernel, its float32 dQ accumulator 2.1 GB of workspace; at 128
+    the two passes in one grid). The first, a middle and the last head against the oracle."""
+    torch = G.require_gpu()
+    bh, n_q, n_k = 65535, 3, 5
+    tag = f"bwd/maxheads/{d}"
+    q, k, v = G.inputs(tag, bh, n_q, n_k, d, "bf16")
+    d_o = synth.tensor(tag + "/do", (bh, n_q, d), "bf16")
+    qd, kd, vd, dod = (G.to_device(x, "bf16") for x in (q, k, v, d_o))
+    scale = 1 / math.sqrt(d)
+    o = G.empty((bh, n_q, d), "bf16")
+    lse = torch.empty((bh, n_q), dtype=torch.float32, device="cuda")
+    binding.fa2_forward(qd, kd, vd, o, lse, scale)
+    grads = [G.empty(tuple(x.shape), "bf16") for x in (q, k, v)]
+    ws = torch.empty(binding.fa2_backward_workspace_size(bh, n_q, n_k, d, binding.DTYPE_BF16), dtype=torch.uint8,
+                     device="cuda")
+    binding.fa2_backward(qd, kd, vd, o, dod, lse, *grads, ws, scale)
+    assert binding.fa2_last_launch_info()["bwd_one_pass"] == (1 if one_pass(bh, n_k, d) else 0) == (d <= 64)
+    binding.fa2_device_status()
+    w = lambda x: synth.widen(x, "bf16")  # noqa: E731
+    o_st, l_st = G.to_f64(o), G.to_f64(lse)
+    dq, dk, dv = (G.to_f64(g) for g in grads)
+    for b in (0, bh // 2, bh - 1):
+        one = slice(b, b + 1)
+        o_ref, l_ref = A.forward(w(q[one]), w(k[one]), w(v[one]), scale)
+        check_16bit(o_st[b], o_ref[0], f"O head {b}")
+        check_lse(l_st[b], l_ref[0], f"LSE head {b}")
+        rq, rk, rv, sq, sk, sv = A.backward_slice(w(q[one]), w(k[one]), w(v[one]), w(d_o[one]), scale, 0,
+                                                  o=o_st[one], lse=l_st[one], rounding_scales=True)
+        check_16bit_grad(dq[b], rq, sq, "bf16", f"dQ head {b}")
+        check_16bit_grad(dk[b], rk, sk, "bf16", f"dK head {b}")
+        check_16bit_grad(dv[b], rv, sv, "bf16", f"dV head {b}")
